@@ -1,0 +1,454 @@
+"""Benchmark: frames/s of the forward renderer on the 1M-Gaussian, SH degree 3,
+1920x1080 workload (one orbit view), through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config 1M|100k|5M|stress|tiny] [--no-graph] [--no-cpu-baseline]
+
+Prints ONE JSON line (rank 0). A step is one whole frame (projection, binning,
+sort, ranges, compositing) of gs_render, replayed from a CUDA graph, with the
+scene resident in HBM (236 MB of parameters: larger than the 126 MB L2, so no
+flush is needed between frames). Per-stage CUDA-event times come from a
+second pass of K frames through the stage entry points on the same stream.
+`e2e` renders the same frames through gs_render_from_host: the parameters are
+copied from pinned host memory and the image read back inside the timed
+region. Under torchrun each rank renders its own replica (independent frames:
+replicas only, no collective on the data path).
+
+--impl reference times the CPU oracle (the plain fp64 renderer) on the host
+cores on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6400.0
+SM_COUNT = 148
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ = 2032.0
+# algorithmic FP32 work per (pixel, Gaussian) evaluation: dx, dy (2), the
+# exponent with the conic pre-scaled (5), min with 0.99 (1), the 1/255 test (1)
+OPS_PER_EVAL = 9
+# per contribution: alpha*T, three colour FMAs, T update, the 1e-4 test
+OPS_PER_CONTRIB = 6
+PARAM_BYTES_PER_G = 12 + 16 + 12 + 4 + 192       # SH degree 3
+PROJ_BYTES_PER_G = 8 + 16 + 12 + 4 + 4 + 4 + 8
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="1M")
+    ap.add_argument("--view", type=int, default=0)
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured", d
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback", {}
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    rows.append(parts)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        load = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in load if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in load:
+            for i, n in enumerate(names):
+                if r[6 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": sorted(reasons), "samples": len(rows),
+                "samples_under_load": len(load),
+                "power_w_max": max((num(r[3]) or 0) for r in rows)}
+
+
+def traffic_from_profile(kernel_file: str, profile: str):
+    """Per-launch DRAM bytes recorded in a committed ncu summary, if the kernel source is unchanged."""
+    try:
+        src = open(os.path.join(ROOT, "gaussian_splatting_tile_02_b300", "csrc", kernel_file), "rb").read()
+        sha = hashlib.sha256(src).hexdigest()[:16]
+        rec = {}
+        with open(os.path.join(ROOT, "profiles", profile)) as f:
+            for line in f:
+                if ":" in line and line.startswith("- "):
+                    k, v = line[2:].split(":", 1)
+                    rec[k.strip()] = v.strip()
+        if rec.get("source_sha256_16") == sha:
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from gaussian_splatting_tile_02_b300 import scenes
+    cfg = scenes.CONFIGS[args.config]
+    scene = scenes.make_scene(cfg)
+    cam = scenes.make_cameras(cfg)[args.view]
+    oracle.build()
+    cores = oracle.get_threads()
+    # warm-up (one frame at most), then full frames until K are done or ~90 s pass
+    for _ in range(min(args.warmup, 1)):
+        oracle.render(scene, cam)
+    t0 = time.perf_counter()
+    done = 0
+    budget = 90.0
+    while done < args.steps:
+        oracle.render(scene, cam)
+        done += 1
+        if time.perf_counter() - t0 > budget:
+            break
+    dt = time.perf_counter() - t0
+    fps = done / dt
+    line = {"impl": "reference", "metric": f"frames/s at {cfg.width}x{cfg.height}, {cfg.n:,} Gaussians SH{cfg.sh_degree}",
+            "value": fps, "unit": "frames/s", "n_gpus": args.gpus, "steps": done, "warmup": min(args.warmup, 1),
+            "ms_per_step": 1e3 * dt / done, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.description, "n": cfg.n, "width": cfg.width, "height": cfg.height,
+                       "sh_degree": cfg.sh_degree, "view": args.view},
+            "cpu_baseline": {"value": fps, "unit": "frames/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{done} full frame(s) of the {args.steps} requested steps "
+                                       f"(capped at ~{budget:.0f} s), all stages, fp64 oracle"},
+            "e2e": {"value": fps, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+    import gaussian_splatting_tile_02_b300 as gs
+    from gaussian_splatting_tile_02_b300 import native, scenes
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = scenes.CONFIGS[args.config]
+    scene = scenes.make_scene(cfg)
+    cams = scenes.make_cameras(cfg)
+    cam = cams[args.view % len(cams)]
+    g = gs.gaussians_to_device(scene, dev)
+    r = gs.Renderer.for_scene(g, cam, headroom=1.1)
+    stream = torch.cuda.Stream(device=dev)
+    K_keys = gs.Renderer.count_keys(g, cam)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # --- warm-up and optional graph capture
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            r.render(cam, stream=stream, aux=False)
+        stream.synchronize()
+        st, flags, k = r.status(stream)
+        if st != native.GS_OK:
+            raise RuntimeError(f"render status {st} flags {flags} keys {k}")
+        graph = None
+        if not args.no_graph:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                r.render(cam, stream=stream, aux=False)
+            for _ in range(3):
+                graph.replay()
+            stream.synchronize()
+
+    hbm_peak, peak_kind, peaks = measured_peaks()
+    sampler = ClockSampler(local_rank)
+    with sampler:
+        time.sleep(0.3)
+        # --- main timed region: K whole frames
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                if graph is not None:
+                    graph.replay()
+                else:
+                    r.render(cam, stream=stream, aux=False)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        frame_ms = e0.elapsed_time(e1) / args.steps
+        frame_ms_max = max_over_ranks(frame_ms)
+
+        # --- per-stage times: K frames through the stage entry points, events between stages
+        stage_names = ["preprocess", "bin", "sort", "ranges", "rasterize"]
+        st_ms = {k: 0.0 for k in stage_names}
+        p = gs.alloc_projected(int(g["n"]), dev)
+        cap = r.key_capacity
+        keys = torch.empty(cap, dtype=torch.int64, device=dev)
+        vals = torch.empty(cap, dtype=torch.int32, device=dev)
+        keys_alt = torch.empty_like(keys)
+        vals_alt = torch.empty_like(vals)
+        offsets = torch.empty(int(g["n"]), dtype=torch.int32, device=dev)
+        nk = torch.zeros(1, dtype=torch.int64, device=dev)
+        tx, ty = gs.tiles_xy(cam)
+        ranges = torch.empty((tx * ty, 2), dtype=torch.int32, device=dev)
+        img = torch.empty((cam["height"], cam["width"], 3), dtype=torch.float32, device=dev)
+        fT = torch.empty((cam["height"], cam["width"]), dtype=torch.float32, device=dev)
+        ncon = torch.empty((cam["height"], cam["width"]), dtype=torch.int32, device=dev)
+        bws = torch.empty(int(gs.lib().gs_bin_workspace_bytes(int(g["n"]))), dtype=torch.uint8, device=dev)
+        sws = torch.empty(int(gs.lib().gs_sort_workspace_bytes(cap)), dtype=torch.uint8, device=dev)
+        import ctypes
+        L = gs.lib()
+        cs = gs.camera_struct(cam)
+        gst = gs.gaussians_struct(g)
+        pst = gs.projected_struct(p)
+        sp = ctypes.c_void_p(stream.cuda_stream)
+        kb = gs.key_bits(cam)
+        ptr = lambda t: t.data_ptr()
+
+        def stages(evs):
+            evs[0].record(stream)
+            native.check(L.gs_preprocess(ctypes.byref(gst), ctypes.byref(cs), ctypes.byref(pst), sp), "pre")
+            evs[1].record(stream)
+            native.check(L.gs_bin(ctypes.byref(pst), int(g["n"]), ctypes.byref(cs), ptr(offsets), ptr(keys),
+                                  ptr(vals), cap, ptr(nk), ptr(bws), bws.numel(), sp), "bin")
+            evs[2].record(stream)
+            native.check(L.gs_sort(ptr(keys), ptr(vals), ptr(keys_alt), ptr(vals_alt), ptr(nk), cap, kb,
+                                   ptr(sws), sws.numel(), sp), "sort")
+            evs[3].record(stream)
+            native.check(L.gs_tile_ranges(ptr(keys), ptr(nk), cap, ctypes.byref(cs), ptr(ranges), sp), "ranges")
+            evs[4].record(stream)
+            native.check(L.gs_rasterize(ctypes.byref(pst), int(g["n"]), ptr(vals), ptr(ranges), ctypes.byref(cs),
+                                        ptr(img), ptr(fT), ptr(ncon), sp), "raster")
+            evs[5].record(stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                stages([torch.cuda.Event(enable_timing=True) for _ in range(6)])
+            stream.synchronize()
+            all_evs = []
+            for _ in range(args.steps):
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+                stages(evs)
+                all_evs.append(evs)
+        torch.cuda.synchronize(dev)
+        for evs in all_evs:
+            for i, k in enumerate(stage_names):
+                st_ms[k] += evs[i].elapsed_time(evs[i + 1]) / args.steps
+        stage_total = sum(st_ms.values())
+
+        # --- end to end from host memory
+        e2e = None
+        if not args.no_e2e:
+            host = {k: torch.from_numpy(np.ascontiguousarray(scene[k])).pin_memory()
+                    for k in ("means", "quats", "log_scales", "opacity_logits", "sh")}
+            dst = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+            dst.update(n=g["n"], sh_degree=g["sh_degree"])
+            r2 = gs.Renderer(dst, cam["width"], cam["height"], r.key_capacity)
+            himg = torch.empty((cam["height"], cam["width"], 3), dtype=torch.float32).pin_memory()
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    gs.render_from_host(host, r2, cam, himg, stream=stream)
+                stream.synchronize()
+                n_e2e = max(3, min(args.steps, 50))
+                barrier()
+                t0 = time.perf_counter()
+                for _ in range(n_e2e):
+                    gs.render_from_host(host, r2, cam, himg, stream=stream)
+                stream.synchronize()
+                t_e2e = max_over_ranks(time.perf_counter() - t0)
+                barrier()
+            h2d = sum(v.numel() * v.element_size() for v in host.values())
+            d2h = himg.numel() * himg.element_size()
+            e2e = {"value": world * n_e2e / t_e2e, "unit": "frames/s", "h2d_bytes_per_step": int(h2d),
+                   "d2h_bytes_per_step": int(d2h), "steps": n_e2e}
+            del dst, r2
+    clocks = sampler.summary()
+
+    # --- algorithmic work of the last frame (from its outputs)
+    rng_np = ranges.cpu().numpy().astype(np.int64)
+    lens = (rng_np[:, 1] - rng_np[:, 0]).reshape(ty, tx)
+    L_pix = np.kron(lens, np.ones((16, 16), np.int64))[: cam["height"], : cam["width"]]
+    nc = ncon.cpu().numpy().astype(np.int64)
+    Tf = fT.cpu().numpy()
+    evals = int(np.where(Tf < 1e-4, nc, L_pix).sum())
+    n = int(g["n"])
+    K = K_keys
+    passes = (kb + 7) // 8
+    launches_per_frame = 1 + 3 + 2 + passes + (passes % 2) + 1 + 1
+    ras_ms = st_ms["rasterize"]
+    clk = clocks.get("sm_mhz") or SM_MAX_MHZ
+    fp32_peak = SM_COUNT * FP32_LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12     # T lane-ops/s at max clock
+    ras_ops = OPS_PER_EVAL * evals
+    ras_achieved = ras_ops / (ras_ms * 1e-3) / 1e12
+    pre_bytes = (PARAM_BYTES_PER_G + PROJ_BYTES_PER_G) * n
+    bin_bytes = 8 * n + 16 * n + 4 * n + 12 * K
+    sort_bytes = 8 * K + 24 * K * passes + (24 * K if passes % 2 else 0)
+    range_bytes = 8 * K + 8 * tx * ty
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
+    stages_out = {
+        "preprocess": {"ms": st_ms["preprocess"], "bound": "hbm", "GB/s": gbs(pre_bytes, st_ms["preprocess"]),
+                       "frac": gbs(pre_bytes, st_ms["preprocess"]) / hbm_peak, "bytes": pre_bytes},
+        "bin": {"ms": st_ms["bin"], "bound": "hbm", "GB/s": gbs(bin_bytes, st_ms["bin"]),
+                "frac": gbs(bin_bytes, st_ms["bin"]) / hbm_peak, "bytes": bin_bytes},
+        "sort": {"ms": st_ms["sort"], "bound": "hbm", "GB/s": gbs(sort_bytes, st_ms["sort"]),
+                 "frac": gbs(sort_bytes, st_ms["sort"]) / hbm_peak, "bytes": sort_bytes, "passes": passes},
+        "ranges": {"ms": st_ms["ranges"], "bound": "hbm", "GB/s": gbs(range_bytes, st_ms["ranges"]),
+                   "frac": gbs(range_bytes, st_ms["ranges"]) / hbm_peak, "bytes": range_bytes},
+        "rasterize": {"ms": ras_ms, "bound": "alu", "Top/s": ras_achieved, "frac": ras_achieved / fp32_peak,
+                      "evaluations": evals, "ops": ras_ops,
+                      "frac_at_sampled_clock": ras_achieved / (fp32_peak * clk / SM_MAX_MHZ)},
+    }
+    dominant = max(stages_out, key=lambda k: stages_out[k]["ms"])
+    if dominant == "rasterize":
+        roof = {"kernel": "rasterize_kernel", "bound": "alu", "achieved": ras_achieved, "peak": fp32_peak,
+                "unit": "T FP32 lane-ops/s", "frac": ras_achieved / fp32_peak,
+                "peak_kind": f"derived: {SM_COUNT} SMs x {FP32_LANES_PER_SM} FP32 lanes x {SM_MAX_MHZ:.0f} MHz",
+                "traffic": traffic_from_profile("rasterize.cu", "rasterize_1M.md"),
+                "units": f"{evals} pixel-Gaussian evaluations x {OPS_PER_EVAL} FP32 ops"}
+    else:
+        d = stages_out[dominant]
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": d["GB/s"], "peak": hbm_peak, "unit": "GB/s",
+                "frac": d["frac"], "peak_kind": peak_kind, "traffic": None}
+
+    result = {
+        "metric": f"frames/s at {cfg.width}x{cfg.height}, {cfg.n // 1000 if cfg.n < 10**6 else cfg.n // 10**6}"
+                  f"{'k' if cfg.n < 10**6 else 'M'} Gaussians SH{cfg.sh_degree}",
+        "value": world * 1e3 / frame_ms_max, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": frame_ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": cfg.description, "n": cfg.n, "width": cfg.width, "height": cfg.height,
+                   "sh_degree": cfg.sh_degree, "view": args.view, "keys": K, "key_capacity": r.key_capacity,
+                   "graph": graph is not None,
+                   "l2": "inputs larger than L2: 236 MB of Gaussian parameters per frame (L2 126 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": launches_per_frame * args.steps,
+        "roofline": roof,
+        "stages": stages_out,
+        "stage_sum_ms": stage_total,
+        "hbm_peak_gbs": hbm_peak,
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        cores = oracle.get_threads()
+        t0 = time.perf_counter()
+        frames = 0
+        while frames < 5:
+            oracle.render(scene, cam)
+            frames += 1
+            if time.perf_counter() - t0 > args.cpu_seconds:
+                break
+        dt = time.perf_counter() - t0
+        result["cpu_baseline"] = {"value": frames / dt, "unit": "frames/s", "cores": cores, "kind": "oracle",
+                                  "sample": f"{frames} full frame(s) of this workload, all stages, fp64"}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def main():
+    args = parse()
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, local_rank, world)
+
+
+if __name__ == "__main__":
+    main()

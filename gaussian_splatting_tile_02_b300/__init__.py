@@ -1,0 +1,247 @@
+"""B300 forward renderer for 3D Gaussian Splatting.
+
+Python front end of the C-ABI library ``libgs_b300.so`` (include/gs.h). The
+five steps of the lesson page "3D Gaussian Splatting à partir de zéro"
+(section "Rastérisation, non rayée": project to 2D, assign to 16x16 tiles,
+depth-sort per tile, alpha-composite front to back, pixel colour) each run as
+hand-written sm_103a CUDA kernels; this module only allocates device memory
+with PyTorch, passes pointers and the current stream, and checks status codes.
+
+    from gaussian_splatting_tile_02_b300 import Renderer, scenes
+    scene = scenes.make_scene("1M"); cam = scenes.make_cameras("1M")[0]
+    r = Renderer.for_scene(scene, cam)          # device copy + workspace
+    image = r.render(cam)                      # [H, W, 3] float32 on cuda
+
+Stage-wise calls (preprocess, bin_keys, sort_pairs, tile_ranges, rasterize)
+expose each step for testing and composition.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import native
+from .native import GsCamera, GsGaussians, GsProjected, check, lib
+
+__all__ = ["GsCamera", "camera_struct", "gaussians_to_device", "gaussians_struct", "preprocess",
+           "bin_keys", "sort_pairs", "tile_ranges", "rasterize", "Renderer", "read_status",
+           "key_bits", "tiles_xy", "lib", "render_from_host"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def tiles_xy(cam: dict) -> tuple:
+    return (int(cam["width"]) + 15) // 16, (int(cam["height"]) + 15) // 16
+
+
+def key_bits(cam: dict) -> int:
+    tx, ty = tiles_xy(cam)
+    return 32 + max(0, (tx * ty - 1).bit_length())
+
+
+def camera_struct(cam: dict) -> GsCamera:
+    c = GsCamera()
+    R = np.asarray(cam["R"], np.float32).reshape(9)
+    t = np.asarray(cam["t"], np.float32).reshape(3)
+    bg = np.asarray(cam.get("bg", (0.0, 0.0, 0.0)), np.float32).reshape(3)
+    for i in range(9):
+        c.R[i] = float(R[i])
+    for i in range(3):
+        c.t[i] = float(t[i])
+        c.bg[i] = float(bg[i])
+    c.fx, c.fy, c.cx, c.cy = (float(np.float32(cam[k])) for k in ("fx", "fy", "cx", "cy"))
+    c.near_z = float(np.float32(cam["near"]))
+    c.width, c.height = int(cam["width"]), int(cam["height"])
+    return c
+
+
+_FIELDS = ("means", "quats", "log_scales", "opacity_logits", "sh")
+
+
+def gaussians_to_device(scene: dict, device="cuda") -> dict:
+    torch = _torch()
+    out = {k: torch.from_numpy(np.ascontiguousarray(scene[k], np.float32)).to(device) for k in _FIELDS}
+    out["sh_degree"] = int(scene["sh_degree"])
+    out["n"] = int(scene["means"].shape[0])
+    return out
+
+
+def gaussians_struct(g: dict) -> GsGaussians:
+    s = GsGaussians()
+    for k in _FIELDS:
+        setattr(s, k, _ptr(g[k]))
+    s.n = int(g["n"])
+    s.sh_degree = int(g["sh_degree"])
+    return s
+
+
+def alloc_projected(n: int, device="cuda") -> dict:
+    torch = _torch()
+    return {"mean2d": torch.empty((n, 2), dtype=torch.float32, device=device),
+            "conic_opacity": torch.empty((n, 4), dtype=torch.float32, device=device),
+            "rgb": torch.empty((n, 3), dtype=torch.float32, device=device),
+            "depth": torch.empty(n, dtype=torch.float32, device=device),
+            "radius": torch.empty(n, dtype=torch.int32, device=device),
+            "tiles_touched": torch.empty(n, dtype=torch.int32, device=device),
+            "rect": torch.empty((n, 4), dtype=torch.int16, device=device)}
+
+
+def projected_struct(p: dict) -> GsProjected:
+    s = GsProjected()
+    for k in ("mean2d", "conic_opacity", "rgb", "depth", "radius", "tiles_touched", "rect"):
+        setattr(s, k, _ptr(p[k]))
+    return s
+
+
+# ------------------------------------------------------------------------------ stages
+
+def preprocess(g: dict, cam: dict, stream=None) -> dict:
+    """Step 1: projection. Returns the projected record (device tensors)."""
+    p = alloc_projected(int(g["n"]), g["means"].device)
+    check(lib().gs_preprocess(ctypes.byref(gaussians_struct(g)), ctypes.byref(camera_struct(cam)),
+                              ctypes.byref(projected_struct(p)), _stream_ptr(stream)), "gs_preprocess")
+    return p
+
+
+def bin_keys(p: dict, cam: dict, key_capacity: int, stream=None) -> dict:
+    """Step 2: scan + duplication into 64-bit tile|depth keys (device tensors)."""
+    torch = _torch()
+    n = int(p["depth"].shape[0])
+    dev = p["depth"].device
+    cap = int(key_capacity)
+    out = {"offsets": torch.empty(n, dtype=torch.int32, device=dev),
+           "keys": torch.empty(max(cap, 1), dtype=torch.int64, device=dev),
+           "vals": torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+           "num_keys": torch.zeros(1, dtype=torch.int64, device=dev)}
+    wsb = int(lib().gs_bin_workspace_bytes(n))
+    out["ws"] = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    check(lib().gs_bin(ctypes.byref(projected_struct(p)), n, ctypes.byref(camera_struct(cam)),
+                       _ptr(out["offsets"]), _ptr(out["keys"]), _ptr(out["vals"]), cap,
+                       _ptr(out["num_keys"]), _ptr(out["ws"]), wsb, _stream_ptr(stream)), "gs_bin")
+    return out
+
+
+def sort_pairs(keys, vals, num_keys, key_bits_: int, key_capacity: int | None = None, stream=None,
+               ws=None) -> dict:
+    """Step 3: stable radix sort in place (keys/vals end sorted). Returns scratch for status reads."""
+    torch = _torch()
+    cap = int(keys.shape[0] if key_capacity is None else key_capacity)
+    dev = keys.device
+    keys_alt = torch.empty_like(keys)
+    vals_alt = torch.empty_like(vals)
+    wsb = int(lib().gs_sort_workspace_bytes(cap))
+    if ws is None:
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    check(lib().gs_sort(_ptr(keys), _ptr(vals), _ptr(keys_alt), _ptr(vals_alt), _ptr(num_keys), cap,
+                        int(key_bits_), _ptr(ws), wsb, _stream_ptr(stream)), "gs_sort")
+    return {"keys": keys, "vals": vals, "ws": ws, "keys_alt": keys_alt, "vals_alt": vals_alt}
+
+
+def tile_ranges(sorted_keys, num_keys, cam: dict, key_capacity: int | None = None, stream=None):
+    """Step 4: [start, end) of every tile in the sorted keys, [tiles, 2] int32 (uint32 values)."""
+    torch = _torch()
+    tx, ty = tiles_xy(cam)
+    ranges = torch.empty((tx * ty, 2), dtype=torch.int32, device=sorted_keys.device)
+    cap = int(sorted_keys.shape[0] if key_capacity is None else key_capacity)
+    check(lib().gs_tile_ranges(_ptr(sorted_keys), _ptr(num_keys), cap, ctypes.byref(camera_struct(cam)),
+                               _ptr(ranges), _stream_ptr(stream)), "gs_tile_ranges")
+    return ranges
+
+
+def rasterize(p: dict, sorted_vals, ranges, cam: dict, stream=None, want_aux: bool = True) -> dict:
+    """Step 5: composite. Returns image [H,W,3], final_T [H,W], n_contrib [H,W]."""
+    torch = _torch()
+    H, W = int(cam["height"]), int(cam["width"])
+    dev = ranges.device
+    out = {"image": torch.empty((H, W, 3), dtype=torch.float32, device=dev)}
+    if want_aux:
+        out["final_T"] = torch.empty((H, W), dtype=torch.float32, device=dev)
+        out["n_contrib"] = torch.empty((H, W), dtype=torch.int32, device=dev)
+    n = int(p["depth"].shape[0])
+    check(lib().gs_rasterize(ctypes.byref(projected_struct(p)), n, _ptr(sorted_vals), _ptr(ranges),
+                             ctypes.byref(camera_struct(cam)), _ptr(out["image"]), _ptr(out.get("final_T")),
+                             _ptr(out.get("n_contrib")), _stream_ptr(stream)), "gs_rasterize")
+    return out
+
+
+def read_status(ws, stream=None) -> tuple:
+    """(status, flags, num_keys) from a workspace header; synchronises the stream."""
+    flags = ctypes.c_uint32(0)
+    nk = ctypes.c_uint64(0)
+    st = lib().gs_read_status(_ptr(ws), _stream_ptr(stream), ctypes.byref(flags), ctypes.byref(nk))
+    return int(st), int(flags.value), int(nk.value)
+
+
+# ------------------------------------------------------------------------------ whole frame
+
+class Renderer:
+    """Owns a device copy of a scene and a gs_render workspace sized for it."""
+
+    def __init__(self, g: dict, width: int, height: int, key_capacity: int):
+        torch = _torch()
+        self.g = g
+        self.width, self.height = int(width), int(height)
+        self.key_capacity = int(key_capacity)
+        self.ws_bytes = int(lib().gs_render_workspace_bytes(int(g["n"]), self.width, self.height,
+                                                           self.key_capacity))
+        dev = g["means"].device
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.image = torch.empty((self.height, self.width, 3), dtype=torch.float32, device=dev)
+        self.final_T = torch.empty((self.height, self.width), dtype=torch.float32, device=dev)
+        self.n_contrib = torch.empty((self.height, self.width), dtype=torch.int32, device=dev)
+        self._gs = gaussians_struct(g)
+
+    @staticmethod
+    def count_keys(g: dict, cam: dict) -> int:
+        """K for one view (runs preprocess + binning with zero capacity; synchronises)."""
+        p = preprocess(g, cam)
+        b = bin_keys(p, cam, 0)
+        return int(b["num_keys"].item())
+
+    @classmethod
+    def for_scene(cls, scene: dict, cams, headroom: float = 1.25, device="cuda") -> "Renderer":
+        g = gaussians_to_device(scene, device) if isinstance(scene["means"], np.ndarray) else scene
+        cams = cams if isinstance(cams, (list, tuple)) else [cams]
+        k = max(cls.count_keys(g, c) for c in cams)
+        w = max(int(c["width"]) for c in cams)
+        h = max(int(c["height"]) for c in cams)
+        return cls(g, w, h, int(k * headroom) + 1024)
+
+    def render(self, cam: dict, stream=None, aux: bool = True):
+        """Renders one frame into self.image (no host synchronisation)."""
+        assert int(cam["width"]) == self.width and int(cam["height"]) == self.height
+        c = camera_struct(cam)
+        check(lib().gs_render(ctypes.byref(self._gs), ctypes.byref(c), self.key_capacity, _ptr(self.ws),
+                              self.ws_bytes, _ptr(self.image), _ptr(self.final_T) if aux else None,
+                              _ptr(self.n_contrib) if aux else None, _stream_ptr(stream)), "gs_render")
+        return self.image
+
+    def status(self, stream=None) -> tuple:
+        return read_status(self.ws, stream)
+
+
+def render_from_host(host: dict, renderer: Renderer, cam: dict, host_image, stream=None) -> None:
+    """One frame from host (pinned) parameter arrays into a host image through gs_render_from_host."""
+    hs = GsGaussians()
+    for k in _FIELDS:
+        setattr(hs, k, host[k].data_ptr())
+    hs.n = int(renderer.g["n"])
+    hs.sh_degree = int(renderer.g["sh_degree"])
+    check(lib().gs_render_from_host(ctypes.byref(hs), ctypes.byref(renderer._gs),
+                                    ctypes.byref(camera_struct(cam)), renderer.key_capacity,
+                                    _ptr(renderer.ws), renderer.ws_bytes, _ptr(renderer.image),
+                                    host_image.data_ptr(), _stream_ptr(stream)), "gs_render_from_host")

@@ -1,0 +1,292 @@
+// Host side of the C ABI declared in include/gs.h: argument validation,
+// workspace layout and the chaining of the five steps on one stream.
+#include <math.h>
+#include <string.h>
+
+#include "gs_internal.cuh"
+
+namespace gs {
+
+long long g_spin_limit = 1ll << 22;   // ~1 s of polling with backoff
+constexpr long long kDefaultSpin = 1ll << 22;
+constexpr int64_t kMaxKeyCapacity = (1ll << 30) - 1;   // look-back status words keep 30 bits
+constexpr int64_t kMaxGaussians = (1ll << 32) - 1;     // values are uint32 indices
+
+CamConst make_cam_const(const gs_camera& c) {
+    CamConst k;
+    for (int i = 0; i < 9; i++) k.R[i] = c.R[i];
+    for (int i = 0; i < 3; i++) {
+        k.t[i] = c.t[i];
+        k.bg[i] = c.bg[i];
+    }
+    k.fx = c.fx; k.fy = c.fy; k.cx = c.cx; k.cy = c.cy; k.near_z = c.near_z;
+    k.width = c.width; k.height = c.height;
+    k.tiles_x = tiles_x(c);
+    k.tiles_y = tiles_y(c);
+    // camera centre -R^T t, in double then rounded
+    for (int i = 0; i < 3; i++) {
+        double s = 0.0;
+        for (int j = 0; j < 3; j++) s += (double)c.R[3 * j + i] * (double)c.t[j];
+        k.campos[i] = (float)(-s);
+    }
+    return k;
+}
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool camera_ok(const gs_camera* c) {
+    if (!c) return false;
+    if (c->width < 1 || c->height < 1 || c->width > 32768 || c->height > 32768) return false;
+    if (!(c->near_z > 0.0f) || !isfinite(c->near_z)) return false;
+    const float v[] = {c->fx, c->fy, c->cx, c->cy, c->bg[0], c->bg[1], c->bg[2]};
+    for (float x : v)
+        if (!isfinite(x)) return false;
+    for (int i = 0; i < 9; i++)
+        if (!isfinite(c->R[i])) return false;
+    for (int i = 0; i < 3; i++)
+        if (!isfinite(c->t[i])) return false;
+    return true;
+}
+
+bool gaussians_ok(const gs_gaussians* g) {
+    if (!g || g->n < 0 || g->n > kMaxGaussians || g->sh_degree < 0 || g->sh_degree > 3) return false;
+    if (g->n == 0) return true;
+    if (!g->means || !g->quats || !g->log_scales || !g->opacity_logits || !g->sh) return false;
+    if (!aligned(g->quats, 16) || !aligned(g->means, 4) || !aligned(g->log_scales, 4) ||
+        !aligned(g->opacity_logits, 4) || !aligned(g->sh, 16))
+        return false;
+    return true;
+}
+
+bool projected_ok(const gs_projected* p, int64_t n) {
+    if (!p) return false;
+    if (n == 0) return true;
+    return p->mean2d && p->conic_opacity && p->rgb && p->depth && p->radius && p->tiles_touched && p->rect &&
+           aligned(p->mean2d, 8) && aligned(p->conic_opacity, 16) && aligned(p->rgb, 4) && aligned(p->depth, 4) &&
+           aligned(p->radius, 4) && aligned(p->tiles_touched, 4) && aligned(p->rect, 8);
+}
+
+int key_bits_for(const gs_camera& c) {
+    const int64_t tiles = (int64_t)tiles_x(c) * tiles_y(c);
+    int b = 0;
+    while ((1ll << b) < tiles) b++;
+    return 32 + b;
+}
+
+gs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GS_OK : GS_ERR_CUDA; }
+
+// gs_render workspace layout
+struct RenderLayout {
+    size_t header, mean2d, conic, rgb, depth, radius, touched, rect, offsets, bin, keys, vals, keys_alt,
+        vals_alt, sort, ranges, num_keys, total;
+};
+
+RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
+    RenderLayout L;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o += align_up(bytes);
+        return at;
+    };
+    const size_t un = (size_t)(n > 0 ? n : 0), uc = (size_t)(cap > 0 ? cap : 0);
+    const size_t tiles = (size_t)((w + kTile - 1) / kTile) * (size_t)((h + kTile - 1) / kTile);
+    L.header = take(sizeof(StatusHeader));
+    L.num_keys = take(sizeof(uint64_t));
+    L.mean2d = take(8 * un);
+    L.conic = take(16 * un);
+    L.rgb = take(12 * un);
+    L.depth = take(4 * un);
+    L.radius = take(4 * un);
+    L.touched = take(4 * un);
+    L.rect = take(8 * un);
+    L.offsets = take(4 * un);
+    L.bin = take(bin_scratch_bytes(n));
+    L.keys = take(8 * uc);
+    L.vals = take(4 * uc);
+    L.keys_alt = take(8 * uc);
+    L.vals_alt = take(4 * uc);
+    L.sort = take(sort_scratch_bytes(cap));
+    L.ranges = take(8 * tiles);
+    L.total = o;
+    return L;
+}
+
+}  // namespace
+}  // namespace gs
+
+using namespace gs;
+
+extern "C" {
+
+const char* gs_status_string(int32_t s) {
+    switch (s) {
+        case GS_OK: return "ok";
+        case GS_ERR_INVALID_ARG: return "invalid argument";
+        case GS_ERR_CAPACITY: return "key capacity exceeded";
+        case GS_ERR_CUDA: return "CUDA error";
+        case GS_ERR_TIMEOUT: return "device wait timed out";
+        case GS_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        default: return "unknown status";
+    }
+}
+
+int32_t gs_abi_version(void) { return GS_ABI_VERSION; }
+
+void gs_set_spin_limit(int64_t iterations) { g_spin_limit = iterations > 0 ? iterations : kDefaultSpin; }
+
+gs_status gs_preprocess(const gs_gaussians* g, const gs_camera* cam, const gs_projected* out, void* stream) {
+    if (!gaussians_ok(g) || !camera_ok(cam) || !projected_ok(out, g ? g->n : 0)) return GS_ERR_INVALID_ARG;
+    return cuda_status(launch_preprocess(*g, make_cam_const(*cam), *out, (cudaStream_t)stream));
+}
+
+size_t gs_bin_workspace_bytes(int64_t n) { return sizeof(StatusHeader) + bin_scratch_bytes(n < 0 ? 0 : n); }
+
+gs_status gs_bin(const gs_projected* p, int64_t n, const gs_camera* cam, uint32_t* offsets, uint64_t* keys,
+                 uint32_t* vals, int64_t key_capacity, uint64_t* num_keys, void* ws, size_t ws_bytes,
+                 void* stream) {
+    if (n < 0 || n > kMaxGaussians || !camera_ok(cam) || !projected_ok(p, n) || !num_keys) return GS_ERR_INVALID_ARG;
+    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
+    if (n > 0 && !offsets) return GS_ERR_INVALID_ARG;
+    if (key_capacity > 0 && (!keys || !vals || !aligned(keys, 8) || !aligned(vals, 4))) return GS_ERR_INVALID_ARG;
+    if (!aligned(num_keys, 8)) return GS_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < gs_bin_workspace_bytes(n)) return GS_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    auto* header = static_cast<StatusHeader*>(ws);
+    cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
+    if (e != cudaSuccess) return GS_ERR_CUDA;
+    return cuda_status(launch_bin(*p, n, make_cam_const(*cam), offsets, keys, vals, key_capacity, num_keys, header,
+                                  static_cast<char*>(ws) + sizeof(StatusHeader), s));
+}
+
+size_t gs_sort_workspace_bytes(int64_t key_capacity) {
+    return sizeof(StatusHeader) + sort_scratch_bytes(key_capacity < 0 ? 0 : key_capacity);
+}
+
+gs_status gs_sort(uint64_t* keys, uint32_t* vals, uint64_t* keys_alt, uint32_t* vals_alt, const uint64_t* num_keys,
+                  int64_t key_capacity, int32_t key_bits, void* ws, size_t ws_bytes, void* stream) {
+    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity || key_bits < 1 || key_bits > 64 || !num_keys)
+        return GS_ERR_INVALID_ARG;
+    if (key_capacity > 0 && (!keys || !vals || !keys_alt || !vals_alt || !aligned(keys, 8) || !aligned(keys_alt, 8) ||
+                             !aligned(vals, 4) || !aligned(vals_alt, 4)))
+        return GS_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < gs_sort_workspace_bytes(key_capacity)) return GS_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    auto* header = static_cast<StatusHeader*>(ws);
+    cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
+    if (e != cudaSuccess) return GS_ERR_CUDA;
+    return cuda_status(launch_sort(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, key_bits, header,
+                                   static_cast<char*>(ws) + sizeof(StatusHeader), g_spin_limit, s));
+}
+
+gs_status gs_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_keys, int64_t key_capacity,
+                         const gs_camera* cam, uint32_t* ranges, void* stream) {
+    if (!camera_ok(cam) || !ranges || !num_keys || key_capacity < 0 || key_capacity > kMaxKeyCapacity)
+        return GS_ERR_INVALID_ARG;
+    if (key_capacity > 0 && !sorted_keys) return GS_ERR_INVALID_ARG;
+    if (!aligned(ranges, 8)) return GS_ERR_INVALID_ARG;
+    return cuda_status(launch_tile_ranges(sorted_keys, num_keys, key_capacity, tiles_x(*cam) * tiles_y(*cam), ranges,
+                                          (cudaStream_t)stream));
+}
+
+gs_status gs_rasterize(const gs_projected* p, int64_t n, const uint32_t* sorted_vals, const uint32_t* ranges,
+                       const gs_camera* cam, float* image, float* final_T, uint32_t* n_contrib, void* stream) {
+    if (n < 0 || !camera_ok(cam) || !projected_ok(p, n) || !ranges || !image || !aligned(ranges, 8))
+        return GS_ERR_INVALID_ARG;
+    if (n > 0 && !sorted_vals) return GS_ERR_INVALID_ARG;
+    return cuda_status(launch_rasterize(*p, n, sorted_vals, ranges, make_cam_const(*cam), image, final_T, n_contrib,
+                                        (cudaStream_t)stream));
+}
+
+size_t gs_render_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity) {
+    if (n < 0 || width < 1 || height < 1 || key_capacity < 0) return 0;
+    return render_layout(n, width, height, key_capacity).total;
+}
+
+gs_status gs_render(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, void* ws, size_t ws_bytes,
+                    float* image, float* final_T, uint32_t* n_contrib, void* stream) {
+    if (!gaussians_ok(g) || !camera_ok(cam) || !image) return GS_ERR_INVALID_ARG;
+    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
+    const RenderLayout L = render_layout(g->n, cam->width, cam->height, key_capacity);
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GS_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* w = static_cast<char*>(ws);
+    auto* header = reinterpret_cast<StatusHeader*>(w + L.header);
+    auto* num_keys = reinterpret_cast<uint64_t*>(w + L.num_keys);
+    gs_projected p;
+    p.mean2d = reinterpret_cast<float*>(w + L.mean2d);
+    p.conic_opacity = reinterpret_cast<float*>(w + L.conic);
+    p.rgb = reinterpret_cast<float*>(w + L.rgb);
+    p.depth = reinterpret_cast<float*>(w + L.depth);
+    p.radius = reinterpret_cast<int32_t*>(w + L.radius);
+    p.tiles_touched = reinterpret_cast<uint32_t*>(w + L.touched);
+    p.rect = reinterpret_cast<uint16_t*>(w + L.rect);
+    auto* offsets = reinterpret_cast<uint32_t*>(w + L.offsets);
+    auto* keys = reinterpret_cast<uint64_t*>(w + L.keys);
+    auto* vals = reinterpret_cast<uint32_t*>(w + L.vals);
+    auto* keys_alt = reinterpret_cast<uint64_t*>(w + L.keys_alt);
+    auto* vals_alt = reinterpret_cast<uint32_t*>(w + L.vals_alt);
+    auto* ranges = reinterpret_cast<uint32_t*>(w + L.ranges);
+    const CamConst cc = make_cam_const(*cam);
+
+    cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
+    if (e == cudaSuccess) e = launch_preprocess(*g, cc, p, s);
+    if (e == cudaSuccess)
+        e = launch_bin(p, g->n, cc, offsets, keys, vals, key_capacity, num_keys, header, w + L.bin, s);
+    if (e == cudaSuccess)
+        e = launch_sort(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, key_bits_for(*cam), header,
+                        w + L.sort, g_spin_limit, s);
+    if (e == cudaSuccess)
+        e = launch_tile_ranges(keys, num_keys, key_capacity, cc.tiles_x * cc.tiles_y, ranges, s);
+    if (e == cudaSuccess) e = launch_rasterize(p, g->n, vals, ranges, cc, image, final_T, n_contrib, s);
+    return cuda_status(e);
+}
+
+gs_status gs_render_from_host(const gs_gaussians* hg, const gs_gaussians* dg, const gs_camera* cam,
+                              int64_t key_capacity, void* ws, size_t ws_bytes, float* device_image,
+                              float* host_image, void* stream) {
+    if (!hg || !dg || hg->n != dg->n || hg->sh_degree != dg->sh_degree || !gaussians_ok(dg) || !host_image)
+        return GS_ERR_INVALID_ARG;
+    if (dg->n > 0 && (!hg->means || !hg->quats || !hg->log_scales || !hg->opacity_logits || !hg->sh))
+        return GS_ERR_INVALID_ARG;
+    if (!camera_ok(cam) || !device_image) return GS_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t n = (size_t)dg->n, nk = (size_t)((dg->sh_degree + 1) * (dg->sh_degree + 1));
+    struct { const void* src; const void* dst; size_t bytes; } cp[5] = {
+        {hg->means, dg->means, 12 * n}, {hg->quats, dg->quats, 16 * n}, {hg->log_scales, dg->log_scales, 12 * n},
+        {hg->opacity_logits, dg->opacity_logits, 4 * n}, {hg->sh, dg->sh, 12 * nk * n}};
+    for (auto& c : cp) {
+        if (c.bytes == 0) continue;
+        if (cudaMemcpyAsync(const_cast<void*>(c.dst), c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return GS_ERR_CUDA;
+    }
+    gs_status st = gs_render(dg, cam, key_capacity, ws, ws_bytes, device_image, nullptr, nullptr, stream);
+    if (st != GS_OK) return st;
+    const size_t img = (size_t)cam->width * cam->height * 3 * sizeof(float);
+    return cuda_status(cudaMemcpyAsync(host_image, device_image, img, cudaMemcpyDeviceToHost, s));
+}
+
+gs_status gs_read_status(const void* ws, void* stream, uint32_t* flags, uint64_t* num_keys) {
+    if (!ws || !aligned(ws, kAlign)) return GS_ERR_WORKSPACE;
+    StatusHeader h;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return GS_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GS_ERR_CUDA;
+    if (flags) *flags = h.flags;
+    if (num_keys) *num_keys = h.num_keys;
+    if (h.flags & GS_FLAG_TIMEOUT) return GS_ERR_TIMEOUT;
+    if (h.flags & GS_FLAG_CAPACITY) return GS_ERR_CAPACITY;
+    return GS_OK;
+}
+
+gs_status gs_test_spin_timeout(void* ws, int64_t iterations, void* stream) {
+    if (!ws || !aligned(ws, kAlign) || iterations < 0) return GS_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    auto* header = static_cast<StatusHeader*>(ws);
+    if (cudaMemsetAsync(header, 0, sizeof(StatusHeader), s) != cudaSuccess) return GS_ERR_CUDA;
+    return cuda_status(launch_spin_timeout_test(header, iterations, s));
+}
+
+}  // extern "C"

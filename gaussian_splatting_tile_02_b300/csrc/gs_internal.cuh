@@ -1,0 +1,89 @@
+// Internal declarations shared by the CUDA translation units of the renderer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gs.h"
+
+namespace gs {
+
+constexpr int kTile = 16;
+
+// Status header at the start of every workspace (256 bytes reserved).
+struct StatusHeader {
+    uint32_t flags;          // GS_FLAG_*
+    uint32_t timeout_site;   // which wait ran out (debug aid)
+    unsigned long long num_keys;
+    uint32_t pad[60];
+};
+static_assert(sizeof(StatusHeader) == 256, "status header is 256 bytes");
+
+constexpr size_t kAlign = 256;
+__host__ __device__ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+inline int tiles_x(const gs_camera& c) { return (c.width + kTile - 1) / kTile; }
+inline int tiles_y(const gs_camera& c) { return (c.height + kTile - 1) / kTile; }
+
+// Camera constants as passed by value to kernels.
+struct CamConst {
+    float R[9];
+    float t[3];
+    float fx, fy, cx, cy, near_z;
+    int32_t width, height;
+    int32_t tiles_x, tiles_y;
+    float bg[3];
+    float campos[3];   // camera centre in world space, -R^T t
+};
+CamConst make_cam_const(const gs_camera& c);
+
+// Default bound of every device-side spin, in polling iterations.
+extern long long g_spin_limit;
+
+// ---------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void raise_flag(StatusHeader* h, uint32_t flag, uint32_t site) {
+    atomicOr(&h->flags, flag);
+    if (flag == GS_FLAG_TIMEOUT) atomicMax(&h->timeout_site, site);
+}
+
+// ---------------------------------------------------------------- launchers
+
+// preprocess.cu
+cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const gs_projected& out,
+                              cudaStream_t s);
+
+// binning.cu
+size_t bin_scratch_bytes(int64_t n);
+cudaError_t launch_bin(const gs_projected& p, int64_t n, const CamConst& cam, uint32_t* offsets,
+                       uint64_t* keys, uint32_t* vals, int64_t key_capacity, uint64_t* num_keys,
+                       StatusHeader* status, void* scratch, cudaStream_t s);
+
+// sort.cu
+size_t sort_scratch_bytes(int64_t key_capacity);
+cudaError_t launch_sort(uint64_t* keys, uint32_t* vals, uint64_t* keys_alt, uint32_t* vals_alt,
+                        const uint64_t* num_keys, int64_t key_capacity, int key_bits,
+                        StatusHeader* status, void* scratch, long long spin_limit, cudaStream_t s);
+cudaError_t launch_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_keys,
+                               int64_t key_capacity, int n_tiles, uint32_t* ranges, cudaStream_t s);
+cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations, cudaStream_t s);
+
+// rasterize.cu
+cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* sorted_vals, const uint32_t* ranges,
+                             const CamConst& cam, float* image, float* final_T, uint32_t* n_contrib,
+                             cudaStream_t s);
+
+}  // namespace gs

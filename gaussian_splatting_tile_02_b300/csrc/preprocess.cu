@@ -1,0 +1,276 @@
+// Step 1 of the forward renderer: per-Gaussian projection.
+//
+// Method: lesson page "3D Gaussian Splatting à partir de zéro", sections
+// "Ce qu'un Gaussien porte" (Sigma = R S S^T R^T, scale = exp(log-scale),
+// opacity = sigmoid), "L'étape de projection" (mu' = project(mu),
+// Sigma' = J W Sigma W^T J^T), "Étape 5" (quaternion rotation, camera-space
+// depth) and "Étape 6" (SH colour along the view direction).
+//
+// One thread per Gaussian; the kernel is bound by the HBM stream of the
+// parameters (236 B per Gaussian at SH degree 3) and its outputs.
+//
+// The integer results (culling, depth bits, radius, pixel and tile rectangles)
+// are computed by a fixed binary32 program: every product, quotient, sum and
+// square root is a separately rounded __f*_rn intrinsic (never contracted into
+// an FMA), in this order:
+//   p_i  = ((R_i0 m0 + R_i1 m1) + R_i2 m2) + t_i ;  z = p_2 ;  cull unless z > near
+//   n2   = ((qw^2 + qx^2) + qy^2) + qz^2 ; cull unless 0 < n2 <= FLT_MAX ;
+//          (w, x, y, z) = q / sqrt(n2)
+//   G    = rotation of (w, x, y, z): G00 = 1 - 2(yy + zz), G01 = 2(xy - wz),
+//          G02 = 2(xz + wy), G10 = 2(xy + wz), G11 = 1 - 2(xx + zz),
+//          G12 = 2(yz - wx), G20 = 2(xz - wy), G21 = 2(yz + wx), G22 = 1 - 2(xx + yy)
+//   s_k  = float(exp(double(log_scale_k)))
+//   B_ij = ((R_i0 G_0j + R_i1 G_1j) + R_i2 G_2j) s_j          (B = W R S)
+//   j00  = fx / z, j11 = fy / z, j02 = -((fx p0) / (z z)), j12 = -((fy p1) / (z z))
+//   M_0k = j00 B_0k + j02 B_2k,  M_1k = j11 B_1k + j12 B_2k   (M = J W R S)
+//   a = (M00^2 + M01^2) + M02^2,  b = (M00 M10 + M01 M11) + M02 M12,
+//   c = (M10^2 + M11^2) + M12^2                               (Sigma' = M M^T)
+//   det = a c - b b ; cull unless 0 < det <= FLT_MAX
+//   lam = 0.5 (a + c) + sqrt((0.5 (a - c))^2 + b^2) ; r = ceil(3 sqrt(lam))
+//   u = (fx p0) / z + cx,  v = (fy p1) / z + cy ; cull unless u, v, r finite
+//   x0 = max(ceil(u - r), 0), x1 = min(floor(u + r), W - 1), same for y;
+//   tiles [x0>>4 .. x1>>4] x [y0>>4 .. y1>>4] if x0 <= x1 and y0 <= y1.
+// Sigma' = M M^T is the pages' J W Sigma W^T J^T with Sigma = (R S)(R S)^T.
+// The continuous outputs (conic, opacity, colour) use ordinary fp32 arithmetic.
+#include <float.h>
+
+#include "gs_internal.cuh"
+
+namespace gs {
+namespace {
+
+__device__ __forceinline__ float mul(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ float add(float a, float b) { return __fadd_rn(a, b); }
+__device__ __forceinline__ float sub(float a, float b) { return __fsub_rn(a, b); }
+__device__ __forceinline__ float dv(float a, float b) { return __fdiv_rn(a, b); }
+__device__ __forceinline__ float sq(float a) { return __fsqrt_rn(a); }
+
+// Real SH basis constants, from their closed forms: sqrt(1/4pi), sqrt(3/4pi),
+// sqrt(15/4pi), sqrt(5/16pi), sqrt(15/16pi), sqrt(35/32pi), sqrt(105/4pi),
+// sqrt(21/32pi), sqrt(7/16pi), sqrt(105/16pi).
+constexpr float kY0 = 0.28209479177387814f;
+constexpr float kY1 = 0.48860251190291992f;
+constexpr float kY2a = 1.0925484305920792f;
+constexpr float kY2b = 0.31539156525252005f;
+constexpr float kY2c = 0.54627421529603959f;
+constexpr float kY3a = 0.59004358992664352f;
+constexpr float kY3b = 2.8906114426405538f;
+constexpr float kY3c = 0.45704579946446572f;
+constexpr float kY3d = 0.3731763325901154f;
+constexpr float kY3e = 1.4453057213202769f;
+
+// Colour along unit direction (x, y, z): sum_k Y_k c_k + 0.5, clamped at 0.
+// Signs follow the printed code of "Étape 6" for bands 0..2 (band 1: -y, +z,
+// -x; band 2 all +); band 3 (not printed) uses the band-1 pattern, odd m
+// negative.
+template <int D>
+__device__ __forceinline__ float3 eval_sh(const float* __restrict__ c, float x, float y, float z) {
+    constexpr int NK = (D + 1) * (D + 1);
+    float co[NK * 3];
+    if constexpr (D == 3 || D == 1) {
+        const float4* c4 = reinterpret_cast<const float4*>(c);
+#pragma unroll
+        for (int i = 0; i < NK * 3 / 4; i++) {
+            float4 q = __ldg(c4 + i);
+            co[4 * i] = q.x; co[4 * i + 1] = q.y; co[4 * i + 2] = q.z; co[4 * i + 3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < NK * 3; i++) co[i] = __ldg(c + i);
+    }
+    float Y[NK];
+    Y[0] = kY0;
+    if constexpr (D >= 1) {
+        Y[1] = -kY1 * y;
+        Y[2] = kY1 * z;
+        Y[3] = -kY1 * x;
+    }
+    if constexpr (D >= 2) {
+        const float xx = x * x, yy = y * y, zz = z * z;
+        Y[4] = kY2a * x * y;
+        Y[5] = kY2a * y * z;
+        Y[6] = kY2b * (2.0f * zz - xx - yy);
+        Y[7] = kY2a * x * z;
+        Y[8] = kY2c * (xx - yy);
+        if constexpr (D >= 3) {
+            Y[9] = -kY3a * y * (3.0f * xx - yy);
+            Y[10] = kY3b * x * y * z;
+            Y[11] = -kY3c * y * (4.0f * zz - xx - yy);
+            Y[12] = kY3d * z * (2.0f * zz - 3.0f * xx - 3.0f * yy);
+            Y[13] = -kY3c * x * (4.0f * zz - xx - yy);
+            Y[14] = kY3e * z * (xx - yy);
+            Y[15] = -kY3a * x * (xx - 3.0f * yy);
+        }
+    }
+    float r = 0.5f, g = 0.5f, b = 0.5f;
+#pragma unroll
+    for (int k = 0; k < NK; k++) {
+        r = fmaf(Y[k], co[3 * k], r);
+        g = fmaf(Y[k], co[3 * k + 1], g);
+        b = fmaf(Y[k], co[3 * k + 2], b);
+    }
+    return make_float3(fmaxf(r, 0.0f), fmaxf(g, 0.0f), fmaxf(b, 0.0f));
+}
+
+struct PreArgs {
+    const float* means;
+    const float4* quats;
+    const float* log_scales;
+    const float* logits;
+    const float* sh;
+    int64_t n;
+    CamConst cam;
+    float2* mean2d;
+    float4* conic_opacity;
+    float* rgb;
+    float* depth;
+    int32_t* radius;
+    uint32_t* tiles_touched;
+    ushort4* rect;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= a.n) return;
+    const CamConst& C = a.cam;
+    const float m0 = __ldg(a.means + 3 * g), m1 = __ldg(a.means + 3 * g + 1), m2 = __ldg(a.means + 3 * g + 2);
+
+    float p[3];
+#pragma unroll
+    for (int i = 0; i < 3; i++)
+        p[i] = add(add(add(mul(C.R[3 * i], m0), mul(C.R[3 * i + 1], m1)), mul(C.R[3 * i + 2], m2)), C.t[i]);
+    const float z = p[2];
+    a.depth[g] = z;
+
+    bool ok = z > C.near_z;
+    float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ok) {
+        q = __ldg(a.quats + g);
+    }
+    const float n2 = add(add(add(mul(q.x, q.x), mul(q.y, q.y)), mul(q.z, q.z)), mul(q.w, q.w));
+    ok = ok && n2 > 0.0f && n2 <= FLT_MAX;
+    if (!ok) {
+        a.radius[g] = 0;
+        a.tiles_touched[g] = 0;
+        a.rect[g] = make_ushort4(0, 0, 0, 0);
+        return;
+    }
+    const float rn = sq(n2);
+    const float w = dv(q.x, rn), x = dv(q.y, rn), y = dv(q.z, rn), zq = dv(q.w, rn);
+    float G[9];
+    {
+        const float xx = mul(x, x), yy = mul(y, y), zz = mul(zq, zq);
+        const float xy = mul(x, y), xz = mul(x, zq), yz = mul(y, zq);
+        const float wx = mul(w, x), wy = mul(w, y), wz = mul(w, zq);
+        G[0] = sub(1.0f, mul(2.0f, add(yy, zz)));
+        G[1] = mul(2.0f, sub(xy, wz));
+        G[2] = mul(2.0f, add(xz, wy));
+        G[3] = mul(2.0f, add(xy, wz));
+        G[4] = sub(1.0f, mul(2.0f, add(xx, zz)));
+        G[5] = mul(2.0f, sub(yz, wx));
+        G[6] = mul(2.0f, sub(xz, wy));
+        G[7] = mul(2.0f, add(yz, wx));
+        G[8] = sub(1.0f, mul(2.0f, add(xx, yy)));
+    }
+    float s[3];
+#pragma unroll
+    for (int k = 0; k < 3; k++) s[k] = __double2float_rn(exp((double)__ldg(a.log_scales + 3 * g + k)));
+    float B[9];
+#pragma unroll
+    for (int i = 0; i < 3; i++)
+#pragma unroll
+        for (int j = 0; j < 3; j++)
+            B[3 * i + j] = mul(add(add(mul(C.R[3 * i], G[j]), mul(C.R[3 * i + 1], G[3 + j])), mul(C.R[3 * i + 2], G[6 + j])), s[j]);
+    const float j00 = dv(C.fx, z), j11 = dv(C.fy, z);
+    const float zz2 = mul(z, z);
+    const float fxp0 = mul(C.fx, p[0]), fyp1 = mul(C.fy, p[1]);
+    const float j02 = -dv(fxp0, zz2), j12 = -dv(fyp1, zz2);
+    float M0[3], M1[3];
+#pragma unroll
+    for (int k = 0; k < 3; k++) {
+        M0[k] = add(mul(j00, B[k]), mul(j02, B[6 + k]));
+        M1[k] = add(mul(j11, B[3 + k]), mul(j12, B[6 + k]));
+    }
+    const float ca = add(add(mul(M0[0], M0[0]), mul(M0[1], M0[1])), mul(M0[2], M0[2]));
+    const float cb = add(add(mul(M0[0], M1[0]), mul(M0[1], M1[1])), mul(M0[2], M1[2]));
+    const float cc = add(add(mul(M1[0], M1[0]), mul(M1[1], M1[1])), mul(M1[2], M1[2]));
+    const float det = sub(mul(ca, cc), mul(cb, cb));
+    const float hm = mul(0.5f, sub(ca, cc));
+    const float mid = mul(0.5f, add(ca, cc));
+    const float lam = add(mid, sq(add(mul(hm, hm), mul(cb, cb))));
+    const float rf = ceilf(mul(3.0f, sq(lam)));
+    const float u = add(dv(fxp0, z), C.cx);
+    const float v = add(dv(fyp1, z), C.cy);
+    if (!(det > 0.0f && det <= FLT_MAX) || !(fabsf(u) <= FLT_MAX && fabsf(v) <= FLT_MAX && rf <= FLT_MAX)) {
+        a.radius[g] = 0;
+        a.tiles_touched[g] = 0;
+        a.rect[g] = make_ushort4(0, 0, 0, 0);
+        return;
+    }
+    float x0 = ceilf(sub(u, rf)), x1 = floorf(add(u, rf));
+    float y0 = ceilf(sub(v, rf)), y1 = floorf(add(v, rf));
+    x0 = x0 > 0.0f ? x0 : 0.0f;
+    y0 = y0 > 0.0f ? y0 : 0.0f;
+    const float wm1 = (float)(C.width - 1), hm1 = (float)(C.height - 1);
+    x1 = x1 < wm1 ? x1 : wm1;
+    y1 = y1 < hm1 ? y1 : hm1;
+    uint32_t touched = 0;
+    ushort4 rect = make_ushort4(0, 0, 0, 0);
+    if (x0 <= x1 && y0 <= y1) {
+        const int tx0 = (int)x0 >> 4, tx1 = (int)x1 >> 4, ty0 = (int)y0 >> 4, ty1 = (int)y1 >> 4;
+        touched = (uint32_t)((tx1 - tx0 + 1) * (ty1 - ty0 + 1));
+        rect = make_ushort4((unsigned short)tx0, (unsigned short)ty0, (unsigned short)tx1, (unsigned short)ty1);
+    }
+    a.radius[g] = rf <= 1073741824.0f ? (int32_t)rf : 1073741824;
+    a.tiles_touched[g] = touched;
+    a.rect[g] = rect;
+    a.mean2d[g] = make_float2(u, v);
+
+    // continuous values (ordinary fp32)
+    const float inv_det = 1.0f / det;
+    const float logit = __ldg(a.logits + g);
+    const float o = 1.0f / (1.0f + expf(-logit));
+    a.conic_opacity[g] = make_float4(cc * inv_det, -cb * inv_det, ca * inv_det, o);
+
+    float dx = m0 - C.campos[0], dy = m1 - C.campos[1], dz = m2 - C.campos[2];
+    const float il = rsqrtf(dx * dx + dy * dy + dz * dz);
+    dx *= il; dy *= il; dz *= il;
+    constexpr int NK3 = (D + 1) * (D + 1) * 3;
+    const float3 col = eval_sh<D>(a.sh + g * NK3, dx, dy, dz);
+    a.rgb[3 * g] = col.x;
+    a.rgb[3 * g + 1] = col.y;
+    a.rgb[3 * g + 2] = col.z;
+}
+
+}  // namespace
+
+cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const gs_projected& out,
+                              cudaStream_t s) {
+    if (g.n == 0) return cudaSuccess;
+    PreArgs a;
+    a.means = g.means;
+    a.quats = reinterpret_cast<const float4*>(g.quats);
+    a.log_scales = g.log_scales;
+    a.logits = g.opacity_logits;
+    a.sh = g.sh;
+    a.n = g.n;
+    a.cam = cam;
+    a.mean2d = reinterpret_cast<float2*>(out.mean2d);
+    a.conic_opacity = reinterpret_cast<float4*>(out.conic_opacity);
+    a.rgb = out.rgb;
+    a.depth = out.depth;
+    a.radius = out.radius;
+    a.tiles_touched = out.tiles_touched;
+    a.rect = reinterpret_cast<ushort4*>(out.rect);
+    const unsigned blocks = (unsigned)((g.n + 255) / 256);
+    switch (g.sh_degree) {
+        case 0: preprocess_kernel<0><<<blocks, 256, 0, s>>>(a); break;
+        case 1: preprocess_kernel<1><<<blocks, 256, 0, s>>>(a); break;
+        case 2: preprocess_kernel<2><<<blocks, 256, 0, s>>>(a); break;
+        default: preprocess_kernel<3><<<blocks, 256, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gs

@@ -1,0 +1,219 @@
+/*
+ * gs.h -- C ABI of the B300 forward renderer for 3D Gaussian Splatting.
+ *
+ * The method is the one on the lesson page "3D Gaussian Splatting à partir de
+ * zéro": each Gaussian carries a mean, a unit quaternion, log-scales, an
+ * opacity logit and spherical-harmonic colour (section "Ce qu'un Gaussien
+ * porte"); a frame is rendered in five steps -- project to 2D, assign to 16x16
+ * screen tiles, depth-sort per tile, alpha-composite front to back, pixel
+ * colour (section "Rastérisation, non rayée", flowchart).
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA global-memory addresses on the current
+ *     device; the caller owns every buffer. The library never allocates, frees
+ *     or synchronises, except where an entry point says so.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). All work is enqueued on it in order; results are ready when the
+ *     stream is.
+ *   - Argument errors are found on the host before anything is enqueued and
+ *     return GS_ERR_INVALID_ARG (or GS_ERR_WORKSPACE for a short workspace).
+ *     A failed launch returns GS_ERR_CUDA. Device-side conditions (key
+ *     capacity exceeded, a bounded wait that ran out) set flags in the
+ *     workspace status header, read with gs_read_status.
+ *   - Nothing throws across the ABI.
+ *   - All per-Gaussian arrays are C-contiguous float32 (int32/uint32 where
+ *     stated). Images are HWC float32.
+ *   - Tiles are 16x16 pixels, tiles_x = ceil(width/16), tiles_y =
+ *     ceil(height/16), tile id = ty * tiles_x + tx.
+ */
+#ifndef GS_B300_H
+#define GS_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GS_ABI_VERSION 1
+
+typedef enum gs_status {
+    GS_OK = 0,
+    GS_ERR_INVALID_ARG = 1,  /* bad pointer, size, degree, camera */
+    GS_ERR_CAPACITY = 2,     /* more keys than key_capacity (count still reported) */
+    GS_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    GS_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out */
+    GS_ERR_WORKSPACE = 5     /* workspace missing, misaligned or too small */
+} gs_status;
+
+/* Workspace status flags (bit set). */
+#define GS_FLAG_CAPACITY 1u
+#define GS_FLAG_TIMEOUT 2u
+
+/* Pinhole camera (host memory). x_cam = R x_world + t with R row-major;
+ * camera x right, y down, z forward. Pixel (x, y) is sampled at the integer
+ * coordinates (x, y), as the integer grid of rasterise_2d ("Étape 2") does.
+ * near_z > 0: Gaussians with camera z <= near_z are culled. bg is the
+ * background colour added with the final transmittance. */
+typedef struct gs_camera {
+    float R[9];
+    float t[3];
+    float fx, fy, cx, cy, near_z;
+    int32_t width, height;   /* 1 .. 32768 */
+    float bg[3];
+} gs_camera;
+
+/* Gaussian parameters (section "Ce qu'un Gaussien porte"). All device
+ * pointers, 16-byte aligned (quats is read as float4).
+ *   means          [n][3]  world-space centres mu
+ *   quats          [n][4]  (w, x, y, z); normalised on the fly, so any
+ *                          non-zero quaternion is accepted (zero -> culled)
+ *   log_scales     [n][3]  s, scale = exp(s) at render time
+ *   opacity_logits [n]     opacity = sigmoid(logit)
+ *   sh             [n][(D+1)^2][3]  SH coefficient k of colour channel c
+ *   sh_degree      D in 0..3 */
+typedef struct gs_gaussians {
+    const float* means;
+    const float* quats;
+    const float* log_scales;
+    const float* opacity_logits;
+    const float* sh;
+    int64_t n;
+    int32_t sh_degree;
+} gs_gaussians;
+
+/* Per-Gaussian output of the projection step (device pointers, caller
+ * allocated, each [n] rows; mean2d 8-byte aligned, conic_opacity 16-byte
+ * aligned, rect 8-byte aligned).
+ *   mean2d         [n][2]  projected centre mu' (pixels)
+ *   conic_opacity  [n][4]  (A, B, C, o): Sigma'^-1 = [[A, B], [B, C]], opacity o
+ *   rgb            [n][3]  colour from SH along the view direction, + 0.5, >= 0
+ *   depth          [n]     camera-space z (the sort key's low 32 bits)
+ *   radius         [n]     ceil(3 sqrt(lambda_max(Sigma'))) pixels, 0 if culled
+ *   tiles_touched  [n]     number of 16x16 tiles the pixel rectangle
+ *                          [u-r, u+r] x [v-r, v+r] (clipped) covers, 0 if culled
+ *   rect           [n][4]  uint16 tile rectangle (tx0, ty0, tx1, ty1), inclusive
+ * For culled Gaussians only radius and tiles_touched are defined (both 0). */
+typedef struct gs_projected {
+    float* mean2d;
+    float* conic_opacity;
+    float* rgb;
+    float* depth;
+    int32_t* radius;
+    uint32_t* tiles_touched;
+    uint16_t* rect;
+} gs_projected;
+
+const char* gs_status_string(int32_t status);
+int32_t gs_abi_version(void);
+
+/* Step 1 -- projection (sections "L'étape de projection", "Étape 5",
+ * "Étape 6"). Per Gaussian: R from the normalised quaternion,
+ * Sigma = R S S^T R^T, camera-space centre, near-plane cull, mu', the EWA
+ * screen covariance Sigma' = J W Sigma W^T J^T, its inverse (the conic), the
+ * 3-sigma radius, the pixel and tile rectangles, opacity = sigmoid(logit) and
+ * the SH colour. The integer results (culling, depth bits, radius, rectangles)
+ * come from a fixed binary32 program with no fused multiply-add, so they are
+ * reproducible bit for bit on any IEEE machine.
+ * Errors: GS_ERR_INVALID_ARG for null/misaligned pointers, n < 0,
+ * sh_degree outside 0..3, a bad camera. */
+gs_status gs_preprocess(const gs_gaussians* gaussians, const gs_camera* camera,
+                        const gs_projected* out, void* stream);
+
+/* Step 2 -- tile binning (flowchart box "Assign to tiles (16x16
+ * screen-space)"). A device prefix scan of tiles_touched gives
+ * offsets[i] = sum_{j<=i} tiles_touched[j] (inclusive) and the key count
+ * K = offsets[n-1], written to *num_keys (device uint64). Then each Gaussian
+ * i writes one key per touched tile, in row-major order over its tile
+ * rectangle, at positions offsets[i]-tiles_touched[i] ...:
+ *     key = (uint64)tile_id << 32 | float_bits(depth[i]),   value = i.
+ * Keys beyond key_capacity are not written; K is still reported and
+ * GS_FLAG_CAPACITY is set in the workspace header.
+ * ws: device scratch of at least gs_bin_workspace_bytes(n), 256-byte aligned.
+ * keys/vals: device, key_capacity entries each. */
+size_t gs_bin_workspace_bytes(int64_t n);
+gs_status gs_bin(const gs_projected* projected, int64_t n, const gs_camera* camera,
+                 uint32_t* offsets, uint64_t* keys, uint32_t* vals, int64_t key_capacity,
+                 uint64_t* num_keys, void* ws, size_t ws_bytes, void* stream);
+
+/* Step 3 -- sort (flowchart box "Depth-sort per tile"). Stable ascending
+ * least-significant-digit radix sort of the first min(K, key_capacity) (key,
+ * value) pairs, K read from *num_keys on the device. Only the low key_bits
+ * bits of the keys take part (1..64; the binning keys need 32 +
+ * ceil(log2(tiles))). Equal keys keep their input order, which for binning
+ * output is Gaussian-index order. The sorted pairs end in keys/vals;
+ * keys_alt/vals_alt are ping-pong buffers of the same capacity.
+ * ws: device scratch of at least gs_sort_workspace_bytes(key_capacity).
+ * A bounded wait that runs out sets GS_FLAG_TIMEOUT (the output is then
+ * unspecified but every access stays in bounds). */
+size_t gs_sort_workspace_bytes(int64_t key_capacity);
+gs_status gs_sort(uint64_t* keys, uint32_t* vals, uint64_t* keys_alt, uint32_t* vals_alt,
+                  const uint64_t* num_keys, int64_t key_capacity, int32_t key_bits,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* Step 4 -- per-tile ranges: ranges[t] = [first, one past last) position of
+ * tile id t in the sorted keys, (0, 0) for tiles without keys.
+ * ranges: device uint32 [tiles_y * tiles_x][2]. */
+gs_status gs_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_keys,
+                         int64_t key_capacity, const gs_camera* camera, uint32_t* ranges,
+                         void* stream);
+
+/* Step 5 -- composite (sections "La règle de composition alpha", "Étape 2").
+ * Each pixel walks its tile's sorted list front to back:
+ *     alpha = min(0.99, o exp(-0.5 d^T Sigma'^-1 d)), d = pixel - mu';
+ *     skipped if alpha < 1/255; C += alpha T c; T *= (1 - alpha);
+ *     the pixel stops once T < 1e-4 (after that Gaussian);
+ *     image = C + T * bg.
+ * image: device float [height][width][3]. final_T (device float [h][w]) and
+ * n_contrib (device uint32 [h][w], 1 + list position of the last
+ * contributing Gaussian, 0 if none) may be NULL. */
+gs_status gs_rasterize(const gs_projected* projected, int64_t n, const uint32_t* sorted_vals,
+                       const uint32_t* ranges, const gs_camera* camera, float* image,
+                       float* final_T, uint32_t* n_contrib, void* stream);
+
+/* The whole frame: steps 1-5 chained on `stream` with no host
+ * synchronisation (so the call can be captured into a CUDA graph). All
+ * intermediates live in ws (device, 256-byte aligned, at least
+ * gs_render_workspace_bytes(n, width, height, key_capacity) bytes); the first
+ * 256 bytes of ws are the status header read by gs_read_status.
+ * key_capacity bounds the (Gaussian, tile) pairs of the frame; if the frame
+ * needs more, GS_FLAG_CAPACITY is set, the image is unspecified and
+ * gs_read_status reports the count needed. */
+size_t gs_render_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity);
+gs_status gs_render(const gs_gaussians* gaussians, const gs_camera* camera, int64_t key_capacity,
+                    void* ws, size_t ws_bytes, float* image, float* final_T,
+                    uint32_t* n_contrib, void* stream);
+
+/* The whole frame from host memory: copies the five parameter arrays from
+ * host to the caller's device buffers in `device_gaussians` (same n and
+ * degree), renders with gs_render, and copies the image back to host_image
+ * (host float [h][w][3]). All copies are cudaMemcpyAsync on `stream`; host
+ * buffers should be page-locked for them to overlap. device_image is the
+ * device image buffer. The call does not wait for the stream. */
+gs_status gs_render_from_host(const gs_gaussians* host_gaussians,
+                              const gs_gaussians* device_gaussians, const gs_camera* camera,
+                              int64_t key_capacity, void* ws, size_t ws_bytes,
+                              float* device_image, float* host_image, void* stream);
+
+/* Reads the status header at the start of a gs_bin, gs_sort or gs_render
+ * workspace. SYNCHRONISES `stream`. flags/num_keys may be NULL. Returns
+ * GS_ERR_TIMEOUT, GS_ERR_CAPACITY or GS_OK from the flags. num_keys is the
+ * key count of the last gs_bin/gs_render on that workspace. */
+gs_status gs_read_status(const void* ws, void* stream, uint32_t* flags, uint64_t* num_keys);
+
+/* Upper bound on the wait of every device-side spin (look-back of the radix
+ * sort), in polling iterations; <= 0 restores the default (about a second).
+ * Applies to launches made after the call; not thread-safe. */
+void gs_set_spin_limit(int64_t iterations);
+
+/* Test hook: launches one block whose wait on a flag in ws (which nothing
+ * sets) runs out after `iterations` polls; sets GS_FLAG_TIMEOUT in the ws
+ * status header. ws: at least 256 bytes. */
+gs_status gs_test_spin_timeout(void* ws, int64_t iterations, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GS_B300_H */

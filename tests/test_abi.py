@@ -1,0 +1,100 @@
+"""CPU-side checks of the C-ABI library: it builds for sm_103a, loads, exports
+every entry point include/gs.h declares, and rejects bad arguments on the host
+before touching the GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gaussian_splatting_tile_02_b300 as gs
+from gaussian_splatting_tile_02_b300 import build, native, scenes
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gs.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gs_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    build.build()
+    L = native.lib()
+    names = declared_functions()
+    assert len(names) >= 14
+    for name in names:
+        assert hasattr(L, name), name
+    assert set(names) == set(native._SIGNATURES), "binding must cover exactly the declared entry points"
+    assert L.gs_abi_version() == 1
+
+
+def test_status_strings():
+    L = native.lib()
+    for s in range(6):
+        assert L.gs_status_string(s)
+    assert L.gs_status_string(99) == b"unknown status"
+
+
+def test_workspace_sizes():
+    L = native.lib()
+    a = L.gs_render_workspace_bytes(1000, 64, 64, 5000)
+    b = L.gs_render_workspace_bytes(2000, 64, 64, 5000)
+    c = L.gs_render_workspace_bytes(1000, 64, 64, 50000)
+    assert 0 < a < b and a < c
+    assert L.gs_render_workspace_bytes(-1, 64, 64, 10) == 0
+    assert L.gs_sort_workspace_bytes(0) > 0 and L.gs_bin_workspace_bytes(0) > 0
+    # 256-byte status header + aligned scratch
+    assert L.gs_sort_workspace_bytes(1 << 20) % 256 == 0
+
+
+def _cam(**over):
+    cam = scenes.axis_camera(4.0, 64.0, 64, 64)
+    cam.update(over)
+    return cam
+
+
+def test_host_validation_rejects_bad_arguments():
+    L = native.lib()
+    cam = gs.camera_struct(_cam())
+    g = native.GsGaussians()
+    p = native.GsProjected()
+    # n < 0, degree out of range, null arrays with n > 0, null camera
+    g.n = -1
+    assert L.gs_preprocess(ctypes.byref(g), ctypes.byref(cam), ctypes.byref(p), None) == native.GS_ERR_INVALID_ARG
+    g.n, g.sh_degree = 0, 4
+    assert L.gs_preprocess(ctypes.byref(g), ctypes.byref(cam), ctypes.byref(p), None) == native.GS_ERR_INVALID_ARG
+    g.n, g.sh_degree = 10, 0
+    assert L.gs_preprocess(ctypes.byref(g), ctypes.byref(cam), ctypes.byref(p), None) == native.GS_ERR_INVALID_ARG
+    assert L.gs_preprocess(ctypes.byref(g), None, ctypes.byref(p), None) == native.GS_ERR_INVALID_ARG
+    # misaligned quaternion pointer
+    g.means = g.log_scales = g.opacity_logits = g.sh = 1 << 20
+    g.quats = (1 << 20) + 4
+    assert L.gs_preprocess(ctypes.byref(g), ctypes.byref(cam), ctypes.byref(p), None) == native.GS_ERR_INVALID_ARG
+    # bad cameras: near <= 0, zero width, non-finite focal
+    for bad in (dict(near=0.0), dict(width=0), dict(fx=float("nan")), dict(height=40000)):
+        c = gs.camera_struct(_cam(**bad))
+        g2 = native.GsGaussians()
+        g2.n = 0
+        assert L.gs_preprocess(ctypes.byref(g2), ctypes.byref(c), ctypes.byref(p), None) == \
+            native.GS_ERR_INVALID_ARG, bad
+    # sort: bad key_bits, capacity beyond the 30-bit status words, short workspace
+    assert L.gs_sort(None, None, None, None, 8, 0, 0, None, 0, None) == native.GS_ERR_INVALID_ARG
+    assert L.gs_sort(None, None, None, None, 8, 0, 65, None, 0, None) == native.GS_ERR_INVALID_ARG
+    assert L.gs_sort(8, 8, 8, 8, 8, 1 << 30, 40, 256, 1 << 40, None) == native.GS_ERR_INVALID_ARG
+    assert L.gs_sort(8, 8, 8, 8, 8, 100, 40, 256, 16, None) == native.GS_ERR_WORKSPACE
+    assert L.gs_sort(8, 8, 8, 8, 8, 100, 40, 260, 1 << 20, None) == native.GS_ERR_WORKSPACE
+    # render: short workspace
+    g3 = native.GsGaussians()
+    g3.n = 0
+    assert L.gs_render(ctypes.byref(g3), ctypes.byref(cam), 10, 256, 8, 256, None, None, None) == \
+        native.GS_ERR_WORKSPACE
+    assert L.gs_read_status(None, None, None, None) == native.GS_ERR_WORKSPACE
+
+
+def test_key_bits():
+    assert gs.key_bits(scenes.make_cameras("1M")[0]) == 45        # 8160 tiles
+    assert gs.key_bits(scenes.make_cameras("100k")[0]) == 43      # 1200 tiles
+    assert gs.key_bits(scenes.make_cameras("tiny")[0]) == 36      # 16 tiles
+    assert gs.key_bits(scenes.axis_camera(1, 1, 16, 16)) == 32    # one tile

@@ -1,0 +1,281 @@
+"""GPU path (through the C ABI) against the CPU oracle, stage by stage.
+
+Integer results -- culling, depth key bits, radius, tile rectangles, tile
+counts, prefix offsets, key lists, sorted order, tile ranges -- must match bit
+for bit. Images must match the fp64 composite within 1e-4 per channel, with
+the threshold-flip rule of tests/parity.py. Configurations: the five seeded
+workloads (tiny, 100k, 1M, 5M x 4 views, stress x 8 views) at full size, plus
+edge cases.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import gaussian_splatting_tile_02_b300 as gs
+from gaussian_splatting_tile_02_b300 import native, scenes
+
+from parity import assert_image_parity, check_image, oracle_render
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_only():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    native.lib()
+
+
+_SCENES = {}
+
+
+def scene_of(name, n=None):
+    key = (name, n)
+    if key not in _SCENES:
+        _SCENES.clear()
+        s = scenes.make_scene(name, n=n)
+        _SCENES[key] = (s, gs.gaussians_to_device(s))
+    return _SCENES[key]
+
+
+def run_stages(g, cam, capacity=None):
+    p = gs.preprocess(g, cam)
+    if capacity is None:
+        b0 = gs.bin_keys(p, cam, 0)
+        capacity = int(b0["num_keys"].item())
+    b = gs.bin_keys(p, cam, capacity)
+    K = int(b["num_keys"].item())
+    keys_unsorted = b["keys"][:min(K, capacity)].clone()
+    vals_unsorted = b["vals"][:min(K, capacity)].clone()
+    srt = gs.sort_pairs(b["keys"], b["vals"], b["num_keys"], gs.key_bits(cam), capacity)
+    ranges = gs.tile_ranges(srt["keys"], b["num_keys"], cam, capacity)
+    r = gs.rasterize(p, srt["vals"], ranges, cam)
+    torch.cuda.synchronize()
+    st = gs.read_status(srt["ws"])
+    u = lambda t: t.cpu().numpy()
+    return {"p": {k: u(v) for k, v in p.items()}, "offsets": u(b["offsets"]).view(np.uint32), "K": K,
+            "keys": u(keys_unsorted).view(np.uint64), "vals": u(vals_unsorted).view(np.uint32),
+            "sorted_keys": u(srt["keys"][:min(K, capacity)]).view(np.uint64),
+            "sorted_vals": u(srt["vals"][:min(K, capacity)]).view(np.uint32),
+            "ranges": u(ranges).view(np.uint32), "image": u(r["image"]), "final_T": u(r["final_T"]),
+            "n_contrib": u(r["n_contrib"]), "sort_status": st, "bin_status": gs.read_status(b["ws"])}
+
+
+def check_decisions(oracle, scene, cam, out):
+    d = oracle.decide_f32(scene, cam)
+    p = out["p"]
+    tt = p["tiles_touched"].view(np.uint32)
+    np.testing.assert_array_equal(tt, d["tiles_touched"])
+    np.testing.assert_array_equal(p["radius"], d["radius"])
+    v = d["valid"] > 0
+    np.testing.assert_array_equal(p["depth"][v].view(np.uint32), d["depth"][v].view(np.uint32))
+    np.testing.assert_array_equal(p["mean2d"][v].view(np.uint32), d["mean2d"][v].view(np.uint32))
+    has = tt > 0
+    np.testing.assert_array_equal(p["rect"][has].view(np.uint16).astype(np.int32), d["tile_rect"][has])
+    return d
+
+
+def check_keys(oracle, ref, out):
+    assert out["K"] == ref["num_keys"]
+    np.testing.assert_array_equal(out["offsets"].astype(np.uint64), ref["offsets"])
+    np.testing.assert_array_equal(out["keys"], ref["keys"])
+    np.testing.assert_array_equal(out["vals"], ref["vals"])
+    np.testing.assert_array_equal(out["sorted_keys"], ref["sorted_keys"])
+    np.testing.assert_array_equal(out["sorted_vals"], ref["sorted_vals"])
+    np.testing.assert_array_equal(out["ranges"], ref["ranges"])
+
+
+def check_continuous(ref, out):
+    p, rp = out["p"], ref["proj"]
+    v = ref["dec"]["tiles_touched"] > 0
+    np.testing.assert_allclose(p["conic_opacity"][v, 3], rp["opacity"][v], rtol=2e-6, atol=1e-7)
+    np.testing.assert_allclose(p["rgb"][v], rp["rgb"][v], atol=2e-6)
+    con = p["conic_opacity"][v, :3].astype(np.float64)
+    scale = np.abs(rp["conic"][v]).max(1, keepdims=True)
+    # fp32 conic from fp32 Sigma' entries: error grows with the condition number of Sigma'
+    cond = rp["lam_max"][v] ** 2 / (rp["cov2d"][v, 0] * rp["cov2d"][v, 2] - rp["cov2d"][v, 1] ** 2)
+    assert (np.abs(con - rp["conic"][v]) <= (1e-5 + 4e-7 * cond[:, None]) * scale).all()
+
+
+CASES = [("tiny", 0), ("100k", 0), ("1M", 0)] + [("5M", i) for i in range(4)] + [("stress", i) for i in range(8)]
+
+
+@pytest.mark.parametrize("name,view", CASES, ids=[f"{n}-v{v}" for n, v in CASES])
+def test_full_path_parity(oracle_mod, name, view):
+    scene, g = scene_of(name)
+    cam = scenes.make_cameras(name)[view]
+    out = run_stages(g, cam)
+    assert out["sort_status"][0] == native.GS_OK
+    check_decisions(oracle_mod, scene, cam, out)
+    ref = oracle_render(oracle_mod, scene, cam)
+    check_keys(oracle_mod, ref, out)
+    check_continuous(ref, out)
+    stats = check_image(oracle_mod, ref, cam, out["image"], out["final_T"], out["n_contrib"])
+    print(name, view, "K", out["K"], stats)
+    assert_image_parity(stats)
+
+
+def test_render_equals_stages_and_graph_replay(oracle_mod):
+    scene, g = scene_of("100k")
+    cam = scenes.make_cameras("100k")[0]
+    cam = dict(cam, bg=np.array([0.1, 0.5, 0.9], np.float32))
+    out = run_stages(g, cam)
+    r = gs.Renderer(g, cam["width"], cam["height"], out["K"] + 100)
+    r.render(cam)
+    torch.cuda.synchronize()
+    st, flags, K = r.status()
+    assert st == native.GS_OK and K == out["K"]
+    np.testing.assert_array_equal(r.image.cpu().numpy(), out["image"])
+    np.testing.assert_array_equal(r.final_T.cpu().numpy(), out["final_T"])
+    np.testing.assert_array_equal(r.n_contrib.cpu().numpy(), out["n_contrib"])
+    # the whole frame captured once into a CUDA graph and replayed
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        r.render(cam, stream=s)
+        s.synchronize()
+        with torch.cuda.graph(graph, stream=s):
+            r.render(cam, stream=s)
+    r.image.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(r.image.cpu().numpy(), out["image"])
+    ref = oracle_render(oracle_mod, scene, cam)
+    assert_image_parity(check_image(oracle_mod, ref, cam, out["image"], out["final_T"], out["n_contrib"]))
+
+
+@pytest.mark.parametrize("degree", [0, 1, 2, 3])
+def test_sh_degrees_and_ragged_image(oracle_mod, degree):
+    base = scenes.make_scene("100k", n=5000)
+    k = (degree + 1) ** 2
+    scene = dict(base, sh=np.ascontiguousarray(base["sh"][:, :k, :]), sh_degree=degree)
+    cam = scenes.axis_camera(6.0, 90.0, 70, 37, 0.2, (0.3, 0.2, 0.1))
+    g = gs.gaussians_to_device(scene)
+    out = run_stages(g, cam)
+    check_decisions(oracle_mod, scene, cam, out)
+    ref = oracle_render(oracle_mod, scene, cam)
+    check_keys(oracle_mod, ref, out)
+    check_continuous(ref, out)
+    assert_image_parity(check_image(oracle_mod, ref, cam, out["image"], out["final_T"], out["n_contrib"]))
+
+
+def _tiny_scene(means, quats=None, log_scales=None, logits=None):
+    n = len(means)
+    return {"means": np.asarray(means, np.float32).reshape(n, 3),
+            "quats": np.asarray(quats if quats is not None else [[1, 0, 0, 0]] * n, np.float32).reshape(n, 4),
+            "log_scales": np.asarray(log_scales if log_scales is not None else [[-2.0] * 3] * n,
+                                     np.float32).reshape(n, 3),
+            "opacity_logits": np.asarray(logits if logits is not None else [1.0] * n, np.float32).reshape(n),
+            "sh": np.full((n, 1, 3), 0.4, np.float32), "sh_degree": 0, "n": n}
+
+
+def test_empty_and_all_culled(oracle_mod):
+    cam = scenes.axis_camera(4.0, 64.0, 64, 64, 0.2, (0.25, 0.5, 0.75))
+    for scene in (_tiny_scene(np.zeros((0, 3))),
+                  _tiny_scene([[0, 0, -5.0], [0.3, 0.1, -4.5]]),                  # behind the camera
+                  _tiny_scene([[0, 0, 0]], quats=[[0, 0, 0, 0]]),                 # zero quaternion
+                  _tiny_scene([[40.0, 0, 0], [0, -40.0, 0]])):                    # off screen
+        g = gs.gaussians_to_device(scene)
+        if scene["n"] == 0:
+            r = gs.Renderer(g, 64, 64, 16)
+            r.render(cam)
+            torch.cuda.synchronize()
+            assert r.status()[0] == native.GS_OK and r.status()[2] == 0
+            img = r.image.cpu().numpy()
+        else:
+            out = run_stages(g, cam, capacity=16)
+            assert out["K"] == 0
+            img = out["image"]
+        np.testing.assert_array_equal(img, np.broadcast_to(np.float32([0.25, 0.5, 0.75]), (64, 64, 3)))
+
+
+def test_border_clipping_and_large_footprints(oracle_mod):
+    # centres on and beyond the image border, and one Gaussian covering many tiles
+    scene = _tiny_scene([[-0.99, -0.99, 0], [0.99, 0.99, 0], [1.3, 0, 0], [0, 0, 0.5], [0.2, 0.2, 0.1]],
+                        log_scales=[[-2.5] * 3, [-2.5] * 3, [-2.0] * 3, [-0.7, -1.0, -0.8], [-3.0] * 3],
+                        logits=[2.0, 0.5, 1.0, -1.0, 3.0])
+    cam = scenes.axis_camera(4.0, 64.0, 64, 64, 0.2, (0.0, 0.1, 0.2))
+    g = gs.gaussians_to_device(scene)
+    out = run_stages(g, cam)
+    check_decisions(oracle_mod, scene, cam, out)
+    ref = oracle_render(oracle_mod, scene, cam)
+    check_keys(oracle_mod, ref, out)
+    assert_image_parity(check_image(oracle_mod, ref, cam, out["image"], out["final_T"], out["n_contrib"]))
+
+
+def test_capacity_overflow_reports_count(oracle_mod):
+    scene, g = scene_of("100k", 20000)
+    cam = scenes.make_cameras("100k")[0]
+    ref = oracle_mod.render(scene, cam)
+    K = ref["num_keys"]
+    cap = K - 1000
+    p = gs.preprocess(g, cam)
+    b = gs.bin_keys(p, cam, cap)
+    torch.cuda.synchronize()
+    st, flags, nk = gs.read_status(b["ws"])
+    assert st == native.GS_ERR_CAPACITY and flags & native.GS_FLAG_CAPACITY and nk == K
+    assert int(b["num_keys"].item()) == K
+    np.testing.assert_array_equal(b["keys"][:cap].cpu().numpy().view(np.uint64), ref["keys"][:cap])
+    # whole frame with too small a capacity: flagged, count reported, no fault
+    r = gs.Renderer(g, cam["width"], cam["height"], cap)
+    r.render(cam)
+    torch.cuda.synchronize()
+    st, flags, nk = r.status()
+    assert st == native.GS_ERR_CAPACITY and nk == K
+
+
+@pytest.mark.parametrize("count,bits", [(0, 40), (1, 40), (4096, 45), (4097, 45), (12289, 20), (100_000, 64),
+                                        (300_001, 13), (65536, 36)])
+def test_sort_random_keys(oracle_mod, count, bits):
+    rng = np.random.default_rng(count + bits)
+    hi = (1 << bits) - 1 if bits < 64 else (1 << 64) - 1
+    keys = rng.integers(0, min(hi, 1 << 63), size=count, dtype=np.uint64)
+    if bits == 64:
+        keys |= (rng.integers(0, 2, size=count, dtype=np.uint64) << np.uint64(63))
+    keys[: count // 3] = keys[count // 3: 2 * (count // 3)]          # many duplicates
+    keys &= np.uint64(hi)
+    vals = rng.permutation(count).astype(np.uint32)
+    cap = count + 17
+    kd = torch.zeros(max(cap, 1), dtype=torch.int64, device="cuda")
+    vd = torch.zeros(max(cap, 1), dtype=torch.int32, device="cuda")
+    kd[:count] = torch.from_numpy(keys.view(np.int64))
+    vd[:count] = torch.from_numpy(vals.view(np.int32))
+    nk = torch.tensor([count], dtype=torch.int64, device="cuda")
+    out = gs.sort_pairs(kd, vd, nk, bits, cap)
+    torch.cuda.synchronize()
+    assert gs.read_status(out["ws"])[0] == native.GS_OK
+    sk, sv = oracle_mod.sort_pairs(keys, np.arange(count, dtype=np.uint32))   # stable: ties by position
+    np.testing.assert_array_equal(kd[:count].cpu().numpy().view(np.uint64), sk)
+    np.testing.assert_array_equal(vd[:count].cpu().numpy().view(np.uint32), vals[sv])
+
+
+def test_bounded_wait_times_out():
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    assert native.lib().gs_test_spin_timeout(ctypes.c_void_p(ws.data_ptr()), 1000, None) == native.GS_OK
+    st, flags, _ = gs.read_status(ws, torch.cuda.default_stream())
+    torch.cuda.synchronize()
+    st, flags, _ = gs.read_status(ws)
+    assert st == native.GS_ERR_TIMEOUT and flags & native.GS_FLAG_TIMEOUT
+    # the context is still usable afterwards
+    x = torch.ones(10, device="cuda")
+    assert float(x.sum().item()) == 10.0
+
+
+def test_render_from_host(oracle_mod):
+    scene, g = scene_of("100k", 20000)
+    cam = scenes.make_cameras("100k")[0]
+    r = gs.Renderer.for_scene(g, cam)
+    host = {k: torch.from_numpy(np.ascontiguousarray(scene[k])).pin_memory()
+            for k in ("means", "quats", "log_scales", "opacity_logits", "sh")}
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    dev.update(n=g["n"], sh_degree=g["sh_degree"])
+    r2 = gs.Renderer(dev, cam["width"], cam["height"], r.key_capacity)
+    himg = torch.empty((cam["height"], cam["width"], 3), dtype=torch.float32).pin_memory()
+    gs.render_from_host(host, r2, cam, himg)
+    torch.cuda.synchronize()
+    r.render(cam)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(himg.numpy(), r.image.cpu().numpy())
