@@ -48,6 +48,11 @@ PARAM_BYTES_PER_G = 12 + 16 + 12 + 4 + 192       # SH degree 3
 PROJ_BYTES_PER_G = 8 + 16 + 12 + 4 + 4 + 4 + 8
 
 
+def metric_name(cfg) -> str:
+    n = f"{cfg.n // 10**6}M" if cfg.n >= 10**6 else f"{cfg.n // 1000}k" if cfg.n >= 1000 else str(cfg.n)
+    return f"frames/s at {cfg.width}x{cfg.height}, {n} Gaussians SH{cfg.sh_degree}"
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -183,7 +188,7 @@ def run_reference(args, rank, world):
             break
     dt = time.perf_counter() - t0
     fps = done / dt
-    line = {"impl": "reference", "metric": f"frames/s at {cfg.width}x{cfg.height}, {cfg.n:,} Gaussians SH{cfg.sh_degree}",
+    line = {"impl": "reference", "metric": metric_name(cfg),
             "value": fps, "unit": "frames/s", "n_gpus": args.gpus, "steps": done, "warmup": min(args.warmup, 1),
             "ms_per_step": 1e3 * dt / done, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
@@ -401,8 +406,7 @@ def run_ours(args, rank, local_rank, world):
                 "frac": d["frac"], "peak_kind": peak_kind, "traffic": None}
 
     result = {
-        "metric": f"frames/s at {cfg.width}x{cfg.height}, {cfg.n // 1000 if cfg.n < 10**6 else cfg.n // 10**6}"
-                  f"{'k' if cfg.n < 10**6 else 'M'} Gaussians SH{cfg.sh_degree}",
+        "metric": metric_name(cfg),
         "value": world * 1e3 / frame_ms_max, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": frame_ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
