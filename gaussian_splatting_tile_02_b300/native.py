@@ -46,6 +46,8 @@ _SIGNATURES = {
     "gs_bin": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, ctypes.POINTER(GsCamera),
                               c_void_p, c_void_p, c_void_p, ctypes.c_int64, c_void_p, c_void_p,
                               ctypes.c_size_t, c_void_p]),
+    "gs_bin_static": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, ctypes.POINTER(GsCamera),
+                                     c_void_p, c_void_p, c_void_p, ctypes.c_int64, c_void_p, c_void_p]),
     "gs_sort_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64]),
     "gs_sort": (ctypes.c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, ctypes.c_int64,
                                ctypes.c_int32, c_void_p, ctypes.c_size_t, c_void_p]),

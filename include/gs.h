@@ -137,6 +137,28 @@ gs_status gs_bin(const gs_projected* projected, int64_t n, const gs_camera* came
                  uint32_t* offsets, uint64_t* keys, uint32_t* vals, int64_t key_capacity,
                  uint64_t* num_keys, void* ws, size_t ws_bytes, void* stream);
 
+/* Binning that allocates nothing (the pages have no counterpart: this is a
+ * deployment variant of gs_bin). For callers that cannot allocate device
+ * memory -- plugins whose host application owns all GPU memory through its
+ * own pools, real-time loops that forbid cudaMalloc after start-up because it
+ * can synchronise the device. Same inputs, outputs and results as gs_bin, but
+ * the scratch lives in a file-scope device array of the library (65,792
+ * bytes per device that loads the library, held until the process exits), so
+ * there is no ws argument.
+ *   - n must be <= GS_BIN_STATIC_MAX_GAUSSIANS, else GS_ERR_INVALID_ARG.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array. Calls whose work overlaps
+ *     on the GPU (e.g. issued on different streams without ordering) race and
+ *     give wrong results; order them on one stream.
+ *   - Capacity overflow is visible in the outputs: *num_keys > key_capacity
+ *     means only the first key_capacity keys were written. */
+#define GS_BIN_STATIC_MAX_GAUSSIANS 16777216
+gs_status gs_bin_static(const gs_projected* projected, int64_t n, const gs_camera* camera,
+                        uint32_t* offsets, uint64_t* keys, uint32_t* vals, int64_t key_capacity,
+                        uint64_t* num_keys, void* stream);
+
 /* Step 3 -- sort (flowchart box "Depth-sort per tile"). Stable ascending
  * least-significant-digit radix sort of the first min(K, key_capacity) (key,
  * value) pairs, K read from *num_keys on the device. Only the low key_bits
