@@ -19,7 +19,7 @@
 //   G    = rotation of (w, x, y, z): G00 = 1 - 2(yy + zz), G01 = 2(xy - wz),
 //          G02 = 2(xz + wy), G10 = 2(xy + wz), G11 = 1 - 2(xx + zz),
 //          G12 = 2(yz - wx), G20 = 2(xz - wy), G21 = 2(yz + wx), G22 = 1 - 2(xx + yy)
-//   s_k  = float(exp(double(log_scale_k)))
+//   s_k  = exp32(log_scale_k)   (binary32 exp below)
 //   B_ij = ((R_i0 G_0j + R_i1 G_1j) + R_i2 G_2j) s_j          (B = W R S)
 //   j00  = fx / z, j11 = fy / z, j02 = -((fx p0) / (z z)), j12 = -((fy p1) / (z z))
 //   M_0k = j00 B_0k + j02 B_2k,  M_1k = j11 B_1k + j12 B_2k   (M = J W R S)
@@ -44,6 +44,30 @@ __device__ __forceinline__ float add(float a, float b) { return __fadd_rn(a, b);
 __device__ __forceinline__ float sub(float a, float b) { return __fsub_rn(a, b); }
 __device__ __forceinline__ float dv(float a, float b) { return __fdiv_rn(a, b); }
 __device__ __forceinline__ float sq(float a) { return __fsqrt_rn(a); }
+
+// Scale activation e^l in binary32 with a fixed operation sequence (so the
+// result is reproducible bit for bit): Cody and Waite's range reduction
+// (Software Manual for the Elementary Functions, 1980), l = k ln2 + r with ln2
+// split into the 12-bit head 2839/4096 (k * head is exact) and a rounded tail,
+// then the degree-7 Taylor polynomial of e^r (|r| <= ln2/2) in Horner form,
+// then the exact product with 2^k. l is clamped to [-80, 80] so that 2^k and
+// the result are normal numbers. Constants: ln 2 and 1/j! rounded to binary32.
+__device__ __forceinline__ float exp32(float x) {
+    if (x != x) return x;
+    x = x > 80.0f ? 80.0f : x;
+    x = x < -80.0f ? -80.0f : x;
+    const float k = rintf(mul(x, 0x1.715476p+0f));                       // x / ln2
+    const float r = sub(sub(x, mul(k, 0x1.62ep-1f)), mul(k, 0x1.0bfbe8p-15f));
+    float p = 0x1.a01a02p-13f;                                           // 1/7!
+    p = add(0x1.6c16c2p-10f, mul(r, p));                                 // 1/6!
+    p = add(0x1.111112p-7f, mul(r, p));                                  // 1/5!
+    p = add(0x1.555556p-5f, mul(r, p));                                  // 1/4!
+    p = add(0x1.555556p-3f, mul(r, p));                                  // 1/3!
+    p = add(0.5f, mul(r, p));
+    p = add(1.0f, mul(r, p));
+    p = add(1.0f, mul(r, p));
+    return mul(p, __int_as_float((127 + (int)k) << 23));
+}
 
 // Real SH basis constants, from their closed forms: sqrt(1/4pi), sqrt(3/4pi),
 // sqrt(15/4pi), sqrt(5/16pi), sqrt(15/16pi), sqrt(35/32pi), sqrt(105/4pi),
@@ -175,7 +199,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
     }
     float s[3];
 #pragma unroll
-    for (int k = 0; k < 3; k++) s[k] = __double2float_rn(exp((double)__ldg(a.log_scales + 3 * g + k)));
+    for (int k = 0; k < 3; k++) s[k] = exp32(__ldg(a.log_scales + 3 * g + k));
     float B[9];
 #pragma unroll
     for (int i = 0; i < 3; i++)

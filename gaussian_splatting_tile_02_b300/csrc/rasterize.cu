@@ -7,14 +7,19 @@
 // loop over the depth order). Contributions with alpha < 1/255 are skipped
 // and a pixel stops once T < 1e-4, after the Gaussian that took it there.
 //
-// One block per tile, one thread per pixel. The tile's sorted Gaussian list
-// is walked in batches of 256: each thread gathers one projected record
-// (centre, conic with the exponent's constants folded in, opacity, colour)
-// into shared memory, then every thread evaluates the batch for its pixel.
-// The block leaves the loop as soon as all its pixels are done
-// (__syncthreads_count). The work is FP32-issue bound: per (pixel, Gaussian)
-// two subtractions, the quadratic form, an ex2 on the MUFU pipe, a min and a
-// compare, plus the blend for contributing pairs.
+// One block per tile, one thread per pixel; warp w covers the 8x4 pixel block
+// (8 (w & 1), 4 (w >> 1)) of the tile. The tile's sorted list is walked in
+// batches of 256 entries. Staging: each thread gathers one projected record
+// into shared memory with the exponent's constants folded in
+// (alpha = 2^(log2 o + quadratic form)) and the box that holds the region where
+// alpha can reach 1/255 (o exp(-q/2) >= 1/255, i.e. q <= 2 ln(255 o), widened
+// by a safety margin). Each warp then ballots which of the 256 entries' boxes
+// meet its 8x4 block and evaluates only those, in list order, for its 32
+// pixels: an entry whose box misses the block cannot contribute to any of its
+// pixels, so skipping it changes no result. The block leaves the list as soon
+// as all its pixels are done (__syncthreads_count). Per evaluated (pixel,
+// entry): two subtractions, the quadratic form (5 FP32 ops), ex2 on the MUFU
+// pipe, a min and a compare, plus the blend for contributing pairs.
 #include "gs_internal.cuh"
 
 namespace gs {
@@ -22,6 +27,7 @@ namespace {
 
 constexpr int kRastThreads = kTile * kTile;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kAlphaMin = 1.0f / 255.0f;
 
 // 2^x on the MUFU pipe (PTX ex2.approx; relative error about 2^-22).
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -51,14 +57,17 @@ struct RastArgs {
 };
 
 __global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs a) {
-    __shared__ float4 s_q[kRastThreads];   // (mx, my, qa, qb)
-    __shared__ float4 s_r[kRastThreads];   // (qc, log2 o, r, g)
-    __shared__ float s_b[kRastThreads];    // b
+    __shared__ float4 s_q[kRastThreads];    // (mx, my, qa, qb)
+    __shared__ float4 s_r[kRastThreads];    // (qc, log2 o, r, g)
+    __shared__ float s_b[kRastThreads];     // b
+    __shared__ float4 s_box[kRastThreads];  // (x lo, x hi, y lo, y hi) of the alpha >= 1/255 region
 
     const int tile = blockIdx.x;
     const int tx = tile % a.tiles_x, ty = tile / a.tiles_x;
-    const int px = tx * kTile + (threadIdx.x & (kTile - 1));
-    const int py = ty * kTile + (threadIdx.x >> 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bx0 = tx * kTile + 8 * (warp & 1), by0 = ty * kTile + 4 * (warp >> 1);
+    const int px = bx0 + (lane & 7), py = by0 + (lane >> 3);
+    const float fbx0 = (float)bx0, fbx1 = (float)(bx0 + 7), fby0 = (float)by0, fby1 = (float)(by0 + 3);
     const bool inside = px < a.width && py < a.height;
     const uint2 range = a.ranges[tile];
     const float fpx = (float)px, fpy = (float)py;
@@ -77,32 +86,63 @@ __global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs 
             if (g >= a.n) g = 0;
             const float2 m = __ldg(a.mean2d + g);
             const float4 co = __ldg(a.conic_opacity + g);
-            // exponent in base 2: log2(alpha) = log2 o - (log2 e / 2)(A dx^2 + C dy^2) - log2 e B dx dy
             s_q[threadIdx.x] = make_float4(m.x, m.y, -0.5f * kLog2e * co.x, -kLog2e * co.y);
             s_r[threadIdx.x] = make_float4(-0.5f * kLog2e * co.z, fast_log2(co.w), __ldg(a.rgb + 3 * g),
                                            __ldg(a.rgb + 3 * g + 1));
             s_b[threadIdx.x] = __ldg(a.rgb + 3 * g + 2);
+            // box of {d : d^T conic d <= tau}, tau = 2 ln(255 o): half-extents
+            // sqrt(tau Sigma'_xx) and sqrt(tau Sigma'_yy) with Sigma' = conic^-1;
+            // tau is raised by 0.02 and the half-extents widened by 1% + 0.05 px,
+            // far more than the rounding of the per-pixel alpha can move it.
+            // The rounding of det(conic) is about 3e-8 (A + C)^2 / det relative:
+            // conics with (A + C)^2 > 1e4 det keep an unbounded box (never culled).
+            const float detc = co.x * co.z - co.y * co.y;
+            const float tau = 2.0f * __logf(255.0f * co.w) + 0.02f;
+            float4 box = make_float4(-INFINITY, INFINITY, -INFINITY, INFINITY);
+            if (!(tau > 0.0f)) {  // o below 1/255 (margin included): never contributes
+                box = make_float4(INFINITY, -INFINITY, INFINITY, -INFINITY);
+            } else if (detc > 0.0f && (co.x + co.z) * (co.x + co.z) <= 1e4f * detc) {
+                const float hx = 1.01f * sqrtf(tau * co.z / detc) + 0.05f;
+                const float hy = 1.01f * sqrtf(tau * co.x / detc) + 0.05f;
+                if (hx < INFINITY && hy < INFINITY) box = make_float4(m.x - hx, m.x + hx, m.y - hy, m.y + hy);
+            }
+            s_box[threadIdx.x] = box;
         }
         __syncthreads();
-        const int cnt = (int)min((uint32_t)kRastThreads, range.y - base);
-        if (!done) {
-            for (int j = 0; j < cnt; j++) {
+        const uint32_t cnt = min((uint32_t)kRastThreads, range.y - base);
+        // which of the batch entries can touch this warp's 8x4 pixel block
+        uint32_t mask[kRastThreads / 32];
+#pragma unroll
+        for (int i = 0; i < kRastThreads / 32; i++) {
+            const uint32_t j = (uint32_t)(i * 32 + lane);
+            bool hit = false;
+            if (j < cnt) {
+                const float4 bx = s_box[j];
+                hit = bx.x <= fbx1 && bx.y >= fbx0 && bx.z <= fby1 && bx.w >= fby0;
+            }
+            mask[i] = __ballot_sync(0xffffffffu, hit);
+        }
+#pragma unroll
+        for (int i = 0; i < kRastThreads / 32; i++) {
+            if (__all_sync(0xffffffffu, done)) break;
+            uint32_t m = mask[i];
+            while (m) {
+                const int j = i * 32 + __ffs(m) - 1;
+                m &= m - 1;
+                if (done) continue;
                 const float4 q = s_q[j];
                 const float4 r = s_r[j];
                 const float dx = q.x - fpx, dy = q.y - fpy;
                 const float e = r.y + dx * (q.z * dx + q.w * dy) + r.x * dy * dy;
                 const float alpha = fminf(0.99f, fast_exp2(e));
-                if (alpha < (1.0f / 255.0f)) continue;
+                if (alpha < kAlphaMin) continue;
                 const float w = alpha * T;
                 C0 += w * r.z;
                 C1 += w * r.w;
                 C2 += w * s_b[j];
                 T -= w;
-                last = base - range.x + j + 1;
-                if (T < 1e-4f) {
-                    done = true;
-                    break;
-                }
+                last = base - range.x + (uint32_t)j + 1;
+                if (T < 1e-4f) done = true;
             }
         }
     }

@@ -147,13 +147,21 @@ def decide_f32(scene: dict, cam: dict) -> dict:
            "mean2d": np.empty((n, 2), dtype=np.float32), "cov2d": np.empty((n, 3), dtype=np.float32),
            "radius": np.empty(n, dtype=np.int32), "pix_rect": np.empty((n, 4), dtype=np.int32),
            "tile_rect": np.empty((n, 4), dtype=np.int32),
-           "tiles_touched": np.empty(n, dtype=np.uint32), "hazard": np.empty(n, dtype=np.uint8)}
+           "tiles_touched": np.empty(n, dtype=np.uint32)}
     c = make_camera(cam)
     lib().or_decide_f32(ctypes.c_int64(n), _p(means), _p(quats), _p(ls), ctypes.byref(c),
                         _p(out["valid"]), _p(out["depth"]), _p(out["mean2d"]), _p(out["cov2d"]),
                         _p(out["radius"]), _p(out["pix_rect"]), _p(out["tile_rect"]),
-                        _p(out["tiles_touched"]), _p(out["hazard"]))
+                        _p(out["tiles_touched"]))
     return out
+
+
+def exp32(x: np.ndarray) -> np.ndarray:
+    """The decision program's binary32 exp (Cody-Waite reduction + degree-7 Taylor)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    y = np.empty_like(x)
+    lib().or_exp32_batch(ctypes.c_int64(x.shape[0]), _p(x), _p(y))
+    return y
 
 
 def rect_f64(proj: dict, cam: dict) -> dict:

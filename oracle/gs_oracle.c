@@ -265,15 +265,37 @@ void or_project_f64(int64_t n, const float *means, const float *quats, const flo
 /* fp32 decision program                                                      */
 /* ------------------------------------------------------------------------- */
 
-/* 1 if the double value e lies so close to a binary32 rounding midpoint that
- * two correctly-rounded-within-1-ulp double exp implementations could round
- * it to different floats. */
-static int exp_midpoint_hazard(double e) {
-    float f = (float)e;
-    double up = ((double)f + (double)nextafterf(f, INFINITY)) * 0.5;
-    double dn = ((double)f + (double)nextafterf(f, 0.0f)) * 0.5;
-    double tol = 8.0 * (nextafter(e, INFINITY) - e);
-    return fabs(e - up) <= tol || fabs(e - dn) <= tol;
+/* Scale activation of the decision program, scale = e^l ("Ce qu'un Gaussien
+ * porte": log-scales exponentiated at render time), evaluated in binary32 by
+ * Cody and Waite's range reduction (Software Manual for the Elementary
+ * Functions, 1980): l = k ln2 + r with ln2 split into a 12-bit head (exact
+ * products k*head) and a rounded tail, then e^r by its Taylor polynomial of
+ * degree 7 (|r| <= ln2/2, truncation below 6e-9 relative) in Horner form,
+ * then the exact scaling by 2^k. Every operation is rounded on its own; l is
+ * clamped to [-80, 80] so that 2^k and the result stay normal numbers.
+ * The constants are ln 2 and 1/j!, rounded to binary32. */
+float or_exp32(float x) {
+    if (x != x) return x;
+    if (x > 80.0f) x = 80.0f;
+    if (x < -80.0f) x = -80.0f;
+    const float ln2_hi = 2839.0f / 4096.0f;
+    const float ln2_lo = (float)(log(2.0) - 2839.0 / 4096.0);
+    const float inv_ln2 = (float)(1.0 / log(2.0));
+    float c[8];
+    double f = 1.0;
+    for (int j = 0; j < 8; j++) {
+        if (j > 0) f *= j;
+        c[j] = (float)(1.0 / f);
+    }
+    const float k = rintf(x * inv_ln2);
+    const float r = (x - k * ln2_hi) - k * ln2_lo;
+    float p = c[7];
+    for (int j = 6; j >= 0; j--) p = c[j] + r * p;
+    return ldexpf(p, (int)k);
+}
+
+void or_exp32_batch(int64_t n, const float *x, float *y) {
+    for (int64_t i = 0; i < n; i++) y[i] = or_exp32(x[i]);
 }
 
 /* The decision program, step by step (binary32, each operation rounded to
@@ -284,7 +306,7 @@ static int exp_midpoint_hazard(double e) {
  *      r = sqrt(n2); (w,x,y,z) = q / r
  *  D4  G = textbook rotation of (w,x,y,z): e.g. G00 = 1 - 2 (yy + zz),
  *      G01 = 2 (xy - wz), each product rounded first
- *  D5  s_k = float(exp(double(l_k)))
+ *  D5  s_k = exp32(l_k)   (or_exp32: binary32 Cody-Waite + Taylor, above)
  *  D6  A_ij = (R_i0 G_0j + R_i1 G_1j) + R_i2 G_2j;  B_ij = A_ij s_j
  *  D7  j00 = fx/z, j11 = fy/z, zz = z z, j02 = -((fx p0)/zz), j12 = -((fy p1)/zz)
  *  D8  M_0k = j00 B_0k + j02 B_2k;  M_1k = j11 B_1k + j12 B_2k
@@ -300,12 +322,11 @@ static int exp_midpoint_hazard(double e) {
  * Sigma' = M M^T with M = J W R S is the pages' J W Sigma W^T J^T with
  * Sigma = (R S)(R S)^T, re-associated.
  * Outputs per Gaussian: valid, depth, mean2d, cov2d (a, b, c), radius,
- * pixel rect, tile rect, tiles_touched, exp hazard flag. */
+ * pixel rect, tile rect, tiles_touched. */
 void or_decide_f32(int64_t n, const float *means, const float *quats, const float *log_scales,
                    const or_camera *cam, uint8_t *valid, float *depth, float *mean2d, float *cov2d,
                    int32_t *radius, int32_t *pix_rect /* [n][4] x0 y0 x1 y1 */,
-                   int32_t *tile_rect /* [n][4] tx0 ty0 tx1 ty1 */, uint32_t *tiles_touched,
-                   uint8_t *hazard) {
+                   int32_t *tile_rect /* [n][4] tx0 ty0 tx1 ty1 */, uint32_t *tiles_touched) {
     const float *R = cam->R, *t = cam->t;
     const float fx = cam->fx, fy = cam->fy, cx = cam->cx, cy = cam->cy, nearz = cam->near_z;
     const float Wm1 = (float)(cam->width - 1), Hm1 = (float)(cam->height - 1);
@@ -328,7 +349,6 @@ void or_decide_f32(int64_t n, const float *means, const float *quats, const floa
         /* an empty rectangle is stored as (0, 0, -1, -1) */
         for (int k = 0; k < 4; k++) pix_rect[4 * g + k] = tile_rect[4 * g + k] = k < 2 ? 0 : -1;
         tiles_touched[g] = 0;
-        hazard[g] = 0;
         const float z = p[2];
         if (!(z > nearz)) continue;                                  /* D2 */
 
@@ -351,11 +371,7 @@ void or_decide_f32(int64_t n, const float *means, const float *quats, const floa
             G[6] = 2.0f * (xz - wy);        G[7] = 2.0f * (yz + wx);        G[8] = 1.0f - 2.0f * (xx + yy);
         }
         float s[3];                                                  /* D5 */
-        for (int k = 0; k < 3; k++) {
-            double e = exp((double)log_scales[3 * g + k]);
-            s[k] = (float)e;
-            if (exp_midpoint_hazard(e)) hazard[g] = 1;
-        }
+        for (int k = 0; k < 3; k++) s[k] = or_exp32(log_scales[3 * g + k]);
         float B[9];                                                  /* D6 */
         for (int i = 0; i < 3; i++)
             for (int j = 0; j < 3; j++) {

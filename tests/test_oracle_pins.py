@@ -441,6 +441,37 @@ def test_empty_scene(oracle_mod):
 
 # ----------------------------------------------------------------------------- decision program
 
+def exp32_numpy(x):
+    """Cody-Waite reduction x = k ln2 + r (ln2 = 2839/4096 + tail) and the
+    degree-7 Taylor polynomial of e^r, in numpy float32 (each op rounded)."""
+    f = np.float32
+    x = np.clip(np.asarray(x, f), f(-80), f(80))
+    hi = f(2839 / 4096)
+    lo = f(math.log(2) - 2839 / 4096)
+    k = np.rint(x * f(1 / math.log(2)))
+    r = (x - k * hi) - k * lo
+    c = [f(1 / math.factorial(j)) for j in range(8)]
+    p = np.full_like(r, c[7])
+    for j in range(6, -1, -1):
+        p = c[j] + r * p
+    return np.ldexp(p, k.astype(np.int32)).astype(f)
+
+
+def test_exp32_accuracy_and_special_values(oracle_mod):
+    """The decision program's exp: within 3 ulp of e^x, exact at 0, NaN kept, clamped beyond +-80."""
+    x = np.concatenate([np.linspace(-30, 30, 200001, dtype=np.float32),
+                        np.random.default_rng(1).normal(-4, 1, 100000).astype(np.float32)])
+    y = oracle_mod.exp32(x).astype(np.float64)
+    ref = np.exp(x.astype(np.float64))
+    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
+    assert (np.abs(y - ref) <= 3 * ulp).all()
+    np.testing.assert_array_equal(oracle_mod.exp32(x), exp32_numpy(x))
+    assert oracle_mod.exp32(np.float32([0.0]))[0] == 1.0
+    assert np.isnan(oracle_mod.exp32(np.float32([np.nan]))[0])
+    np.testing.assert_array_equal(oracle_mod.exp32(np.float32([100.0, -100.0])),
+                                  oracle_mod.exp32(np.float32([80.0, -80.0])))
+
+
 def decide_numpy_f32(s, cam):
     """The binary32 decision program restated with numpy float32 element-wise ops
     (each op rounded, no FMA) -- a second build of the same program, to catch a
@@ -462,7 +493,7 @@ def decide_numpy_f32(s, cam):
         G = [[one - two * (yy + zz), two * (xy - wz), two * (xz + wy)],
              [two * (xy + wz), one - two * (xx + zz), two * (yz - wx)],
              [two * (xz - wy), two * (yz + wx), one - two * (xx + yy)]]
-        sc = np.array([[math.exp(float(v)) for v in row] for row in s["log_scales"]], np.float64).astype(f)
+        sc = exp32_numpy(s["log_scales"].astype(f))
         B = [[((R[i, 0] * G[0][j] + R[i, 1] * G[1][j]) + R[i, 2] * G[2][j]) * sc[:, j] for j in range(3)]
              for i in range(3)]
         fx, fy, cx, cy = (f(cam[k]) for k in ("fx", "fy", "cx", "cy"))
@@ -520,7 +551,6 @@ def test_decision_program_agrees_with_fp64_track(oracle_mod, name):
     d = oracle_mod.decide_f32(s, cam)
     p = oracle_mod.project_f64(s, cam)
     np.testing.assert_array_equal(d["valid"], p["valid"])
-    assert d["hazard"].sum() == 0
     v = d["valid"] > 0
     ulp = np.spacing(np.abs(p["depth"][v]).astype(np.float32)).astype(np.float64)
     assert (np.abs(d["depth"][v] - p["depth"][v]) <= 4 * ulp).all()
