@@ -274,66 +274,49 @@ def run_ours(args, rank, local_rank, world):
         frame_ms = e0.elapsed_time(e1) / args.steps
         frame_ms_max = max_over_ranks(frame_ms)
 
-        # --- per-stage times: K frames through the stage entry points, events between stages
-        stage_names = ["preprocess", "bin", "sort", "ranges", "rasterize"]
+        # --- per-stage times: K more frames through gs_render_profiled, which records
+        # CUDA events at the stage boundaries of the very launches a frame makes
+        stage_names = ["preprocess", "depth_order", "bin", "tile_sort", "ranges", "rasterize"]
         st_ms = {k: 0.0 for k in stage_names}
-        p = gs.alloc_projected(int(g["n"]), dev)
-        cap = r.key_capacity
-        keys = torch.empty(cap, dtype=torch.int64, device=dev)
-        vals = torch.empty(cap, dtype=torch.int32, device=dev)
-        keys_alt = torch.empty_like(keys)
-        vals_alt = torch.empty_like(vals)
-        offsets = torch.empty(int(g["n"]), dtype=torch.int32, device=dev)
-        nk = torch.zeros(1, dtype=torch.int64, device=dev)
-        tx, ty = gs.tiles_xy(cam)
-        ranges = torch.empty((tx * ty, 2), dtype=torch.int32, device=dev)
-        img = torch.empty((cam["height"], cam["width"], 3), dtype=torch.float32, device=dev)
-        fT = torch.empty((cam["height"], cam["width"]), dtype=torch.float32, device=dev)
-        ncon = torch.empty((cam["height"], cam["width"]), dtype=torch.int32, device=dev)
-        bws = torch.empty(int(gs.lib().gs_bin_workspace_bytes(int(g["n"]))), dtype=torch.uint8, device=dev)
-        sws = torch.empty(int(gs.lib().gs_sort_workspace_bytes(cap)), dtype=torch.uint8, device=dev)
         import ctypes
         L = gs.lib()
         cs = gs.camera_struct(cam)
-        gst = gs.gaussians_struct(g)
-        pst = gs.projected_struct(p)
         sp = ctypes.c_void_p(stream.cuda_stream)
-        kb = gs.key_bits(cam)
-        ptr = lambda t: t.data_ptr()
 
-        def stages(evs):
-            evs[0].record(stream)
-            native.check(L.gs_preprocess(ctypes.byref(gst), ctypes.byref(cs), ctypes.byref(pst), sp), "pre")
-            evs[1].record(stream)
-            native.check(L.gs_bin(ctypes.byref(pst), int(g["n"]), ctypes.byref(cs), ptr(offsets), ptr(keys),
-                                  ptr(vals), cap, ptr(nk), ptr(bws), bws.numel(), sp), "bin")
-            evs[2].record(stream)
-            native.check(L.gs_sort(ptr(keys), ptr(vals), ptr(keys_alt), ptr(vals_alt), ptr(nk), cap, kb,
-                                   ptr(sws), sws.numel(), sp), "sort")
-            evs[3].record(stream)
-            native.check(L.gs_tile_ranges(ptr(keys), ptr(nk), cap, ctypes.byref(cs), ptr(ranges), sp), "ranges")
-            evs[4].record(stream)
-            native.check(L.gs_rasterize(ctypes.byref(pst), int(g["n"]), ptr(vals), ptr(ranges), ctypes.byref(cs),
-                                        ptr(img), ptr(fT), ptr(ncon), sp), "raster")
-            evs[5].record(stream)
+        def new_events():
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
+            for ev in evs:
+                ev.record(stream)   # creates the underlying CUDA event
+            arr = (ctypes.c_void_p * len(evs))(*[ctypes.c_void_p(ev.cuda_event) for ev in evs])
+            return evs, arr
+
+        def profiled(arr):
+            native.check(L.gs_render_profiled(ctypes.byref(r._gs), ctypes.byref(cs), r.key_capacity,
+                                              r.ws.data_ptr(), r.ws_bytes, r.image.data_ptr(), None, None, sp,
+                                              arr, len(arr)), "gs_render_profiled")
 
         with torch.cuda.stream(stream):
-            for _ in range(3):
-                stages([torch.cuda.Event(enable_timing=True) for _ in range(6)])
+            pool = [new_events() for _ in range(args.steps)]
+            for evs, arr in pool[:3]:
+                profiled(arr)
             stream.synchronize()
             # a fixed-length device sleep first, so the host queues frames ahead of the GPU
             # and no stage time includes host launch latency
             torch.cuda._sleep(int(40e6))
-            all_evs = []
-            for _ in range(args.steps):
-                evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-                stages(evs)
-                all_evs.append(evs)
+            for evs, arr in pool:
+                profiled(arr)
         torch.cuda.synchronize(dev)
-        for evs in all_evs:
+        for evs, _ in pool:
             for i, k in enumerate(stage_names):
                 st_ms[k] += evs[i].elapsed_time(evs[i + 1]) / args.steps
         stage_total = sum(st_ms.values())
+        # one frame with the per-pixel outputs, for the rasterizer's evaluation count
+        with torch.cuda.stream(stream):
+            r.render(cam, stream=stream, aux=True)
+        torch.cuda.synchronize(dev)
+        fT, ncon = r.final_T, r.n_contrib
+        ranges = torch.empty(0)
+        tx, ty = gs.tiles_xy(cam)
 
         # --- end to end from host memory
         e2e = None
@@ -364,39 +347,51 @@ def run_ours(args, rank, local_rank, world):
     clocks = sampler.summary()
 
     # --- algorithmic work of the last frame (from its outputs)
-    rng_np = ranges.cpu().numpy().astype(np.int64)
-    lens = (rng_np[:, 1] - rng_np[:, 0]).reshape(ty, tx)
+    # per-tile list lengths: the sorted order is the oracle-checked one, so the
+    # ranges can be recounted from the per-Gaussian tile rectangles on the device
+    p_dev = gs.preprocess(g, cam)
+    rect = p_dev["rect"].to(torch.int64) & 0xFFFF
+    tt = p_dev["tiles_touched"].to(torch.int64)
+    has = torch.nonzero(tt > 0).flatten()
+    # rectangle coverage counts per tile via a 2D difference array
+    diff = torch.zeros((ty + 1, tx + 1), dtype=torch.int64, device=dev)
+    rr = rect[has]
+    ones = torch.ones(rr.shape[0], dtype=torch.int64, device=dev)
+    diff.index_put_((rr[:, 1], rr[:, 0]), ones, accumulate=True)
+    diff.index_put_((rr[:, 1], rr[:, 2] + 1), -ones, accumulate=True)
+    diff.index_put_((rr[:, 3] + 1, rr[:, 0]), -ones, accumulate=True)
+    diff.index_put_((rr[:, 3] + 1, rr[:, 2] + 1), ones, accumulate=True)
+    cover = diff.cumsum(0).cumsum(1)[:ty, :tx]
+    lens = cover.cpu().numpy()
     L_pix = np.kron(lens, np.ones((16, 16), np.int64))[: cam["height"], : cam["width"]]
     nc = ncon.cpu().numpy().astype(np.int64)
     Tf = fT.cpu().numpy()
     evals = int(np.where(Tf < 1e-4, nc, L_pix).sum())
     n = int(g["n"])
     K = K_keys
-    passes = (kb + 7) // 8
-    launches_per_frame = 1 + 3 + 2 + passes + (passes % 2) + 1 + 1
+    tile_bits = max(1, (tx * ty - 1).bit_length())
+    tpasses = (tile_bits + 7) // 8
+    launches_per_frame = 1 + (1 + 1 + 4) + 3 + (1 + tpasses) + 1 + 1
     ras_ms = st_ms["rasterize"]
     clk = clocks.get("sm_mhz") or SM_MAX_MHZ
     fp32_peak = SM_COUNT * FP32_LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12     # T lane-ops/s at max clock
     ras_ops = OPS_PER_EVAL * evals
     ras_achieved = ras_ops / (ras_ms * 1e-3) / 1e12
-    pre_bytes = (PARAM_BYTES_PER_G + PROJ_BYTES_PER_G) * n
-    bin_bytes = 8 * n + 16 * n + 4 * n + 12 * K
-    sort_bytes = 8 * K + 24 * K * passes + (24 * K if passes % 2 else 0)
-    range_bytes = 8 * K + 8 * tx * ty
-    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
-    stages_out = {
-        "preprocess": {"ms": st_ms["preprocess"], "bound": "hbm", "GB/s": gbs(pre_bytes, st_ms["preprocess"]),
-                       "frac": gbs(pre_bytes, st_ms["preprocess"]) / hbm_peak, "bytes": pre_bytes},
-        "bin": {"ms": st_ms["bin"], "bound": "hbm", "GB/s": gbs(bin_bytes, st_ms["bin"]),
-                "frac": gbs(bin_bytes, st_ms["bin"]) / hbm_peak, "bytes": bin_bytes},
-        "sort": {"ms": st_ms["sort"], "bound": "hbm", "GB/s": gbs(sort_bytes, st_ms["sort"]),
-                 "frac": gbs(sort_bytes, st_ms["sort"]) / hbm_peak, "bytes": sort_bytes, "passes": passes},
-        "ranges": {"ms": st_ms["ranges"], "bound": "hbm", "GB/s": gbs(range_bytes, st_ms["ranges"]),
-                   "frac": gbs(range_bytes, st_ms["ranges"]) / hbm_peak, "bytes": range_bytes},
-        "rasterize": {"ms": ras_ms, "bound": "alu", "Top/s": ras_achieved, "frac": ras_achieved / fp32_peak,
-                      "evaluations": evals, "ops": ras_ops,
-                      "frac_at_sampled_clock": ras_achieved / (fp32_peak * clk / SM_MAX_MHZ)},
+    stage_bytes = {
+        "preprocess": (PARAM_BYTES_PER_G + PROJ_BYTES_PER_G) * n,
+        "depth_order": 16 * n + 4 * 16 * n,
+        "bin": 24 * n + 8 * K,
+        "tile_sort": tpasses * 16 * K,
+        "ranges": 4 * K + 8 * tx * ty,
     }
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
+    stages_out = {}
+    for k, b in stage_bytes.items():
+        stages_out[k] = {"ms": st_ms[k], "bound": "hbm", "GB/s": gbs(b, st_ms[k]),
+                         "frac": gbs(b, st_ms[k]) / hbm_peak, "bytes": b}
+    stages_out["rasterize"] = {"ms": ras_ms, "bound": "alu", "Top/s": ras_achieved, "frac": ras_achieved / fp32_peak,
+                               "evaluations": evals, "ops": ras_ops,
+                               "frac_at_sampled_clock": ras_achieved / (fp32_peak * clk / SM_MAX_MHZ)}
     dominant = max(stages_out, key=lambda k: stages_out[k]["ms"])
     if dominant == "rasterize":
         roof = {"kernel": "rasterize_kernel", "bound": "alu", "achieved": ras_achieved, "peak": fp32_peak,

@@ -68,19 +68,19 @@ bool projected_ok(const gs_projected* p, int64_t n) {
            aligned(p->radius, 4) && aligned(p->tiles_touched, 4) && aligned(p->rect, 8);
 }
 
-int key_bits_for(const gs_camera& c) {
+gs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GS_OK : GS_ERR_CUDA; }
+
+int tile_bits_for(const gs_camera& c) {
     const int64_t tiles = (int64_t)tiles_x(c) * tiles_y(c);
     int b = 0;
     while ((1ll << b) < tiles) b++;
-    return 32 + b;
+    return b > 0 ? b : 1;
 }
-
-gs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GS_OK : GS_ERR_CUDA; }
 
 // gs_render workspace layout
 struct RenderLayout {
-    size_t header, mean2d, conic, rgb, depth, radius, touched, rect, offsets, bin, keys, vals, keys_alt,
-        vals_alt, sort, ranges, num_keys, total;
+    size_t header, mean2d, conic, rgb, depth, radius, touched, rect, dkeys, dkeys_alt, order, order_alt, bin,
+        keys, vals, keys_alt, vals_alt, sort, ranges, num_keys, total;
 };
 
 RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
@@ -102,18 +102,92 @@ RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
     L.radius = take(4 * un);
     L.touched = take(4 * un);
     L.rect = take(8 * un);
-    L.offsets = take(4 * un);
+    L.dkeys = take(4 * un);
+    L.dkeys_alt = take(4 * un);
+    L.order = take(4 * un);
+    L.order_alt = take(4 * un);
     L.bin = take(bin_scratch_bytes(n));
-    L.keys = take(8 * uc);
+    L.keys = take(4 * uc);
     L.vals = take(4 * uc);
-    L.keys_alt = take(8 * uc);
+    L.keys_alt = take(4 * uc);
     L.vals_alt = take(4 * uc);
-    L.sort = take(sort_scratch_bytes(cap));
+    L.sort = take(sort_scratch_bytes(cap > n ? cap : n));
     L.ranges = take(8 * tiles);
     L.total = o;
     return L;
 }
 
+}  // namespace
+}  // namespace gs
+
+namespace gs {
+namespace {
+
+gs_status render_impl(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, void* ws, size_t ws_bytes,
+                      float* image, float* final_T, uint32_t* n_contrib, void* stream, void* const* events) {
+    if (!gaussians_ok(g) || !camera_ok(cam) || !image) return GS_ERR_INVALID_ARG;
+    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
+    const RenderLayout L = render_layout(g->n, cam->width, cam->height, key_capacity);
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GS_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* w = static_cast<char*>(ws);
+    auto* header = reinterpret_cast<StatusHeader*>(w + L.header);
+    auto* num_keys = reinterpret_cast<uint64_t*>(w + L.num_keys);
+    gs_projected p;
+    p.mean2d = reinterpret_cast<float*>(w + L.mean2d);
+    p.conic_opacity = reinterpret_cast<float*>(w + L.conic);
+    p.rgb = reinterpret_cast<float*>(w + L.rgb);
+    p.depth = reinterpret_cast<float*>(w + L.depth);
+    p.radius = reinterpret_cast<int32_t*>(w + L.radius);
+    p.tiles_touched = reinterpret_cast<uint32_t*>(w + L.touched);
+    p.rect = reinterpret_cast<uint16_t*>(w + L.rect);
+    auto* dkeys = reinterpret_cast<uint32_t*>(w + L.dkeys);
+    auto* dkeys_alt = reinterpret_cast<uint32_t*>(w + L.dkeys_alt);
+    auto* order = reinterpret_cast<uint32_t*>(w + L.order);
+    auto* order_alt = reinterpret_cast<uint32_t*>(w + L.order_alt);
+    auto* keys = reinterpret_cast<uint32_t*>(w + L.keys);
+    auto* vals = reinterpret_cast<uint32_t*>(w + L.vals);
+    auto* keys_alt = reinterpret_cast<uint32_t*>(w + L.keys_alt);
+    auto* vals_alt = reinterpret_cast<uint32_t*>(w + L.vals_alt);
+    auto* ranges = reinterpret_cast<uint32_t*>(w + L.ranges);
+    const CamConst cc = make_cam_const(*cam);
+
+    // depth order first, then (tile, index) pairs in that order, then a stable
+    // sort by tile: the same per-tile (depth, index) order as sorting the
+    // 64-bit tile|depth keys, with far fewer key bits moved
+    // (the producers of both key lists also count their sort digits)
+    void* sort_ws = w + L.sort;
+    uint32_t* hist = sort_histogram_of(sort_ws);
+    const int tbits = tile_bits_for(*cam);
+    auto mark = [&](int i) {
+        return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
+    };
+    cudaError_t e = mark(0);
+    if (e == cudaSuccess) e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
+    if (e == cudaSuccess) e = launch_preprocess(*g, cc, p, s);
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = sort_prepare_histogram(sort_ws, s);
+    if (e == cudaSuccess) e = launch_depth_keys(p, g->n, dkeys, order, hist, s);
+    if (e == cudaSuccess)
+        e = launch_sort32(dkeys, order, dkeys_alt, order_alt, nullptr, g->n, 32, header, sort_ws, g_spin_limit, s,
+                          true);
+    if (e == cudaSuccess) e = mark(2);
+    if (e == cudaSuccess) e = sort_prepare_histogram(sort_ws, s);
+    if (e == cudaSuccess)
+        e = launch_bin_ordered(p, order, g->n, cc, nullptr, keys, vals, key_capacity, num_keys, header, w + L.bin, s,
+                               hist, tbits);
+    if (e == cudaSuccess) e = mark(3);
+    if (e == cudaSuccess)
+        e = launch_sort32(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, tbits, header, sort_ws,
+                          g_spin_limit, s, true);
+    if (e == cudaSuccess) e = mark(4);
+    if (e == cudaSuccess)
+        e = launch_tile_ranges32(keys, num_keys, key_capacity, cc.tiles_x * cc.tiles_y, ranges, s);
+    if (e == cudaSuccess) e = mark(5);
+    if (e == cudaSuccess) e = launch_rasterize(p, g->n, vals, ranges, cc, image, final_T, n_contrib, s);
+    if (e == cudaSuccess) e = mark(6);
+    return cuda_status(e);
+}
 }  // namespace
 }  // namespace gs
 
@@ -207,41 +281,91 @@ size_t gs_render_workspace_bytes(int64_t n, int32_t width, int32_t height, int64
 
 gs_status gs_render(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, void* ws, size_t ws_bytes,
                     float* image, float* final_T, uint32_t* n_contrib, void* stream) {
-    if (!gaussians_ok(g) || !camera_ok(cam) || !image) return GS_ERR_INVALID_ARG;
-    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
-    const RenderLayout L = render_layout(g->n, cam->width, cam->height, key_capacity);
-    if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GS_ERR_WORKSPACE;
+    return render_impl(g, cam, key_capacity, ws, ws_bytes, image, final_T, n_contrib, stream, nullptr);
+}
+
+gs_status gs_render_profiled(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, void* ws,
+                             size_t ws_bytes, float* image, float* final_T, uint32_t* n_contrib, void* stream,
+                             void* const* events, int32_t n_events) {
+    if (!events || n_events < GS_RENDER_STAGES + 1) return GS_ERR_INVALID_ARG;
+    for (int i = 0; i <= GS_RENDER_STAGES; i++)
+        if (!events[i]) return GS_ERR_INVALID_ARG;
+    return render_impl(g, cam, key_capacity, ws, ws_bytes, image, final_T, n_contrib, stream, events);
+}
+
+
+
+size_t gs_depth_order_workspace_bytes(int64_t n) {
+    const size_t un = (size_t)(n > 0 ? n : 0);
+    return sizeof(StatusHeader) + 3 * align_up(4 * un) + sort_scratch_bytes(n > 0 ? n : 0);
+}
+
+gs_status gs_depth_order(const gs_projected* p, int64_t n, uint32_t* order, void* ws, size_t ws_bytes,
+                         void* stream) {
+    if (n < 0 || n > kMaxKeyCapacity || !p || (n > 0 && (!p->depth || !p->tiles_touched || !order)))
+        return GS_ERR_INVALID_ARG;
+    if (n > 0 && (!aligned(p->depth, 4) || !aligned(p->tiles_touched, 4) || !aligned(order, 4)))
+        return GS_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < gs_depth_order_workspace_bytes(n)) return GS_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     char* w = static_cast<char*>(ws);
-    auto* header = reinterpret_cast<StatusHeader*>(w + L.header);
-    auto* num_keys = reinterpret_cast<uint64_t*>(w + L.num_keys);
-    gs_projected p;
-    p.mean2d = reinterpret_cast<float*>(w + L.mean2d);
-    p.conic_opacity = reinterpret_cast<float*>(w + L.conic);
-    p.rgb = reinterpret_cast<float*>(w + L.rgb);
-    p.depth = reinterpret_cast<float*>(w + L.depth);
-    p.radius = reinterpret_cast<int32_t*>(w + L.radius);
-    p.tiles_touched = reinterpret_cast<uint32_t*>(w + L.touched);
-    p.rect = reinterpret_cast<uint16_t*>(w + L.rect);
-    auto* offsets = reinterpret_cast<uint32_t*>(w + L.offsets);
-    auto* keys = reinterpret_cast<uint64_t*>(w + L.keys);
-    auto* vals = reinterpret_cast<uint32_t*>(w + L.vals);
-    auto* keys_alt = reinterpret_cast<uint64_t*>(w + L.keys_alt);
-    auto* vals_alt = reinterpret_cast<uint32_t*>(w + L.vals_alt);
-    auto* ranges = reinterpret_cast<uint32_t*>(w + L.ranges);
-    const CamConst cc = make_cam_const(*cam);
-
+    auto* header = reinterpret_cast<StatusHeader*>(w);
+    const size_t un = align_up(4 * (size_t)n);
+    auto* keys = reinterpret_cast<uint32_t*>(w + sizeof(StatusHeader));
+    auto* keys_alt = reinterpret_cast<uint32_t*>(w + sizeof(StatusHeader) + un);
+    auto* order_alt = reinterpret_cast<uint32_t*>(w + sizeof(StatusHeader) + 2 * un);
+    void* scratch = w + sizeof(StatusHeader) + 3 * un;
     cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
-    if (e == cudaSuccess) e = launch_preprocess(*g, cc, p, s);
+    if (e == cudaSuccess) e = sort_prepare_histogram(scratch, s);
+    if (e == cudaSuccess) e = launch_depth_keys(*p, n, keys, order, sort_histogram_of(scratch), s);
     if (e == cudaSuccess)
-        e = launch_bin(p, g->n, cc, offsets, keys, vals, key_capacity, num_keys, header, w + L.bin, s);
-    if (e == cudaSuccess)
-        e = launch_sort(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, key_bits_for(*cam), header,
-                        w + L.sort, g_spin_limit, s);
-    if (e == cudaSuccess)
-        e = launch_tile_ranges(keys, num_keys, key_capacity, cc.tiles_x * cc.tiles_y, ranges, s);
-    if (e == cudaSuccess) e = launch_rasterize(p, g->n, vals, ranges, cc, image, final_T, n_contrib, s);
+        e = launch_sort32(keys, order, keys_alt, order_alt, nullptr, n, 32, header, scratch, g_spin_limit, s, true);
     return cuda_status(e);
+}
+
+gs_status gs_bin_ordered(const gs_projected* p, int64_t n, const uint32_t* order, const gs_camera* cam,
+                         uint32_t* offsets, uint32_t* tile_keys, uint32_t* vals, int64_t key_capacity,
+                         uint64_t* num_keys, void* ws, size_t ws_bytes, void* stream) {
+    if (n < 0 || n > kMaxGaussians || !camera_ok(cam) || !projected_ok(p, n) || !num_keys) return GS_ERR_INVALID_ARG;
+    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
+    if (n > 0 && (!order || !aligned(order, 4))) return GS_ERR_INVALID_ARG;
+    if (key_capacity > 0 && (!tile_keys || !vals || !aligned(tile_keys, 4) || !aligned(vals, 4)))
+        return GS_ERR_INVALID_ARG;
+    if (!aligned(num_keys, 8)) return GS_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < gs_bin_workspace_bytes(n)) return GS_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    auto* header = static_cast<StatusHeader*>(ws);
+    cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
+    if (e != cudaSuccess) return GS_ERR_CUDA;
+    return cuda_status(launch_bin_ordered(*p, order, n, make_cam_const(*cam), offsets, tile_keys, vals, key_capacity,
+                                          num_keys, header, static_cast<char*>(ws) + sizeof(StatusHeader), s));
+}
+
+gs_status gs_sort32(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt, const uint64_t* num_keys,
+                    int64_t key_capacity, int32_t key_bits, void* ws, size_t ws_bytes, void* stream) {
+    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity || key_bits < 1 || key_bits > 32)
+        return GS_ERR_INVALID_ARG;
+    if (key_capacity > 0 && (!keys || !vals || !keys_alt || !vals_alt || !aligned(keys, 4) || !aligned(keys_alt, 4) ||
+                             !aligned(vals, 4) || !aligned(vals_alt, 4)))
+        return GS_ERR_INVALID_ARG;
+    if (num_keys && !aligned(num_keys, 8)) return GS_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < gs_sort_workspace_bytes(key_capacity)) return GS_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    auto* header = static_cast<StatusHeader*>(ws);
+    cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
+    if (e != cudaSuccess) return GS_ERR_CUDA;
+    return cuda_status(launch_sort32(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, key_bits, header,
+                                     static_cast<char*>(ws) + sizeof(StatusHeader), g_spin_limit, s));
+}
+
+gs_status gs_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* num_keys, int64_t key_capacity,
+                           const gs_camera* cam, uint32_t* ranges, void* stream) {
+    if (!camera_ok(cam) || !ranges || !num_keys || key_capacity < 0 || key_capacity > kMaxKeyCapacity)
+        return GS_ERR_INVALID_ARG;
+    if (key_capacity > 0 && !sorted_tiles) return GS_ERR_INVALID_ARG;
+    if (!aligned(ranges, 8)) return GS_ERR_INVALID_ARG;
+    return cuda_status(launch_tile_ranges32(sorted_tiles, num_keys, key_capacity, tiles_x(*cam) * tiles_y(*cam),
+                                            ranges, (cudaStream_t)stream));
 }
 
 gs_status gs_render_from_host(const gs_gaussians* hg, const gs_gaussians* dg, const gs_camera* cam,

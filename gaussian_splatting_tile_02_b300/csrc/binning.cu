@@ -6,6 +6,10 @@
 // first key and the frame's key count K; the Gaussian's keys are then written
 // in row-major order over its tile rectangle:
 //     key = (uint64)(ty * tiles_x + tx) << 32 | float_bits(depth),  value = index.
+// The same kernels also run over the Gaussians in a given order (the depth
+// order) and then write 32-bit keys holding the tile id alone: a stable sort
+// of those by tile gives the same per-tile (depth, index) order as the sort of
+// the 64-bit keys, with a 13-bit key at 1080p instead of a 45-bit one.
 //
 // Three kernels: a per-chunk reduction (2048 Gaussians per block), a
 // single-block scan of the chunk sums (which also publishes K), and the
@@ -50,7 +54,30 @@ __device__ __forceinline__ unsigned long long block_scan_incl(unsigned long long
     return v;
 }
 
-__global__ void __launch_bounds__(kBinThreads) bin_reduce_kernel(const uint32_t* __restrict__ tiles_touched, int64_t n,
+// 8-bit digit histograms of 32-bit keys, laid out as the radix sort expects
+// them ([pass][256]); accumulated in shared memory, flushed with one global
+// atomic per non-zero bin.
+constexpr int kHistPasses = 4;
+__device__ __forceinline__ void count_digits(uint32_t* s_hist, uint32_t key, int key_bits) {
+#pragma unroll
+    for (int p = 0; p < kHistPasses; p++) {
+        const int w = key_bits - 8 * p;
+        if (w > 0) atomicAdd(&s_hist[p * 256 + ((key >> (8 * p)) & ((1u << (w < 8 ? w : 8)) - 1u))], 1u);
+    }
+}
+__device__ __forceinline__ void flush_digits(const uint32_t* s_hist, uint32_t* hist, int key_bits) {
+    const int n = ((key_bits + 7) / 8) * 256;
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+        if (s_hist[i]) atomicAdd(&hist[i], s_hist[i]);
+}
+
+// Gaussian at list position i: the identity, or order[i]
+__device__ __forceinline__ uint32_t at(const uint32_t* __restrict__ order, int64_t i) {
+    return order ? __ldg(order + i) : (uint32_t)i;
+}
+
+__global__ void __launch_bounds__(kBinThreads) bin_reduce_kernel(const uint32_t* __restrict__ tiles_touched,
+                                                                 const uint32_t* __restrict__ order, int64_t n,
                                                                  unsigned long long* __restrict__ block_sums) {
     __shared__ unsigned long long warp_tot[kBinThreads / 32];
     __shared__ unsigned long long total;
@@ -58,7 +85,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_reduce_kernel(const uint32_t*
     unsigned long long s = 0;
 #pragma unroll
     for (int i = 0; i < kBinItems; i++)
-        if (base + i < n) s += __ldg(tiles_touched + base + i);
+        if (base + i < n) s += __ldg(tiles_touched + at(order, base + i));
     block_scan_incl(s, warp_tot, &total);
     if (threadIdx.x == 0) block_sums[blockIdx.x] = total;
 }
@@ -106,23 +133,35 @@ __global__ void __launch_bounds__(1024) bin_scan_sums_kernel(unsigned long long*
     }
 }
 
+// KeyT = uint64_t: key = tile << 32 | depth bits; KeyT = uint32_t: key = tile.
+// hist (32-bit keys only, nullable): digit histograms of the written keys for
+// the radix sort that follows (key_bits significant bits).
+template <typename KeyT>
 __global__ void __launch_bounds__(kBinThreads) bin_duplicate_kernel(
     const uint32_t* __restrict__ tiles_touched, const ushort4* __restrict__ rect, const float* __restrict__ depth,
-    int64_t n, int tiles_x, const unsigned long long* __restrict__ block_prefix, int64_t key_capacity,
-    uint32_t* __restrict__ offsets, uint64_t* __restrict__ keys, uint32_t* __restrict__ vals) {
-    __shared__ unsigned long long s_incl[kBinChunk];
+    const uint32_t* __restrict__ order, int64_t n, int tiles_x, const unsigned long long* __restrict__ block_prefix,
+    int64_t key_capacity, uint32_t* __restrict__ offsets, KeyT* __restrict__ keys, uint32_t* __restrict__ vals,
+    uint32_t* __restrict__ hist, int key_bits) {
+    __shared__ uint32_t s_dhist[kHistPasses * 256];
+    // inclusive offsets inside the chunk, saturated at 2^32 - 1: only slots below
+    // the key capacity (< 2^30) are ever searched for
+    __shared__ uint32_t s_incl[kBinChunk];
     __shared__ ushort4 s_rect[kBinChunk];
     __shared__ uint32_t s_depth[kBinChunk];
+    __shared__ uint32_t s_g[kBinChunk];
     __shared__ unsigned long long warp_tot[kBinThreads / 32];
     __shared__ unsigned long long total;
 
     const int64_t chunk0 = (int64_t)blockIdx.x * kBinChunk;
     const int64_t base = chunk0 + (int64_t)threadIdx.x * kBinItems;
-    uint32_t t[kBinItems];
+    if (hist)
+        for (int i = threadIdx.x; i < kHistPasses * 256; i += kBinThreads) s_dhist[i] = 0;
+    uint32_t t[kBinItems], gi[kBinItems];
     unsigned long long s = 0;
 #pragma unroll
     for (int i = 0; i < kBinItems; i++) {
-        t[i] = base + i < n ? __ldg(tiles_touched + base + i) : 0u;
+        gi[i] = base + i < n ? at(order, base + i) : 0u;
+        t[i] = base + i < n ? __ldg(tiles_touched + gi[i]) : 0u;
         s += t[i];
     }
     const unsigned long long incl = block_scan_incl(s, warp_tot, &total);
@@ -132,18 +171,19 @@ __global__ void __launch_bounds__(kBinThreads) bin_duplicate_kernel(
     for (int i = 0; i < kBinItems; i++) {
         run += t[i];
         const int li = threadIdx.x * kBinItems + i;
-        s_incl[li] = run;
+        s_incl[li] = run < 0xffffffffull ? (uint32_t)run : 0xffffffffu;
         if (base + i < n) {
-            offsets[base + i] = (uint32_t)(prefix + run);
+            if (offsets) offsets[base + i] = (uint32_t)(prefix + run);
             if (t[i]) {
-                s_rect[li] = __ldg(rect + base + i);
-                s_depth[li] = __float_as_uint(__ldg(depth + base + i));
+                s_rect[li] = __ldg(rect + gi[i]);
+                s_g[li] = gi[i];
+                if (sizeof(KeyT) == 8) s_depth[li] = __float_as_uint(__ldg(depth + gi[i]));
             }
         }
     }
     __syncthreads();
-    if ((long long)prefix >= key_capacity) return;
-    const unsigned long long room = (unsigned long long)key_capacity - prefix;
+    const unsigned long long room =
+        (long long)prefix < key_capacity ? (unsigned long long)key_capacity - prefix : 0ull;
     const unsigned long long limit = total < room ? total : room;
     for (unsigned long long j = threadIdx.x; j < limit; j += kBinThreads) {
         // first chunk slot whose inclusive offset exceeds j
@@ -152,14 +192,47 @@ __global__ void __launch_bounds__(kBinThreads) bin_duplicate_kernel(
             const int mid = (lo + hi) >> 1;
             if (s_incl[mid] > j) hi = mid; else lo = mid + 1;
         }
-        const unsigned long long first = lo > 0 ? s_incl[lo - 1] : 0ull;
+        const unsigned long long first = lo > 0 ? (unsigned long long)s_incl[lo - 1] : 0ull;
         const uint32_t rank = (uint32_t)(j - first);
         const ushort4 r = s_rect[lo];
         const uint32_t w = (uint32_t)r.z - r.x + 1u;
         const uint32_t ty = r.y + rank / w, tx = r.x + rank % w;
         const uint64_t tile = (uint64_t)ty * (uint64_t)tiles_x + tx;
-        keys[prefix + j] = (tile << 32) | s_depth[lo];
-        vals[prefix + j] = (uint32_t)(chunk0 + lo);
+        if (sizeof(KeyT) == 8) {
+            keys[prefix + j] = (KeyT)((tile << 32) | s_depth[lo]);
+        } else {
+            keys[prefix + j] = (KeyT)tile;
+            if (hist) count_digits(s_dhist, (uint32_t)tile, key_bits);
+        }
+        vals[prefix + j] = s_g[lo];
+    }
+    if (hist) {
+        __syncthreads();
+        flush_digits(s_dhist, hist, key_bits);
+    }
+}
+
+// Depth-order sort input: key = depth bits for Gaussians with tiles (depth >
+// near > 0, so the bits order like the depths), 0xffffffff for the others
+// (sorted last); value = index.
+__global__ void __launch_bounds__(256) depth_keys_kernel(const float* __restrict__ depth,
+                                                         const uint32_t* __restrict__ tiles_touched, int64_t n,
+                                                         uint32_t* __restrict__ keys, uint32_t* __restrict__ vals,
+                                                         uint32_t* __restrict__ hist) {
+    __shared__ uint32_t s_dhist[kHistPasses * 256];
+    if (hist)
+        for (int i = threadIdx.x; i < kHistPasses * 256; i += blockDim.x) s_dhist[i] = 0;
+    __syncthreads();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const uint32_t k = __ldg(tiles_touched + i) ? __float_as_uint(__ldg(depth + i)) : 0xffffffffu;
+        keys[i] = k;
+        vals[i] = (uint32_t)i;
+        if (hist) count_digits(s_dhist, k, 32);
+    }
+    if (hist) {
+        __syncthreads();
+        flush_digits(s_dhist, hist, 32);
     }
 }
 
@@ -170,9 +243,11 @@ size_t bin_scratch_bytes(int64_t n) {
     return align_up((size_t)(nb > 0 ? nb : 1) * sizeof(unsigned long long));
 }
 
-cudaError_t launch_bin(const gs_projected& p, int64_t n, const CamConst& cam, uint32_t* offsets,
-                       uint64_t* keys, uint32_t* vals, int64_t key_capacity, uint64_t* num_keys,
-                       StatusHeader* status, void* scratch, cudaStream_t s) {
+template <typename KeyT>
+cudaError_t launch_bin_t(const gs_projected& p, const uint32_t* order, int64_t n, const CamConst& cam,
+                         uint32_t* offsets, KeyT* keys, uint32_t* vals, int64_t key_capacity, uint64_t* num_keys,
+                         StatusHeader* status, void* scratch, cudaStream_t s, uint32_t* hist = nullptr,
+                         int key_bits = 0) {
     if (n == 0) {
         cudaError_t e = cudaMemsetAsync(num_keys, 0, sizeof(uint64_t), s);
         if (e != cudaSuccess) return e;
@@ -180,11 +255,35 @@ cudaError_t launch_bin(const gs_projected& p, int64_t n, const CamConst& cam, ui
     }
     const int nb = (int)((n + kBinChunk - 1) / kBinChunk);
     auto* sums = static_cast<unsigned long long*>(scratch);
-    bin_reduce_kernel<<<nb, kBinThreads, 0, s>>>(p.tiles_touched, n, sums);
+    bin_reduce_kernel<<<nb, kBinThreads, 0, s>>>(p.tiles_touched, order, n, sums);
     bin_scan_sums_kernel<<<1, 1024, 0, s>>>(sums, nb, key_capacity, num_keys, status);
-    bin_duplicate_kernel<<<nb, kBinThreads, 0, s>>>(p.tiles_touched, reinterpret_cast<const ushort4*>(p.rect),
-                                                    p.depth, n, cam.tiles_x, sums, key_capacity, offsets, keys,
-                                                    vals);
+    bin_duplicate_kernel<KeyT><<<nb, kBinThreads, 0, s>>>(p.tiles_touched, reinterpret_cast<const ushort4*>(p.rect),
+                                                          p.depth, order, n, cam.tiles_x, sums, key_capacity,
+                                                          offsets, keys, vals, hist, key_bits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bin(const gs_projected& p, int64_t n, const CamConst& cam, uint32_t* offsets, uint64_t* keys,
+                       uint32_t* vals, int64_t key_capacity, uint64_t* num_keys, StatusHeader* status,
+                       void* scratch, cudaStream_t s) {
+    return launch_bin_t<uint64_t>(p, nullptr, n, cam, offsets, keys, vals, key_capacity, num_keys, status, scratch,
+                                  s);
+}
+
+cudaError_t launch_bin_ordered(const gs_projected& p, const uint32_t* order, int64_t n, const CamConst& cam,
+                               uint32_t* offsets, uint32_t* tile_keys, uint32_t* vals, int64_t key_capacity,
+                               uint64_t* num_keys, StatusHeader* status, void* scratch, cudaStream_t s,
+                               uint32_t* hist, int key_bits) {
+    return launch_bin_t<uint32_t>(p, order, n, cam, offsets, tile_keys, vals, key_capacity, num_keys, status,
+                                  scratch, s, hist, key_bits);
+}
+
+cudaError_t launch_depth_keys(const gs_projected& p, int64_t n, uint32_t* keys, uint32_t* vals, uint32_t* hist,
+                              cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    int64_t b = (n + 1023) / 1024;
+    depth_keys_kernel<<<(unsigned)(b < 148 * 4 ? b : 148 * 4), 256, 0, s>>>(p.depth, p.tiles_touched, n, keys,
+                                                                            vals, hist);
     return cudaGetLastError();
 }
 

@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/gs.h"
+#include "gs.h"
 
 namespace gs {
 
@@ -72,13 +72,33 @@ cudaError_t launch_bin(const gs_projected& p, int64_t n, const CamConst& cam, ui
                        uint64_t* keys, uint32_t* vals, int64_t key_capacity, uint64_t* num_keys,
                        StatusHeader* status, void* scratch, cudaStream_t s);
 
+// hist (nullable): digit histograms of the written keys for the radix sort
+// that follows, key_bits significant bits (32-bit keys)
+cudaError_t launch_bin_ordered(const gs_projected& p, const uint32_t* order, int64_t n, const CamConst& cam,
+                               uint32_t* offsets, uint32_t* tile_keys, uint32_t* vals, int64_t key_capacity,
+                               uint64_t* num_keys, StatusHeader* status, void* scratch, cudaStream_t s,
+                               uint32_t* hist = nullptr, int key_bits = 0);
+cudaError_t launch_depth_keys(const gs_projected& p, int64_t n, uint32_t* keys, uint32_t* vals, uint32_t* hist,
+                              cudaStream_t s);
+
 // sort.cu
 size_t sort_scratch_bytes(int64_t key_capacity);
 cudaError_t launch_sort(uint64_t* keys, uint32_t* vals, uint64_t* keys_alt, uint32_t* vals_alt,
                         const uint64_t* num_keys, int64_t key_capacity, int key_bits,
                         StatusHeader* status, void* scratch, long long spin_limit, cudaStream_t s);
+// hist_ready: the producer of the keys already filled the digit histograms
+// (sort_histogram_of(scratch), zeroed by sort_prepare_histogram) with
+// sort_count_digits for every key
+cudaError_t launch_sort32(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
+                          const uint64_t* num_keys, int64_t key_capacity, int key_bits,
+                          StatusHeader* status, void* scratch, long long spin_limit, cudaStream_t s,
+                          bool hist_ready = false);
+uint32_t* sort_histogram_of(void* scratch);
+cudaError_t sort_prepare_histogram(void* scratch, cudaStream_t s);
 cudaError_t launch_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_keys,
                                int64_t key_capacity, int n_tiles, uint32_t* ranges, cudaStream_t s);
+cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* num_keys,
+                                 int64_t key_capacity, int n_tiles, uint32_t* ranges, cudaStream_t s);
 cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations, cudaStream_t s);
 
 // rasterize.cu

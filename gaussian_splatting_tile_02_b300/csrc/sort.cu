@@ -1,43 +1,61 @@
 // Step 3 (flowchart box "Depth-sort per tile" on the lesson page "3D Gaussian
 // Splatting à partir de zéro") and step 4 (per-tile ranges).
 //
-// Stable least-significant-digit radix sort of (uint64 key, uint32 value)
-// pairs with 8-bit digits. Sorting the binning keys (tile id in the high
-// word, depth bits in the low word) orders each tile's entries by depth, with
-// equal keys kept in Gaussian-index order.
+// Stable least-significant-digit radix sort of (key, uint32 value) pairs with
+// 8-bit digits, for 64-bit keys (the binning keys: tile id in the high word,
+// depth bits in the low word) and 32-bit keys (depth bits; tile ids). Equal
+// keys keep their input order.
 //
 //   sort_histogram : one read of all keys; 256-bin histograms of every digit
 //                    position at once (shared-memory counters, then global
-//                    atomics). Also clears the look-back status rows.
+//                    atomics). Also clears the look-back rows the passes use.
 //   sort_bases     : exclusive scan of each histogram -> digit base offsets.
-//   onesweep pass  : one kernel per digit. Each block takes the next 4096-key
-//                    tile (tile ids from an atomic counter, so a block only
-//                    ever waits on blocks that are already running), ranks its
-//                    keys stably with warp match/popc counters, publishes its
-//                    per-digit counts, and finds its global offsets by
+//   onesweep pass  : one kernel per digit. Each block takes the next tile of
+//                    keys (tile ids from an atomic counter, so a block only
+//                    ever waits on blocks that are already running), ranks
+//                    its keys stably with warp match/popc counters, publishes
+//                    its per-digit counts, and finds its global offsets by
 //                    decoupled look-back over earlier tiles. Keys are then
 //                    reordered in shared memory and written out in
 //                    digit-contiguous runs (coalesced), values likewise.
 //   copy back      : only when the pass count is odd.
 //
-// Every wait in the look-back is bounded (polling iterations, with backoff);
-// a wait that runs out sets GS_FLAG_TIMEOUT in the workspace header and the
-// block still publishes a status so that no other block waits on it. All
-// stores are bounds-checked against the key count.
+// A look-back status word is (flag << 30 | count), written and read as one
+// relaxed 32-bit access: the count travels with its flag, so no fence is
+// needed. Every wait is bounded (polling iterations, with backoff); a wait
+// that runs out sets GS_FLAG_TIMEOUT in the workspace header and the block
+// still publishes a status so that no other block waits on it. All stores are
+// bounds-checked against the key count.
 #include "gs_internal.cuh"
+
+#ifndef GS_SORT_THREADS
+#define GS_SORT_THREADS 512
+#endif
+#ifndef GS_SORT_ITEMS
+#define GS_SORT_ITEMS 8
+#endif
+#ifndef GS_SORT_MIN_BLOCKS
+#define GS_SORT_MIN_BLOCKS 2
+#endif
+#ifndef GS_SORT_LOOKBACK
+#define GS_SORT_LOOKBACK 8
+#endif
 
 namespace gs {
 namespace {
 
-constexpr int kSortThreads = 256;
+constexpr int kSortThreads = GS_SORT_THREADS;
+constexpr int kSortItems = GS_SORT_ITEMS;
 constexpr int kSortWarps = kSortThreads / 32;
-constexpr int kSortItems = 16;
-constexpr int kSortTile = kSortThreads * kSortItems;  // 4096 keys per tile
+constexpr int kSortTile = kSortThreads * kSortItems;
 constexpr int kRadix = 256;
 constexpr int kMaxPasses = 8;
+constexpr int kLookback = GS_SORT_LOOKBACK;
 constexpr uint32_t kFlagAgg = 1u << 30;
 constexpr uint32_t kFlagIncl = 2u << 30;
 constexpr uint32_t kValueMask = (1u << 30) - 1u;
+static_assert(kSortThreads >= kRadix, "one thread per digit");
+static_assert(kSortTile <= 65535, "tile offsets are 16-bit");
 
 struct SortScratch {
     uint32_t* hist;      // [kMaxPasses][256], becomes the digit bases
@@ -60,7 +78,9 @@ SortScratch carve(void* scratch, int64_t cap) {
     return s;
 }
 
+// number of keys: min(*num_keys, cap), or cap when the count is known on the host
 __device__ __forceinline__ int64_t key_count(const uint64_t* num_keys, int64_t cap) {
+    if (!num_keys) return cap;
     const unsigned long long k = *num_keys;
     return k < (unsigned long long)cap ? (int64_t)k : cap;
 }
@@ -71,12 +91,21 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Polls *p until a status flag is present. Returns false if the bound ran out
 // or another block already reported a timeout.
 __device__ bool bounded_wait(const uint32_t* p, uint32_t& v, long long limit, const StatusHeader* h) {
     long long it = 0;
     while (true) {
-        v = ld_acquire_u32(p);
+        v = ld_relaxed_u32(p);
         if (v & (kFlagAgg | kFlagIncl)) return true;
         if (++it > limit) return false;
         if ((it & 31) == 0 && (ld_volatile_u32(&h->flags) & GS_FLAG_TIMEOUT)) return false;
@@ -84,38 +113,49 @@ __device__ bool bounded_wait(const uint32_t* p, uint32_t& v, long long limit, co
     }
 }
 
-__global__ void __launch_bounds__(kSortThreads) sort_histogram_kernel(const uint64_t* __restrict__ keys,
-                                                                      const uint64_t* __restrict__ num_keys,
-                                                                      int64_t cap, int passes, int key_bits,
-                                                                      uint32_t* __restrict__ hist,
-                                                                      uint32_t* __restrict__ lookback,
-                                                                      int64_t max_tiles) {
+template <typename KeyT>
+__device__ __forceinline__ uint32_t digit_of(KeyT k, int shift, uint32_t mask) {
+    return (uint32_t)(k >> shift) & mask;
+}
+
+template <typename KeyT>
+__global__ void __launch_bounds__(256) sort_histogram_kernel(const KeyT* __restrict__ keys,
+                                                             const uint64_t* __restrict__ num_keys, int64_t cap,
+                                                             int passes, int key_bits, uint32_t* __restrict__ hist) {
     __shared__ uint32_t s_hist[kMaxPasses * kRadix];
-    for (int i = threadIdx.x; i < passes * kRadix; i += kSortThreads) s_hist[i] = 0;
+    for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x) s_hist[i] = 0;
     __syncthreads();
     const int64_t K = key_count(num_keys, cap);
-    const int64_t stride = (int64_t)gridDim.x * kSortThreads;
-    for (int64_t i = (int64_t)blockIdx.x * kSortThreads + threadIdx.x; i < K; i += stride) {
-        const uint64_t k = keys[i];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < K; i += stride) {
+        const KeyT k = keys[i];
         for (int p = 0; p < passes; p++) {
             const int w = key_bits - 8 * p < 8 ? key_bits - 8 * p : 8;
-            const uint32_t d = (uint32_t)(k >> (8 * p)) & ((1u << w) - 1u);
-            atomicAdd(&s_hist[p * kRadix + d], 1u);
+            atomicAdd(&s_hist[p * kRadix + digit_of(k, 8 * p, (1u << w) - 1u)], 1u);
         }
     }
-    // clear the look-back rows this sort will use (both ping-pong arrays)
-    const int64_t tiles = (K + kSortTile - 1) / kSortTile;
-    for (int64_t i = (int64_t)blockIdx.x * kSortThreads + threadIdx.x; i < tiles * kRadix; i += stride) {
-        lookback[i] = 0;
-        lookback[max_tiles * kRadix + i] = 0;
-    }
     __syncthreads();
-    for (int i = threadIdx.x; i < passes * kRadix; i += kSortThreads)
+    for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x)
         if (s_hist[i]) atomicAdd(&hist[i], s_hist[i]);
 }
 
-__global__ void __launch_bounds__(kRadix) sort_bases_kernel(uint32_t* __restrict__ hist) {
+// Blocks [0, passes): exclusive scan of one digit histogram -> digit bases.
+// The other blocks clear the look-back rows the passes will use (both
+// ping-pong arrays), for the tiles of this sort only.
+__global__ void __launch_bounds__(kRadix) sort_bases_kernel(uint32_t* __restrict__ hist, int passes,
+                                                            const uint64_t* __restrict__ num_keys, int64_t cap,
+                                                            uint32_t* __restrict__ lookback, int64_t max_tiles) {
     __shared__ uint32_t warp_tot[kRadix / 32];
+    if ((int)blockIdx.x >= passes) {
+        const int64_t K = key_count(num_keys, cap);
+        const int64_t words = (K + kSortTile - 1) / kSortTile * kRadix;
+        const int64_t stride = (int64_t)(gridDim.x - passes) * kRadix;
+        for (int64_t i = (int64_t)(blockIdx.x - passes) * kRadix + threadIdx.x; i < words; i += stride) {
+            lookback[i] = 0;
+            lookback[max_tiles * kRadix + i] = 0;
+        }
+        return;
+    }
     uint32_t* h = hist + blockIdx.x * kRadix;
     const uint32_t x = h[threadIdx.x];
     uint32_t v = x;
@@ -132,10 +172,11 @@ __global__ void __launch_bounds__(kRadix) sort_bases_kernel(uint32_t* __restrict
     h[threadIdx.x] = v + add - x;
 }
 
+template <typename KeyT>
 struct PassArgs {
-    const uint64_t* keys_in;
+    const KeyT* keys_in;
     const uint32_t* vals_in;
-    uint64_t* keys_out;
+    KeyT* keys_out;
     uint32_t* vals_out;
     const uint64_t* num_keys;
     int64_t cap;
@@ -149,12 +190,13 @@ struct PassArgs {
     long long spin_limit;
 };
 
-__global__ void __launch_bounds__(kSortThreads) onesweep_kernel(const PassArgs a) {
-    __shared__ uint32_t s_hist[kSortWarps * kRadix];  // per-warp digit counters -> offsets
+template <typename KeyT>
+__global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_kernel(const PassArgs<KeyT> a) {
+    __shared__ uint16_t s_hist[kSortWarps * kRadix];  // per-warp digit counters -> offsets
     __shared__ uint32_t s_dstart[kRadix];
     __shared__ uint32_t s_goff[kRadix];
-    __shared__ uint32_t s_warp_tot[kSortWarps];
-    __shared__ __align__(16) uint64_t s_keys[kSortTile];
+    __shared__ uint32_t s_warp_tot[kRadix / 32];
+    __shared__ __align__(16) KeyT s_keys[kSortTile];
     __shared__ uint32_t s_tile;
     __shared__ int s_timed_out;
 
@@ -170,7 +212,7 @@ __global__ void __launch_bounds__(kSortThreads) onesweep_kernel(const PassArgs a
     const int64_t start = (int64_t)tile * kSortTile;
     if (start >= K) return;
     const int n_valid = (int)(K - start < kSortTile ? K - start : kSortTile);
-    if (a.status_clear) {
+    if (a.status_clear && tid < kRadix) {
         // rows used by the previous pass are not read again until two passes on
         a.status_clear[(int64_t)tile * kRadix + tid] = 0;
     }
@@ -178,68 +220,86 @@ __global__ void __launch_bounds__(kSortThreads) onesweep_kernel(const PassArgs a
     const int shift = 8 * a.pass;
     const uint32_t dmask = (1u << a.digit_bits) - 1u;
     const int warp_base = warp * (kSortItems * 32);
-    uint64_t key[kSortItems];
+    KeyT key[kSortItems];
+    uint32_t val[kSortItems];
 #pragma unroll
     for (int i = 0; i < kSortItems; i++) {
         const int li = warp_base + i * 32 + lane;
-        key[i] = li < n_valid ? a.keys_in[start + li] : 0ull;
+        key[i] = li < n_valid ? a.keys_in[start + li] : (KeyT)0;
+    }
+#pragma unroll
+    for (int i = 0; i < kSortItems; i++) {
+        const int li = warp_base + i * 32 + lane;
+        val[i] = li < n_valid ? a.vals_in[start + li] : 0u;
     }
 
     // stable rank within the warp: position order is (i, lane)
-    uint32_t* wh = s_hist + warp * kRadix;
+    uint16_t* wh = s_hist + warp * kRadix;
     const uint32_t lt = lanemask_lt();
-    uint16_t rank[kSortItems];
+    uint32_t rank[kSortItems];
 #pragma unroll
     for (int i = 0; i < kSortItems; i++) {
         const int li = warp_base + i * 32 + lane;
         const bool v = li < n_valid;
-        const uint32_t d = v ? ((uint32_t)(key[i] >> shift) & dmask) : 0xffffu;
-        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        const uint32_t d = digit_of(key[i], shift, dmask);
+        const uint32_t peers = __match_any_sync(0xffffffffu, v ? d : 0xffffu) & __ballot_sync(0xffffffffu, v);
         uint32_t r = 0;
         if (v) r = wh[d] + __popc(peers & lt);
         __syncwarp();
-        if (v && (peers & lt) == 0) wh[d] += __popc(peers);
+        if (v && (peers & lt) == 0) wh[d] = (uint16_t)(wh[d] + __popc(peers));
         __syncwarp();
-        rank[i] = (uint16_t)r;
+        rank[i] = r;
     }
     __syncthreads();
 
-    // per digit (thread = digit): offsets of each warp inside the block
-    {
+    // per digit (thread = digit): offsets of each warp inside the block, the
+    // tile's count published for later tiles, and the look-back over earlier ones
+    uint32_t sum = 0;
+    if (tid < kRadix) {
         const int d = tid;
-        uint32_t sum = 0;
 #pragma unroll
         for (int w = 0; w < kSortWarps; w++) {
             const uint32_t c = s_hist[w * kRadix + d];
-            s_hist[w * kRadix + d] = sum;
+            s_hist[w * kRadix + d] = (uint16_t)sum;
             sum += c;
         }
-        // publish this tile's count, then look back over earlier tiles
         uint32_t* row = a.status + (int64_t)tile * kRadix;
         if (tile == 0) {
-            st_release_u32(row + d, kFlagIncl | sum);
+            st_relaxed_u32(row + d, kFlagIncl | sum);
             s_goff[d] = a.bases[d];
         } else {
-            st_release_u32(row + d, kFlagAgg | sum);
+            st_relaxed_u32(row + d, kFlagAgg | sum);
+            // look back in windows of kLookback earlier tiles: the window's
+            // loads are issued together, then consumed nearest first until an
+            // inclusive prefix is met (a not-yet-published one is waited for)
             uint32_t excl = 0;
-            bool ok = true;
-            for (int64_t j = (int64_t)tile - 1; j >= 0; j--) {
-                uint32_t v;
-                if (!bounded_wait(a.status + j * kRadix + d, v, a.spin_limit, a.header)) {
-                    ok = false;
-                    break;
+            bool ok = true, found = false;
+            for (int64_t j = (int64_t)tile - 1; j >= 0 && ok && !found; j -= kLookback) {
+                uint32_t v[kLookback];
+#pragma unroll
+                for (int k = 0; k < kLookback; k++)
+                    v[k] = j - k >= 0 ? ld_relaxed_u32(a.status + (j - k) * kRadix + d) : 0u;
+#pragma unroll
+                for (int k = 0; k < kLookback; k++) {
+                    if (found || !ok || j - k < 0) break;
+                    uint32_t x = v[k];
+                    if (!(x & (kFlagAgg | kFlagIncl)) &&
+                        !bounded_wait(a.status + (j - k) * kRadix + d, x, a.spin_limit, a.header)) {
+                        ok = false;
+                        break;
+                    }
+                    excl += x & kValueMask;
+                    if (x & kFlagIncl) found = true;
                 }
-                excl += v & kValueMask;
-                if (v & kFlagIncl) break;
             }
             if (!ok) {
                 raise_flag(a.header, GS_FLAG_TIMEOUT, 1u);
                 s_timed_out = 1;
             }
-            st_release_u32(row + d, kFlagIncl | ((excl + sum) & kValueMask));
+            st_relaxed_u32(row + d, kFlagIncl | ((excl + sum) & kValueMask));
             s_goff[d] = a.bases[d] + excl;
         }
-        // block-wide exclusive scan of the counts -> digit run starts in the tile
+        // warp-level inclusive scan of the counts (block scan finished below)
         uint32_t v = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -247,22 +307,26 @@ __global__ void __launch_bounds__(kSortThreads) onesweep_kernel(const PassArgs a
             if (lane >= o) v += t;
         }
         if (lane == 31) s_warp_tot[warp] = v;
-        __syncthreads();
+        sum = v - sum;  // exclusive within the warp
+    }
+    __syncthreads();
+    if (tid < kRadix) {
         uint32_t add = 0;
         for (int w = 0; w < warp; w++) add += s_warp_tot[w];
-        s_dstart[d] = v + add - sum;
+        s_dstart[tid] = sum + add;
     }
     __syncthreads();
     const bool skip = s_timed_out != 0;
 
     // reorder keys in shared memory by (digit, rank)
-    uint16_t loc[kSortItems];
+    uint32_t loc[kSortItems];
 #pragma unroll
     for (int i = 0; i < kSortItems; i++) {
         const int li = warp_base + i * 32 + lane;
+        loc[i] = 0xffffffffu;
         if (li < n_valid) {
-            const uint32_t d = (uint32_t)(key[i] >> shift) & dmask;
-            loc[i] = (uint16_t)(s_dstart[d] + s_hist[warp * kRadix + d] + rank[i]);
+            const uint32_t d = digit_of(key[i], shift, dmask);
+            loc[i] = s_dstart[d] + s_hist[warp * kRadix + d] + rank[i];
             s_keys[loc[i]] = key[i];
         }
     }
@@ -273,8 +337,8 @@ __global__ void __launch_bounds__(kSortThreads) onesweep_kernel(const PassArgs a
         const int j = k * kSortThreads + tid;
         dest[k] = 0xffffffffu;
         if (j < n_valid) {
-            const uint64_t kk = s_keys[j];
-            const uint32_t d = (uint32_t)(kk >> shift) & dmask;
+            const KeyT kk = s_keys[j];
+            const uint32_t d = digit_of(kk, shift, dmask);
             const uint32_t o = s_goff[d] + (uint32_t)j - s_dstart[d];
             if (!skip && (int64_t)o < K) {
                 a.keys_out[o] = kk;
@@ -285,10 +349,8 @@ __global__ void __launch_bounds__(kSortThreads) onesweep_kernel(const PassArgs a
     __syncthreads();
     uint32_t* s_vals = reinterpret_cast<uint32_t*>(s_keys);
 #pragma unroll
-    for (int i = 0; i < kSortItems; i++) {
-        const int li = warp_base + i * 32 + lane;
-        if (li < n_valid) s_vals[loc[i]] = a.vals_in[start + li];
-    }
+    for (int i = 0; i < kSortItems; i++)
+        if (loc[i] != 0xffffffffu) s_vals[loc[i]] = val[i];
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < kSortItems; k++) {
@@ -297,8 +359,9 @@ __global__ void __launch_bounds__(kSortThreads) onesweep_kernel(const PassArgs a
     }
 }
 
-__global__ void copy_back_kernel(const uint64_t* __restrict__ ks, const uint32_t* __restrict__ vs,
-                                 uint64_t* __restrict__ kd, uint32_t* __restrict__ vd,
+template <typename KeyT>
+__global__ void copy_back_kernel(const KeyT* __restrict__ ks, const uint32_t* __restrict__ vs,
+                                 KeyT* __restrict__ kd, uint32_t* __restrict__ vd,
                                  const uint64_t* __restrict__ num_keys, int64_t cap) {
     const int64_t K = key_count(num_keys, cap);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -308,15 +371,17 @@ __global__ void copy_back_kernel(const uint64_t* __restrict__ ks, const uint32_t
     }
 }
 
-__global__ void tile_ranges_kernel(const uint64_t* __restrict__ keys, const uint64_t* __restrict__ num_keys,
-                                   int64_t cap, int n_tiles, uint2* __restrict__ ranges) {
+// ranges from sorted keys whose tile id is (key >> shift)
+template <typename KeyT>
+__global__ void tile_ranges_kernel(const KeyT* __restrict__ keys, const uint64_t* __restrict__ num_keys,
+                                   int64_t cap, int shift, int n_tiles, uint2* __restrict__ ranges) {
     const int64_t K = key_count(num_keys, cap);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < K; i += stride) {
-        const uint32_t t = (uint32_t)(keys[i] >> 32);
+        const uint32_t t = (uint32_t)(keys[i] >> shift);
         if (t >= (uint32_t)n_tiles) continue;
-        const uint32_t prev = i > 0 ? (uint32_t)(keys[i - 1] >> 32) : 0xffffffffu;
-        const uint32_t next = i + 1 < K ? (uint32_t)(keys[i + 1] >> 32) : 0xffffffffu;
+        const uint32_t prev = i > 0 ? (uint32_t)(keys[i - 1] >> shift) : 0xffffffffu;
+        const uint32_t next = i + 1 < K ? (uint32_t)(keys[i + 1] >> shift) : 0xffffffffu;
         if (t != prev) ranges[t].x = (uint32_t)i;
         if (t != next) ranges[t].y = (uint32_t)(i + 1);
     }
@@ -334,29 +399,31 @@ int grid_for(int64_t work, int threads, int max_blocks) {
     return (int)(b < max_blocks ? b : max_blocks);
 }
 
-}  // namespace
-
-size_t sort_scratch_bytes(int64_t cap) {
-    return align_up(sizeof(uint32_t) * kMaxPasses * kRadix) + align_up(sizeof(uint32_t) * kMaxPasses) +
-           align_up(sizeof(uint32_t) * 2 * (size_t)sort_max_tiles(cap > 0 ? cap : 1) * kRadix);
-}
-
-cudaError_t launch_sort(uint64_t* keys, uint32_t* vals, uint64_t* keys_alt, uint32_t* vals_alt,
-                        const uint64_t* num_keys, int64_t cap, int key_bits, StatusHeader* status,
-                        void* scratch, long long spin_limit, cudaStream_t s) {
+// hist_ready: the digit histograms were already accumulated into the
+// scratch's histogram array (zeroed by sort_prepare_histogram) by the kernel
+// that produced the keys.
+template <typename KeyT>
+cudaError_t launch_sort_t(KeyT* keys, uint32_t* vals, KeyT* keys_alt, uint32_t* vals_alt, const uint64_t* num_keys,
+                          int64_t cap, int key_bits, StatusHeader* status, void* scratch, long long spin_limit,
+                          cudaStream_t s, bool hist_ready) {
     if (cap == 0) return cudaSuccess;
     const SortScratch sc = carve(scratch, cap);
     const int passes = (key_bits + 7) / 8;
-    cudaError_t e = cudaMemsetAsync(sc.hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
+    if (!hist_ready) {
+        e = cudaMemsetAsync(sc.hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, s);
+        if (e != cudaSuccess) return e;
+        sort_histogram_kernel<KeyT><<<grid_for(cap, 256 * 16, 148 * 8), 256, 0, s>>>(keys, num_keys, cap, passes,
+                                                                                     key_bits, sc.hist);
+    }
     e = cudaMemsetAsync(sc.counters, 0, sizeof(uint32_t) * kMaxPasses, s);
     if (e != cudaSuccess) return e;
-    sort_histogram_kernel<<<grid_for(cap, kSortThreads * 16, 148 * 8), kSortThreads, 0, s>>>(
-        keys, num_keys, cap, passes, key_bits, sc.hist, sc.lookback, sc.max_tiles);
-    sort_bases_kernel<<<passes, kRadix, 0, s>>>(sc.hist);
+    const int clear_blocks = grid_for(2 * sc.max_tiles * kRadix, kRadix * 8, 148 * 2);
+    sort_bases_kernel<<<passes + clear_blocks, kRadix, 0, s>>>(sc.hist, passes, num_keys, cap, sc.lookback,
+                                                              sc.max_tiles);
     const unsigned tiles = (unsigned)sc.max_tiles;
     for (int p = 0; p < passes; p++) {
-        PassArgs a;
+        PassArgs<KeyT> a;
         const bool even = (p % 2) == 0;
         a.keys_in = even ? keys : keys_alt;
         a.vals_in = even ? vals : vals_alt;
@@ -372,19 +439,56 @@ cudaError_t launch_sort(uint64_t* keys, uint32_t* vals, uint64_t* keys_alt, uint
         a.status_clear = p >= 1 ? sc.lookback + (int64_t)((p + 1) % 2) * sc.max_tiles * kRadix : nullptr;
         a.header = status;
         a.spin_limit = spin_limit;
-        onesweep_kernel<<<tiles, kSortThreads, 0, s>>>(a);
+        onesweep_kernel<KeyT><<<tiles, kSortThreads, 0, s>>>(a);
     }
     if (passes % 2 == 1)
-        copy_back_kernel<<<grid_for(cap, 256 * 8, 148 * 8), 256, 0, s>>>(keys_alt, vals_alt, keys, vals, num_keys, cap);
+        copy_back_kernel<KeyT><<<grid_for(cap, 256 * 8, 148 * 8), 256, 0, s>>>(keys_alt, vals_alt, keys, vals,
+                                                                               num_keys, cap);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t sort_scratch_bytes(int64_t cap) {
+    return align_up(sizeof(uint32_t) * kMaxPasses * kRadix) + align_up(sizeof(uint32_t) * kMaxPasses) +
+           align_up(sizeof(uint32_t) * 2 * (size_t)sort_max_tiles(cap > 0 ? cap : 1) * kRadix);
+}
+
+cudaError_t launch_sort(uint64_t* keys, uint32_t* vals, uint64_t* keys_alt, uint32_t* vals_alt,
+                        const uint64_t* num_keys, int64_t cap, int key_bits, StatusHeader* status, void* scratch,
+                        long long spin_limit, cudaStream_t s) {
+    return launch_sort_t<uint64_t>(keys, vals, keys_alt, vals_alt, num_keys, cap, key_bits, status, scratch,
+                                   spin_limit, s, false);
+}
+
+cudaError_t launch_sort32(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
+                          const uint64_t* num_keys, int64_t cap, int key_bits, StatusHeader* status, void* scratch,
+                          long long spin_limit, cudaStream_t s, bool hist_ready) {
+    return launch_sort_t<uint32_t>(keys, vals, keys_alt, vals_alt, num_keys, cap, key_bits, status, scratch,
+                                   spin_limit, s, hist_ready);
+}
+
+uint32_t* sort_histogram_of(void* scratch) { return static_cast<uint32_t*>(scratch); }
+
+cudaError_t sort_prepare_histogram(void* scratch, cudaStream_t s) {
+    return cudaMemsetAsync(scratch, 0, sizeof(uint32_t) * kMaxPasses * kRadix, s);
 }
 
 cudaError_t launch_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_keys, int64_t cap, int n_tiles,
                                uint32_t* ranges, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(ranges, 0, sizeof(uint32_t) * 2 * (size_t)n_tiles, s);
     if (e != cudaSuccess || cap == 0) return e;
-    tile_ranges_kernel<<<grid_for(cap, 256 * 8, 148 * 8), 256, 0, s>>>(sorted_keys, num_keys, cap, n_tiles,
-                                                                      reinterpret_cast<uint2*>(ranges));
+    tile_ranges_kernel<uint64_t><<<grid_for(cap, 256 * 8, 148 * 8), 256, 0, s>>>(
+        sorted_keys, num_keys, cap, 32, n_tiles, reinterpret_cast<uint2*>(ranges));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* num_keys, int64_t cap, int n_tiles,
+                                 uint32_t* ranges, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(ranges, 0, sizeof(uint32_t) * 2 * (size_t)n_tiles, s);
+    if (e != cudaSuccess || cap == 0) return e;
+    tile_ranges_kernel<uint32_t><<<grid_for(cap, 256 * 8, 148 * 8), 256, 0, s>>>(
+        sorted_tiles, num_keys, cap, 0, n_tiles, reinterpret_cast<uint2*>(ranges));
     return cudaGetLastError();
 }
 

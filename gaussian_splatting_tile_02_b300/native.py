@@ -53,12 +53,25 @@ _SIGNATURES = {
                                ctypes.c_int32, c_void_p, ctypes.c_size_t, c_void_p]),
     "gs_tile_ranges": (ctypes.c_int, [c_void_p, c_void_p, ctypes.c_int64, ctypes.POINTER(GsCamera),
                                       c_void_p, c_void_p]),
+    "gs_depth_order_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64]),
+    "gs_depth_order": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, c_void_p, c_void_p,
+                                      ctypes.c_size_t, c_void_p]),
+    "gs_bin_ordered": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, c_void_p,
+                                      ctypes.POINTER(GsCamera), c_void_p, c_void_p, c_void_p, ctypes.c_int64,
+                                      c_void_p, c_void_p, ctypes.c_size_t, c_void_p]),
+    "gs_sort32": (ctypes.c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, ctypes.c_int64,
+                                 ctypes.c_int32, c_void_p, ctypes.c_size_t, c_void_p]),
+    "gs_tile_ranges32": (ctypes.c_int, [c_void_p, c_void_p, ctypes.c_int64, ctypes.POINTER(GsCamera),
+                                        c_void_p, c_void_p]),
     "gs_rasterize": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, c_void_p, c_void_p,
                                     ctypes.POINTER(GsCamera), c_void_p, c_void_p, c_void_p, c_void_p]),
     "gs_render_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                                     ctypes.c_int64]),
     "gs_render": (ctypes.c_int, [ctypes.POINTER(GsGaussians), ctypes.POINTER(GsCamera), ctypes.c_int64,
                                  c_void_p, ctypes.c_size_t, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "gs_render_profiled": (ctypes.c_int, [ctypes.POINTER(GsGaussians), ctypes.POINTER(GsCamera), ctypes.c_int64,
+                                          c_void_p, ctypes.c_size_t, c_void_p, c_void_p, c_void_p, c_void_p,
+                                          ctypes.POINTER(c_void_p), ctypes.c_int32]),
     "gs_render_from_host": (ctypes.c_int, [ctypes.POINTER(GsGaussians), ctypes.POINTER(GsGaussians),
                                            ctypes.POINTER(GsCamera), ctypes.c_int64, c_void_p,
                                            ctypes.c_size_t, c_void_p, c_void_p, c_void_p]),

@@ -181,6 +181,41 @@ gs_status gs_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_keys,
                          int64_t key_capacity, const gs_camera* camera, uint32_t* ranges,
                          void* stream);
 
+/* Depth-first variant of steps 2-4, used by gs_render. Sorting the N
+ * Gaussians by depth once, then emitting each Gaussian's tiles in that order
+ * and sorting stably by tile id alone, gives exactly the per-tile order of
+ * steps 2-4 (tile, then depth bits, then Gaussian index) while moving 32-bit
+ * keys of ceil(log2(tiles)) bits instead of 64-bit keys of 32 + that many.
+ *
+ * gs_depth_order: order[0..n) = the Gaussian indices sorted by (float bits of
+ * depth, index) -- a stable sort of the depth bits -- with the Gaussians that
+ * touch no tile (tiles_touched == 0) last, in index order. Reads depth and
+ * tiles_touched of `projected`. ws: >= gs_depth_order_workspace_bytes(n).
+ *
+ * gs_bin_ordered: step 2 over the Gaussians in the given order (n entries of
+ * `order`): for each, in order, one 32-bit key per touched tile holding the
+ * tile id (row-major over the rectangle), value = Gaussian index. K goes to
+ * *num_keys; offsets (nullable) receives the inclusive prefix sums in list
+ * order. Capacity rules as gs_bin; ws: >= gs_bin_workspace_bytes(n).
+ *
+ * gs_sort32: gs_sort for 32-bit keys (key_bits 1..32). num_keys may be NULL,
+ * in which case key_capacity is the key count. ws: >= gs_sort_workspace_bytes.
+ *
+ * gs_tile_ranges32: step 4 for sorted 32-bit tile-id keys. */
+size_t gs_depth_order_workspace_bytes(int64_t n);
+gs_status gs_depth_order(const gs_projected* projected, int64_t n, uint32_t* order, void* ws,
+                         size_t ws_bytes, void* stream);
+gs_status gs_bin_ordered(const gs_projected* projected, int64_t n, const uint32_t* order,
+                         const gs_camera* camera, uint32_t* offsets, uint32_t* tile_keys,
+                         uint32_t* vals, int64_t key_capacity, uint64_t* num_keys, void* ws,
+                         size_t ws_bytes, void* stream);
+gs_status gs_sort32(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
+                    const uint64_t* num_keys, int64_t key_capacity, int32_t key_bits, void* ws,
+                    size_t ws_bytes, void* stream);
+gs_status gs_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* num_keys,
+                           int64_t key_capacity, const gs_camera* camera, uint32_t* ranges,
+                           void* stream);
+
 /* Step 5 -- composite (sections "La règle de composition alpha", "Étape 2").
  * Each pixel walks its tile's sorted list front to back:
  *     alpha = min(0.99, o exp(-0.5 d^T Sigma'^-1 d)), d = pixel - mu';
@@ -194,8 +229,11 @@ gs_status gs_rasterize(const gs_projected* projected, int64_t n, const uint32_t*
                        const uint32_t* ranges, const gs_camera* camera, float* image,
                        float* final_T, uint32_t* n_contrib, void* stream);
 
-/* The whole frame: steps 1-5 chained on `stream` with no host
- * synchronisation (so the call can be captured into a CUDA graph). All
+/* The whole frame: step 1, the depth-first steps 2-4 (gs_depth_order,
+ * gs_bin_ordered, gs_sort32, gs_tile_ranges32) and step 5, chained on
+ * `stream` with no host synchronisation (so the call can be captured into a
+ * CUDA graph). The image equals the one of the staged path
+ * gs_preprocess/gs_bin/gs_sort/gs_tile_ranges/gs_rasterize bit for bit. All
  * intermediates live in ws (device, 256-byte aligned, at least
  * gs_render_workspace_bytes(n, width, height, key_capacity) bytes); the first
  * 256 bytes of ws are the status header read by gs_read_status.
@@ -206,6 +244,18 @@ size_t gs_render_workspace_bytes(int64_t n, int32_t width, int32_t height, int64
 gs_status gs_render(const gs_gaussians* gaussians, const gs_camera* camera, int64_t key_capacity,
                     void* ws, size_t ws_bytes, float* image, float* final_T,
                     uint32_t* n_contrib, void* stream);
+
+/* gs_render that also records CUDA events at its stage boundaries, for
+ * per-stage timing of the very launches a frame makes. events[0..6] are
+ * caller-created cudaEvent_t handles (as void*), recorded on `stream`:
+ *   0 start, 1 after projection, 2 after the depth order, 3 after binning,
+ *   4 after the tile sort, 5 after the ranges, 6 after compositing.
+ * n_events must be >= GS_RENDER_STAGES + 1. */
+#define GS_RENDER_STAGES 6
+gs_status gs_render_profiled(const gs_gaussians* gaussians, const gs_camera* camera,
+                             int64_t key_capacity, void* ws, size_t ws_bytes, float* image,
+                             float* final_T, uint32_t* n_contrib, void* stream,
+                             void* const* events, int32_t n_events);
 
 /* The whole frame from host memory: copies the five parameter arrays from
  * host to the caller's device buffers in `device_gaussians` (same n and

@@ -279,3 +279,100 @@ def test_render_from_host(oracle_mod):
     r.render(cam)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(himg.numpy(), r.image.cpu().numpy())
+
+
+# ----------------------------------------------------------------------------- depth-first path
+
+def depth_first_stages(g, cam, cap):
+    L = native.lib()
+    n = int(g["n"])
+    p = gs.preprocess(g, cam)
+    ps = gs.projected_struct(p)
+    order = torch.empty(max(n, 1), dtype=torch.int32, device="cuda")
+    wsb = int(L.gs_depth_order_workspace_bytes(n))
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    native.check(L.gs_depth_order(ctypes.byref(ps), n, order.data_ptr(), ws.data_ptr(), wsb, None), "order")
+    keys = torch.empty(max(cap, 1), dtype=torch.int32, device="cuda")
+    vals = torch.empty(max(cap, 1), dtype=torch.int32, device="cuda")
+    nk = torch.zeros(1, dtype=torch.int64, device="cuda")
+    bwsb = int(L.gs_bin_workspace_bytes(n))
+    bws = torch.empty(bwsb, dtype=torch.uint8, device="cuda")
+    native.check(L.gs_bin_ordered(ctypes.byref(ps), n, order.data_ptr(), ctypes.byref(gs.camera_struct(cam)), None,
+                                  keys.data_ptr(), vals.data_ptr(), cap, nk.data_ptr(), bws.data_ptr(), bwsb, None),
+                 "bin_ordered")
+    torch.cuda.synchronize()
+    K = int(nk.item())
+    m = min(K, cap)
+    unsorted = (keys[:m].cpu().numpy().view(np.uint32).copy(), vals[:m].cpu().numpy().view(np.uint32).copy())
+    tx, ty = gs.tiles_xy(cam)
+    bits = max(1, (tx * ty - 1).bit_length())
+    ka, va = torch.empty_like(keys), torch.empty_like(vals)
+    swsb = int(L.gs_sort_workspace_bytes(cap))
+    sws = torch.empty(swsb, dtype=torch.uint8, device="cuda")
+    native.check(L.gs_sort32(keys.data_ptr(), vals.data_ptr(), ka.data_ptr(), va.data_ptr(), nk.data_ptr(), cap, bits,
+                             sws.data_ptr(), swsb, None), "sort32")
+    ranges = torch.empty((tx * ty, 2), dtype=torch.int32, device="cuda")
+    native.check(L.gs_tile_ranges32(keys.data_ptr(), nk.data_ptr(), cap, ctypes.byref(gs.camera_struct(cam)),
+                                    ranges.data_ptr(), None), "ranges32")
+    torch.cuda.synchronize()
+    assert gs.read_status(sws)[0] == native.GS_OK and gs.read_status(ws)[0] == native.GS_OK
+    return {"order": order[:n].cpu().numpy().view(np.uint32), "K": K, "unsorted": unsorted,
+            "sorted_tiles": keys[:m].cpu().numpy().view(np.uint32), "sorted_vals": vals[:m].cpu().numpy().view(np.uint32),
+            "ranges": ranges.cpu().numpy().view(np.uint32)}
+
+
+DF_CASES = [("tiny", 0), ("100k", 0), ("1M", 0), ("5M", 1), ("stress", 3)]
+
+
+@pytest.mark.parametrize("name,view", DF_CASES, ids=[f"{n}-v{v}" for n, v in DF_CASES])
+def test_depth_first_path_parity(oracle_mod, name, view):
+    scene, g = scene_of(name)
+    cam = scenes.make_cameras(name)[view]
+    d = oracle_mod.decide_f32(scene, cam)
+    off, K = oracle_mod.scan(d["tiles_touched"])
+    out = depth_first_stages(g, cam, K)
+    assert out["K"] == K
+    # depth order: stable sort of (depth bits, or 0xffffffff without tiles), ties by index
+    dk = np.where(d["tiles_touched"] > 0, d["depth"].view(np.uint32), np.uint32(0xFFFFFFFF))
+    np.testing.assert_array_equal(out["order"], np.argsort(dk, kind="stable").astype(np.uint32))
+    # keys in depth order: each Gaussian's oracle keys (row-major tiles), Gaussians in that order
+    keys, vals = oracle_mod.duplicate(d, cam, K)
+    first = (off - d["tiles_touched"]).astype(np.int64)
+    o = out["order"][d["tiles_touched"][out["order"]] > 0]
+    cnt = d["tiles_touched"][o].astype(np.int64)
+    starts = np.cumsum(cnt) - cnt
+    idx = np.repeat(first[o], cnt) + (np.arange(int(cnt.sum())) - np.repeat(starts, cnt))
+    np.testing.assert_array_equal(out["unsorted"][0], (keys[idx] >> np.uint64(32)).astype(np.uint32))
+    np.testing.assert_array_equal(out["unsorted"][1], vals[idx])
+    # after the stable tile sort: the oracle's sorted order and ranges
+    sk, sv = oracle_mod.sort_pairs(keys, vals)
+    np.testing.assert_array_equal(out["sorted_tiles"], (sk >> np.uint64(32)).astype(np.uint32))
+    np.testing.assert_array_equal(out["sorted_vals"], sv)
+    tx, ty = gs.tiles_xy(cam)
+    np.testing.assert_array_equal(out["ranges"], oracle_mod.tile_ranges(sk, tx * ty))
+
+
+@pytest.mark.parametrize("count,bits", [(0, 20), (1, 32), (4096, 13), (4097, 32), (100_003, 17), (1_000_000, 32),
+                                        (2_500_000, 13)])
+def test_sort32_random_keys(oracle_mod, count, bits):
+    rng = np.random.default_rng(count + bits)
+    keys = rng.integers(0, 1 << bits, size=count, dtype=np.uint64).astype(np.uint32)
+    keys[: count // 4] = keys[count // 4: 2 * (count // 4)]
+    vals = rng.permutation(count).astype(np.uint32)
+    cap = count + 5
+    kd = torch.zeros(max(cap, 1), dtype=torch.int32, device="cuda")
+    vd = torch.zeros(max(cap, 1), dtype=torch.int32, device="cuda")
+    kd[:count] = torch.from_numpy(keys.view(np.int32))
+    vd[:count] = torch.from_numpy(vals.view(np.int32))
+    L = native.lib()
+    ka, va = torch.empty_like(kd), torch.empty_like(vd)
+    wsb = int(L.gs_sort_workspace_bytes(cap))
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    # count known on the host: num_keys = NULL and key_capacity = count
+    native.check(L.gs_sort32(kd.data_ptr(), vd.data_ptr(), ka.data_ptr(), va.data_ptr(), None, count, bits,
+                             ws.data_ptr(), wsb, None), "sort32")
+    torch.cuda.synchronize()
+    assert gs.read_status(ws)[0] == native.GS_OK
+    sk, sv = oracle_mod.sort_pairs(keys.astype(np.uint64), np.arange(count, dtype=np.uint32))
+    np.testing.assert_array_equal(kd[:count].cpu().numpy().view(np.uint32), sk.astype(np.uint32))
+    np.testing.assert_array_equal(vd[:count].cpu().numpy().view(np.uint32), vals[sv])
