@@ -97,13 +97,14 @@ def alloc_projected(n: int, device="cuda") -> dict:
             "depth": torch.empty(n, dtype=torch.float32, device=device),
             "radius": torch.empty(n, dtype=torch.int32, device=device),
             "tiles_touched": torch.empty(n, dtype=torch.int32, device=device),
-            "rect": torch.empty((n, 4), dtype=torch.int16, device=device)}
+            "rect": torch.empty((n, 4), dtype=torch.int16, device=device),
+            "raster": torch.empty((n, 12), dtype=torch.float32, device=device)}
 
 
 def projected_struct(p: dict) -> GsProjected:
     s = GsProjected()
-    for k in ("mean2d", "conic_opacity", "rgb", "depth", "radius", "tiles_touched", "rect"):
-        setattr(s, k, _ptr(p[k]))
+    for k in ("mean2d", "conic_opacity", "rgb", "depth", "radius", "tiles_touched", "rect", "raster"):
+        setattr(s, k, _ptr(p.get(k)))
     return s
 
 

@@ -60,12 +60,13 @@ bool gaussians_ok(const gs_gaussians* g) {
     return true;
 }
 
+// fields the binning reads (the projection writes those and any non-null rest)
 bool projected_ok(const gs_projected* p, int64_t n) {
     if (!p) return false;
     if (n == 0) return true;
-    return p->mean2d && p->conic_opacity && p->rgb && p->depth && p->radius && p->tiles_touched && p->rect &&
-           aligned(p->mean2d, 8) && aligned(p->conic_opacity, 16) && aligned(p->rgb, 4) && aligned(p->depth, 4) &&
-           aligned(p->radius, 4) && aligned(p->tiles_touched, 4) && aligned(p->rect, 8);
+    return p->depth && p->tiles_touched && p->rect && aligned(p->mean2d, 8) && aligned(p->conic_opacity, 16) &&
+           aligned(p->rgb, 4) && aligned(p->depth, 4) && aligned(p->radius, 4) && aligned(p->tiles_touched, 4) &&
+           aligned(p->rect, 8) && aligned(p->raster, 16);
 }
 
 gs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GS_OK : GS_ERR_CUDA; }
@@ -79,7 +80,7 @@ int tile_bits_for(const gs_camera& c) {
 
 // gs_render workspace layout
 struct RenderLayout {
-    size_t header, mean2d, conic, rgb, depth, radius, touched, rect, dkeys, dkeys_alt, order, order_alt, bin,
+    size_t header, raster, depth, touched, rect, dkeys, dkeys_alt, order, order_alt, bin,
         keys, vals, keys_alt, vals_alt, sort, ranges, num_keys, total;
 };
 
@@ -95,11 +96,8 @@ RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
     const size_t tiles = (size_t)((w + kTile - 1) / kTile) * (size_t)((h + kTile - 1) / kTile);
     L.header = take(sizeof(StatusHeader));
     L.num_keys = take(sizeof(uint64_t));
-    L.mean2d = take(8 * un);
-    L.conic = take(16 * un);
-    L.rgb = take(12 * un);
+    L.raster = take(48 * un);
     L.depth = take(4 * un);
-    L.radius = take(4 * un);
     L.touched = take(4 * un);
     L.rect = take(8 * un);
     L.dkeys = take(4 * un);
@@ -133,12 +131,13 @@ gs_status render_impl(const gs_gaussians* g, const gs_camera* cam, int64_t key_c
     char* w = static_cast<char*>(ws);
     auto* header = reinterpret_cast<StatusHeader*>(w + L.header);
     auto* num_keys = reinterpret_cast<uint64_t*>(w + L.num_keys);
-    gs_projected p;
-    p.mean2d = reinterpret_cast<float*>(w + L.mean2d);
-    p.conic_opacity = reinterpret_cast<float*>(w + L.conic);
-    p.rgb = reinterpret_cast<float*>(w + L.rgb);
+    gs_projected p;   // only what binning and compositing read
+    p.mean2d = nullptr;
+    p.conic_opacity = nullptr;
+    p.rgb = nullptr;
+    p.radius = nullptr;
+    p.raster = reinterpret_cast<float*>(w + L.raster);
     p.depth = reinterpret_cast<float*>(w + L.depth);
-    p.radius = reinterpret_cast<int32_t*>(w + L.radius);
     p.tiles_touched = reinterpret_cast<uint32_t*>(w + L.touched);
     p.rect = reinterpret_cast<uint16_t*>(w + L.rect);
     auto* dkeys = reinterpret_cast<uint32_t*>(w + L.dkeys);
@@ -269,6 +268,7 @@ gs_status gs_rasterize(const gs_projected* p, int64_t n, const uint32_t* sorted_
                        const gs_camera* cam, float* image, float* final_T, uint32_t* n_contrib, void* stream) {
     if (n < 0 || !camera_ok(cam) || !projected_ok(p, n) || !ranges || !image || !aligned(ranges, 8))
         return GS_ERR_INVALID_ARG;
+    if (n > 0 && !p->raster) return GS_ERR_INVALID_ARG;
     if (n > 0 && !sorted_vals) return GS_ERR_INVALID_ARG;
     return cuda_status(launch_rasterize(*p, n, sorted_vals, ranges, make_cam_const(*cam), image, final_T, n_contrib,
                                         (cudaStream_t)stream));

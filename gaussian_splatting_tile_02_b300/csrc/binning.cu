@@ -13,11 +13,10 @@
 //
 // Three kernels: a per-chunk reduction (2048 Gaussians per block), a
 // single-block scan of the chunk sums (which also publishes K), and the
-// duplication, which re-scans its chunk in shared memory and then writes the
-// chunk's keys load-balanced: consecutive threads write consecutive key slots
-// (coalesced 8- and 4-byte stores) and find their Gaussian by binary search
-// over the chunk's inclusive offsets, so a Gaussian with many tiles does not
-// serialise one thread.
+// duplication, which re-scans its chunk and writes the keys warp by warp:
+// the 32 lanes of a warp share the keys of 32 consecutive Gaussians
+// (coalesced stores), so a Gaussian with many tiles does not serialise one
+// thread.
 #include "gs_internal.cuh"
 
 namespace gs {
@@ -134,6 +133,22 @@ __global__ void __launch_bounds__(1024) bin_scan_sums_kernel(unsigned long long*
 }
 
 // KeyT = uint64_t: key = tile << 32 | depth bits; KeyT = uint32_t: key = tile.
+// q = floor(r / w) for r < 2^24, 1 <= w < 2^16: a float quotient, then one
+// exact correction step either way.
+__device__ __forceinline__ uint32_t div_small(uint32_t r, uint32_t w) {
+    uint32_t q = (uint32_t)__fdiv_rz((float)r, (float)w);
+    if (q * w > r) q--;
+    else if ((q + 1u) * w <= r) q++;
+    return q;
+}
+
+// Keys of a chunk of 2048 list positions, in four rounds of 512 (one
+// position per thread). Per round a block scan gives every position its key
+// slot; then each warp writes the keys of its 32 consecutive positions
+// together: lane j takes the warp's keys j, j + 32, ... (coalesced stores),
+// finds the position that owns key j by a 5-step search over the lanes'
+// offsets (shuffles), and the tile from the key's rank in that position's
+// row-major tile rectangle.
 // hist (32-bit keys only, nullable): digit histograms of the written keys for
 // the radix sort that follows (key_bits significant bits).
 template <typename KeyT>
@@ -143,68 +158,67 @@ __global__ void __launch_bounds__(kBinThreads) bin_duplicate_kernel(
     int64_t key_capacity, uint32_t* __restrict__ offsets, KeyT* __restrict__ keys, uint32_t* __restrict__ vals,
     uint32_t* __restrict__ hist, int key_bits) {
     __shared__ uint32_t s_dhist[kHistPasses * 256];
-    // inclusive offsets inside the chunk, saturated at 2^32 - 1: only slots below
-    // the key capacity (< 2^30) are ever searched for
-    __shared__ uint32_t s_incl[kBinChunk];
-    __shared__ ushort4 s_rect[kBinChunk];
-    __shared__ uint32_t s_depth[kBinChunk];
-    __shared__ uint32_t s_g[kBinChunk];
     __shared__ unsigned long long warp_tot[kBinThreads / 32];
     __shared__ unsigned long long total;
 
-    const int64_t chunk0 = (int64_t)blockIdx.x * kBinChunk;
-    const int64_t base = chunk0 + (int64_t)threadIdx.x * kBinItems;
+    const int lane = threadIdx.x & 31;
     if (hist)
         for (int i = threadIdx.x; i < kHistPasses * 256; i += kBinThreads) s_dhist[i] = 0;
-    uint32_t t[kBinItems], gi[kBinItems];
-    unsigned long long s = 0;
+    const int64_t chunk0 = (int64_t)blockIdx.x * kBinChunk;
+    unsigned long long carry = block_prefix[blockIdx.x];   // key slot of the chunk's first key
+
+    for (int round = 0; round < kBinItems; round++) {
+        const int64_t pos = chunk0 + (int64_t)round * kBinThreads + threadIdx.x;
+        const bool in = pos < n;
+        const uint32_t g = in ? at(order, pos) : 0u;
+        const uint32_t t = in ? __ldg(tiles_touched + g) : 0u;
+        ushort4 r = make_ushort4(0, 0, 0, 0);
+        uint32_t db = 0;
+        if (t) {
+            r = __ldg(rect + g);
+            if (sizeof(KeyT) == 8) db = __float_as_uint(__ldg(depth + g));
+        }
+        const unsigned long long incl = block_scan_incl((unsigned long long)t, warp_tot, &total);
+        const unsigned long long first = carry + incl - t;   // global slot of this position's first key
+        if (in && offsets) offsets[pos] = (uint32_t)(carry + incl);
+
+        // keys of this warp's 32 positions, relative to the warp's first key
+        const unsigned long long wbase = __shfl_sync(0xffffffffu, first, 0);
+        const uint32_t rel_excl = (uint32_t)(first - wbase);            // < 2^32 for any sane input
+        const uint32_t wcount = __shfl_sync(0xffffffffu, (uint32_t)(first - wbase) + t, 31);
+        const uint32_t w_rect = (uint32_t)r.z - r.x + 1u;
+        const uint32_t packed_xy = (uint32_t)r.x | ((uint32_t)r.y << 16);
+        for (uint32_t j0 = 0; j0 < wcount; j0 += 32) {
+            const uint32_t j = j0 + lane;
+            // owner: the last lane whose first key is <= j
+            int owner = 0;
 #pragma unroll
-    for (int i = 0; i < kBinItems; i++) {
-        gi[i] = base + i < n ? at(order, base + i) : 0u;
-        t[i] = base + i < n ? __ldg(tiles_touched + gi[i]) : 0u;
-        s += t[i];
-    }
-    const unsigned long long incl = block_scan_incl(s, warp_tot, &total);
-    const unsigned long long prefix = block_prefix[blockIdx.x];
-    unsigned long long run = incl - s;
-#pragma unroll
-    for (int i = 0; i < kBinItems; i++) {
-        run += t[i];
-        const int li = threadIdx.x * kBinItems + i;
-        s_incl[li] = run < 0xffffffffull ? (uint32_t)run : 0xffffffffu;
-        if (base + i < n) {
-            if (offsets) offsets[base + i] = (uint32_t)(prefix + run);
-            if (t[i]) {
-                s_rect[li] = __ldg(rect + gi[i]);
-                s_g[li] = gi[i];
-                if (sizeof(KeyT) == 8) s_depth[li] = __float_as_uint(__ldg(depth + gi[i]));
+            for (int step = 16; step >= 1; step >>= 1) {
+                const uint32_t cand_first = __shfl_sync(0xffffffffu, rel_excl, owner + step);
+                if (cand_first <= j) owner += step;
+            }
+            const uint32_t o_first = __shfl_sync(0xffffffffu, rel_excl, owner);
+            const uint32_t o_w = __shfl_sync(0xffffffffu, w_rect, owner);
+            const uint32_t o_xy = __shfl_sync(0xffffffffu, packed_xy, owner);
+            const uint32_t o_g = __shfl_sync(0xffffffffu, g, owner);
+            const uint32_t o_db = __shfl_sync(0xffffffffu, db, owner);
+            const unsigned long long slot = wbase + j;
+            if (j < wcount && (long long)slot < key_capacity) {
+                const uint32_t rank = j - o_first;
+                const uint32_t dy = div_small(rank, o_w);
+                const uint32_t tx = (o_xy & 0xffffu) + (rank - dy * o_w), ty = (o_xy >> 16) + dy;
+                const uint64_t tile = (uint64_t)ty * (uint64_t)tiles_x + tx;
+                if (sizeof(KeyT) == 8) {
+                    keys[slot] = (KeyT)((tile << 32) | o_db);
+                } else {
+                    keys[slot] = (KeyT)tile;
+                    if (hist) count_digits(s_dhist, (uint32_t)tile, key_bits);
+                }
+                vals[slot] = o_g;
             }
         }
-    }
-    __syncthreads();
-    const unsigned long long room =
-        (long long)prefix < key_capacity ? (unsigned long long)key_capacity - prefix : 0ull;
-    const unsigned long long limit = total < room ? total : room;
-    for (unsigned long long j = threadIdx.x; j < limit; j += kBinThreads) {
-        // first chunk slot whose inclusive offset exceeds j
-        int lo = 0, hi = kBinChunk - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (s_incl[mid] > j) hi = mid; else lo = mid + 1;
-        }
-        const unsigned long long first = lo > 0 ? (unsigned long long)s_incl[lo - 1] : 0ull;
-        const uint32_t rank = (uint32_t)(j - first);
-        const ushort4 r = s_rect[lo];
-        const uint32_t w = (uint32_t)r.z - r.x + 1u;
-        const uint32_t ty = r.y + rank / w, tx = r.x + rank % w;
-        const uint64_t tile = (uint64_t)ty * (uint64_t)tiles_x + tx;
-        if (sizeof(KeyT) == 8) {
-            keys[prefix + j] = (KeyT)((tile << 32) | s_depth[lo]);
-        } else {
-            keys[prefix + j] = (KeyT)tile;
-            if (hist) count_digits(s_dhist, (uint32_t)tile, key_bits);
-        }
-        vals[prefix + j] = s_g[lo];
+        carry += total;
+        __syncthreads();   // warp_tot and total are reused by the next round's scan
     }
     if (hist) {
         __syncthreads();

@@ -32,6 +32,7 @@
 //   tiles [x0>>4 .. x1>>4] x [y0>>4 .. y1>>4] if x0 <= x1 and y0 <= y1.
 // Sigma' = M M^T is the pages' J W Sigma W^T J^T with Sigma = (R S)(R S)^T.
 // The continuous outputs (conic, opacity, colour) use ordinary fp32 arithmetic.
+#include <cuda_fp16.h>
 #include <float.h>
 
 #include "gs_internal.cuh"
@@ -67,6 +68,54 @@ __device__ __forceinline__ float exp32(float x) {
     p = add(1.0f, mul(r, p));
     p = add(1.0f, mul(r, p));
     return mul(p, __int_as_float((127 + (int)k) << 23));
+}
+
+// Error-free transformations of binary32 arithmetic (Dekker's product via
+// FMA, Knuth's two-sum): a*b = p + e and a+b = s + e exactly.
+__device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
+    p = __fmul_rn(a, b);
+    e = fmaf(a, b, -p);
+}
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Camera-space point and projected centre carried as unevaluated sums
+// hi + lo of two floats (compensated dot product in the manner of Ogita, Rump
+// and Oishi, "Accurate sum and dot product", 2005), good to ~1e-13 relative:
+// the projected centre is then known to ~1e-9 px where the binary32 decision
+// value u carries up to ~1e-4 px of rounding at u ~ 1000.
+__device__ __forceinline__ void dot3_add(const float* r, float m0, float m1, float m2, float t, float& hi,
+                                         float& lo) {
+    float p, s, h, e, q;
+    two_prod(r[0], m0, p, s);
+    two_prod(r[1], m1, h, e);
+    two_sum(p, h, p, q);
+    s += q + e;
+    two_prod(r[2], m2, h, e);
+    two_sum(p, h, p, q);
+    s += q + e;
+    two_sum(p, t, p, q);
+    s += q;
+    hi = p;
+    lo = s;
+}
+// f * (xh + xl) / (zh + zl) + c, returned as hi + lo
+__device__ __forceinline__ void project_df(float f, float xh, float xl, float zh, float zl, float c, float& hi,
+                                          float& lo) {
+    const float q1 = xh / zh;
+    float ph, pl;
+    two_prod(q1, zh, ph, pl);
+    const float rr = ((xh - ph) - pl) + xl - q1 * zl;
+    const float q2 = rr / zh;
+    float h, l, s, e;
+    two_prod(f, q1, h, l);
+    l = fmaf(f, q2, l);
+    two_sum(h, c, s, e);
+    hi = s;
+    lo = e + l;
 }
 
 // Real SH basis constants, from their closed forms: sqrt(1/4pi), sqrt(3/4pi),
@@ -145,6 +194,7 @@ struct PreArgs {
     int64_t n;
     CamConst cam;
     float2* mean2d;
+    float4* raster;
     float4* conic_opacity;
     float* rgb;
     float* depth;
@@ -175,7 +225,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
     const float n2 = add(add(add(mul(q.x, q.x), mul(q.y, q.y)), mul(q.z, q.z)), mul(q.w, q.w));
     ok = ok && n2 > 0.0f && n2 <= FLT_MAX;
     if (!ok) {
-        a.radius[g] = 0;
+        if (a.radius) a.radius[g] = 0;
         a.tiles_touched[g] = 0;
         a.rect[g] = make_ushort4(0, 0, 0, 0);
         return;
@@ -200,12 +250,14 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
     float s[3];
 #pragma unroll
     for (int k = 0; k < 3; k++) s[k] = exp32(__ldg(a.log_scales + 3 * g + k));
-    float B[9];
+    float Arot[9], B[9];   // Arot = W R (the Gaussian's axes in camera space), B = Arot S
 #pragma unroll
     for (int i = 0; i < 3; i++)
 #pragma unroll
-        for (int j = 0; j < 3; j++)
-            B[3 * i + j] = mul(add(add(mul(C.R[3 * i], G[j]), mul(C.R[3 * i + 1], G[3 + j])), mul(C.R[3 * i + 2], G[6 + j])), s[j]);
+        for (int j = 0; j < 3; j++) {
+            Arot[3 * i + j] = add(add(mul(C.R[3 * i], G[j]), mul(C.R[3 * i + 1], G[3 + j])), mul(C.R[3 * i + 2], G[6 + j]));
+            B[3 * i + j] = mul(Arot[3 * i + j], s[j]);
+        }
     const float j00 = dv(C.fx, z), j11 = dv(C.fy, z);
     const float zz2 = mul(z, z);
     const float fxp0 = mul(C.fx, p[0]), fyp1 = mul(C.fy, p[1]);
@@ -227,7 +279,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
     const float u = add(dv(fxp0, z), C.cx);
     const float v = add(dv(fyp1, z), C.cy);
     if (!(det > 0.0f && det <= FLT_MAX) || !(fabsf(u) <= FLT_MAX && fabsf(v) <= FLT_MAX && rf <= FLT_MAX)) {
-        a.radius[g] = 0;
+        if (a.radius) a.radius[g] = 0;
         a.tiles_touched[g] = 0;
         a.rect[g] = make_ushort4(0, 0, 0, 0);
         return;
@@ -246,25 +298,85 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
         touched = (uint32_t)((tx1 - tx0 + 1) * (ty1 - ty0 + 1));
         rect = make_ushort4((unsigned short)tx0, (unsigned short)ty0, (unsigned short)tx1, (unsigned short)ty1);
     }
-    a.radius[g] = rf <= 1073741824.0f ? (int32_t)rf : 1073741824;
+    if (a.radius) a.radius[g] = rf <= 1073741824.0f ? (int32_t)rf : 1073741824;
     a.tiles_touched[g] = touched;
     a.rect[g] = rect;
-    a.mean2d[g] = make_float2(u, v);
+    if (a.mean2d) a.mean2d[g] = make_float2(u, v);
 
     // continuous values (ordinary fp32)
-    const float inv_det = 1.0f / det;
+    // det Sigma' without cancellation: Sigma' = M M^T with M = J Arot S, so by
+    // the Lagrange identity det = |M_0 x M_1|^2, and (Lu) x (Lv) = cof(L)(u x v)
+    // with L = (Arot S)^T gives M_0 x M_1 = diag(s1 s2, s0 s2, s0 s1) Arot^T
+    // (J_0 x J_1), J_0 x J_1 = (fx fy / z^3) p: a sum of three squares, each a
+    // scaled dot product that is small only when its term does not matter.
+    float det_acc;
+    {
+        const float kz = (C.fx * C.fy) / (z * z * z);
+        const float sp[3] = {s[1] * s[2], s[0] * s[2], s[0] * s[1]};
+        det_acc = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 3; k++) {
+            const float dk = sp[k] * kz * (Arot[k] * p[0] + Arot[3 + k] * p[1] + Arot[6 + k] * p[2]);
+            det_acc = fmaf(dk, dk, det_acc);
+        }
+        if (!(det_acc > 0.0f) || !isfinite(det_acc)) det_acc = det;
+    }
+    const float inv_det = 1.0f / det_acc;
     const float logit = __ldg(a.logits + g);
     const float o = 1.0f / (1.0f + expf(-logit));
-    a.conic_opacity[g] = make_float4(cc * inv_det, -cb * inv_det, ca * inv_det, o);
+    const float conA = cc * inv_det, conB = -cb * inv_det, conC = ca * inv_det;
+    if (a.conic_opacity) a.conic_opacity[g] = make_float4(conA, conB, conC, o);
 
     float dx = m0 - C.campos[0], dy = m1 - C.campos[1], dz = m2 - C.campos[2];
     const float il = rsqrtf(dx * dx + dy * dy + dz * dz);
     dx *= il; dy *= il; dz *= il;
     constexpr int NK3 = (D + 1) * (D + 1) * 3;
     const float3 col = eval_sh<D>(a.sh + g * NK3, dx, dy, dz);
-    a.rgb[3 * g] = col.x;
-    a.rgb[3 * g + 1] = col.y;
-    a.rgb[3 * g + 2] = col.z;
+    if (a.rgb) {
+        a.rgb[3 * g] = col.x;
+        a.rgb[3 * g + 1] = col.y;
+        a.rgb[3 * g + 2] = col.z;
+    }
+    if (a.raster && touched) {
+        // the compositor's record (three float4):
+        //  {u, v, du, dv}: decision centre and the residual to the accurate
+        //      centre, from a compensated evaluation of the projection
+        //  {k1, k2, k3, log2 o}: log2(alpha) = log2 o - (k1 dx)^2 - (k2 dy + k3 dx)^2
+        //  {r, g, b, half2(hx, hy)}: colour and the half-extents (rounded up) of
+        //      the box holding {d : o exp(-d^T conic d / 2) >= 1/255}, i.e.
+        //      sqrt(tau Sigma'_xx), sqrt(tau Sigma'_yy), tau = 2 ln(255 o),
+        //      widened by margins far above the rounding of the per-pixel alpha;
+        //      +inf (never culled) when Sigma' is too ill-conditioned for them,
+        //      -1 (always culled) when o < 1/255 (margin included)
+        float xh, xl, yh, yl, zh, zl, uh, ul, vh, vl;
+        dot3_add(C.R, m0, m1, m2, C.t[0], xh, xl);
+        dot3_add(C.R + 3, m0, m1, m2, C.t[1], yh, yl);
+        dot3_add(C.R + 6, m0, m1, m2, C.t[2], zh, zl);
+        project_df(C.fx, xh, xl, zh, zl, C.cx, uh, ul);
+        project_df(C.fy, yh, yl, zh, zl, C.cy, vh, vl);
+        const float tau = 2.0f * logf(255.0f * o) + 0.02f;
+        float hx = INFINITY, hy = INFINITY;
+        if (!(tau > 0.0f)) {
+            hx = hy = -1.0f;
+        } else if ((ca + cc) * (ca + cc) <= 1e8f * det_acc) {
+            hx = 1.01f * sqrtf(tau * ca) + 0.05f;
+            hy = 1.01f * sqrtf(tau * cc) + 0.05f;
+        }
+        const __half2 h = __halves2half2(__float2half_ru(hx), __float2half_ru(hy));
+        float4* rec = a.raster + 3 * g;
+        rec[0] = make_float4(u, v, (uh - u) + ul, (vh - v) + vl);
+        // q = d^T Sigma'^-1 d = (dx / sqrt(a))^2 + ((a dy - b dx) / sqrt(a det))^2:
+        // a sum of two squares (relative error ~eps sqrt(cond), where the
+        // expanded conic form loses ~eps cond); scaled by sqrt(log2(e) / 2) so
+        // that log2(alpha) = log2 o - t1^2 - t2^2, t1 = k1 dx, t2 = k2 dy + k3 dx
+        const float sc = 0.84932180028801907f;   // sqrt(log2(e) / 2)
+        const float ra = rsqrtf(ca);
+        const float k1 = sc * ra;
+        const float k2 = sc * sqrtf(ca * inv_det);
+        const float k3 = -sc * cb * ra * rsqrtf(det_acc);
+        rec[1] = make_float4(k1, k2, k3, log2f(o));
+        rec[2] = make_float4(col.x, col.y, col.z, __uint_as_float(*reinterpret_cast<const uint32_t*>(&h)));
+    }
 }
 
 }  // namespace
@@ -281,6 +393,7 @@ cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const 
     a.n = g.n;
     a.cam = cam;
     a.mean2d = reinterpret_cast<float2*>(out.mean2d);
+    a.raster = reinterpret_cast<float4*>(out.raster);
     a.conic_opacity = reinterpret_cast<float4*>(out.conic_opacity);
     a.rgb = out.rgb;
     a.depth = out.depth;

@@ -9,24 +9,32 @@
 //
 // One block per tile, one thread per pixel; warp w covers the 8x4 pixel block
 // (8 (w & 1), 4 (w >> 1)) of the tile. The tile's sorted list is walked in
-// batches of 256 entries. Staging: each thread gathers one projected record
-// into shared memory with the exponent's constants folded in
-// (alpha = 2^(log2 o + quadratic form)) and the box that holds the region where
-// alpha can reach 1/255 (o exp(-q/2) >= 1/255, i.e. q <= 2 ln(255 o), widened
-// by a safety margin). Each warp then ballots which of the 256 entries' boxes
-// meet its 8x4 block and evaluates only those, in list order, for its 32
-// pixels: an entry whose box misses the block cannot contribute to any of its
-// pixels, so skipping it changes no result. The block leaves the list as soon
-// as all its pixels are done (__syncthreads_count). Per evaluated (pixel,
-// entry): two subtractions, the quadratic form (5 FP32 ops), ex2 on the MUFU
-// pipe, a min and a compare, plus the blend for contributing pairs.
+// batches of 256 entries, double-buffered in shared memory: while the block
+// evaluates batch b, each thread already holds in registers the packed record
+// (three float4 written by the projection step) of its entry of batch b + 1,
+// and stores it to the other buffer afterwards, so the gathers overlap the
+// arithmetic. Each warp ballots which of the batch's entries have an
+// alpha >= 1/255 box (part of the record) that meets its 8x4 block and
+// evaluates only those, in list order, for its 32 pixels: an entry whose box
+// misses the block cannot contribute to any of its pixels, so skipping it
+// changes no result. The block leaves the list once all its pixels are done.
+//
+// Coordinates are relative to the tile's first pixel: a centre enters as
+// (u - x0) + residual (an exact subtraction, then one rounding at small
+// magnitude), so d = pixel - centre keeps ~1e-6 px where a binary32 centre
+// near x = 1000 carries ~1e-4 px. The quadratic form is a sum of two squares,
+// log2(alpha) = log2 o - (k1 dx)^2 - (k2 dy + k3 dx)^2, which keeps its
+// accuracy for elongated footprints. Per evaluated (pixel, entry): two
+// subtractions, the form (5 FP32 ops), ex2 on the MUFU pipe, a min and a
+// compare, plus the blend for contributing pairs.
+#include <cuda_fp16.h>
+
 #include "gs_internal.cuh"
 
 namespace gs {
 namespace {
 
 constexpr int kRastThreads = kTile * kTile;
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kAlphaMin = 1.0f / 255.0f;
 
 // 2^x on the MUFU pipe (PTX ex2.approx; relative error about 2^-22).
@@ -35,17 +43,9 @@ __device__ __forceinline__ float fast_exp2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// log2(x) on the MUFU pipe (PTX lg2.approx).
-__device__ __forceinline__ float fast_log2(float x) {
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 struct RastArgs {
-    const float2* mean2d;
-    const float4* conic_opacity;
-    const float* rgb;
+    const float4* raster;   // [n][3]
     const uint32_t* sorted_vals;
     const uint2* ranges;
     uint32_t n;
@@ -57,58 +57,65 @@ struct RastArgs {
 };
 
 __global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs a) {
-    __shared__ float4 s_q[kRastThreads];    // (mx, my, qa, qb)
-    __shared__ float4 s_r[kRastThreads];    // (qc, log2 o, r, g)
-    __shared__ float s_b[kRastThreads];     // b
-    __shared__ float4 s_box[kRastThreads];  // (x lo, x hi, y lo, y hi) of the alpha >= 1/255 region
+    __shared__ float4 s_q[2][kRastThreads];    // (mx, my, k1, k2), centre tile-local
+    __shared__ float4 s_r[2][kRastThreads];    // (k3, log2 o, r, g)
+    __shared__ float s_b[2][kRastThreads];     // b
+    __shared__ float4 s_box[2][kRastThreads];  // (x lo, x hi, y lo, y hi), tile-local
 
     const int tile = blockIdx.x;
     const int tx = tile % a.tiles_x, ty = tile / a.tiles_x;
+    const float tile_x0 = (float)(tx * kTile), tile_y0 = (float)(ty * kTile);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bx0 = tx * kTile + 8 * (warp & 1), by0 = ty * kTile + 4 * (warp >> 1);
-    const int px = bx0 + (lane & 7), py = by0 + (lane >> 3);
-    const float fbx0 = (float)bx0, fbx1 = (float)(bx0 + 7), fby0 = (float)by0, fby1 = (float)(by0 + 3);
+    const int lbx0 = 8 * (warp & 1), lby0 = 4 * (warp >> 1);   // warp's 8x4 block, tile-local
+    const int lx = lbx0 + (lane & 7), ly = lby0 + (lane >> 3);
+    const int px = tx * kTile + lx, py = ty * kTile + ly;
+    const float fbx0 = (float)lbx0, fbx1 = (float)(lbx0 + 7), fby0 = (float)lby0, fby1 = (float)(lby0 + 3);
     const bool inside = px < a.width && py < a.height;
     const uint2 range = a.ranges[tile];
-    const float fpx = (float)px, fpy = (float)py;
+    const float fpx = (float)lx, fpy = (float)ly;
 
     float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
     uint32_t last = 0;
     bool done = !inside;
 
-    for (uint32_t base = range.x; base < range.y; base += kRastThreads) {
-        if (__syncthreads_count(done) == kRastThreads) break;
-        const uint32_t idx = base + threadIdx.x;
-        if (idx < range.y) {
-            uint32_t g = __ldg(a.sorted_vals + idx);
-            // an index outside the scene can only come from a sort that was cut
-            // short (its status is flagged); never read past the arrays
-            if (g >= a.n) g = 0;
-            const float2 m = __ldg(a.mean2d + g);
-            const float4 co = __ldg(a.conic_opacity + g);
-            s_q[threadIdx.x] = make_float4(m.x, m.y, -0.5f * kLog2e * co.x, -kLog2e * co.y);
-            s_r[threadIdx.x] = make_float4(-0.5f * kLog2e * co.z, fast_log2(co.w), __ldg(a.rgb + 3 * g),
-                                           __ldg(a.rgb + 3 * g + 1));
-            s_b[threadIdx.x] = __ldg(a.rgb + 3 * g + 2);
-            // box of {d : d^T conic d <= tau}, tau = 2 ln(255 o): half-extents
-            // sqrt(tau Sigma'_xx) and sqrt(tau Sigma'_yy) with Sigma' = conic^-1;
-            // tau is raised by 0.02 and the half-extents widened by 1% + 0.05 px,
-            // far more than the rounding of the per-pixel alpha can move it.
-            // The rounding of det(conic) is about 3e-8 (A + C)^2 / det relative:
-            // conics with (A + C)^2 > 1e4 det keep an unbounded box (never culled).
-            const float detc = co.x * co.z - co.y * co.y;
-            const float tau = 2.0f * __logf(255.0f * co.w) + 0.02f;
-            float4 box = make_float4(-INFINITY, INFINITY, -INFINITY, INFINITY);
-            if (!(tau > 0.0f)) {  // o below 1/255 (margin included): never contributes
-                box = make_float4(INFINITY, -INFINITY, INFINITY, -INFINITY);
-            } else if (detc > 0.0f && (co.x + co.z) * (co.x + co.z) <= 1e4f * detc) {
-                const float hx = 1.01f * sqrtf(tau * co.z / detc) + 0.05f;
-                const float hy = 1.01f * sqrtf(tau * co.x / detc) + 0.05f;
-                if (hx < INFINITY && hy < INFINITY) box = make_float4(m.x - hx, m.x + hx, m.y - hy, m.y + hy);
-            }
-            s_box[threadIdx.x] = box;
-        }
-        __syncthreads();
+    auto fetch = [&](uint32_t idx, float4& r0, float4& r1, float4& r2) {
+        uint32_t g = __ldg(a.sorted_vals + idx);
+        // an index outside the scene can only come from a sort that was cut
+        // short (its status is flagged); never read past the arrays
+        if (g >= a.n) g = 0;
+        r0 = __ldg(a.raster + 3 * g);
+        r1 = __ldg(a.raster + 3 * g + 1);
+        r2 = __ldg(a.raster + 3 * g + 2);
+    };
+    auto store = [&](int buf, const float4& r0, const float4& r1, const float4& r2) {
+        const float mx = (r0.x - tile_x0) + r0.z, my = (r0.y - tile_y0) + r0.w;
+        const uint32_t hb = __float_as_uint(r2.w);
+        const __half2 h = *reinterpret_cast<const __half2*>(&hb);
+        const float hx = __low2float(h), hy = __high2float(h);
+        s_q[buf][threadIdx.x] = make_float4(mx, my, r1.x, r1.y);   // (mx, my, k1, k2)
+        s_r[buf][threadIdx.x] = make_float4(r1.z, r1.w, r2.x, r2.y);   // (k3, log2 o, r, g)
+        s_b[buf][threadIdx.x] = r2.z;
+        s_box[buf][threadIdx.x] = make_float4(mx - hx, mx + hx, my - hy, my + hy);
+    };
+
+    const uint32_t len = range.y - range.x;
+    const uint32_t nbatch = (len + kRastThreads - 1) / kRastThreads;
+    if (threadIdx.x < len) {
+        float4 r0, r1, r2;
+        fetch(range.x + threadIdx.x, r0, r1, r2);
+        store(0, r0, r1, r2);
+    }
+    __syncthreads();
+
+    for (uint32_t b = 0; b < nbatch; b++) {
+        const int buf = b & 1;
+        const uint32_t base = range.x + b * kRastThreads;
+        // gather the next batch's record now; it is stored after the arithmetic
+        const uint32_t nidx = base + kRastThreads + threadIdx.x;
+        const bool have_next = b + 1 < nbatch && nidx < range.y;
+        float4 n0, n1, n2;
+        if (have_next) fetch(nidx, n0, n1, n2);
+
         const uint32_t cnt = min((uint32_t)kRastThreads, range.y - base);
         // which of the batch entries can touch this warp's 8x4 pixel block
         uint32_t mask[kRastThreads / 32];
@@ -117,7 +124,7 @@ __global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs 
             const uint32_t j = (uint32_t)(i * 32 + lane);
             bool hit = false;
             if (j < cnt) {
-                const float4 bx = s_box[j];
+                const float4 bx = s_box[buf][j];
                 hit = bx.x <= fbx1 && bx.y >= fbx0 && bx.z <= fby1 && bx.w >= fby0;
             }
             mask[i] = __ballot_sync(0xffffffffu, hit);
@@ -130,21 +137,24 @@ __global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs 
                 const int j = i * 32 + __ffs(m) - 1;
                 m &= m - 1;
                 if (done) continue;
-                const float4 q = s_q[j];
-                const float4 r = s_r[j];
+                const float4 q = s_q[buf][j];
+                const float4 r = s_r[buf][j];
                 const float dx = q.x - fpx, dy = q.y - fpy;
-                const float e = r.y + dx * (q.z * dx + q.w * dy) + r.x * dy * dy;
+                const float t1 = q.z * dx, t2 = fmaf(r.x, dx, q.w * dy);
+                const float e = fmaf(-t2, t2, fmaf(-t1, t1, r.y));
                 const float alpha = fminf(0.99f, fast_exp2(e));
                 if (alpha < kAlphaMin) continue;
                 const float w = alpha * T;
                 C0 += w * r.z;
                 C1 += w * r.w;
-                C2 += w * s_b[j];
+                C2 += w * s_b[buf][j];
                 T -= w;
                 last = base - range.x + (uint32_t)j + 1;
                 if (T < 1e-4f) done = true;
             }
         }
+        if (have_next) store(buf ^ 1, n0, n1, n2);
+        if (__syncthreads_count(done) == kRastThreads) break;
     }
     if (inside) {
         const int64_t p = (int64_t)py * a.width + px;
@@ -162,9 +172,7 @@ cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* s
                              const CamConst& cam, float* image, float* final_T, uint32_t* n_contrib,
                              cudaStream_t s) {
     RastArgs a;
-    a.mean2d = reinterpret_cast<const float2*>(p.mean2d);
-    a.conic_opacity = reinterpret_cast<const float4*>(p.conic_opacity);
-    a.rgb = p.rgb;
+    a.raster = reinterpret_cast<const float4*>(p.raster);
     a.sorted_vals = sorted_vals;
     a.ranges = reinterpret_cast<const uint2*>(ranges);
     a.n = (uint32_t)n;

@@ -30,7 +30,7 @@ class GsGaussians(ctypes.Structure):
 class GsProjected(ctypes.Structure):
     _fields_ = [("mean2d", c_void_p), ("conic_opacity", c_void_p), ("rgb", c_void_p),
                 ("depth", c_void_p), ("radius", c_void_p), ("tiles_touched", c_void_p),
-                ("rect", c_void_p)]
+                ("rect", c_void_p), ("raster", c_void_p)]
 
 
 GS_OK, GS_ERR_INVALID_ARG, GS_ERR_CAPACITY, GS_ERR_CUDA, GS_ERR_TIMEOUT, GS_ERR_WORKSPACE = range(6)

@@ -84,9 +84,12 @@ typedef struct gs_gaussians {
 } gs_gaussians;
 
 /* Per-Gaussian output of the projection step (device pointers, caller
- * allocated, each [n] rows; mean2d 8-byte aligned, conic_opacity 16-byte
- * aligned, rect 8-byte aligned).
- *   mean2d         [n][2]  projected centre mu' (pixels)
+ * allocated, each [n] rows). depth, tiles_touched and rect are required; the
+ * others may be NULL, and are then not written (gs_render writes only the
+ * fields binning and compositing read). Alignment: mean2d 8 bytes,
+ * conic_opacity and raster 16 bytes, rect 8 bytes.
+ *   mean2d         [n][2]  projected centre mu' (pixels), the binary32 value of
+ *                          the decision program (rectangles are cut from it)
  *   conic_opacity  [n][4]  (A, B, C, o): Sigma'^-1 = [[A, B], [B, C]], opacity o
  *   rgb            [n][3]  colour from SH along the view direction, + 0.5, >= 0
  *   depth          [n]     camera-space z (the sort key's low 32 bits)
@@ -94,6 +97,17 @@ typedef struct gs_gaussians {
  *   tiles_touched  [n]     number of 16x16 tiles the pixel rectangle
  *                          [u-r, u+r] x [v-r, v+r] (clipped) covers, 0 if culled
  *   rect           [n][4]  uint16 tile rectangle (tx0, ty0, tx1, ty1), inclusive
+ *   raster         [n][12] the compositor's packed record, written for
+ *                          Gaussians with tiles_touched > 0 (required by
+ *                          gs_rasterize): {u, v, du, dv} with mu' = (u + du,
+ *                          v + dv) from a compensated (double-float) evaluation
+ *                          of the projection, good to ~1e-9 px; {k1, k2, k3,
+ *                          log2 o} with log2(alpha) = log2 o - (k1 dx)^2 -
+ *                          (k2 dy + k3 dx)^2, the Gaussian's quadratic form as
+ *                          a sum of two squares; {r, g, b, h} with h the bits of
+ *                          a half2 holding the half-extents (rounded up) of a
+ *                          box that contains every pixel offset where alpha can
+ *                          reach 1/255 (+inf: no box, -1: never reaches it).
  * For culled Gaussians only radius and tiles_touched are defined (both 0). */
 typedef struct gs_projected {
     float* mean2d;
@@ -103,6 +117,7 @@ typedef struct gs_projected {
     int32_t* radius;
     uint32_t* tiles_touched;
     uint16_t* rect;
+    float* raster;
 } gs_projected;
 
 const char* gs_status_string(int32_t status);

@@ -47,7 +47,9 @@ def check_image(oracle, ref, cam, image, final_T=None, n_contrib=None, tol=TOL, 
             flipped[y, x] = True
         else:
             unexplained.append((int(y), int(x), float(err[y, x]), nev))
+    quiet = ref["n_events"] == 0     # pixels with no decision near a threshold
     stats = {"max_err": float(err.max()) if err.size else 0.0,
+             "max_err_no_events": float(err[quiet].max()) if quiet.any() else 0.0,
              "max_err_unflipped": float(err[~flipped].max()) if (~flipped).any() else 0.0,
              "n_pixels": int(err.size), "n_flipped": int(flipped.sum()),
              "unexplained": unexplained[:max_report], "n_unexplained": len(unexplained)}

@@ -90,13 +90,46 @@ def check_keys(oracle, ref, out):
 def check_continuous(ref, out):
     p, rp = out["p"], ref["proj"]
     v = ref["dec"]["tiles_touched"] > 0
+    # the compositor's record: decision centre + compensated residual = the fp64
+    # centre (to ~1e-10 px); exponent coefficients, colour; a conservative box
+    rec = p["raster"][v].astype(np.float64)
+    np.testing.assert_array_equal(p["raster"][v][:, :2].view(np.uint32), p["mean2d"][v].view(np.uint32))
+    np.testing.assert_allclose(rec[:, :2] + rec[:, 2:4], rp["mean2d"][v], rtol=0, atol=1e-7)
+    assert np.abs(rec[:, 2:4]).max() < 1e-2
+    # (k1 dx)^2 + (k2 dy + k3 dx)^2 = log2(e)/2 d^T conic d for any d: check on the
+    # axes and the diagonal against the fp64 conic
+    l2e = 1.0 / np.log(2.0)
+    k1, k2, k3 = rec[:, 4], rec[:, 5], rec[:, 6]
+    A, B, C = (rp["conic"][v, i] for i in range(3))
+    for dx, dy in ((1.0, 0.0), (0.0, 1.0), (1.0, 1.0), (1.0, -1.0)):
+        q_gpu = (k1 * dx) ** 2 + (k2 * dy + k3 * dx) ** 2
+        q_ref = 0.5 * l2e * (A * dx * dx + 2 * B * dx * dy + C * dy * dy)
+        cond = rp["lam_max"][v] ** 2 / (rp["cov2d"][v, 0] * rp["cov2d"][v, 2] - rp["cov2d"][v, 1] ** 2)
+        scale = 0.5 * l2e * (np.abs(A) + np.abs(C)) * (dx * dx + dy * dy)
+        err = np.abs(q_gpu - q_ref)
+        well = cond < 1e4
+        assert (err[well] <= 1e-5 * scale[well] * np.sqrt(cond[well]) + 1e-6 * q_ref[well]).all()
+        assert (err <= 1e-3 * scale * np.sqrt(cond)).all()
+    np.testing.assert_allclose(rec[:, 7], np.log2(rp["opacity"][v]), rtol=1e-5, atol=1e-5)
+    np.testing.assert_array_equal(p["raster"][v][:, 8:11], p["rgb"][v])
+    h = p["raster"][v][:, 11].copy().view(np.uint32)
+    hx = (h & 0xFFFF).astype(np.uint16).view(np.float16).astype(np.float64)
+    hy = (h >> 16).astype(np.uint16).view(np.float16).astype(np.float64)
+    tau = 2 * np.log(255 * rp["opacity"][v])
+    pos = tau > 0
+    need_x = np.sqrt(np.where(pos, tau, 0) * rp["cov2d"][v, 0])
+    need_y = np.sqrt(np.where(pos, tau, 0) * rp["cov2d"][v, 2])
+    assert ((hx >= need_x) | ~pos).all() and ((hy >= need_y) | ~pos).all()
+    assert (hx[tau < -0.05] < 0).all() and (hx[tau > 0.05] > 0).all()
     np.testing.assert_allclose(p["conic_opacity"][v, 3], rp["opacity"][v], rtol=2e-6, atol=1e-7)
     np.testing.assert_allclose(p["rgb"][v], rp["rgb"][v], atol=2e-6)
     con = p["conic_opacity"][v, :3].astype(np.float64)
     scale = np.abs(rp["conic"][v]).max(1, keepdims=True)
-    # fp32 conic from fp32 Sigma' entries: error grows with the condition number of Sigma'
+    # fp32 conic from the decision program's fp32 Sigma' entries over a
+    # cancellation-free det. The entries are good to ~1e-6 relative, except for
+    # needles seen end-on, whose long axis nearly cancels in M = J W R S (~1e-5)
     cond = rp["lam_max"][v] ** 2 / (rp["cov2d"][v, 0] * rp["cov2d"][v, 2] - rp["cov2d"][v, 1] ** 2)
-    assert (np.abs(con - rp["conic"][v]) <= (1e-5 + 4e-7 * cond[:, None]) * scale).all()
+    assert (np.abs(con - rp["conic"][v]) <= (5e-5 + 1e-6 * np.sqrt(cond[:, None])) * scale).all()
 
 
 CASES = [("tiny", 0), ("100k", 0), ("1M", 0)] + [("5M", i) for i in range(4)] + [("stress", i) for i in range(8)]
