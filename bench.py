@@ -73,6 +73,29 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def rank_view(view0: int, rank: int, n_views: int) -> int:
+    """The view a rank renders: replicas of a one-view scene, views dealt out
+    round-robin for multi-view scenes (independent frames, no exchange)."""
+    return (view0 + rank) % n_views
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank number over all ranks (the job takes as long as its slowest rank)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(frame_ms_max: float, world: int) -> float:
+    """Whole-job frames/s: every rank renders one frame per step, a step lasts
+    as long as the slowest rank's frame."""
+    return world * 1e3 / frame_ms_max
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -216,7 +239,7 @@ def run_ours(args, rank, local_rank, world):
     cfg = scenes.CONFIGS[args.config]
     scene = scenes.make_scene(cfg)
     cams = scenes.make_cameras(cfg)
-    cam = cams[args.view % len(cams)]
+    cam = cams[rank_view(args.view, rank, len(cams))]
     g = gs.gaussians_to_device(scene, dev)
     r = gs.Renderer.for_scene(g, cam, headroom=1.1)
     stream = torch.cuda.Stream(device=dev)
@@ -227,13 +250,6 @@ def run_ours(args, rank, local_rank, world):
             import torch.distributed as dist
             dist.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     # --- warm-up and optional graph capture
     with torch.cuda.stream(stream):
@@ -272,7 +288,7 @@ def run_ours(args, rank, local_rank, world):
         torch.cuda.synchronize(dev)
         barrier()
         frame_ms = e0.elapsed_time(e1) / args.steps
-        frame_ms_max = max_over_ranks(frame_ms)
+        frame_ms_max = max_over_ranks(frame_ms, world, dev)
 
         # --- per-stage times: K more frames through gs_render_profiled, which records
         # CUDA events at the stage boundaries of the very launches a frame makes
@@ -337,7 +353,7 @@ def run_ours(args, rank, local_rank, world):
                 for _ in range(n_e2e):
                     gs.render_from_host(host, r2, cam, himg, stream=stream)
                 stream.synchronize()
-                t_e2e = max_over_ranks(time.perf_counter() - t0)
+                t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
                 barrier()
             h2d = sum(v.numel() * v.element_size() for v in host.values())
             d2h = himg.numel() * himg.element_size()
@@ -406,7 +422,7 @@ def run_ours(args, rank, local_rank, world):
 
     result = {
         "metric": metric_name(cfg),
-        "value": world * 1e3 / frame_ms_max, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
+        "value": job_value(frame_ms_max, world), "unit": "frames/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": frame_ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": cfg.description, "n": cfg.n, "width": cfg.width, "height": cfg.height,

@@ -104,7 +104,7 @@ RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
     L.dkeys_alt = take(4 * un);
     L.order = take(4 * un);
     L.order_alt = take(4 * un);
-    L.bin = take(bin_scratch_bytes(n));
+    L.bin = take(bin_ordered_scratch_bytes(n, cap));
     L.keys = take(4 * uc);
     L.vals = take(4 * uc);
     L.keys_alt = take(4 * uc);
@@ -234,6 +234,10 @@ gs_status gs_bin(const gs_projected* p, int64_t n, const gs_camera* cam, uint32_
                                   static_cast<char*>(ws) + sizeof(StatusHeader), s));
 }
 
+size_t gs_bin_ordered_workspace_bytes(int64_t n, int64_t key_capacity) {
+    return sizeof(StatusHeader) + bin_ordered_scratch_bytes(n < 0 ? 0 : n, key_capacity < 0 ? 0 : key_capacity);
+}
+
 size_t gs_sort_workspace_bytes(int64_t key_capacity) {
     return sizeof(StatusHeader) + sort_scratch_bytes(key_capacity < 0 ? 0 : key_capacity);
 }
@@ -332,7 +336,8 @@ gs_status gs_bin_ordered(const gs_projected* p, int64_t n, const uint32_t* order
     if (key_capacity > 0 && (!tile_keys || !vals || !aligned(tile_keys, 4) || !aligned(vals, 4)))
         return GS_ERR_INVALID_ARG;
     if (!aligned(num_keys, 8)) return GS_ERR_INVALID_ARG;
-    if (!ws || !aligned(ws, kAlign) || ws_bytes < gs_bin_workspace_bytes(n)) return GS_ERR_WORKSPACE;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < gs_bin_ordered_workspace_bytes(n, key_capacity))
+        return GS_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     auto* header = static_cast<StatusHeader*>(ws);
     cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);

@@ -226,6 +226,182 @@ __global__ void __launch_bounds__(kBinThreads) bin_duplicate_kernel(
     }
 }
 
+// ---------------------------------------------------------------- key-balanced expansion
+// Used for a given order (the depth order). A chunk of Gaussians can hold
+// wildly different numbers of keys (in depth order the many-tile Gaussians of
+// one dense region sit together), so the expansion is balanced by keys: one
+// block per kKeysPerBlock key slots.
+//   bin_offsets_kernel : each position's first key slot (exclusive prefix), and
+//                        for every block boundary k * kKeysPerBlock the position
+//                        that owns that slot.
+//   bin_expand_kernel  : block k writes slots [k, k + 1) * kKeysPerBlock; it
+//                        loads the positions from the owner of its first slot
+//                        on, and finds each slot's position by binary search.
+constexpr int kKeysPerBlock = 2048;
+constexpr int kExpandThreads = 256;
+constexpr int kWindow = 1024;   // positions staged per step
+
+// Rectangles in list order (coalesced reads for the three kernels below); a
+// Gaussian without tiles gets the marker x0 = 0xffff.
+__global__ void gather_rect_kernel(const uint32_t* __restrict__ tiles_touched, const ushort4* __restrict__ rect,
+                                   const uint32_t* __restrict__ order, int64_t n, ushort4* __restrict__ rs) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const uint32_t g = __ldg(order + i);
+        rs[i] = __ldg(tiles_touched + g) ? __ldg(rect + g) : make_ushort4(0xffff, 0, 0, 0);
+    }
+}
+
+__device__ __forceinline__ uint32_t rect_tiles(const ushort4 r) {
+    return r.x == 0xffff ? 0u : ((uint32_t)r.z - r.x + 1u) * ((uint32_t)r.w - r.y + 1u);
+}
+
+__global__ void __launch_bounds__(kBinThreads) bin_reduce_rect_kernel(const ushort4* __restrict__ rs, int64_t n,
+                                                                      unsigned long long* __restrict__ block_sums) {
+    __shared__ unsigned long long warp_tot[kBinThreads / 32];
+    __shared__ unsigned long long total;
+    const int64_t base = (int64_t)blockIdx.x * kBinChunk + (int64_t)threadIdx.x * kBinItems;
+    unsigned long long s = 0;
+#pragma unroll
+    for (int i = 0; i < kBinItems; i++)
+        if (base + i < n) s += rect_tiles(__ldg(rs + base + i));
+    block_scan_incl(s, warp_tot, &total);
+    if (threadIdx.x == 0) block_sums[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kBinThreads) bin_offsets_kernel(
+    const ushort4* __restrict__ rs, int64_t n,
+    const unsigned long long* __restrict__ block_prefix, int64_t key_capacity, uint32_t* __restrict__ first_slot,
+    uint32_t* __restrict__ owner, uint32_t* __restrict__ offsets) {
+    __shared__ unsigned long long warp_tot[kBinThreads / 32];
+    __shared__ unsigned long long total;
+    const int64_t chunk0 = (int64_t)blockIdx.x * kBinChunk;
+    unsigned long long carry = block_prefix[blockIdx.x];
+    for (int round = 0; round < kBinItems; round++) {
+        const int64_t pos = chunk0 + (int64_t)round * kBinThreads + threadIdx.x;
+        const bool in = pos < n;
+        const uint32_t t = in ? rect_tiles(__ldg(rs + pos)) : 0u;
+        const unsigned long long incl = block_scan_incl((unsigned long long)t, warp_tot, &total);
+        const unsigned long long first = carry + incl - t;
+        if (in) {
+            first_slot[pos] = first < 0xffffffffull ? (uint32_t)first : 0xffffffffu;
+            if (offsets) offsets[pos] = (uint32_t)(carry + incl);
+            if (t) {
+                const unsigned long long last = first + t - 1;
+                const unsigned long long lim = (unsigned long long)key_capacity;
+                for (unsigned long long k = (first + kKeysPerBlock - 1) / kKeysPerBlock;
+                     k * kKeysPerBlock <= last && k * kKeysPerBlock < lim; k++)
+                    owner[k] = (uint32_t)pos;
+            }
+        }
+        carry += total;
+        __syncthreads();
+    }
+}
+
+// hist (nullable): digit histograms of the written tile keys (key_bits bits).
+// Each thread owns kRun consecutive slots of the block's range: one binary
+// search for the position owning its first slot, then a walk along that
+// position's tile rectangle (and on to the next positions). Keys go through
+// shared memory so that the global stores are coalesced.
+constexpr int kRun = kKeysPerBlock / kExpandThreads;   // 8 slots per thread
+__global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
+    const ushort4* __restrict__ rs, const uint32_t* __restrict__ order, int64_t n, int tiles_x,
+    const uint32_t* __restrict__ first_slot, const uint32_t* __restrict__ owner,
+    const uint64_t* __restrict__ num_keys, int64_t key_capacity, uint32_t* __restrict__ keys,
+    uint32_t* __restrict__ vals, uint32_t* __restrict__ hist, int key_bits) {
+    __shared__ uint32_t s_first[kWindow];
+    __shared__ ushort4 s_rect[kWindow];
+    __shared__ uint32_t s_g[kWindow];
+    __shared__ uint32_t s_key[kKeysPerBlock];
+    __shared__ uint32_t s_val[kKeysPerBlock];
+    __shared__ uint32_t s_dhist[kHistPasses * 256];
+    __shared__ uint32_t s_end;
+
+    const unsigned long long K = *num_keys;
+    const unsigned long long Keff = K < (unsigned long long)key_capacity ? K : (unsigned long long)key_capacity;
+    const unsigned long long S0 = (unsigned long long)blockIdx.x * kKeysPerBlock;
+    if (S0 >= Keff) return;
+    const unsigned long long S1 = S0 + kKeysPerBlock < Keff ? S0 + kKeysPerBlock : Keff;
+    if (hist)
+        for (int i = threadIdx.x; i < kHistPasses * 256; i += kExpandThreads) s_dhist[i] = 0;
+    const int hi_bits = key_bits - 8 < 8 ? key_bits - 8 : 8;   // second digit (tile ids < 2^16)
+    const unsigned long long r0 = S0 + (unsigned long long)threadIdx.x * kRun;   // this thread's slots
+    const unsigned long long r1 = r0 + kRun < S1 ? r0 + kRun : S1;
+
+    int64_t p = owner[blockIdx.x];
+    const int64_t p_last = S1 < Keff ? (int64_t)owner[blockIdx.x + 1] : n - 1;
+    while (true) {
+        __syncthreads();
+        int64_t wn = p_last - p + 1;
+        wn = wn < kWindow ? wn : kWindow;
+        wn = wn < n - p ? wn : n - p;
+        for (int i = threadIdx.x; i < wn; i += kExpandThreads) {
+            s_first[i] = __ldg(first_slot + p + i);
+            s_g[i] = __ldg(order + p + i);
+            s_rect[i] = __ldg(rs + p + i);
+        }
+        if (threadIdx.x == 0)
+            s_end = p + wn < n ? __ldg(first_slot + p + wn) : (uint32_t)(K < 0xffffffffull ? K : 0xffffffffull);
+        __syncthreads();
+        // this thread's slots that this window owns
+        const unsigned long long a0 = r0 > (unsigned long long)s_first[0] ? r0 : (unsigned long long)s_first[0];
+        const unsigned long long a1 = r1 < (unsigned long long)s_end ? r1 : (unsigned long long)s_end;
+        if (a0 < a1) {
+            int lo = 0, hi = (int)wn - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_first[mid] <= a0) lo = mid; else hi = mid - 1;
+            }
+            ushort4 r = s_rect[lo];
+            uint32_t w = (uint32_t)r.z - r.x + 1u;
+            uint32_t rank = (uint32_t)(a0 - s_first[lo]);
+            uint32_t dy = div_small(rank, w);
+            uint32_t ty = r.y + dy, tx = r.x + (rank - dy * w);
+            uint32_t run_hi = 0xffffffffu, run_n = 0;
+            for (unsigned long long j = a0; j < a1; j++) {
+                // step to the next position once this one's tiles are used up
+                while (lo + 1 < wn && s_first[lo + 1] <= j) {
+                    lo++;
+                    r = s_rect[lo];
+                    w = (uint32_t)r.z - r.x + 1u;
+                    tx = r.x;
+                    ty = r.y;
+                }
+                const uint32_t tile = ty * (uint32_t)tiles_x + tx;
+                s_key[j - S0] = tile;
+                s_val[j - S0] = s_g[lo];
+                if (hist) {
+                    atomicAdd(&s_dhist[tile & 255u], 1u);
+                    if (hi_bits > 0) {
+                        const uint32_t h = (tile >> 8) & ((1u << hi_bits) - 1u);
+                        if (h != run_hi) {
+                            if (run_n) atomicAdd(&s_dhist[256 + run_hi], run_n);
+                            run_hi = h;
+                            run_n = 0;
+                        }
+                        run_n++;
+                    }
+                }
+                if (++tx > r.z) {
+                    tx = r.x;
+                    ty++;
+                }
+            }
+            if (hist && run_n) atomicAdd(&s_dhist[256 + run_hi], run_n);
+        }
+        if (s_end >= S1 || p + wn >= n) break;
+        p += wn;
+    }
+    __syncthreads();
+    const int cnt = (int)(S1 - S0);
+    for (int i = threadIdx.x; i < cnt; i += kExpandThreads) {
+        keys[S0 + i] = s_key[i];
+        vals[S0 + i] = s_val[i];
+    }
+    if (hist) flush_digits(s_dhist, hist, key_bits);
+}
+
 // Depth-order sort input: key = depth bits for Gaussians with tiles (depth >
 // near > 0, so the bits order like the depths), 0xffffffff for the others
 // (sorted last); value = index.
@@ -284,12 +460,40 @@ cudaError_t launch_bin(const gs_projected& p, int64_t n, const CamConst& cam, ui
                                   s);
 }
 
+size_t bin_ordered_scratch_bytes(int64_t n, int64_t key_capacity) {
+    const size_t un = (size_t)(n > 0 ? n : 0);
+    const size_t blocks = (size_t)((key_capacity > 0 ? key_capacity : 0) + kKeysPerBlock - 1) / kKeysPerBlock + 1;
+    return bin_scratch_bytes(n) + align_up(4 * un) + align_up(4 * blocks) + align_up(8 * un);
+}
+
 cudaError_t launch_bin_ordered(const gs_projected& p, const uint32_t* order, int64_t n, const CamConst& cam,
                                uint32_t* offsets, uint32_t* tile_keys, uint32_t* vals, int64_t key_capacity,
                                uint64_t* num_keys, StatusHeader* status, void* scratch, cudaStream_t s,
                                uint32_t* hist, int key_bits) {
-    return launch_bin_t<uint32_t>(p, order, n, cam, offsets, tile_keys, vals, key_capacity, num_keys, status,
-                                  scratch, s, hist, key_bits);
+    if (n == 0) {
+        cudaError_t e = cudaMemsetAsync(num_keys, 0, sizeof(uint64_t), s);
+        if (e != cudaSuccess) return e;
+        return cudaMemsetAsync(&status->num_keys, 0, sizeof(unsigned long long), s);
+    }
+    const int nb = (int)((n + kBinChunk - 1) / kBinChunk);
+    char* w = static_cast<char*>(scratch);
+    auto* sums = reinterpret_cast<unsigned long long*>(w);
+    auto* first_slot = reinterpret_cast<uint32_t*>(w + bin_scratch_bytes(n));
+    const size_t blocks_b = (size_t)((key_capacity > 0 ? key_capacity : 0) + kKeysPerBlock - 1) / kKeysPerBlock + 1;
+    auto* owner = reinterpret_cast<uint32_t*>(w + bin_scratch_bytes(n) + align_up(4 * (size_t)n));
+    auto* rs = reinterpret_cast<ushort4*>(w + bin_scratch_bytes(n) + align_up(4 * (size_t)n) + align_up(4 * blocks_b));
+    const int64_t gb = (n + 255) / 256;
+    gather_rect_kernel<<<(unsigned)(gb < 148 * 16 ? gb : 148 * 16), 256, 0, s>>>(
+        p.tiles_touched, reinterpret_cast<const ushort4*>(p.rect), order, n, rs);
+    bin_reduce_rect_kernel<<<nb, kBinThreads, 0, s>>>(rs, n, sums);
+    bin_scan_sums_kernel<<<1, 1024, 0, s>>>(sums, nb, key_capacity, num_keys, status);
+    bin_offsets_kernel<<<nb, kBinThreads, 0, s>>>(rs, n, sums, key_capacity, first_slot, owner, offsets);
+    if (key_capacity > 0) {
+        const unsigned blocks = (unsigned)((key_capacity + kKeysPerBlock - 1) / kKeysPerBlock);
+        bin_expand_kernel<<<blocks, kExpandThreads, 0, s>>>(rs, order, n, cam.tiles_x, first_slot, owner, num_keys,
+                                                            key_capacity, tile_keys, vals, hist, key_bits);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_depth_keys(const gs_projected& p, int64_t n, uint32_t* keys, uint32_t* vals, uint32_t* hist,

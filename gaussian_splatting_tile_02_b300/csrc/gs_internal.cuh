@@ -73,7 +73,9 @@ cudaError_t launch_bin(const gs_projected& p, int64_t n, const CamConst& cam, ui
                        StatusHeader* status, void* scratch, cudaStream_t s);
 
 // hist (nullable): digit histograms of the written keys for the radix sort
-// that follows, key_bits significant bits (32-bit keys)
+// that follows, key_bits significant bits (32-bit keys). Scratch:
+// bin_ordered_scratch_bytes(n, key_capacity).
+size_t bin_ordered_scratch_bytes(int64_t n, int64_t key_capacity);
 cudaError_t launch_bin_ordered(const gs_projected& p, const uint32_t* order, int64_t n, const CamConst& cam,
                                uint32_t* offsets, uint32_t* tile_keys, uint32_t* vals, int64_t key_capacity,
                                uint64_t* num_keys, StatusHeader* status, void* scratch, cudaStream_t s,

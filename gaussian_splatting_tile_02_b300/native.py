@@ -54,6 +54,7 @@ _SIGNATURES = {
     "gs_tile_ranges": (ctypes.c_int, [c_void_p, c_void_p, ctypes.c_int64, ctypes.POINTER(GsCamera),
                                       c_void_p, c_void_p]),
     "gs_depth_order_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64]),
+    "gs_bin_ordered_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "gs_depth_order": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, c_void_p, c_void_p,
                                       ctypes.c_size_t, c_void_p]),
     "gs_bin_ordered": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, c_void_p,

@@ -211,13 +211,16 @@ gs_status gs_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_keys,
  * `order`): for each, in order, one 32-bit key per touched tile holding the
  * tile id (row-major over the rectangle), value = Gaussian index. K goes to
  * *num_keys; offsets (nullable) receives the inclusive prefix sums in list
- * order. Capacity rules as gs_bin; ws: >= gs_bin_workspace_bytes(n).
+ * order. Capacity rules as gs_bin; ws: >= gs_bin_ordered_workspace_bytes(n,
+ * key_capacity). The keys are written load-balanced by key slot (one block
+ * per 2048 slots), so Gaussians with many tiles do not stall a block.
  *
  * gs_sort32: gs_sort for 32-bit keys (key_bits 1..32). num_keys may be NULL,
  * in which case key_capacity is the key count. ws: >= gs_sort_workspace_bytes.
  *
  * gs_tile_ranges32: step 4 for sorted 32-bit tile-id keys. */
 size_t gs_depth_order_workspace_bytes(int64_t n);
+size_t gs_bin_ordered_workspace_bytes(int64_t n, int64_t key_capacity);
 gs_status gs_depth_order(const gs_projected* projected, int64_t n, uint32_t* order, void* ws,
                          size_t ws_bytes, void* stream);
 gs_status gs_bin_ordered(const gs_projected* projected, int64_t n, const uint32_t* order,

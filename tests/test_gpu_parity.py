@@ -328,7 +328,7 @@ def depth_first_stages(g, cam, cap):
     keys = torch.empty(max(cap, 1), dtype=torch.int32, device="cuda")
     vals = torch.empty(max(cap, 1), dtype=torch.int32, device="cuda")
     nk = torch.zeros(1, dtype=torch.int64, device="cuda")
-    bwsb = int(L.gs_bin_workspace_bytes(n))
+    bwsb = int(L.gs_bin_ordered_workspace_bytes(n, cap))
     bws = torch.empty(bwsb, dtype=torch.uint8, device="cuda")
     native.check(L.gs_bin_ordered(ctypes.byref(ps), n, order.data_ptr(), ctypes.byref(gs.camera_struct(cam)), None,
                                   keys.data_ptr(), vals.data_ptr(), cap, nk.data_ptr(), bws.data_ptr(), bwsb, None),

@@ -1,0 +1,58 @@
+"""Multi-rank logic of bench.py on CPU with the gloo backend (world size 2):
+each rank renders its own frames (replicas / views dealt round-robin) and only
+the timing is reduced; no collective touches the data path."""
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    r, lr, w = bench.dist_env()
+    frame_ms = 2.0 + 3.0 * rank                  # rank 1 is the slow one
+    m = bench.max_over_ranks(frame_ms, w, "cpu")
+    out[rank] = (r, lr, w, m, bench.job_value(m, w), bench.rank_view(0, r, 8), bench.rank_view(0, r, 1))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_timing_and_views():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        procs = [ctx.Process(target=_worker, args=(r, world, port, out)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        res = dict(out)
+    for rank in range(world):
+        r, lr, w, m, value, view8, view1 = res[rank]
+        assert (r, lr, w) == (rank, rank, world)
+        assert m == 5.0                          # the slowest rank's frame time
+        assert value == pytest.approx(world * 1e3 / 5.0)
+        assert view8 == rank and view1 == 0      # views dealt out; one-view scenes are replicated
+
+
+def test_single_rank_helpers():
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.job_value(2.0, 1) == 500.0
+    assert [bench.rank_view(2, r, 4) for r in range(4)] == [2, 3, 0, 1]
