@@ -313,8 +313,10 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
     __shared__ uint32_t s_first[kWindow];
     __shared__ ushort4 s_rect[kWindow];
     __shared__ uint32_t s_g[kWindow];
-    __shared__ uint32_t s_key[kKeysPerBlock];
-    __shared__ uint32_t s_val[kKeysPerBlock];
+    // staged keys, one padding word per 32 so that the per-thread runs of 8
+    // (stride-8 writes across a warp) fall in distinct banks
+    __shared__ uint32_t s_key[kKeysPerBlock + kKeysPerBlock / 32];
+    __shared__ uint32_t s_val[kKeysPerBlock + kKeysPerBlock / 32];
     __shared__ uint32_t s_dhist[kHistPasses * 256];
     __shared__ uint32_t s_end;
 
@@ -369,8 +371,9 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
                     ty = r.y;
                 }
                 const uint32_t tile = ty * (uint32_t)tiles_x + tx;
-                s_key[j - S0] = tile;
-                s_val[j - S0] = s_g[lo];
+                const uint32_t si = (uint32_t)(j - S0);
+                s_key[si + (si >> 5)] = tile;
+                s_val[si + (si >> 5)] = s_g[lo];
                 if (hist) {
                     atomicAdd(&s_dhist[tile & 255u], 1u);
                     if (hi_bits > 0) {
@@ -396,8 +399,8 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
     __syncthreads();
     const int cnt = (int)(S1 - S0);
     for (int i = threadIdx.x; i < cnt; i += kExpandThreads) {
-        keys[S0 + i] = s_key[i];
-        vals[S0 + i] = s_val[i];
+        keys[S0 + i] = s_key[i + (i >> 5)];
+        vals[S0 + i] = s_val[i + (i >> 5)];
     }
     if (hist) flush_digits(s_dhist, hist, key_bits);
 }

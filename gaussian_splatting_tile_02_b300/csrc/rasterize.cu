@@ -35,7 +35,7 @@ namespace gs {
 namespace {
 
 constexpr int kRastThreads = kTile * kTile;
-constexpr float kAlphaMin = 1.0f / 255.0f;
+constexpr float kLog2AlphaMin = -7.99435343685886f;   // log2(1/255)
 
 // 2^x on the MUFU pipe (PTX ex2.approx; relative error about 2^-22).
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -61,11 +61,15 @@ __global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs 
     __shared__ float4 s_r[2][kRastThreads];    // (k3, log2 o, r, g)
     __shared__ float s_b[2][kRastThreads];     // b
     __shared__ float4 s_box[2][kRastThreads];  // (x lo, x hi, y lo, y hi), tile-local
+    __shared__ float4 w_q[kRastThreads / 32][32];   // per-warp list of the entries that meet its block
+    __shared__ float4 w_r[kRastThreads / 32][32];
+    __shared__ float2 w_bj[kRastThreads / 32][32];  // (b, list position + 1 as bits)
 
     const int tile = blockIdx.x;
     const int tx = tile % a.tiles_x, ty = tile / a.tiles_x;
     const float tile_x0 = (float)(tx * kTile), tile_y0 = (float)(ty * kTile);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t lt_mask = (1u << lane) - 1u;
     const int lbx0 = 8 * (warp & 1), lby0 = 4 * (warp >> 1);   // warp's 8x4 block, tile-local
     const int lx = lbx0 + (lane & 7), ly = lby0 + (lane >> 3);
     const int px = tx * kTile + lx, py = ty * kTile + ly;
@@ -117,41 +121,49 @@ __global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs 
         if (have_next) fetch(nidx, n0, n1, n2);
 
         const uint32_t cnt = min((uint32_t)kRastThreads, range.y - base);
-        // which of the batch entries can touch this warp's 8x4 pixel block
-        uint32_t mask[kRastThreads / 32];
-#pragma unroll
+        // groups of 32 batch entries: ballot the ones whose box meets this
+        // warp's 8x4 pixel block, copy those records into the warp's list, then
+        // evaluate the list in order for the warp's 32 pixels
+#pragma unroll 1
         for (int i = 0; i < kRastThreads / 32; i++) {
+            if (__all_sync(0xffffffffu, done)) break;
             const uint32_t j = (uint32_t)(i * 32 + lane);
             bool hit = false;
             if (j < cnt) {
                 const float4 bx = s_box[buf][j];
                 hit = bx.x <= fbx1 && bx.y >= fbx0 && bx.z <= fby1 && bx.w >= fby0;
             }
-            mask[i] = __ballot_sync(0xffffffffu, hit);
-        }
-#pragma unroll
-        for (int i = 0; i < kRastThreads / 32; i++) {
-            if (__all_sync(0xffffffffu, done)) break;
-            uint32_t m = mask[i];
-            while (m) {
-                const int j = i * 32 + __ffs(m) - 1;
-                m &= m - 1;
-                if (done) continue;
-                const float4 q = s_q[buf][j];
-                const float4 r = s_r[buf][j];
+            const uint32_t m = __ballot_sync(0xffffffffu, hit);
+            if (m == 0) continue;
+            if (hit) {
+                const int pos = __popc(m & lt_mask);
+                w_q[warp][pos] = s_q[buf][j];
+                w_r[warp][pos] = s_r[buf][j];
+                w_bj[warp][pos] = make_float2(s_b[buf][j], __uint_as_float(base - range.x + j + 1));
+            }
+            __syncwarp();
+            const int nh = __popc(m);
+#pragma unroll 2
+            for (int k = 0; k < nh; k++) {
+                const float4 q = w_q[warp][k];
+                const float4 r = w_r[warp][k];
                 const float dx = q.x - fpx, dy = q.y - fpy;
                 const float t1 = q.z * dx, t2 = fmaf(r.x, dx, q.w * dy);
                 const float e = fmaf(-t2, t2, fmaf(-t1, t1, r.y));
+                // alpha = min(0.99, 2^e) < 1/255 is e < log2(1/255) (the same
+                // decision in exact arithmetic; ex2 is only evaluated past it)
+                if (done || e < kLog2AlphaMin) continue;
                 const float alpha = fminf(0.99f, fast_exp2(e));
-                if (alpha < kAlphaMin) continue;
+                const float2 bj = w_bj[warp][k];
                 const float w = alpha * T;
                 C0 += w * r.z;
                 C1 += w * r.w;
-                C2 += w * s_b[buf][j];
+                C2 += w * bj.x;
                 T -= w;
-                last = base - range.x + (uint32_t)j + 1;
+                last = __float_as_uint(bj.y);
                 if (T < 1e-4f) done = true;
             }
+            __syncwarp();
         }
         if (have_next) store(buf ^ 1, n0, n1, n2);
         if (__syncthreads_count(done) == kRastThreads) break;
