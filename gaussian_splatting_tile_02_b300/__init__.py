@@ -163,8 +163,11 @@ def tile_ranges(sorted_keys, num_keys, cam: dict, key_capacity: int | None = Non
     return ranges
 
 
-def rasterize(p: dict, sorted_vals, ranges, cam: dict, stream=None, want_aux: bool = True) -> dict:
-    """Step 5: composite. Returns image [H,W,3], final_T [H,W], n_contrib [H,W]."""
+def rasterize(p: dict, sorted_vals, ranges, cam: dict, stream=None, want_aux: bool = True,
+              heavy_first: bool = True) -> dict:
+    """Step 5: composite. Returns image [H,W,3], final_T [H,W], n_contrib [H,W].
+
+    heavy_first launches the tiles in decreasing list length (the image does not change)."""
     torch = _torch()
     H, W = int(cam["height"]), int(cam["width"])
     dev = ranges.device
@@ -172,10 +175,12 @@ def rasterize(p: dict, sorted_vals, ranges, cam: dict, stream=None, want_aux: bo
     if want_aux:
         out["final_T"] = torch.empty((H, W), dtype=torch.float32, device=dev)
         out["n_contrib"] = torch.empty((H, W), dtype=torch.int32, device=dev)
+    tx, ty = tiles_xy(cam)
+    order = torch.empty(tx * ty, dtype=torch.int32, device=dev) if heavy_first else None
     n = int(p["depth"].shape[0])
     check(lib().gs_rasterize(ctypes.byref(projected_struct(p)), n, _ptr(sorted_vals), _ptr(ranges),
                              ctypes.byref(camera_struct(cam)), _ptr(out["image"]), _ptr(out.get("final_T")),
-                             _ptr(out.get("n_contrib")), _stream_ptr(stream)), "gs_rasterize")
+                             _ptr(out.get("n_contrib")), _ptr(order), _stream_ptr(stream)), "gs_rasterize")
     return out
 
 

@@ -81,7 +81,7 @@ int tile_bits_for(const gs_camera& c) {
 // gs_render workspace layout
 struct RenderLayout {
     size_t header, raster, depth, touched, rect, dkeys, dkeys_alt, order, order_alt, bin,
-        keys, vals, keys_alt, vals_alt, sort, ranges, num_keys, total;
+        keys, vals, keys_alt, vals_alt, sort, ranges, tile_order, num_keys, total;
 };
 
 RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
@@ -111,6 +111,7 @@ RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
     L.vals_alt = take(4 * uc);
     L.sort = take(sort_scratch_bytes(cap > n ? cap : n));
     L.ranges = take(8 * tiles);
+    L.tile_order = take(4 * tiles);
     L.total = o;
     return L;
 }
@@ -183,7 +184,9 @@ gs_status render_impl(const gs_gaussians* g, const gs_camera* cam, int64_t key_c
     if (e == cudaSuccess)
         e = launch_tile_ranges32(keys, num_keys, key_capacity, cc.tiles_x * cc.tiles_y, ranges, s);
     if (e == cudaSuccess) e = mark(5);
-    if (e == cudaSuccess) e = launch_rasterize(p, g->n, vals, ranges, cc, image, final_T, n_contrib, s);
+    if (e == cudaSuccess)
+        e = launch_rasterize(p, g->n, vals, ranges, reinterpret_cast<uint32_t*>(w + L.tile_order), cc, image, final_T,
+                             n_contrib, s);
     if (e == cudaSuccess) e = mark(6);
     return cuda_status(e);
 }
@@ -269,13 +272,14 @@ gs_status gs_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_keys, 
 }
 
 gs_status gs_rasterize(const gs_projected* p, int64_t n, const uint32_t* sorted_vals, const uint32_t* ranges,
-                       const gs_camera* cam, float* image, float* final_T, uint32_t* n_contrib, void* stream) {
+                       const gs_camera* cam, float* image, float* final_T, uint32_t* n_contrib, uint32_t* tile_order,
+                       void* stream) {
     if (n < 0 || !camera_ok(cam) || !projected_ok(p, n) || !ranges || !image || !aligned(ranges, 8))
         return GS_ERR_INVALID_ARG;
     if (n > 0 && !p->raster) return GS_ERR_INVALID_ARG;
     if (n > 0 && !sorted_vals) return GS_ERR_INVALID_ARG;
-    return cuda_status(launch_rasterize(*p, n, sorted_vals, ranges, make_cam_const(*cam), image, final_T, n_contrib,
-                                        (cudaStream_t)stream));
+    return cuda_status(launch_rasterize(*p, n, sorted_vals, ranges, tile_order, make_cam_const(*cam), image, final_T,
+                                        n_contrib, (cudaStream_t)stream));
 }
 
 size_t gs_render_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity) {

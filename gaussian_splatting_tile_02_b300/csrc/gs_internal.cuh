@@ -104,8 +104,10 @@ cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* n
 cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations, cudaStream_t s);
 
 // rasterize.cu
+// tile_order (nullable): [tiles] scratch that receives the heavy-first launch
+// order of the tiles; null launches them in index order (same image)
 cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* sorted_vals, const uint32_t* ranges,
-                             const CamConst& cam, float* image, float* final_T, uint32_t* n_contrib,
-                             cudaStream_t s);
+                             uint32_t* tile_order, const CamConst& cam, float* image, float* final_T,
+                             uint32_t* n_contrib, cudaStream_t s);
 
 }  // namespace gs

@@ -7,17 +7,19 @@
 // loop over the depth order). Contributions with alpha < 1/255 are skipped
 // and a pixel stops once T < 1e-4, after the Gaussian that took it there.
 //
-// One block per tile, one thread per pixel; warp w covers the 8x4 pixel block
-// (8 (w & 1), 4 (w >> 1)) of the tile. The tile's sorted list is walked in
-// batches of 256 entries, double-buffered in shared memory: while the block
-// evaluates batch b, each thread already holds in registers the packed record
-// (three float4 written by the projection step) of its entry of batch b + 1,
-// and stores it to the other buffer afterwards, so the gathers overlap the
-// arithmetic. Each warp ballots which of the batch's entries have an
-// alpha >= 1/255 box (part of the record) that meets its 8x4 block and
-// evaluates only those, in list order, for its 32 pixels: an entry whose box
-// misses the block cannot contribute to any of its pixels, so skipping it
-// changes no result. The block leaves the list once all its pixels are done.
+// One 128-thread block per tile; warp w covers the 8x8 pixel block
+// (8 (w & 1), 8 (w >> 1)) of the tile and each lane two of its pixels, (x, y)
+// and (x, y + 4), which share the entry's loads, dx and the dx term of the
+// quadratic form. The tile's sorted list is walked in batches of 128 entries,
+// double-buffered in shared memory: while the block evaluates batch b, each
+// thread already holds in registers the packed record (three float4 written by
+// the projection step) of its entry of batch b + 1, and stores it to the other
+// buffer afterwards, so the gathers overlap the arithmetic. For each group of
+// 32 batch entries a warp ballots those whose alpha >= 1/255 box (part of the
+// record) meets its 8x8 block, copies their records into a per-warp list and
+// evaluates that list in order with a uniform loop: an entry whose box misses
+// the block cannot contribute to any of its pixels, so skipping it changes no
+// result. The block leaves the list once all its pixels are done.
 //
 // Coordinates are relative to the tile's first pixel: a centre enters as
 // (u - x0) + residual (an exact subtraction, then one rounding at small
@@ -25,8 +27,8 @@
 // near x = 1000 carries ~1e-4 px. The quadratic form is a sum of two squares,
 // log2(alpha) = log2 o - (k1 dx)^2 - (k2 dy + k3 dx)^2, which keeps its
 // accuracy for elongated footprints. Per evaluated (pixel, entry): two
-// subtractions, the form (5 FP32 ops), ex2 on the MUFU pipe, a min and a
-// compare, plus the blend for contributing pairs.
+// subtractions, the form (5 FP32 ops) and a compare; ex2 (MUFU pipe), the
+// 0.99 cap and the blend only for the pairs past the 1/255 test.
 #include <cuda_fp16.h>
 
 #include "gs_internal.cuh"
@@ -34,7 +36,7 @@
 namespace gs {
 namespace {
 
-constexpr int kRastThreads = kTile * kTile;
+constexpr int kRastThreads = 128;   // 4 warps, each an 8x8 pixel block, two pixels per lane
 constexpr float kLog2AlphaMin = -7.99435343685886f;   // log2(1/255)
 
 // 2^x on the MUFU pipe (PTX ex2.approx; relative error about 2^-22).
@@ -44,8 +46,40 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Launch order of the tiles: longest lists first, bucketed by floor(log2
+// length) (ties in tile order), so that the heaviest tiles start in the first
+// wave instead of trailing the last one. One block; per-bucket cursors in
+// shared memory.
+__global__ void __launch_bounds__(1024) tile_order_kernel(const uint2* __restrict__ ranges, int tiles,
+                                                          uint32_t* __restrict__ order) {
+    __shared__ uint32_t s_cnt[33];
+    if (threadIdx.x < 33) s_cnt[threadIdx.x] = 0;
+    __syncthreads();
+    for (int t = threadIdx.x; t < tiles; t += blockDim.x) {
+        const uint2 r = ranges[t];
+        const uint32_t len = r.y - r.x;
+        atomicAdd(&s_cnt[len ? 32 - __clz(len) : 0], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t run = 0;
+        for (int b = 32; b >= 0; b--) {
+            const uint32_t c = s_cnt[b];
+            s_cnt[b] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < tiles; t += blockDim.x) {
+        const uint2 r = ranges[t];
+        const uint32_t len = r.y - r.x;
+        order[atomicAdd(&s_cnt[len ? 32 - __clz(len) : 0], 1u)] = (uint32_t)t;
+    }
+}
+
 struct RastArgs {
     const float4* raster;   // [n][3]
+    const uint32_t* order;  // launch order of the tiles, or null for index order
     const uint32_t* sorted_vals;
     const uint2* ranges;
     uint32_t n;
@@ -56,7 +90,7 @@ struct RastArgs {
     uint32_t* n_contrib;
 };
 
-__global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs a) {
+__global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastArgs a) {
     __shared__ float4 s_q[2][kRastThreads];    // (mx, my, k1, k2), centre tile-local
     __shared__ float4 s_r[2][kRastThreads];    // (k3, log2 o, r, g)
     __shared__ float s_b[2][kRastThreads];     // b
@@ -65,22 +99,24 @@ __global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs 
     __shared__ float4 w_r[kRastThreads / 32][32];
     __shared__ float2 w_bj[kRastThreads / 32][32];  // (b, list position + 1 as bits)
 
-    const int tile = blockIdx.x;
+    const int tile = a.order ? (int)a.order[blockIdx.x] : (int)blockIdx.x;
     const int tx = tile % a.tiles_x, ty = tile / a.tiles_x;
     const float tile_x0 = (float)(tx * kTile), tile_y0 = (float)(ty * kTile);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t lt_mask = (1u << lane) - 1u;
-    const int lbx0 = 8 * (warp & 1), lby0 = 4 * (warp >> 1);   // warp's 8x4 block, tile-local
+    const int lbx0 = 8 * (warp & 1), lby0 = 8 * (warp >> 1);   // warp's 8x8 block, tile-local
+    // the lane's two pixels: (lx, ly) and (lx, ly + 4)
     const int lx = lbx0 + (lane & 7), ly = lby0 + (lane >> 3);
     const int px = tx * kTile + lx, py = ty * kTile + ly;
-    const float fbx0 = (float)lbx0, fbx1 = (float)(lbx0 + 7), fby0 = (float)lby0, fby1 = (float)(lby0 + 3);
-    const bool inside = px < a.width && py < a.height;
+    const float fbx0 = (float)lbx0, fbx1 = (float)(lbx0 + 7), fby0 = (float)lby0, fby1 = (float)(lby0 + 7);
     const uint2 range = a.ranges[tile];
-    const float fpx = (float)lx, fpy = (float)ly;
+    const float fpx = (float)lx, fpy = (float)ly, fpy2 = (float)(ly + 4);
 
     float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
-    uint32_t last = 0;
-    bool done = !inside;
+    float U = 1.0f, D0 = 0.0f, D1 = 0.0f, D2 = 0.0f;   // second pixel
+    uint32_t last = 0, last2 = 0;
+    bool done = !(px < a.width && py < a.height);
+    bool done2 = !(px < a.width && py + 4 < a.height);
 
     auto fetch = [&](uint32_t idx, float4& r0, float4& r1, float4& r2) {
         uint32_t g = __ldg(a.sorted_vals + idx);
@@ -126,7 +162,7 @@ __global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs 
         // evaluate the list in order for the warp's 32 pixels
 #pragma unroll 1
         for (int i = 0; i < kRastThreads / 32; i++) {
-            if (__all_sync(0xffffffffu, done)) break;
+            if (__all_sync(0xffffffffu, done && done2)) break;
             const uint32_t j = (uint32_t)(i * 32 + lane);
             bool hit = false;
             if (j < cnt) {
@@ -147,28 +183,43 @@ __global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs 
             for (int k = 0; k < nh; k++) {
                 const float4 q = w_q[warp][k];
                 const float4 r = w_r[warp][k];
-                const float dx = q.x - fpx, dy = q.y - fpy;
-                const float t1 = q.z * dx, t2 = fmaf(r.x, dx, q.w * dy);
-                const float e = fmaf(-t2, t2, fmaf(-t1, t1, r.y));
+                const float dx = q.x - fpx, dy = q.y - fpy, dy2 = q.y - fpy2;
+                const float t1 = q.z * dx;
+                const float t2 = fmaf(r.x, dx, q.w * dy), t22 = fmaf(r.x, dx, q.w * dy2);
+                const float e1 = fmaf(-t1, t1, r.y);   // shared by the two pixels (same dx)
+                const float e = fmaf(-t2, t2, e1), e2 = fmaf(-t22, t22, e1);
                 // alpha = min(0.99, 2^e) < 1/255 is e < log2(1/255) (the same
                 // decision in exact arithmetic; ex2 is only evaluated past it)
-                if (done || e < kLog2AlphaMin) continue;
-                const float alpha = fminf(0.99f, fast_exp2(e));
+                const bool c = !done && e >= kLog2AlphaMin, c2 = !done2 && e2 >= kLog2AlphaMin;
+                if (!(c || c2)) continue;
                 const float2 bj = w_bj[warp][k];
-                const float w = alpha * T;
-                C0 += w * r.z;
-                C1 += w * r.w;
-                C2 += w * bj.x;
-                T -= w;
-                last = __float_as_uint(bj.y);
-                if (T < 1e-4f) done = true;
+                if (c) {
+                    const float alpha = fminf(0.99f, fast_exp2(e));
+                    const float w = alpha * T;
+                    C0 += w * r.z;
+                    C1 += w * r.w;
+                    C2 += w * bj.x;
+                    T -= w;
+                    last = __float_as_uint(bj.y);
+                    if (T < 1e-4f) done = true;
+                }
+                if (c2) {
+                    const float alpha = fminf(0.99f, fast_exp2(e2));
+                    const float w = alpha * U;
+                    D0 += w * r.z;
+                    D1 += w * r.w;
+                    D2 += w * bj.x;
+                    U -= w;
+                    last2 = __float_as_uint(bj.y);
+                    if (U < 1e-4f) done2 = true;
+                }
             }
             __syncwarp();
         }
         if (have_next) store(buf ^ 1, n0, n1, n2);
-        if (__syncthreads_count(done) == kRastThreads) break;
+        if (__syncthreads_count(done && done2) == kRastThreads) break;
     }
-    if (inside) {
+    if (px < a.width && py < a.height) {
         const int64_t p = (int64_t)py * a.width + px;
         a.image[3 * p] = C0 + T * a.bg0;
         a.image[3 * p + 1] = C1 + T * a.bg1;
@@ -176,15 +227,24 @@ __global__ void __launch_bounds__(kRastThreads) rasterize_kernel(const RastArgs 
         if (a.final_T) a.final_T[p] = T;
         if (a.n_contrib) a.n_contrib[p] = last;
     }
+    if (px < a.width && py + 4 < a.height) {
+        const int64_t p = (int64_t)(py + 4) * a.width + px;
+        a.image[3 * p] = D0 + U * a.bg0;
+        a.image[3 * p + 1] = D1 + U * a.bg1;
+        a.image[3 * p + 2] = D2 + U * a.bg2;
+        if (a.final_T) a.final_T[p] = U;
+        if (a.n_contrib) a.n_contrib[p] = last2;
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* sorted_vals, const uint32_t* ranges,
-                             const CamConst& cam, float* image, float* final_T, uint32_t* n_contrib,
-                             cudaStream_t s) {
+                             uint32_t* tile_order, const CamConst& cam, float* image, float* final_T,
+                             uint32_t* n_contrib, cudaStream_t s) {
     RastArgs a;
     a.raster = reinterpret_cast<const float4*>(p.raster);
+    a.order = tile_order;
     a.sorted_vals = sorted_vals;
     a.ranges = reinterpret_cast<const uint2*>(ranges);
     a.n = (uint32_t)n;
@@ -199,6 +259,7 @@ cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* s
     a.n_contrib = n_contrib;
     const unsigned tiles = (unsigned)(cam.tiles_x * cam.tiles_y);
     if (n == 0) a.sorted_vals = nullptr;
+    if (tile_order) tile_order_kernel<<<1, 1024, 0, s>>>(a.ranges, (int)tiles, tile_order);
     rasterize_kernel<<<tiles, kRastThreads, 0, s>>>(a);
     return cudaGetLastError();
 }

@@ -65,7 +65,7 @@ _SIGNATURES = {
     "gs_tile_ranges32": (ctypes.c_int, [c_void_p, c_void_p, ctypes.c_int64, ctypes.POINTER(GsCamera),
                                         c_void_p, c_void_p]),
     "gs_rasterize": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, c_void_p, c_void_p,
-                                    ctypes.POINTER(GsCamera), c_void_p, c_void_p, c_void_p, c_void_p]),
+                                    ctypes.POINTER(GsCamera), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "gs_render_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                                     ctypes.c_int64]),
     "gs_render": (ctypes.c_int, [ctypes.POINTER(GsGaussians), ctypes.POINTER(GsCamera), ctypes.c_int64,

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define GS_ABI_VERSION 1
+#define GS_ABI_VERSION 2
 
 typedef enum gs_status {
     GS_OK = 0,
@@ -242,10 +242,15 @@ gs_status gs_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* num_key
  *     image = C + T * bg.
  * image: device float [height][width][3]. final_T (device float [h][w]) and
  * n_contrib (device uint32 [h][w], 1 + list position of the last
- * contributing Gaussian, 0 if none) may be NULL. */
+ * contributing Gaussian, 0 if none) may be NULL.
+ * tile_order: NULL, or device uint32 [tiles_x * tiles_y] scratch (caller
+ * owned, contents on entry ignored); when given, a first kernel orders the
+ * tiles by decreasing list length (bucketed by floor(log2 length)) and the
+ * tiles are launched in that order, which shortens the last wave. The image
+ * does not depend on it. */
 gs_status gs_rasterize(const gs_projected* projected, int64_t n, const uint32_t* sorted_vals,
                        const uint32_t* ranges, const gs_camera* camera, float* image,
-                       float* final_T, uint32_t* n_contrib, void* stream);
+                       float* final_T, uint32_t* n_contrib, uint32_t* tile_order, void* stream);
 
 /* The whole frame: step 1, the depth-first steps 2-4 (gs_depth_order,
  * gs_bin_ordered, gs_sort32, gs_tile_ranges32) and step 5, chained on

@@ -27,7 +27,7 @@ def test_library_builds_and_exports_every_declared_symbol():
     for name in names:
         assert hasattr(L, name), name
     assert set(names) == set(native._SIGNATURES), "binding must cover exactly the declared entry points"
-    assert L.gs_abi_version() == 1
+    assert L.gs_abi_version() == 2
 
 
 def test_status_strings():

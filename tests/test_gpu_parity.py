@@ -180,6 +180,40 @@ def test_render_equals_stages_and_graph_replay(oracle_mod):
     assert_image_parity(check_image(oracle_mod, ref, cam, out["image"], out["final_T"], out["n_contrib"]))
 
 
+def test_tile_order_is_heavy_first_and_leaves_image_unchanged():
+    """The heavy-first launch order is a permutation of the tiles with
+    non-increasing floor(log2 length); the image, final T and n_contrib do not
+    depend on it (bit for bit)."""
+    scene, g = scene_of("stress", n=300_000)
+    cam = scenes.make_cameras("stress")[2]
+    p = gs.preprocess(g, cam)
+    b = gs.bin_keys(p, cam, 0)
+    cap = int(b["num_keys"].item())
+    b = gs.bin_keys(p, cam, cap)
+    srt = gs.sort_pairs(b["keys"], b["vals"], b["num_keys"], gs.key_bits(cam), cap)
+    ranges = gs.tile_ranges(srt["keys"], b["num_keys"], cam, cap)
+    plain = gs.rasterize(p, srt["vals"], ranges, cam, heavy_first=False)
+    tx, ty = gs.tiles_xy(cam)
+    order = torch.full((tx * ty,), -1, dtype=torch.int32, device="cuda")
+    img = torch.empty_like(plain["image"])
+    fT = torch.empty_like(plain["final_T"])
+    nc = torch.empty_like(plain["n_contrib"])
+    native.check(gs.lib().gs_rasterize(ctypes.byref(gs.projected_struct(p)), int(g["n"]), srt["vals"].data_ptr(),
+                                       ranges.data_ptr(), ctypes.byref(gs.camera_struct(cam)), img.data_ptr(),
+                                       fT.data_ptr(), nc.data_ptr(), order.data_ptr(), None), "gs_rasterize")
+    torch.cuda.synchronize()
+    o = order.cpu().numpy()
+    assert np.array_equal(np.sort(o), np.arange(tx * ty))
+    rg = ranges.cpu().numpy().view(np.uint32).astype(np.int64)
+    lens = (rg[:, 1] - rg[:, 0])[o]
+    buckets = np.where(lens > 0, np.floor(np.log2(np.maximum(lens, 1))).astype(np.int64) + 1, 0)
+    assert np.all(np.diff(buckets) <= 0)
+    assert lens.max() > 1000      # the workload has heavy tiles
+    np.testing.assert_array_equal(img.cpu().numpy(), plain["image"].cpu().numpy())
+    np.testing.assert_array_equal(fT.cpu().numpy(), plain["final_T"].cpu().numpy())
+    np.testing.assert_array_equal(nc.cpu().numpy(), plain["n_contrib"].cpu().numpy())
+
+
 @pytest.mark.parametrize("degree", [0, 1, 2, 3])
 def test_sh_degrees_and_ragged_image(oracle_mod, degree):
     base = scenes.make_scene("100k", n=5000)
