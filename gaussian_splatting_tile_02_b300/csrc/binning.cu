@@ -53,19 +53,21 @@ __device__ __forceinline__ unsigned long long block_scan_incl(unsigned long long
     return v;
 }
 
-// 8-bit digit histograms of 32-bit keys, laid out as the radix sort expects
-// them ([pass][256]); accumulated in shared memory, flushed with one global
-// atomic per non-zero bin.
+// Digit histograms of 32-bit keys in the radix sort's digit layout
+// (digit_shift / digit_width, [pass][256]); accumulated in shared memory,
+// flushed with one global atomic per non-zero bin.
 constexpr int kHistPasses = 4;
+__device__ __forceinline__ uint32_t digit(uint32_t key, int key_bits, int p) {
+    return (key >> digit_shift(key_bits, p)) & ((1u << digit_width(key_bits, p)) - 1u);
+}
 __device__ __forceinline__ void count_digits(uint32_t* s_hist, uint32_t key, int key_bits) {
+    const int passes = digit_passes(key_bits);
 #pragma unroll
-    for (int p = 0; p < kHistPasses; p++) {
-        const int w = key_bits - 8 * p;
-        if (w > 0) atomicAdd(&s_hist[p * 256 + ((key >> (8 * p)) & ((1u << (w < 8 ? w : 8)) - 1u))], 1u);
-    }
+    for (int p = 0; p < kHistPasses; p++)
+        if (p < passes) atomicAdd(&s_hist[p * 256 + digit(key, key_bits, p)], 1u);
 }
 __device__ __forceinline__ void flush_digits(const uint32_t* s_hist, uint32_t* hist, int key_bits) {
-    const int n = ((key_bits + 7) / 8) * 256;
+    const int n = digit_passes(key_bits) * 256;
     for (int i = threadIdx.x; i < n; i += blockDim.x)
         if (s_hist[i]) atomicAdd(&hist[i], s_hist[i]);
 }
@@ -327,7 +329,12 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
     const unsigned long long S1 = S0 + kKeysPerBlock < Keff ? S0 + kKeysPerBlock : Keff;
     if (hist)
         for (int i = threadIdx.x; i < kHistPasses * 256; i += kExpandThreads) s_dhist[i] = 0;
-    const int hi_bits = key_bits - 8 < 8 ? key_bits - 8 : 8;   // second digit (tile ids < 2^16)
+    // digits above the first are counted per run of keys with equal high bits
+    const int passes = digit_passes(key_bits);
+    const int s1 = passes > 1 ? digit_shift(key_bits, 1) : 0;
+    auto flush_run = [&](uint32_t h, uint32_t cnt) {
+        for (int q = 1; q < passes; q++) atomicAdd(&s_dhist[q * 256 + digit(h << s1, key_bits, q)], cnt);
+    };
     const unsigned long long r0 = S0 + (unsigned long long)threadIdx.x * kRun;   // this thread's slots
     const unsigned long long r1 = r0 + kRun < S1 ? r0 + kRun : S1;
 
@@ -375,11 +382,11 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
                 s_key[si + (si >> 5)] = tile;
                 s_val[si + (si >> 5)] = s_g[lo];
                 if (hist) {
-                    atomicAdd(&s_dhist[tile & 255u], 1u);
-                    if (hi_bits > 0) {
-                        const uint32_t h = (tile >> 8) & ((1u << hi_bits) - 1u);
+                    atomicAdd(&s_dhist[digit(tile, key_bits, 0)], 1u);
+                    if (passes > 1) {
+                        const uint32_t h = tile >> s1;
                         if (h != run_hi) {
-                            if (run_n) atomicAdd(&s_dhist[256 + run_hi], run_n);
+                            if (run_n) flush_run(run_hi, run_n);
                             run_hi = h;
                             run_n = 0;
                         }
@@ -391,7 +398,7 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
                     ty++;
                 }
             }
-            if (hist && run_n) atomicAdd(&s_dhist[256 + run_hi], run_n);
+            if (hist && run_n) flush_run(run_hi, run_n);
         }
         if (s_end >= S1 || p + wn >= n) break;
         p += wn;

@@ -22,6 +22,18 @@ static_assert(sizeof(StatusHeader) == 256, "status header is 256 bytes");
 constexpr size_t kAlign = 256;
 __host__ __device__ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
+// Radix digits of a key_bits-bit key: ceil(key_bits / 8) LSD passes of 8-bit
+// digits from the least significant end, the last one narrower (13 bits ->
+// 8 + 5). The sort and the producers that count its digits share this layout.
+__host__ __device__ inline int digit_passes(int key_bits) { return (key_bits + 7) / 8; }
+__host__ __device__ inline int digit_width(int key_bits, int p) {
+    return key_bits - 8 * p < 8 ? key_bits - 8 * p : 8;
+}
+__host__ __device__ inline int digit_shift(int key_bits, int p) {
+    (void)key_bits;
+    return 8 * p;
+}
+
 inline int tiles_x(const gs_camera& c) { return (c.width + kTile - 1) / kTile; }
 inline int tiles_y(const gs_camera& c) { return (c.height + kTile - 1) / kTile; }
 

@@ -47,33 +47,59 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // Launch order of the tiles: longest lists first, bucketed by floor(log2
-// length) (ties in tile order), so that the heaviest tiles start in the first
-// wave instead of trailing the last one. One block; per-bucket cursors in
-// shared memory.
-__global__ void __launch_bounds__(1024) tile_order_kernel(const uint2* __restrict__ ranges, int tiles,
-                                                          uint32_t* __restrict__ order) {
+// length) (order within a bucket unspecified), so that the heaviest tiles
+// start in the first wave instead of trailing the last one. One block: a
+// count per bucket, a prefix over the 33 buckets, then a scatter through
+// per-bucket cursors; the shared-memory atomics are aggregated per warp over
+// lanes with the same bucket.
+constexpr int kOrderThreads = 1024, kOrderItems = 4;
+__global__ void __launch_bounds__(kOrderThreads) tile_order_kernel(const uint2* __restrict__ ranges, int tiles,
+                                                                   uint32_t* __restrict__ order) {
     __shared__ uint32_t s_cnt[33];
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt = (1u << lane) - 1u;
     if (threadIdx.x < 33) s_cnt[threadIdx.x] = 0;
     __syncthreads();
-    for (int t = threadIdx.x; t < tiles; t += blockDim.x) {
-        const uint2 r = ranges[t];
+    auto bucket = [&](int t) -> uint32_t {
+        if (t >= tiles) return 0xffffffffu;
+        const uint2 r = __ldg(ranges + t);
         const uint32_t len = r.y - r.x;
-        atomicAdd(&s_cnt[len ? 32 - __clz(len) : 0], 1u);
+        return len ? 32u - (uint32_t)__clz(len) : 0u;
+    };
+    for (int t0 = 0; t0 < tiles; t0 += kOrderItems * kOrderThreads) {
+        uint32_t b[kOrderItems];
+#pragma unroll
+        for (int i = 0; i < kOrderItems; i++) b[i] = bucket(t0 + i * kOrderThreads + threadIdx.x);
+#pragma unroll
+        for (int i = 0; i < kOrderItems; i++) {
+            const uint32_t peers = __match_any_sync(0xffffffffu, b[i]);
+            if (b[i] != 0xffffffffu && (peers & lt) == 0) atomicAdd(&s_cnt[b[i]], (uint32_t)__popc(peers));
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         uint32_t run = 0;
-        for (int b = 32; b >= 0; b--) {
-            const uint32_t c = s_cnt[b];
-            s_cnt[b] = run;
+        for (int k = 32; k >= 0; k--) {
+            const uint32_t c = s_cnt[k];
+            s_cnt[k] = run;
             run += c;
         }
     }
     __syncthreads();
-    for (int t = threadIdx.x; t < tiles; t += blockDim.x) {
-        const uint2 r = ranges[t];
-        const uint32_t len = r.y - r.x;
-        order[atomicAdd(&s_cnt[len ? 32 - __clz(len) : 0], 1u)] = (uint32_t)t;
+    for (int t0 = 0; t0 < tiles; t0 += kOrderItems * kOrderThreads) {
+        uint32_t b[kOrderItems];
+#pragma unroll
+        for (int i = 0; i < kOrderItems; i++) b[i] = bucket(t0 + i * kOrderThreads + threadIdx.x);
+#pragma unroll
+        for (int i = 0; i < kOrderItems; i++) {
+            const uint32_t peers = __match_any_sync(0xffffffffu, b[i]);
+            const int leader = __ffs(peers) - 1;
+            uint32_t base = 0;
+            if (b[i] != 0xffffffffu && lane == leader) base = atomicAdd(&s_cnt[b[i]], (uint32_t)__popc(peers));
+            base = __shfl_sync(0xffffffffu, base, leader);
+            if (b[i] != 0xffffffffu)
+                order[base + __popc(peers & lt)] = (uint32_t)(t0 + i * kOrderThreads + threadIdx.x);
+        }
     }
 }
 
@@ -259,7 +285,7 @@ cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* s
     a.n_contrib = n_contrib;
     const unsigned tiles = (unsigned)(cam.tiles_x * cam.tiles_y);
     if (n == 0) a.sorted_vals = nullptr;
-    if (tile_order) tile_order_kernel<<<1, 1024, 0, s>>>(a.ranges, (int)tiles, tile_order);
+    if (tile_order) tile_order_kernel<<<1, kOrderThreads, 0, s>>>(a.ranges, (int)tiles, tile_order);
     rasterize_kernel<<<tiles, kRastThreads, 0, s>>>(a);
     return cudaGetLastError();
 }

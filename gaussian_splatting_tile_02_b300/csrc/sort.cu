@@ -130,8 +130,8 @@ __global__ void __launch_bounds__(256) sort_histogram_kernel(const KeyT* __restr
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < K; i += stride) {
         const KeyT k = keys[i];
         for (int p = 0; p < passes; p++) {
-            const int w = key_bits - 8 * p < 8 ? key_bits - 8 * p : 8;
-            atomicAdd(&s_hist[p * kRadix + digit_of(k, 8 * p, (1u << w) - 1u)], 1u);
+            const int w = digit_width(key_bits, p);
+            atomicAdd(&s_hist[p * kRadix + digit_of(k, digit_shift(key_bits, p), (1u << w) - 1u)], 1u);
         }
     }
     __syncthreads();
@@ -181,6 +181,7 @@ struct PassArgs {
     const uint64_t* num_keys;
     int64_t cap;
     int pass;
+    int shift;
     int digit_bits;
     const uint32_t* bases;    // [256] for this pass
     uint32_t* counter;        // tile-id counter for this pass
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_ker
         a.status_clear[(int64_t)tile * kRadix + tid] = 0;
     }
 
-    const int shift = 8 * a.pass;
+    const int shift = a.shift;
     const uint32_t dmask = (1u << a.digit_bits) - 1u;
     const int warp_base = warp * (kSortItems * 32);
     KeyT key[kSortItems];
@@ -432,7 +433,8 @@ cudaError_t launch_sort_t(KeyT* keys, uint32_t* vals, KeyT* keys_alt, uint32_t* 
         a.num_keys = num_keys;
         a.cap = cap;
         a.pass = p;
-        a.digit_bits = key_bits - 8 * p < 8 ? key_bits - 8 * p : 8;
+        a.digit_bits = digit_width(key_bits, p);
+        a.shift = digit_shift(key_bits, p);
         a.bases = sc.hist + p * kRadix;
         a.counter = sc.counters + p;
         a.status = sc.lookback + (int64_t)(p % 2) * sc.max_tiles * kRadix;

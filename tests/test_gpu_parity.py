@@ -214,6 +214,30 @@ def test_tile_order_is_heavy_first_and_leaves_image_unchanged():
     np.testing.assert_array_equal(nc.cpu().numpy(), plain["n_contrib"].cpu().numpy())
 
 
+def test_8k_image_three_tile_digit_passes(oracle_mod):
+    """8192x4320: 138,240 tiles, 18-bit tile ids, so the tile sort takes three
+    digit passes whose histograms the key expansion counts. The frame must equal
+    the staged path (64-bit keys, histograms counted by the sort) bit for bit
+    and the oracle within the image tolerance."""
+    base = scenes.make_scene("100k", n=30_000)
+    cam = dict(scenes.make_cameras("100k")[0])
+    cam.update(width=8192, height=4320, fx=np.float32(6400.0), fy=np.float32(6400.0),
+               cx=np.float32(4096.0), cy=np.float32(2160.0))
+    tx, ty = gs.tiles_xy(cam)
+    assert (tx * ty - 1).bit_length() == 18
+    g = gs.gaussians_to_device(base)
+    out = run_stages(g, cam)
+    r = gs.Renderer.for_scene(g, cam)
+    r.render(cam)
+    torch.cuda.synchronize()
+    st, flags, K = r.status()
+    assert st == native.GS_OK and K == out["K"] and K > 10_000
+    np.testing.assert_array_equal(r.image.cpu().numpy(), out["image"])
+    np.testing.assert_array_equal(r.n_contrib.cpu().numpy(), out["n_contrib"])
+    ref = oracle_render(oracle_mod, base, cam)
+    assert_image_parity(check_image(oracle_mod, ref, cam, out["image"], out["final_T"], out["n_contrib"]))
+
+
 @pytest.mark.parametrize("degree", [0, 1, 2, 3])
 def test_sh_degrees_and_ragged_image(oracle_mod, degree):
     base = scenes.make_scene("100k", n=5000)
