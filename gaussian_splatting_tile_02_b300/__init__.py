@@ -22,11 +22,12 @@ import ctypes
 import numpy as np
 
 from . import native
-from .native import GsCamera, GsGaussians, GsProjected, check, lib
+from .native import GsCamera, GsGaussians, GsGaussiansGrad, GsProjected, GsProjectedGrad, check, lib
 
 __all__ = ["GsCamera", "camera_struct", "gaussians_to_device", "gaussians_struct", "preprocess",
            "bin_keys", "sort_pairs", "tile_ranges", "rasterize", "Renderer", "read_status",
-           "key_bits", "tiles_xy", "lib", "render_from_host"]
+           "key_bits", "tiles_xy", "lib", "render_from_host", "rasterize_backward", "preprocess_backward",
+           "alloc_param_grads"]
 
 
 def _torch():
@@ -184,6 +185,55 @@ def rasterize(p: dict, sorted_vals, ranges, cam: dict, stream=None, want_aux: bo
     return out
 
 
+# ------------------------------------------------------------------------------ backward
+
+def _pgrad_struct(d: dict) -> GsProjectedGrad:
+    s = GsProjectedGrad()
+    for k in ("mean2d", "conic", "opacity", "rgb"):
+        setattr(s, k, _ptr(d[k]))
+    return s
+
+
+def alloc_param_grads(g: dict) -> dict:
+    """Gradient arrays shaped like the Gaussian parameters (device, float32)."""
+    torch = _torch()
+    return {k: torch.empty_like(g[k]) for k in _FIELDS}
+
+
+def _ggrad_struct(d: dict) -> GsGaussiansGrad:
+    s = GsGaussiansGrad()
+    for k in _FIELDS:
+        setattr(s, k, _ptr(d[k]))
+    return s
+
+
+def rasterize_backward(p: dict, sorted_vals, ranges, cam: dict, final_T, n_contrib, grad_image,
+                       tile_order=None, stream=None) -> dict:
+    """Step 5 backward: dL/d(u, v), dL/d(conic A, B, C), dL/do, dL/dc per Gaussian."""
+    torch = _torch()
+    n = int(p["depth"].shape[0])
+    dev = ranges.device
+    out = {"mean2d": torch.empty((n, 2), dtype=torch.float32, device=dev),
+           "conic": torch.empty((n, 3), dtype=torch.float32, device=dev),
+           "opacity": torch.empty(n, dtype=torch.float32, device=dev),
+           "rgb": torch.empty((n, 3), dtype=torch.float32, device=dev)}
+    check(lib().gs_rasterize_backward(ctypes.byref(projected_struct(p)), n, _ptr(sorted_vals), _ptr(ranges),
+                                      ctypes.byref(camera_struct(cam)), _ptr(final_T), _ptr(n_contrib),
+                                      _ptr(grad_image), _ptr(tile_order), ctypes.byref(_pgrad_struct(out)),
+                                      _stream_ptr(stream)), "gs_rasterize_backward")
+    return out
+
+
+def preprocess_backward(g: dict, cam: dict, p: dict, pgrad: dict, stream=None) -> dict:
+    """Step 1 backward: parameter gradients from the projected ones."""
+    out = alloc_param_grads(g)
+    check(lib().gs_preprocess_backward(ctypes.byref(gaussians_struct(g)), ctypes.byref(camera_struct(cam)),
+                                       ctypes.byref(projected_struct(p)), ctypes.byref(_pgrad_struct(pgrad)),
+                                       ctypes.byref(_ggrad_struct(out)), _stream_ptr(stream)),
+          "gs_preprocess_backward")
+    return out
+
+
 def read_status(ws, stream=None) -> tuple:
     """(status, flags, num_keys) from a workspace header; synchronises the stream."""
     flags = ctypes.c_uint32(0)
@@ -238,6 +288,16 @@ class Renderer:
 
     def status(self, stream=None) -> tuple:
         return read_status(self.ws, stream)
+
+    def render_backward(self, cam: dict, grad_image, grads: dict | None = None, stream=None) -> dict:
+        """Parameter gradients of sum(grad_image * image) for the frame last
+        rendered with render(cam, aux=True) (no host synchronisation)."""
+        grads = alloc_param_grads(self.g) if grads is None else grads
+        check(lib().gs_render_backward(ctypes.byref(self._gs), ctypes.byref(camera_struct(cam)), self.key_capacity,
+                                       _ptr(self.ws), self.ws_bytes, _ptr(self.final_T), _ptr(self.n_contrib),
+                                       _ptr(grad_image), ctypes.byref(_ggrad_struct(grads)), _stream_ptr(stream)),
+              "gs_render_backward")
+        return grads
 
 
 def render_from_host(host: dict, renderer: Renderer, cam: dict, host_image, stream=None) -> None:

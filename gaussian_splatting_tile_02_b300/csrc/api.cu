@@ -81,7 +81,7 @@ int tile_bits_for(const gs_camera& c) {
 // gs_render workspace layout
 struct RenderLayout {
     size_t header, raster, depth, touched, rect, dkeys, dkeys_alt, order, order_alt, bin,
-        keys, vals, keys_alt, vals_alt, sort, ranges, tile_order, num_keys, total;
+        keys, vals, keys_alt, vals_alt, sort, ranges, tile_order, pgrad, num_keys, total;
 };
 
 RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
@@ -112,6 +112,7 @@ RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
     L.sort = take(sort_scratch_bytes(cap > n ? cap : n));
     L.ranges = take(8 * tiles);
     L.tile_order = take(4 * tiles);
+    L.pgrad = take(36 * un);   // backward: dL/d(u, v), dL/d(conic), dL/do, dL/dc
     L.total = o;
     return L;
 }
@@ -399,6 +400,76 @@ gs_status gs_render_from_host(const gs_gaussians* hg, const gs_gaussians* dg, co
     if (st != GS_OK) return st;
     const size_t img = (size_t)cam->width * cam->height * 3 * sizeof(float);
     return cuda_status(cudaMemcpyAsync(host_image, device_image, img, cudaMemcpyDeviceToHost, s));
+}
+
+static bool pgrad_ok(const gs_projected_grad* g, int64_t n) {
+    if (!g) return false;
+    if (n == 0) return true;
+    return g->mean2d && g->conic && g->opacity && g->rgb && aligned(g->mean2d, 8) && aligned(g->conic, 4) &&
+           aligned(g->opacity, 4) && aligned(g->rgb, 4);
+}
+
+static bool ggrad_ok(const gs_gaussians_grad* g, int64_t n) {
+    if (!g) return false;
+    if (n == 0) return true;
+    return g->means && g->quats && g->log_scales && g->opacity_logits && g->sh && aligned(g->means, 4) &&
+           aligned(g->quats, 4) && aligned(g->log_scales, 4) && aligned(g->opacity_logits, 4) && aligned(g->sh, 4);
+}
+
+gs_status gs_rasterize_backward(const gs_projected* p, int64_t n, const uint32_t* sorted_vals, const uint32_t* ranges,
+                                const gs_camera* cam, const float* final_T, const uint32_t* n_contrib,
+                                const float* grad_image, const uint32_t* tile_order, const gs_projected_grad* grad,
+                                void* stream) {
+    if (n < 0 || n > kMaxGaussians || !camera_ok(cam) || !projected_ok(p, n) || !ranges || !aligned(ranges, 8))
+        return GS_ERR_INVALID_ARG;
+    if (!final_T || !n_contrib || !grad_image || !pgrad_ok(grad, n)) return GS_ERR_INVALID_ARG;
+    if (n > 0 && (!p->raster || !sorted_vals)) return GS_ERR_INVALID_ARG;
+    return cuda_status(launch_rasterize_backward(*p, n, sorted_vals, ranges, tile_order, make_cam_const(*cam),
+                                                 final_T, n_contrib, grad_image, *grad, (cudaStream_t)stream));
+}
+
+gs_status gs_preprocess_backward(const gs_gaussians* g, const gs_camera* cam, const gs_projected* p,
+                                 const gs_projected_grad* grad_in, const gs_gaussians_grad* grad_out, void* stream) {
+    if (!gaussians_ok(g) || !camera_ok(cam) || !p || (g->n > 0 && !p->tiles_touched)) return GS_ERR_INVALID_ARG;
+    if (!pgrad_ok(grad_in, g->n) || !ggrad_ok(grad_out, g->n)) return GS_ERR_INVALID_ARG;
+    return cuda_status(launch_preprocess_backward(*g, make_cam_const(*cam), p->tiles_touched, *grad_in, *grad_out,
+                                                  (cudaStream_t)stream));
+}
+
+gs_status gs_render_backward(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, void* ws,
+                             size_t ws_bytes, const float* final_T, const uint32_t* n_contrib, const float* grad_image,
+                             const gs_gaussians_grad* grad_out, void* stream) {
+    if (!gaussians_ok(g) || !camera_ok(cam)) return GS_ERR_INVALID_ARG;
+    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
+    if (!final_T || !n_contrib || !grad_image || !ggrad_ok(grad_out, g->n)) return GS_ERR_INVALID_ARG;
+    const RenderLayout L = render_layout(g->n, cam->width, cam->height, key_capacity);
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GS_ERR_WORKSPACE;
+    if (g->n == 0) return GS_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* w = static_cast<char*>(ws);
+    gs_projected p;
+    p.mean2d = nullptr;
+    p.conic_opacity = nullptr;
+    p.rgb = nullptr;
+    p.radius = nullptr;
+    p.raster = reinterpret_cast<float*>(w + L.raster);
+    p.depth = reinterpret_cast<float*>(w + L.depth);
+    p.tiles_touched = reinterpret_cast<uint32_t*>(w + L.touched);
+    p.rect = reinterpret_cast<uint16_t*>(w + L.rect);
+    const size_t n = (size_t)g->n;
+    float* pg = reinterpret_cast<float*>(w + L.pgrad);
+    gs_projected_grad pgr;
+    pgr.mean2d = pg;
+    pgr.conic = pg + 2 * n;
+    pgr.opacity = pg + 5 * n;
+    pgr.rgb = pg + 6 * n;
+    const CamConst cc = make_cam_const(*cam);
+    cudaError_t e = launch_rasterize_backward(p, g->n, reinterpret_cast<const uint32_t*>(w + L.vals),
+                                              reinterpret_cast<const uint32_t*>(w + L.ranges),
+                                              reinterpret_cast<const uint32_t*>(w + L.tile_order), cc, final_T,
+                                              n_contrib, grad_image, pgr, s);
+    if (e == cudaSuccess) e = launch_preprocess_backward(*g, cc, p.tiles_touched, pgr, *grad_out, s);
+    return cuda_status(e);
 }
 
 gs_status gs_read_status(const void* ws, void* stream, uint32_t* flags, uint64_t* num_keys) {

@@ -116,6 +116,14 @@ cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* n
 cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations, cudaStream_t s);
 
 // rasterize.cu
+cudaError_t launch_rasterize_backward(const gs_projected& p, int64_t n, const uint32_t* sorted_vals,
+                                      const uint32_t* ranges, const uint32_t* tile_order, const CamConst& cam,
+                                      const float* final_T, const uint32_t* n_contrib, const float* grad_image,
+                                      const gs_projected_grad& grad, cudaStream_t s);
+cudaError_t launch_preprocess_backward(const gs_gaussians& g, const CamConst& cam, const uint32_t* tiles_touched,
+                                       const gs_projected_grad& gin, const gs_gaussians_grad& gout,
+                                       cudaStream_t s);
+
 // tile_order (nullable): [tiles] scratch that receives the heavy-first launch
 // order of the tiles; null launches them in index order (same image)
 cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* sorted_vals, const uint32_t* ranges,

@@ -33,6 +33,15 @@ class GsProjected(ctypes.Structure):
                 ("rect", c_void_p), ("raster", c_void_p)]
 
 
+class GsProjectedGrad(ctypes.Structure):
+    _fields_ = [("mean2d", c_void_p), ("conic", c_void_p), ("opacity", c_void_p), ("rgb", c_void_p)]
+
+
+class GsGaussiansGrad(ctypes.Structure):
+    _fields_ = [("means", c_void_p), ("quats", c_void_p), ("log_scales", c_void_p),
+                ("opacity_logits", c_void_p), ("sh", c_void_p)]
+
+
 GS_OK, GS_ERR_INVALID_ARG, GS_ERR_CAPACITY, GS_ERR_CUDA, GS_ERR_TIMEOUT, GS_ERR_WORKSPACE = range(6)
 GS_FLAG_CAPACITY, GS_FLAG_TIMEOUT = 1, 2
 
@@ -76,6 +85,15 @@ _SIGNATURES = {
     "gs_render_from_host": (ctypes.c_int, [ctypes.POINTER(GsGaussians), ctypes.POINTER(GsGaussians),
                                            ctypes.POINTER(GsCamera), ctypes.c_int64, c_void_p,
                                            ctypes.c_size_t, c_void_p, c_void_p, c_void_p]),
+    "gs_rasterize_backward": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, c_void_p, c_void_p,
+                                             ctypes.POINTER(GsCamera), c_void_p, c_void_p, c_void_p, c_void_p,
+                                             ctypes.POINTER(GsProjectedGrad), c_void_p]),
+    "gs_preprocess_backward": (ctypes.c_int, [ctypes.POINTER(GsGaussians), ctypes.POINTER(GsCamera),
+                                              ctypes.POINTER(GsProjected), ctypes.POINTER(GsProjectedGrad),
+                                              ctypes.POINTER(GsGaussiansGrad), c_void_p]),
+    "gs_render_backward": (ctypes.c_int, [ctypes.POINTER(GsGaussians), ctypes.POINTER(GsCamera), ctypes.c_int64,
+                                          c_void_p, ctypes.c_size_t, c_void_p, c_void_p, c_void_p,
+                                          ctypes.POINTER(GsGaussiansGrad), c_void_p]),
     "gs_read_status": (ctypes.c_int, [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_uint32),
                                       ctypes.POINTER(ctypes.c_uint64)]),
     "gs_set_spin_limit": (None, [ctypes.c_int64]),

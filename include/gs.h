@@ -291,6 +291,67 @@ gs_status gs_render_from_host(const gs_gaussians* host_gaussians,
                               int64_t key_capacity, void* ws, size_t ws_bytes,
                               float* device_image, float* host_image, void* stream);
 
+/* ---------------------------------------------------------------- backward
+ * Section "Rastérisation, non rayée": every stage of the renderer is
+ * differentiable, so the parameters can be fitted by gradient descent. The
+ * calls below return the gradient of a scalar loss L(image) given
+ * grad_image = dL/dimage (device float [h][w][3]), by the chain rule through
+ * the forward's functions with its discrete decisions (culling, tile lists,
+ * the 1/255 skip, the 1e-4 stop) held fixed. The forward's 0.99 cap gives a
+ * zero derivative where it is active. Gradient sums over pixels use float
+ * atomics, so their rounding order (not their value beyond rounding) varies
+ * between runs. All arrays are device arrays owned by the caller. */
+
+/* dL/d of the per-Gaussian projected quantities (step 1 outputs):
+ *   mean2d  [n][2] dL/d(u, v)
+ *   conic   [n][3] dL/d(A, B, C) of conic = Sigma'^-1 = [[A, B], [B, C]]
+ *   opacity [n]    dL/do, o = sigmoid(logit)
+ *   rgb     [n][3] dL/dc (the clamped SH colour) */
+typedef struct gs_projected_grad {
+    float* mean2d;
+    float* conic;
+    float* opacity;
+    float* rgb;
+} gs_projected_grad;
+
+/* dL/d of the parameters, same layouts as gs_gaussians (quats (w, x, y, z),
+ * sh [n][(D+1)^2][3]); every entry is written (zero for Gaussians that
+ * touch no tile). */
+typedef struct gs_gaussians_grad {
+    float* means;
+    float* quats;
+    float* log_scales;
+    float* opacity_logits;
+    float* sh;
+} gs_gaussians_grad;
+
+/* Step 5 backward. projected, sorted_vals, ranges: as given to gs_rasterize
+ * (after the forward of the same frame); final_T and n_contrib: the forward's
+ * outputs (device [h][w]). tile_order: NULL, or the tile_order scratch the
+ * forward filled (launch order only). Zeroes the four arrays of `grad`, then
+ * accumulates into them. */
+gs_status gs_rasterize_backward(const gs_projected* projected, int64_t n, const uint32_t* sorted_vals,
+                                const uint32_t* ranges, const gs_camera* camera,
+                                const float* final_T, const uint32_t* n_contrib,
+                                const float* grad_image, const uint32_t* tile_order,
+                                const gs_projected_grad* grad, void* stream);
+
+/* Step 1 backward: maps grad_in (from gs_rasterize_backward) to the
+ * parameters. projected->tiles_touched (from gs_preprocess of the same frame)
+ * marks the Gaussians that enter the image. */
+gs_status gs_preprocess_backward(const gs_gaussians* gaussians, const gs_camera* camera,
+                                 const gs_projected* projected, const gs_projected_grad* grad_in,
+                                 const gs_gaussians_grad* grad_out, void* stream);
+
+/* Backward of a gs_render frame: uses the intermediates that gs_render left
+ * in ws (same gaussians, camera and key_capacity, ws not reused in between)
+ * and the final_T / n_contrib it wrote. Chains gs_rasterize_backward and
+ * gs_preprocess_backward on `stream`; the projected gradients live in ws. */
+gs_status gs_render_backward(const gs_gaussians* gaussians, const gs_camera* camera,
+                             int64_t key_capacity, void* ws, size_t ws_bytes, const float* final_T,
+                             const uint32_t* n_contrib, const float* grad_image,
+                             const gs_gaussians_grad* grad_out, void* stream);
+
 /* Reads the status header at the start of a gs_bin, gs_sort or gs_render
  * workspace. SYNCHRONISES `stream`. flags/num_keys may be NULL. Returns
  * GS_ERR_TIMEOUT, GS_ERR_CAPACITY or GS_OK from the flags. num_keys is the
