@@ -64,6 +64,7 @@ def parse():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     return ap.parse_args()
 
@@ -184,6 +185,30 @@ def traffic_from_profile(kernel_file: str, profile: str):
     except Exception:
         pass
     return None
+
+
+def backward_summary(bwd, n, hbm_peak, fp32_peak):
+    """Backward of one frame (gs_render_backward): whole time, and its two steps.
+    Step 1 backward is HBM-bound: 236 B of parameters + 36 B of projected
+    gradients + 4 B tile count read, 236 B of parameter gradients written per
+    Gaussian. Step 5 backward walks every pixel's list up to its last
+    contributor; 9 FP32 ops per walked entry (the forward's exponent) is a
+    lower bound on its arithmetic, the gradient terms of contributing pairs
+    come on top."""
+    if bwd is None:
+        return None
+    pre_ms = bwd["preprocess_backward_ms"]
+    ras_ms = max(bwd["ms"] - pre_ms, 1e-9)
+    pre_bytes = (PARAM_BYTES_PER_G + 36 + 4 + PARAM_BYTES_PER_G) * n
+    walked = bwd["n_contrib_sum"]
+    ras_tops = OPS_PER_EVAL * walked / (ras_ms * 1e-3) / 1e12
+    return {"ms": bwd["ms"], "frames_per_s": 1e3 / bwd["ms"], "steps": bwd["steps"],
+            "preprocess_backward": {"ms": pre_ms, "bound": "hbm", "bytes": pre_bytes,
+                                    "GB/s": pre_bytes / (pre_ms * 1e-3) / 1e9,
+                                    "frac": pre_bytes / (pre_ms * 1e-3) / 1e9 / hbm_peak},
+            "rasterize_backward": {"ms": ras_ms, "bound": "alu", "walked_entries": walked,
+                                   "ops_lower_bound": OPS_PER_EVAL * walked, "Top/s": ras_tops,
+                                   "frac": ras_tops / fp32_peak}}
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -360,6 +385,43 @@ def run_ours(args, rank, local_rank, world):
             e2e = {"value": world * n_e2e / t_e2e, "unit": "frames/s", "h2d_bytes_per_step": int(h2d),
                    "d2h_bytes_per_step": int(d2h), "steps": n_e2e}
             del dst, r2
+        # --- backward of the same frame: gs_render_backward replayed on the
+        # forward's workspace (one forward with final T / n_contrib first)
+        bwd = None
+        if not args.no_backward:
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(1234)
+            gimg = torch.randn((cam["height"], cam["width"], 3), device=dev, generator=gen)
+            grads = gs.alloc_param_grads(g)
+            nb = max(3, min(args.steps, 50))
+            with torch.cuda.stream(stream):
+                r.render(cam, stream=stream, aux=True)
+                for _ in range(3):
+                    r.render_backward(cam, gimg, grads, stream=stream)
+                stream.synchronize()
+                b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda._sleep(int(40e6))
+                b0.record(stream)
+                for _ in range(nb):
+                    r.render_backward(cam, gimg, grads, stream=stream)
+                b1.record(stream)
+                # step 1 backward alone (the same launch gs_render_backward makes)
+                p_b = gs.preprocess(g, cam, stream=stream)
+                n_g = int(g["n"])
+                pg = {"mean2d": torch.zeros((n_g, 2), device=dev), "conic": torch.zeros((n_g, 3), device=dev),
+                      "opacity": torch.zeros(n_g, device=dev), "rgb": torch.zeros((n_g, 3), device=dev)}
+                for _ in range(3):
+                    gs.preprocess_backward(g, cam, p_b, pg, stream=stream)
+                b2, b3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda._sleep(int(40e6))
+                b2.record(stream)
+                for _ in range(nb):
+                    gs.preprocess_backward(g, cam, p_b, pg, stream=stream)
+                b3.record(stream)
+            torch.cuda.synchronize(dev)
+            bwd = {"ms": b0.elapsed_time(b1) / nb, "preprocess_backward_ms": b2.elapsed_time(b3) / nb,
+                   "steps": nb, "n_contrib_sum": int(r.n_contrib.to(torch.int64).sum().item())}
+            del grads, pg, p_b
     clocks = sampler.summary()
 
     # --- algorithmic work of the last frame (from its outputs)
@@ -439,6 +501,7 @@ def run_ours(args, rank, local_rank, world):
         "stages": stages_out,
         "stage_sum_ms": stage_total,
         "hbm_peak_gbs": hbm_peak,
+        "backward": backward_summary(bwd, int(g["n"]), hbm_peak, fp32_peak),
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -26,8 +26,9 @@
 // The tile, warp and lane layout, the per-warp ballot of entries whose alpha
 // box meets the warp's 8x8 block, and the list staging are the forward's; the
 // list is walked from the last contributor of the tile backwards. Per entry,
-// the warp sums its lanes' contributions with shuffles and one lane adds them
-// to the Gaussian's gradient with global atomics.
+// the warp sums its lanes' contributions (a reduce-scatter of the 9 values
+// over the lanes) and nine lanes add them to the Gaussian's gradient with one
+// global atomic instruction.
 //
 // Step 1 backward (preprocess_backward_kernel): one thread per Gaussian maps
 // dL/d(u, v), dL/d(conic), dL/do, dL/dc to the parameters through
@@ -53,10 +54,30 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Sums 9 per-lane values over the warp as a reduce-scatter: at each butterfly
+// step a lane keeps one half of its slots and receives the partner's partial
+// sums of that half (8 + 4 + 2 + 1 + 1 = 16 shuffles for 16 slots, 7 of them
+// zero). Returns the complete sum of slot slot_of(lane) on even lanes.
+__device__ __forceinline__ float warp_reduce_scatter9(const float (&in)[9], int lane) {
+    float v[16];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+    for (int i = 0; i < 9; i++) v[i] = in[i];
+#pragma unroll
+    for (int i = 9; i < 16; i++) v[i] = 0.0f;
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1) {
+        const bool up = (lane & (2 * w)) != 0;
+#pragma unroll
+        for (int i = 0; i < w; i++) {
+            const float send = up ? v[i] : v[i + w];
+            const float keep = up ? v[i + w] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+__device__ __forceinline__ int slot_of(int lane) {
+    return ((lane >> 1) & 1) | (((lane >> 2) & 1) << 1) | (((lane >> 3) & 1) << 2) | (((lane >> 4) & 1) << 3);
 }
 
 struct BwdArgs {
@@ -218,7 +239,7 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
                 auto accumulate = [&](PixelState& S, float ee, float tt2, float ddy) {
                     const float raw = fast_exp2(ee);
                     const float alpha = fminf(0.99f, raw);
-                    const float Ti = S.T / (1.0f - alpha);
+                    const float Ti = __fdividef(S.T, 1.0f - alpha);   // 1 - alpha >= 0.01
                     const float w = alpha * Ti;
                     gr += w * S.g0;
                     gg += w * S.g1;
@@ -241,28 +262,16 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
                 };
                 if (c1) accumulate(P1, e, t2, dy);
                 if (c2) accumulate(P2, e2, t22, dy2);
-                gu = warp_sum(gu);
-                gv = warp_sum(gv);
-                gA = warp_sum(gA);
-                gB = warp_sum(gB);
-                gC = warp_sum(gC);
-                go = warp_sum(go);
-                gr = warp_sum(gr);
-                gg = warp_sum(gg);
-                gb = warp_sum(gb);
-                if (lane == 0) {
-                    const uint32_t g = __float_as_uint(c.w);
-                    if (g < a.n) {
-                        atomicAdd(a.g_mean2d + 2 * g, gu);
-                        atomicAdd(a.g_mean2d + 2 * g + 1, gv);
-                        atomicAdd(a.g_conic + 3 * g, gA);
-                        atomicAdd(a.g_conic + 3 * g + 1, gB);
-                        atomicAdd(a.g_conic + 3 * g + 2, gC);
-                        atomicAdd(a.g_opacity + g, go);
-                        atomicAdd(a.g_rgb + 3 * g, gr);
-                        atomicAdd(a.g_rgb + 3 * g + 1, gg);
-                        atomicAdd(a.g_rgb + 3 * g + 2, gb);
-                    }
+                const float part[9] = {gu, gv, gA, gB, gC, go, gr, gg, gb};
+                const float sum = warp_reduce_scatter9(part, lane);
+                const int slot = slot_of(lane);
+                const uint32_t g = __float_as_uint(c.w);
+                if (!(lane & 1) && slot < 9 && g < a.n) {
+                    float* dst = slot < 2 ? a.g_mean2d + 2 * g + slot
+                               : slot < 5 ? a.g_conic + 3 * g + (slot - 2)
+                               : slot < 6 ? a.g_opacity + g
+                                          : a.g_rgb + 3 * g + (slot - 6);
+                    atomicAdd(dst, sum);
                 }
             }
             __syncwarp();
@@ -347,20 +356,19 @@ struct PreBwdArgs {
     float* d_sh;
 };
 
+// One Gaussian; row holds its SH coefficients on entry and their gradients on
+// return.
 template <int D>
-__global__ void __launch_bounds__(256) preprocess_backward_kernel(const PreBwdArgs a) {
+__device__ __forceinline__ void gaussian_backward(const PreBwdArgs& a, int64_t g, float* row) {
     constexpr int NK = (D + 1) * (D + 1);
-    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (g >= a.n) return;
     const CamConst& C = a.cam;
-    float* dsh = a.d_sh + g * NK * 3;
     if (__ldg(a.tiles_touched + g) == 0) {
         // culled or off-screen: the image does not depend on this Gaussian
         for (int i = 0; i < 3; i++) a.d_means[3 * g + i] = 0.f;
         for (int i = 0; i < 4; i++) a.d_quats[4 * g + i] = 0.f;
         for (int i = 0; i < 3; i++) a.d_log_scales[3 * g + i] = 0.f;
         a.d_logits[g] = 0.f;
-        for (int i = 0; i < NK * 3; i++) dsh[i] = 0.f;
+        for (int i = 0; i < NK * 3; i++) row[i] = 0.f;
         return;
     }
     const float m[3] = {__ldg(a.means + 3 * g), __ldg(a.means + 3 * g + 1), __ldg(a.means + 3 * g + 2)};
@@ -375,18 +383,17 @@ __global__ void __launch_bounds__(256) preprocess_backward_kernel(const PreBwdAr
         float Y[NK];
         float3 dY[NK];
         sh_basis_grad<NK>(x, y, z, Y, dY);
-        const float* sh = a.sh + g * NK * 3;
         float raw[3] = {0.5f, 0.5f, 0.5f};
         for (int k = 0; k < NK; k++)
-            for (int c = 0; c < 3; c++) raw[c] = fmaf(Y[k], __ldg(sh + 3 * k + c), raw[c]);
+            for (int c = 0; c < 3; c++) raw[c] = fmaf(Y[k], row[3 * k + c], raw[c]);
         float gc[3];
         for (int c = 0; c < 3; c++) gc[c] = raw[c] > 0.f ? __ldg(a.g_rgb + 3 * g + c) : 0.f;
         float gd[3] = {0.f, 0.f, 0.f};
         for (int k = 0; k < NK; k++) {
             float s = 0.f;
             for (int c = 0; c < 3; c++) {
-                dsh[3 * k + c] = Y[k] * gc[c];
-                s = fmaf(__ldg(sh + 3 * k + c), gc[c], s);
+                s = fmaf(row[3 * k + c], gc[c], s);
+                row[3 * k + c] = Y[k] * gc[c];
             }
             gd[0] = fmaf(dY[k].x, s, gd[0]);
             gd[1] = fmaf(dY[k].y, s, gd[1]);
@@ -504,6 +511,30 @@ __global__ void __launch_bounds__(256) preprocess_backward_kernel(const PreBwdAr
     a.d_quats[4 * g + 3] = (dz - dd * zq) * iq;
 }
 
+// The block's SH coefficients (and then their gradients) pass through shared
+// memory, so that global reads and writes of the 48 floats per Gaussian are
+// coalesced across the block; one padding word per Gaussian keeps the
+// per-thread rows (stride NC + 1) in distinct banks.
+constexpr int kPreBwdThreads = 128;
+
+template <int D>
+__global__ void __launch_bounds__(kPreBwdThreads) preprocess_backward_kernel(const PreBwdArgs a) {
+    constexpr int NK = (D + 1) * (D + 1);
+    constexpr int NC = NK * 3, NS = NC + 1;
+    __shared__ float s_sh[kPreBwdThreads * NS];
+    const int64_t g0 = (int64_t)blockIdx.x * kPreBwdThreads;
+    const int cnt = (int)(a.n - g0 < kPreBwdThreads ? a.n - g0 : kPreBwdThreads);
+    for (int i = threadIdx.x; i < cnt * NC; i += kPreBwdThreads)
+        s_sh[(i / NC) * NS + i % NC] = __ldg(a.sh + g0 * NC + i);
+    __syncthreads();
+    const int64_t g = g0 + threadIdx.x;
+    float* row = s_sh + threadIdx.x * NS;
+    if (threadIdx.x < cnt) gaussian_backward<D>(a, g, row);
+    __syncthreads();
+    for (int i = threadIdx.x; i < cnt * NC; i += kPreBwdThreads)
+        a.d_sh[g0 * NC + i] = s_sh[(i / NC) * NS + i % NC];
+}
+
 }  // namespace
 
 cudaError_t launch_rasterize_backward(const gs_projected& p, int64_t n, const uint32_t* sorted_vals,
@@ -562,12 +593,12 @@ cudaError_t launch_preprocess_backward(const gs_gaussians& g, const CamConst& ca
     a.d_log_scales = gout.log_scales;
     a.d_logits = gout.opacity_logits;
     a.d_sh = gout.sh;
-    const unsigned blocks = (unsigned)((g.n + 255) / 256);
+    const unsigned blocks = (unsigned)((g.n + kPreBwdThreads - 1) / kPreBwdThreads);
     switch (g.sh_degree) {
-        case 0: preprocess_backward_kernel<0><<<blocks, 256, 0, s>>>(a); break;
-        case 1: preprocess_backward_kernel<1><<<blocks, 256, 0, s>>>(a); break;
-        case 2: preprocess_backward_kernel<2><<<blocks, 256, 0, s>>>(a); break;
-        default: preprocess_backward_kernel<3><<<blocks, 256, 0, s>>>(a); break;
+        case 0: preprocess_backward_kernel<0><<<blocks, kPreBwdThreads, 0, s>>>(a); break;
+        case 1: preprocess_backward_kernel<1><<<blocks, kPreBwdThreads, 0, s>>>(a); break;
+        case 2: preprocess_backward_kernel<2><<<blocks, kPreBwdThreads, 0, s>>>(a); break;
+        default: preprocess_backward_kernel<3><<<blocks, kPreBwdThreads, 0, s>>>(a); break;
     }
     return cudaGetLastError();
 }
