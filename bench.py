@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-batch", action="store_true")
+    ap.add_argument("--batch-streams", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     return ap.parse_args()
 
@@ -422,6 +424,44 @@ def run_ours(args, rank, local_rank, world):
             bwd = {"ms": b0.elapsed_time(b1) / nb, "preprocess_backward_ms": b2.elapsed_time(b3) / nb,
                    "steps": nb, "n_contrib_sum": int(r.n_contrib.to(torch.int64).sum().item())}
             del grads, pg, p_b
+        # --- several views per call: gs_render_batch against the same views
+        # rendered one gs_render after another
+        batch = None
+        if not args.no_batch:
+            bcams = cams if len(cams) > 1 else [scenes.orbit_camera(th, cfg.cam_distance, cfg.focal, cfg.width,
+                                                                    cfg.height, cfg.near, cfg.bg)
+                                                for th in (0.0, 90.0, 180.0, 270.0)]
+            br = gs.BatchRenderer.for_scene(g, bcams, headroom=1.1, n_streams=args.batch_streams)
+            single = gs.Renderer(g, cfg.width, cfg.height, br.key_capacity)
+            nbt = max(3, min(args.steps // len(bcams), 20))
+            with torch.cuda.stream(stream):
+                for _ in range(2):
+                    br.render(stream=stream)
+                    for c in bcams:
+                        single.render(c, stream=stream, aux=False)
+                stream.synchronize()
+                c0, c1, c2, c3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+                torch.cuda._sleep(int(40e6))
+                c0.record(stream)
+                for _ in range(nbt):
+                    for c in bcams:
+                        single.render(c, stream=stream, aux=False)
+                c1.record(stream)
+                torch.cuda._sleep(int(40e6))
+                c2.record(stream)
+                for _ in range(nbt):
+                    br.render(stream=stream)
+                c3.record(stream)
+            torch.cuda.synchronize(dev)
+            for v in range(len(bcams)):
+                if br.status(v)[0] != native.GS_OK:
+                    raise RuntimeError(f"batch view {v} status {br.status(v)}")
+            seq_ms, bat_ms = c0.elapsed_time(c1) / nbt, c2.elapsed_time(c3) / nbt
+            batch = {"views": len(bcams), "streams": args.batch_streams, "steps": nbt,
+                     "ms_per_batch": bat_ms, "views_per_s": len(bcams) * 1e3 / bat_ms,
+                     "sequential_ms": seq_ms, "sequential_views_per_s": len(bcams) * 1e3 / seq_ms,
+                     "speedup": seq_ms / bat_ms}
+            del br, single
     clocks = sampler.summary()
 
     # --- algorithmic work of the last frame (from its outputs)
@@ -502,6 +542,7 @@ def run_ours(args, rank, local_rank, world):
         "stage_sum_ms": stage_total,
         "hbm_peak_gbs": hbm_peak,
         "backward": backward_summary(bwd, int(g["n"]), hbm_peak, fp32_peak),
+        "batch": batch,
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

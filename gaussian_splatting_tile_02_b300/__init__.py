@@ -27,7 +27,7 @@ from .native import GsCamera, GsGaussians, GsGaussiansGrad, GsProjected, GsProje
 __all__ = ["GsCamera", "camera_struct", "gaussians_to_device", "gaussians_struct", "preprocess",
            "bin_keys", "sort_pairs", "tile_ranges", "rasterize", "Renderer", "read_status",
            "key_bits", "tiles_xy", "lib", "render_from_host", "rasterize_backward", "preprocess_backward",
-           "alloc_param_grads"]
+           "alloc_param_grads", "BatchRenderer"]
 
 
 def _torch():
@@ -298,6 +298,58 @@ class Renderer:
                                        _ptr(grad_image), ctypes.byref(_ggrad_struct(grads)), _stream_ptr(stream)),
               "gs_render_backward")
         return grads
+
+
+class BatchRenderer:
+    """Several views of one scene per call (gs_render_batch): one projection
+    pass over the parameters for all views, then each view's steps 2-5 on one
+    of ``n_streams`` streams so that the views overlap on the GPU."""
+
+    def __init__(self, g: dict, cams: list, key_capacity: int, n_streams: int = 4):
+        torch = _torch()
+        self.g = g
+        self.cams = list(cams)
+        self.views = len(self.cams)
+        self.width, self.height = int(self.cams[0]["width"]), int(self.cams[0]["height"])
+        self.key_capacity = int(key_capacity)
+        n = int(g["n"])
+        self.ws_bytes = int(lib().gs_render_batch_workspace_bytes(n, self.width, self.height, self.key_capacity,
+                                                                 self.views))
+        if self.ws_bytes == 0:
+            raise ValueError("unsupported batch")
+        self.view_ws_bytes = int(lib().gs_render_workspace_bytes(n, self.width, self.height, self.key_capacity))
+        dev = g["means"].device
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        V, H, W = self.views, self.height, self.width
+        self.images = torch.empty((V, H, W, 3), dtype=torch.float32, device=dev)
+        self.final_T = torch.empty((V, H, W), dtype=torch.float32, device=dev)
+        self.n_contrib = torch.empty((V, H, W), dtype=torch.int32, device=dev)
+        self.extra_streams = [torch.cuda.Stream(device=dev) for _ in range(max(0, n_streams - 1))]
+        self._gs = gaussians_struct(g)
+        self._cams = (GsCamera * V)(*[camera_struct(c) for c in self.cams])
+
+    @classmethod
+    def for_scene(cls, scene: dict, cams: list, headroom: float = 1.25, n_streams: int = 4,
+                  device="cuda") -> "BatchRenderer":
+        g = gaussians_to_device(scene, device) if isinstance(scene["means"], np.ndarray) else scene
+        k = max(Renderer.count_keys(g, c) for c in cams)
+        return cls(g, cams, int(k * headroom) + 1024, n_streams)
+
+    def render(self, stream=None, aux: bool = False):
+        """Renders every view into self.images [V, H, W, 3] (no host synchronisation)."""
+        torch = _torch()
+        s0 = stream if stream is not None else torch.cuda.current_stream()
+        handles = [s0.cuda_stream] + [s.cuda_stream for s in self.extra_streams]
+        arr = (ctypes.c_void_p * len(handles))(*handles)
+        check(lib().gs_render_batch(ctypes.byref(self._gs), self._cams, self.views, self.key_capacity,
+                                    _ptr(self.ws), self.ws_bytes, _ptr(self.images),
+                                    _ptr(self.final_T) if aux else None, _ptr(self.n_contrib) if aux else None,
+                                    arr, len(handles)), "gs_render_batch")
+        return self.images
+
+    def status(self, view: int, stream=None) -> tuple:
+        """(status, flags, num_keys) of one view; synchronises the stream."""
+        return read_status(self.ws[view * self.view_ws_bytes:], stream)
 
 
 def render_from_host(host: dict, renderer: Renderer, cam: dict, host_image, stream=None) -> None:

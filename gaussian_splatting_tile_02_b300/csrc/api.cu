@@ -3,6 +3,9 @@
 #include <math.h>
 #include <string.h>
 
+#include <map>
+#include <mutex>
+
 #include "gs_internal.cuh"
 
 namespace gs {
@@ -117,23 +120,10 @@ RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
     return L;
 }
 
-}  // namespace
-}  // namespace gs
-
-namespace gs {
-namespace {
-
-gs_status render_impl(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, void* ws, size_t ws_bytes,
-                      float* image, float* final_T, uint32_t* n_contrib, void* stream, void* const* events) {
-    if (!gaussians_ok(g) || !camera_ok(cam) || !image) return GS_ERR_INVALID_ARG;
-    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
-    const RenderLayout L = render_layout(g->n, cam->width, cam->height, key_capacity);
-    if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GS_ERR_WORKSPACE;
-    cudaStream_t s = (cudaStream_t)stream;
-    char* w = static_cast<char*>(ws);
-    auto* header = reinterpret_cast<StatusHeader*>(w + L.header);
-    auto* num_keys = reinterpret_cast<uint64_t*>(w + L.num_keys);
-    gs_projected p;   // only what binning and compositing read
+// The projected record of a view inside its gs_render workspace (only what
+// binning and compositing read).
+gs_projected view_projected(char* w, const RenderLayout& L) {
+    gs_projected p;
     p.mean2d = nullptr;
     p.conic_opacity = nullptr;
     p.rgb = nullptr;
@@ -142,6 +132,24 @@ gs_status render_impl(const gs_gaussians* g, const gs_camera* cam, int64_t key_c
     p.depth = reinterpret_cast<float*>(w + L.depth);
     p.tiles_touched = reinterpret_cast<uint32_t*>(w + L.touched);
     p.rect = reinterpret_cast<uint16_t*>(w + L.rect);
+    return p;
+}
+
+}  // namespace
+}  // namespace gs
+
+namespace gs {
+namespace {
+
+// Steps 2-5 of one view (and step 1 unless the caller already ran it into
+// this view's workspace), on stream s. events: null, or 7 handles recorded at
+// the stage boundaries.
+cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, char* w,
+                          const RenderLayout& L, float* image, float* final_T, uint32_t* n_contrib, cudaStream_t s,
+                          void* const* events, bool run_preprocess) {
+    auto* header = reinterpret_cast<StatusHeader*>(w + L.header);
+    auto* num_keys = reinterpret_cast<uint64_t*>(w + L.num_keys);
+    gs_projected p = view_projected(w, L);
     auto* dkeys = reinterpret_cast<uint32_t*>(w + L.dkeys);
     auto* dkeys_alt = reinterpret_cast<uint32_t*>(w + L.dkeys_alt);
     auto* order = reinterpret_cast<uint32_t*>(w + L.order);
@@ -165,7 +173,7 @@ gs_status render_impl(const gs_gaussians* g, const gs_camera* cam, int64_t key_c
     };
     cudaError_t e = mark(0);
     if (e == cudaSuccess) e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
-    if (e == cudaSuccess) e = launch_preprocess(*g, cc, p, s);
+    if (e == cudaSuccess && run_preprocess) e = launch_preprocess(*g, cc, p, s);
     if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess) e = sort_prepare_histogram(sort_ws, s);
     if (e == cudaSuccess) e = launch_depth_keys(p, g->n, dkeys, order, hist, s);
@@ -189,8 +197,47 @@ gs_status render_impl(const gs_gaussians* g, const gs_camera* cam, int64_t key_c
         e = launch_rasterize(p, g->n, vals, ranges, reinterpret_cast<uint32_t*>(w + L.tile_order), cc, image, final_T,
                              n_contrib, s);
     if (e == cudaSuccess) e = mark(6);
-    return cuda_status(e);
+    return e;
 }
+
+gs_status render_impl(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, void* ws, size_t ws_bytes,
+                      float* image, float* final_T, uint32_t* n_contrib, void* stream, void* const* events) {
+    if (!gaussians_ok(g) || !camera_ok(cam) || !image) return GS_ERR_INVALID_ARG;
+    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
+    const RenderLayout L = render_layout(g->n, cam->width, cam->height, key_capacity);
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GS_ERR_WORKSPACE;
+    return cuda_status(view_pipeline(g, cam, key_capacity, static_cast<char*>(ws), L, image, final_T, n_contrib,
+                                     (cudaStream_t)stream, events, true));
+}
+
+// Fork/join events for gs_render_batch, created once per device on first use
+// (timing disabled, so recording them costs no timestamp).
+constexpr int kMaxBatchStreams = 8;
+struct BatchEvents {
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t join[kMaxBatchStreams] = {};
+};
+std::mutex g_batch_mutex;
+std::map<int, BatchEvents> g_batch_events;
+
+cudaError_t batch_events(BatchEvents** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_batch_mutex);
+    auto it = g_batch_events.find(dev);
+    if (it == g_batch_events.end()) {
+        BatchEvents be;
+        e = cudaEventCreateWithFlags(&be.fork, cudaEventDisableTiming);
+        for (int i = 0; e == cudaSuccess && i < kMaxBatchStreams; i++)
+            e = cudaEventCreateWithFlags(&be.join[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+        it = g_batch_events.emplace(dev, be).first;
+    }
+    *out = &it->second;
+    return cudaSuccess;
+}
+
 }  // namespace
 }  // namespace gs
 
@@ -447,15 +494,7 @@ gs_status gs_render_backward(const gs_gaussians* g, const gs_camera* cam, int64_
     if (g->n == 0) return GS_OK;
     cudaStream_t s = (cudaStream_t)stream;
     char* w = static_cast<char*>(ws);
-    gs_projected p;
-    p.mean2d = nullptr;
-    p.conic_opacity = nullptr;
-    p.rgb = nullptr;
-    p.radius = nullptr;
-    p.raster = reinterpret_cast<float*>(w + L.raster);
-    p.depth = reinterpret_cast<float*>(w + L.depth);
-    p.tiles_touched = reinterpret_cast<uint32_t*>(w + L.touched);
-    p.rect = reinterpret_cast<uint16_t*>(w + L.rect);
+    const gs_projected p = view_projected(w, L);
     const size_t n = (size_t)g->n;
     float* pg = reinterpret_cast<float*>(w + L.pgrad);
     gs_projected_grad pgr;
@@ -470,6 +509,61 @@ gs_status gs_render_backward(const gs_gaussians* g, const gs_camera* cam, int64_
                                               n_contrib, grad_image, pgr, s);
     if (e == cudaSuccess) e = launch_preprocess_backward(*g, cc, p.tiles_touched, pgr, *grad_out, s);
     return cuda_status(e);
+}
+
+size_t gs_render_batch_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity,
+                                       int32_t views) {
+    if (views < 1 || views > GS_MAX_BATCH_VIEWS) return 0;
+    return (size_t)views * gs_render_workspace_bytes(n, width, height, key_capacity);
+}
+
+gs_status gs_render_batch(const gs_gaussians* g, const gs_camera* cams, int32_t views, int64_t key_capacity,
+                          void* ws, size_t ws_bytes, float* images, float* final_T, uint32_t* n_contrib,
+                          void* const* streams, int32_t n_streams) {
+    if (!gaussians_ok(g) || !cams || views < 1 || views > GS_MAX_BATCH_VIEWS || !images) return GS_ERR_INVALID_ARG;
+    if (!streams || n_streams < 1 || n_streams > kMaxBatchStreams) return GS_ERR_INVALID_ARG;
+    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
+    for (int v = 0; v < views; v++) {
+        if (!camera_ok(cams + v)) return GS_ERR_INVALID_ARG;
+        if (cams[v].width != cams[0].width || cams[v].height != cams[0].height) return GS_ERR_INVALID_ARG;
+    }
+    const RenderLayout L = render_layout(g->n, cams[0].width, cams[0].height, key_capacity);
+    const size_t stride = L.total;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < stride * (size_t)views) return GS_ERR_WORKSPACE;
+    BatchEvents* ev = nullptr;
+    if (batch_events(&ev) != cudaSuccess) return GS_ERR_CUDA;
+    char* w0 = static_cast<char*>(ws);
+    const size_t pix = (size_t)cams[0].width * cams[0].height;
+    cudaStream_t s0 = (cudaStream_t)streams[0];
+    // step 1 for all views, one pass over the parameters (chunks of kMaxBatchViews)
+    for (int v0 = 0; v0 < views; v0 += kMaxBatchViews) {
+        const int nv = views - v0 < kMaxBatchViews ? views - v0 : kMaxBatchViews;
+        CamConst cc[kMaxBatchViews];
+        gs_projected pr[kMaxBatchViews];
+        for (int i = 0; i < nv; i++) {
+            cc[i] = make_cam_const(cams[v0 + i]);
+            pr[i] = view_projected(w0 + (size_t)(v0 + i) * stride, L);
+        }
+        if (launch_preprocess_batch(*g, cc, pr, nv, s0) != cudaSuccess) return GS_ERR_CUDA;
+    }
+    // steps 2-5 per view, round-robin over the streams, forked from and joined into streams[0]
+    if (n_streams > 1) {
+        if (cudaEventRecord(ev->fork, s0) != cudaSuccess) return GS_ERR_CUDA;
+        for (int i = 1; i < n_streams; i++)
+            if (cudaStreamWaitEvent((cudaStream_t)streams[i], ev->fork, 0) != cudaSuccess) return GS_ERR_CUDA;
+    }
+    for (int v = 0; v < views; v++) {
+        cudaStream_t s = (cudaStream_t)streams[v % n_streams];
+        const cudaError_t e = view_pipeline(g, cams + v, key_capacity, w0 + (size_t)v * stride, L,
+                                            images + (size_t)v * pix * 3, final_T ? final_T + (size_t)v * pix : nullptr,
+                                            n_contrib ? n_contrib + (size_t)v * pix : nullptr, s, nullptr, false);
+        if (e != cudaSuccess) return GS_ERR_CUDA;
+    }
+    for (int i = 1; i < n_streams; i++) {
+        if (cudaEventRecord(ev->join[i], (cudaStream_t)streams[i]) != cudaSuccess) return GS_ERR_CUDA;
+        if (cudaStreamWaitEvent(s0, ev->join[i], 0) != cudaSuccess) return GS_ERR_CUDA;
+    }
+    return GS_OK;
 }
 
 gs_status gs_read_status(const void* ws, void* stream, uint32_t* flags, uint64_t* num_keys) {

@@ -116,6 +116,11 @@ cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* n
 cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations, cudaStream_t s);
 
 // rasterize.cu
+// at most this many views per batched preprocess launch
+constexpr int kMaxBatchViews = 8;
+// cams[views], outs[views]: one projected record per view
+cudaError_t launch_preprocess_batch(const gs_gaussians& g, const CamConst* cams, const gs_projected* outs, int views,
+                                    cudaStream_t s);
 cudaError_t launch_rasterize_backward(const gs_projected& p, int64_t n, const uint32_t* sorted_vals,
                                       const uint32_t* ranges, const uint32_t* tile_order, const CamConst& cam,
                                       const float* final_T, const uint32_t* n_contrib, const float* grad_image,

@@ -203,10 +203,9 @@ struct PreArgs {
     ushort4* rect;
 };
 
+// One Gaussian seen by one camera.
 template <int D>
-__global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
-    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (g >= a.n) return;
+__device__ __forceinline__ void preprocess_one(const PreArgs& a, int64_t g) {
     const CamConst& C = a.cam;
     const float m0 = __ldg(a.means + 3 * g), m1 = __ldg(a.means + 3 * g + 1), m2 = __ldg(a.means + 3 * g + 2);
 
@@ -379,11 +378,29 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
     }
 }
 
-}  // namespace
+template <int D>
+__global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g < a.n) preprocess_one<D>(a, g);
+}
 
-cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const gs_projected& out,
-                              cudaStream_t s) {
-    if (g.n == 0) return cudaSuccess;
+// Several cameras in one pass over the parameters: each thread projects its
+// Gaussian for every view in turn, so the 236 B of parameters come from HBM
+// once (the repeated loads of the same thread hit L1/L2) and each view's
+// record is written to that view's arrays.
+struct PreBatchArgs {
+    PreArgs v[kMaxBatchViews];
+    int views;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) preprocess_batch_kernel(const PreBatchArgs a) {
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= a.v[0].n) return;
+    for (int i = 0; i < a.views; i++) preprocess_one<D>(a.v[i], g);
+}
+
+PreArgs pre_args(const gs_gaussians& g, const CamConst& cam, const gs_projected& out) {
     PreArgs a;
     a.means = g.means;
     a.quats = reinterpret_cast<const float4*>(g.quats);
@@ -400,6 +417,32 @@ cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const 
     a.radius = out.radius;
     a.tiles_touched = out.tiles_touched;
     a.rect = reinterpret_cast<ushort4*>(out.rect);
+    return a;
+}
+
+}  // namespace
+
+cudaError_t launch_preprocess_batch(const gs_gaussians& g, const CamConst* cams, const gs_projected* outs, int views,
+                                    cudaStream_t s) {
+    if (g.n == 0 || views <= 0) return cudaSuccess;
+    if (views > kMaxBatchViews) return cudaErrorInvalidValue;
+    PreBatchArgs a;
+    for (int i = 0; i < views; i++) a.v[i] = pre_args(g, cams[i], outs[i]);
+    a.views = views;
+    const unsigned blocks = (unsigned)((g.n + 255) / 256);
+    switch (g.sh_degree) {
+        case 0: preprocess_batch_kernel<0><<<blocks, 256, 0, s>>>(a); break;
+        case 1: preprocess_batch_kernel<1><<<blocks, 256, 0, s>>>(a); break;
+        case 2: preprocess_batch_kernel<2><<<blocks, 256, 0, s>>>(a); break;
+        default: preprocess_batch_kernel<3><<<blocks, 256, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const gs_projected& out,
+                              cudaStream_t s) {
+    if (g.n == 0) return cudaSuccess;
+    const PreArgs a = pre_args(g, cam, out);
     const unsigned blocks = (unsigned)((g.n + 255) / 256);
     switch (g.sh_degree) {
         case 0: preprocess_kernel<0><<<blocks, 256, 0, s>>>(a); break;

@@ -280,6 +280,29 @@ gs_status gs_render_profiled(const gs_gaussians* gaussians, const gs_camera* cam
                              float* final_T, uint32_t* n_contrib, void* stream,
                              void* const* events, int32_t n_events);
 
+/* Several views of the same Gaussians in one call (the multi-view workloads:
+ * orbit poses of one scene). Step 1 runs once for all views: one pass over
+ * the parameters projects each Gaussian for every camera (the 236 B per
+ * Gaussian are read from HBM once, not once per view). Steps 2-5 of each view
+ * then run on streams[v % n_streams], so the views' latency-bound passes (the
+ * radix sorts' look-back chains) overlap on the GPU.
+ * cameras[views]: same width and height. images: device float
+ * [views][h][w][3]; final_T / n_contrib: NULL or [views][h][w].
+ * ws: views consecutive gs_render workspaces; view v's (and its status header,
+ * read with gs_read_status) starts at ws + v * gs_render_workspace_bytes(n,
+ * width, height, key_capacity); key_capacity applies to each view.
+ * streams[0..n_streams-1] (1 <= n_streams <= 8): the call is ordered after
+ * the work already queued on streams[0], and everything it launches is joined
+ * back into streams[0] (fork/join events are created once per device on first
+ * use). Each view's image equals gs_render's for that camera bit for bit.
+ * 1 <= views <= GS_MAX_BATCH_VIEWS. */
+#define GS_MAX_BATCH_VIEWS 64
+size_t gs_render_batch_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity,
+                                       int32_t views);
+gs_status gs_render_batch(const gs_gaussians* gaussians, const gs_camera* cameras, int32_t views,
+                          int64_t key_capacity, void* ws, size_t ws_bytes, float* images, float* final_T,
+                          uint32_t* n_contrib, void* const* streams, int32_t n_streams);
+
 /* The whole frame from host memory: copies the five parameter arrays from
  * host to the caller's device buffers in `device_gaussians` (same n and
  * degree), renders with gs_render, and copies the image back to host_image

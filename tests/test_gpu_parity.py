@@ -467,3 +467,27 @@ def test_sort32_random_keys(oracle_mod, count, bits):
     sk, sv = oracle_mod.sort_pairs(keys.astype(np.uint64), np.arange(count, dtype=np.uint32))
     np.testing.assert_array_equal(kd[:count].cpu().numpy().view(np.uint32), sk.astype(np.uint32))
     np.testing.assert_array_equal(vd[:count].cpu().numpy().view(np.uint32), vals[sv])
+
+
+@pytest.mark.parametrize("views,n_streams", [(8, 3), (10, 4), (1, 1)])
+def test_render_batch_equals_single_views(views, n_streams):
+    """gs_render_batch (one projection pass for all views, views spread over
+    streams, more than 8 views in chunks) gives every view's gs_render image,
+    final T and n_contrib bit for bit, with each view's status."""
+    base = scenes.make_scene("stress", n=200_000)
+    cams = scenes.make_cameras("stress")
+    cams = [cams[i % len(cams)] for i in range(views)]
+    g = gs.gaussians_to_device(base)
+    br = gs.BatchRenderer.for_scene(g, cams, n_streams=n_streams)
+    br.render(aux=True)
+    torch.cuda.synchronize()
+    single = gs.Renderer(g, cams[0]["width"], cams[0]["height"], br.key_capacity)
+    for v, cam in enumerate(cams):
+        single.render(cam)
+        torch.cuda.synchronize()
+        st, flags, K = br.status(v)
+        assert st == native.GS_OK, (v, st, flags)
+        assert K == single.status()[2]
+        np.testing.assert_array_equal(br.images[v].cpu().numpy(), single.image.cpu().numpy())
+        np.testing.assert_array_equal(br.final_T[v].cpu().numpy(), single.final_T.cpu().numpy())
+        np.testing.assert_array_equal(br.n_contrib[v].cpu().numpy(), single.n_contrib.cpu().numpy())
