@@ -9,7 +9,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libgs_b300.so")
-SOURCES = ["api.cu", "preprocess.cu", "binning.cu", "sort.cu", "rasterize.cu", "backward.cu", "bin_static.cu"]
+SOURCES = ["api.cu", "preprocess.cu", "binning.cu", "sort.cu", "rasterize.cu", "backward.cu", "splat2d.cu",
+           "bin_static.cu"]
 HEADERS = ["gs_internal.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-O2",

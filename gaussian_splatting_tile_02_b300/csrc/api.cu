@@ -511,6 +511,70 @@ gs_status gs_render_backward(const gs_gaussians* g, const gs_camera* cam, int64_
     return cuda_status(e);
 }
 
+static gs_camera camera_2d(int32_t width, int32_t height) {
+    gs_camera c;
+    memset(&c, 0, sizeof(c));
+    c.R[0] = c.R[4] = c.R[8] = 1.0f;
+    c.fx = c.fy = 1.0f;
+    c.near_z = 1.0f;
+    c.width = width;
+    c.height = height;
+    return c;
+}
+
+gs_status gs_rasterize_2d(const float* means, const float* covs, const float* colours, const float* opacities,
+                          const float* depths, int64_t n, int32_t width, int32_t height, int64_t key_capacity,
+                          void* ws, size_t ws_bytes, float* image, float* final_T, uint32_t* n_contrib,
+                          void* stream) {
+    if (n < 0 || n > kMaxGaussians || width < 1 || height < 1 || width > 32768 || height > 32768 || !image)
+        return GS_ERR_INVALID_ARG;
+    if (n > 0 && (!means || !covs || !colours || !opacities || !depths || !aligned(means, 8)))
+        return GS_ERR_INVALID_ARG;
+    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
+    const RenderLayout L = render_layout(n, width, height, key_capacity);
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GS_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* w = static_cast<char*>(ws);
+    const gs_camera cam = camera_2d(width, height);
+    gs_gaussians g;
+    memset(&g, 0, sizeof(g));
+    g.n = n;
+    if (launch_preprocess2d(means, covs, colours, opacities, depths, n, width, height, view_projected(w, L), s) !=
+        cudaSuccess)
+        return GS_ERR_CUDA;
+    return cuda_status(view_pipeline(&g, &cam, key_capacity, w, L, image, final_T, n_contrib, s, nullptr, false));
+}
+
+gs_status gs_rasterize_2d_backward(const float* covs, int64_t n, int32_t width, int32_t height, int64_t key_capacity,
+                                   void* ws, size_t ws_bytes, const float* final_T, const uint32_t* n_contrib,
+                                   const float* grad_image, float* grad_means, float* grad_covs, float* grad_colours,
+                                   float* grad_opacities, void* stream) {
+    if (n < 0 || n > kMaxGaussians || width < 1 || height < 1 || width > 32768 || height > 32768)
+        return GS_ERR_INVALID_ARG;
+    if (!final_T || !n_contrib || !grad_image) return GS_ERR_INVALID_ARG;
+    if (n > 0 && (!covs || !grad_means || !grad_covs || !grad_colours || !grad_opacities || !aligned(grad_means, 8)))
+        return GS_ERR_INVALID_ARG;
+    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
+    const RenderLayout L = render_layout(n, width, height, key_capacity);
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GS_ERR_WORKSPACE;
+    if (n == 0) return GS_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* w = static_cast<char*>(ws);
+    const gs_projected p = view_projected(w, L);
+    gs_projected_grad pgr;
+    pgr.mean2d = grad_means;
+    pgr.conic = reinterpret_cast<float*>(w + L.pgrad);
+    pgr.opacity = grad_opacities;
+    pgr.rgb = grad_colours;
+    const gs_camera cam = camera_2d(width, height);
+    cudaError_t e = launch_rasterize_backward(p, n, reinterpret_cast<const uint32_t*>(w + L.vals),
+                                              reinterpret_cast<const uint32_t*>(w + L.ranges),
+                                              reinterpret_cast<const uint32_t*>(w + L.tile_order),
+                                              make_cam_const(cam), final_T, n_contrib, grad_image, pgr, s);
+    if (e == cudaSuccess) e = launch_conic_to_cov_grad(covs, p.tiles_touched, pgr.conic, n, grad_covs, s);
+    return cuda_status(e);
+}
+
 size_t gs_render_batch_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity,
                                        int32_t views) {
     if (views < 1 || views > GS_MAX_BATCH_VIEWS) return 0;

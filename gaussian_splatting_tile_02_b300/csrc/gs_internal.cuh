@@ -116,6 +116,13 @@ cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* n
 cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations, cudaStream_t s);
 
 // rasterize.cu
+// 2D splats: their per-Gaussian record into p (depth, tiles_touched, rect, raster)
+cudaError_t launch_preprocess2d(const float* means, const float* covs, const float* colours, const float* opacities,
+                                const float* depths, int64_t n, int width, int height, const gs_projected& p,
+                                cudaStream_t s);
+cudaError_t launch_conic_to_cov_grad(const float* covs, const uint32_t* tiles_touched, const float* g_conic,
+                                     int64_t n, float* g_covs, cudaStream_t s);
+
 // at most this many views per batched preprocess launch
 constexpr int kMaxBatchViews = 8;
 // cams[views], outs[views]: one projected record per view

@@ -90,6 +90,12 @@ _SIGNATURES = {
     "gs_render_batch": (ctypes.c_int, [ctypes.POINTER(GsGaussians), ctypes.POINTER(GsCamera), ctypes.c_int32,
                                        ctypes.c_int64, c_void_p, ctypes.c_size_t, c_void_p, c_void_p, c_void_p,
                                        ctypes.POINTER(c_void_p), ctypes.c_int32]),
+    "gs_rasterize_2d": (ctypes.c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, ctypes.c_int64,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, c_void_p, ctypes.c_size_t,
+                                       c_void_p, c_void_p, c_void_p, c_void_p]),
+    "gs_rasterize_2d_backward": (ctypes.c_int, [c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                                ctypes.c_int64, c_void_p, ctypes.c_size_t, c_void_p, c_void_p,
+                                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "gs_rasterize_backward": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, c_void_p, c_void_p,
                                              ctypes.POINTER(GsCamera), c_void_p, c_void_p, c_void_p, c_void_p,
                                              ctypes.POINTER(GsProjectedGrad), c_void_p]),

@@ -375,6 +375,38 @@ gs_status gs_render_backward(const gs_gaussians* gaussians, const gs_camera* cam
                              const uint32_t* n_contrib, const float* grad_image,
                              const gs_gaussians_grad* grad_out, void* stream);
 
+/* ---------------------------------------------------------------- 2D splats
+ * Section "Étape 2" (rasterise_2d) and "Étape 3" (a trainable 2D scene): n
+ * Gaussians given directly in image space, composited on the tile pipeline.
+ *   means     [n][2]    (x, y) in pixels (8-byte aligned)
+ *   covs      [n][2][2] image-space covariance (the off-diagonal is taken as
+ *                       the mean of the two entries)
+ *   colours   [n][3]    in [0, 1];  opacities [n] in (0, 1]
+ *   depths    [n]       any real; only orders the Gaussians, smallest first
+ *                       (ties by index)
+ * alpha = min(0.99, o exp(-0.5 d^T cov^-1 d)) at the integer pixel (x, y);
+ * out = sum alpha_i T_i c_i with no background term (zero background). The
+ * tile renderer's cut-offs apply: each Gaussian covers the tiles of its
+ * 3-sigma rectangle, alpha < 1/255 is skipped, a pixel stops once T < 1e-4.
+ * ws: >= gs_render_workspace_bytes(n, width, height, key_capacity), key
+ * capacity and status header as for gs_render. image [h][w][3]; final_T and
+ * n_contrib may be NULL (the backward needs them). */
+gs_status gs_rasterize_2d(const float* means, const float* covs, const float* colours,
+                          const float* opacities, const float* depths, int64_t n, int32_t width,
+                          int32_t height, int64_t key_capacity, void* ws, size_t ws_bytes, float* image,
+                          float* final_T, uint32_t* n_contrib, void* stream);
+
+/* Backward of the last gs_rasterize_2d on ws (same inputs, ws not reused in
+ * between): dL/dmeans [n][2], dL/dcovs [n][2][2] (the off-diagonal gradient
+ * split evenly over the two entries), dL/dcolours [n][3], dL/dopacities [n],
+ * all written (zero for Gaussians that touch no tile). The depths get no
+ * gradient: they only order the Gaussians. */
+gs_status gs_rasterize_2d_backward(const float* covs, int64_t n, int32_t width, int32_t height,
+                                   int64_t key_capacity, void* ws, size_t ws_bytes,
+                                   const float* final_T, const uint32_t* n_contrib,
+                                   const float* grad_image, float* grad_means, float* grad_covs,
+                                   float* grad_colours, float* grad_opacities, void* stream);
+
 /* Reads the status header at the start of a gs_bin, gs_sort or gs_render
  * workspace. SYNCHRONISES `stream`. flags/num_keys may be NULL. Returns
  * GS_ERR_TIMEOUT, GS_ERR_CAPACITY or GS_OK from the flags. num_keys is the

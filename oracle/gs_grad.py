@@ -143,11 +143,13 @@ def pixel_lists(sorted_vals: np.ndarray, ranges: np.ndarray, cam, px: np.ndarray
     return idx
 
 
-def composite_t(pre: dict, idx: np.ndarray, px: np.ndarray, py: np.ndarray, bg, band: float = 2e-3):
+def composite_t(pre: dict, idx: np.ndarray, px: np.ndarray, py: np.ndarray, bg, band: float = 2e-3,
+                cutoffs: bool = True):
     """Front-to-back composite of the listed pixels; returns (out [P,3], final T [P],
     n_contrib [P], events [P]). The skip/stop decisions are constants taken in
     float64 from the values themselves; ``events`` flags pixels with a skip, stop
-    or cap decision within ``band`` (relative) of its threshold."""
+    or cap decision within ``band`` (relative) of its threshold. cutoffs=False
+    drops the 1/255 skip and the 1e-4 stop (the pages' dense rasterise_2d)."""
     torch = _torch()
     P, L = idx.shape
     valid = idx >= 0
@@ -175,12 +177,13 @@ def composite_t(pre: dict, idx: np.ndarray, px: np.ndarray, py: np.ndarray, bg, 
         ai = np.where(live, a_np[:, i], 0.0)
         ev |= live & (np.abs(ai - ALPHA_MIN) <= band * ALPHA_MIN)
         ev |= live & (np.abs(np.where(live, r_np[:, i], 0.0) - ALPHA_MAX) <= band * ALPHA_MAX)
-        ui = live & (ai >= ALPHA_MIN)
+        ui = live & (ai >= ALPHA_MIN) if cutoffs else live
         use[:, i] = ui
         T = np.where(ui, T * (1.0 - ai), T)
         ncon = np.where(ui, i + 1, ncon)
-        ev |= ui & (np.abs(T - T_MIN) <= band * T_MIN)
-        active &= ~(ui & (T < T_MIN))
+        if cutoffs:
+            ev |= ui & (np.abs(T - T_MIN) <= band * T_MIN)
+            active &= ~(ui & (T < T_MIN))
     w = alpha * torch.tensor(use.astype(np.float64))
     one_minus = 1.0 - w
     Tincl = torch.cumprod(one_minus, dim=1)
@@ -275,3 +278,130 @@ def render_grad(scene: dict, cam: dict, grad_image: np.ndarray, ref: dict | None
     res.update(image=out.detach().numpy(), final_T=Tfin.detach().numpy(), n_contrib=ncon, px=st["px"],
                py=st["py"], events=ev, used=used, loss=float(loss.detach()))
     return res
+
+
+# --------------------------------------------------------------------------- 2D splats
+# Section "Étape 2" (rasterise_2d) and "Étape 3" of the lesson page: Gaussians
+# given directly in image space (mean, 2x2 covariance, colour, opacity) and a
+# per-Gaussian scalar that only orders them; no background term.
+
+def order_key(depths: np.ndarray) -> np.ndarray:
+    """Order-preserving uint32 image of float32 values (sign bit flipped for
+    non-negative values, all bits for negative ones)."""
+    u = np.ascontiguousarray(depths, np.float32).view(np.uint32)
+    return np.where(u & np.uint32(0x80000000), ~u, u | np.uint32(0x80000000)).astype(np.uint32)
+
+
+def decide2d_f32(means, covs, opacities, depths, width: int, height: int) -> dict:
+    """The 2D tile rectangles as a binary32 program (numpy float32 element-wise
+    ops, each rounded on its own, no FMA): b = (cov01 + cov10)/2, det = ac - bb,
+    lam = (a+c)/2 + sqrt(((a-c)/2)^2 + b^2), r = ceil(3 sqrt(lam)); culled unless
+    0 < det <= FLT_MAX, u, v, r finite, o > 0 and the depth is a number; pixel
+    rectangle clipped to the image, tiles of 16x16."""
+    f = np.float32
+    m = np.asarray(means, f)
+    c = np.asarray(covs, f).reshape(-1, 4)
+    o = np.asarray(opacities, f)
+    d = np.asarray(depths, f)
+    with np.errstate(all="ignore"):
+        a, cc = c[:, 0], c[:, 3]
+        b = f(0.5) * (c[:, 1] + c[:, 2])
+        det = a * cc - b * b
+        hm = f(0.5) * (a - cc)
+        lam = f(0.5) * (a + cc) + np.sqrt(hm * hm + b * b)
+        r = np.ceil(f(3.0) * np.sqrt(lam))
+        u, v = m[:, 0], m[:, 1]
+        fmax = np.finfo(np.float32).max
+        ok = (det > 0) & (det <= fmax) & (np.abs(u) <= fmax) & (np.abs(v) <= fmax) & (r <= fmax) & (o > 0) & ~np.isnan(d)
+        x0 = np.maximum(np.ceil(u - r), f(0)); x1 = np.minimum(np.floor(u + r), f(width - 1))
+        y0 = np.maximum(np.ceil(v - r), f(0)); y1 = np.minimum(np.floor(v + r), f(height - 1))
+    ok &= (x0 <= x1) & (y0 <= y1)
+    rect = np.zeros((m.shape[0], 4), np.int64)
+    rect[ok] = np.stack([x0[ok].astype(np.int64) >> 4, y0[ok].astype(np.int64) >> 4,
+                         x1[ok].astype(np.int64) >> 4, y1[ok].astype(np.int64) >> 4], 1)
+    touched = np.where(ok, (rect[:, 2] - rect[:, 0] + 1) * (rect[:, 3] - rect[:, 1] + 1), 0)
+    return {"tile_rect": rect, "tiles_touched": touched.astype(np.int64), "key": order_key(d)}
+
+
+def lists2d(dec: dict, width: int, height: int) -> tuple:
+    """Per-tile lists in the order (order key, index): (sorted_vals, ranges)."""
+    tx, ty = (width + 15) // 16, (height + 15) // 16
+    tiles, gids = [], []
+    for gi in np.nonzero(dec["tiles_touched"] > 0)[0]:
+        x0, y0, x1, y1 = dec["tile_rect"][gi]
+        for yy in range(y0, y1 + 1):
+            for xx in range(x0, x1 + 1):
+                tiles.append(yy * tx + xx)
+                gids.append(gi)
+    tiles = np.asarray(tiles, np.int64)
+    gids = np.asarray(gids, np.int64)
+    order = np.lexsort((gids, dec["key"][gids].astype(np.int64), tiles)) if tiles.size else np.zeros(0, np.int64)
+    tiles, gids = tiles[order], gids[order]
+    starts = np.searchsorted(tiles, np.arange(tx * ty), "left")
+    ends = np.searchsorted(tiles, np.arange(tx * ty), "right")
+    return gids.astype(np.uint32), np.stack([starts, ends], 1).astype(np.uint32)
+
+
+def pre2d_t(means, covs, colours, opacities) -> dict:
+    """The per-Gaussian quantities the compositor reads, for 2D splats."""
+    torch = _torch()
+    a, c = covs[:, 0, 0], covs[:, 1, 1]
+    b = 0.5 * (covs[:, 0, 1] + covs[:, 1, 0])
+    det = a * c - b * b
+    return {"mean2d": means, "conic": torch.stack([c / det, -b / det, a / det], 1), "opacity": opacities,
+            "rgb": colours}
+
+
+def render_grad_2d(means, covs, colours, opacities, depths, width: int, height: int, grad_image,
+                   band: float = 2e-3, cutoffs: bool = True, dense: bool = False, exact: bool = False) -> dict:
+    """Image and gradients of L = sum(grad_image * image) for 2D splats, in
+    float64 torch ops. dense=True lists every Gaussian at every pixel (in depth
+    order), as the pages' rasterise_2d does; otherwise each pixel gets its
+    tile's list. Returns numpy ``image`` [H,W,3], ``final_T``, ``n_contrib``,
+    ``events`` [H,W] and gradients ``means``, ``covs`` (full 2x2), ``colours``,
+    ``opacities``. exact=True takes the continuous inputs as given (float64)
+    instead of their float32 values (the decisions always use float32)."""
+    torch = _torch()
+    n = int(np.asarray(means).shape[0])
+    py, px = np.mgrid[0:height, 0:width]
+    px, py = px.ravel(), py.ravel()
+    if dense:
+        order = np.lexsort((np.arange(n), order_key(depths).astype(np.int64)))
+        idx = np.broadcast_to(order[None, :], (px.size, n)).copy()
+    else:
+        dec = decide2d_f32(means, covs, opacities, depths, width, height)
+        sv, rg = lists2d(dec, width, height)
+        idx = pixel_lists(sv, rg, {"width": width}, px, py)
+    cast = (lambda x: np.asarray(x, np.float64)) if exact else (lambda x: np.asarray(x, np.float32).astype(np.float64))
+    leaves = [torch.tensor(cast(x), requires_grad=True) for x in (means, covs, colours, opacities)]
+    pre = pre2d_t(*leaves)
+    out, Tfin, ncon, ev = composite_t(pre, idx, px, py, np.zeros(3), band, cutoffs)
+    g = torch.tensor(np.asarray(grad_image, np.float64).reshape(-1, 3))
+    grads = torch.autograd.grad((g * out).sum(), leaves)
+    return {"image": out.detach().numpy().reshape(height, width, 3),
+            "final_T": Tfin.detach().numpy().reshape(height, width),
+            "n_contrib": ncon.reshape(height, width), "events": ev.reshape(height, width),
+            "means": grads[0].numpy(), "covs": grads[1].numpy(), "colours": grads[2].numpy(),
+            "opacities": grads[3].numpy()}
+
+
+def dense_rasterise_2d(means, covs, colours, opacities, depths, width: int, height: int) -> np.ndarray:
+    """The pages' rasterise_2d written out in numpy float64: every Gaussian at
+    every integer pixel, alpha = clamp(o exp(-0.5 d^T cov^-1 d), 0, 0.99), in
+    increasing depth order, C += T alpha c, T *= 1 - alpha, no background."""
+    m = np.asarray(means, np.float32).astype(np.float64)
+    cv = np.asarray(covs, np.float32).astype(np.float64)
+    col = np.asarray(colours, np.float32).astype(np.float64)
+    o = np.asarray(opacities, np.float32).astype(np.float64)
+    order = np.lexsort((np.arange(m.shape[0]), order_key(depths).astype(np.int64)))
+    y, x = np.mgrid[0:height, 0:width].astype(np.float64)
+    T = np.ones((height, width))
+    out = np.zeros((height, width, 3))
+    for gi in order:
+        inv = np.linalg.inv(0.5 * (cv[gi] + cv[gi].T))
+        dx, dy = x - m[gi, 0], y - m[gi, 1]
+        q = inv[0, 0] * dx * dx + 2 * inv[0, 1] * dx * dy + inv[1, 1] * dy * dy
+        a = np.clip(o[gi] * np.exp(-0.5 * q), 0.0, 0.99)
+        out += (T * a)[..., None] * col[gi][None, None, :]
+        T = T * (1.0 - a)
+    return out

@@ -138,3 +138,67 @@ def test_closed_form_one_pixel_right_of_the_centre():
     assert r["log_scales"][0, 0] == pytest.approx(dLda * alpha * A, rel=1e-12)
     assert abs(r["log_scales"][0, 1]) < 1e-13 and abs(r["log_scales"][0, 2]) < 1e-13
     assert r["conic"][0, 0] == pytest.approx(-dLda * alpha * 0.5, rel=1e-12)
+
+
+def _splats2d(n=40, W=50, H=37, seed=0):
+    rng = np.random.default_rng(seed)
+    means = (rng.random((n, 2)) * [W, H]).astype(np.float32)
+    th = rng.random(n) * np.pi
+    s = np.exp(rng.normal(0.8, 0.5, (n, 2)))
+    R = np.stack([np.stack([np.cos(th), -np.sin(th)], -1), np.stack([np.sin(th), np.cos(th)], -1)], -2)
+    covs = (R @ (s[:, :, None] ** 2 * np.eye(2)[None]) @ R.transpose(0, 2, 1)).astype(np.float32)
+    col = rng.random((n, 3)).astype(np.float32)
+    op = (0.2 + 0.7 * rng.random(n)).astype(np.float32)
+    dep = rng.normal(0, 1, n).astype(np.float32)
+    return means, covs, col, op, dep, W, H
+
+
+def test_2d_dense_mode_is_the_pages_formula():
+    """With every Gaussian listed at every pixel and no cut-offs, the 2D oracle is
+    the pages' rasterise_2d written out separately in numpy."""
+    args = _splats2d()
+    W, H = args[-2], args[-1]
+    dense = gs_grad.dense_rasterise_2d(*args)
+    r = gs_grad.render_grad_2d(*args, np.ones((H, W, 3)), cutoffs=False, dense=True)
+    np.testing.assert_allclose(r["image"], dense, rtol=0, atol=1e-13)
+    # the tile renderer's cut-offs (3-sigma tiles, 1/255 skip, 1e-4 stop) move
+    # pixels by at most about 0.011 per truncated Gaussian
+    t = gs_grad.render_grad_2d(*args, np.ones((H, W, 3)))
+    assert 0.0 < np.abs(t["image"] - dense).max() < 0.02
+
+
+def test_2d_order_key_and_rectangles():
+    keys = gs_grad.order_key(np.float32([-2.0, -0.0, 0.0, 1e-30, 3.0, -1e30]))
+    assert list(np.argsort(keys, kind="stable")) == [5, 0, 1, 2, 3, 4]
+    # an isotropic Gaussian of variance 4 at (20.5, 9): r = ceil(3 * 2) = 6
+    d = gs_grad.decide2d_f32(np.float32([[20.5, 9.0]]), np.float32([[[4, 0], [0, 4]]]), np.float32([0.5]),
+                             np.float32([0.0]), 64, 64)
+    # pixels x in [ceil(14.5), floor(26.5)] = [15, 26], y in [3, 15] -> tiles x 0..1, y 0..0
+    assert list(d["tile_rect"][0]) == [0, 0, 1, 0] and d["tiles_touched"][0] == 2
+
+
+def test_2d_gradients_match_central_differences():
+    means, covs, col, op, dep, W, H = _splats2d(n=12, W=33, H=20, seed=3)
+    g = np.random.default_rng(1).standard_normal((H, W, 3))
+    probe = gs_grad.render_grad_2d(means, covs, col, op, dep, W, H, np.ones((H, W, 3)), band=1e-2)
+    g[probe["events"]] = 0.0
+    r = gs_grad.render_grad_2d(means, covs, col, op, dep, W, H, g)
+    base = {"means": means, "covs": covs, "colours": col, "opacities": op}
+    rng = np.random.default_rng(2)
+    for k, arr in base.items():
+        for _ in range(4):
+            pos = tuple(int(rng.integers(sz)) for sz in arr.shape)
+            h = 1e-6 * max(1.0, abs(float(arr[pos])))
+            vals = []
+            for sgn in (1, -1):
+                a2 = {kk: v.astype(np.float64).copy() for kk, v in base.items()}
+                a2[k][pos] += sgn * h
+                if k == "covs":   # keep the matrix symmetric: perturb both off-diagonal entries
+                    if pos[1] != pos[2]:
+                        a2[k][(pos[0], pos[2], pos[1])] += sgn * h
+                img = gs_grad.render_grad_2d(a2["means"], a2["covs"], a2["colours"], a2["opacities"], dep, W, H,
+                                             g, exact=True)["image"]
+                vals.append(float((g * img).sum()))
+            fd = (vals[0] - vals[1]) / (2 * h)
+            ad = r[k][pos] + (r[k][(pos[0], pos[2], pos[1])] if k == "covs" and pos[1] != pos[2] else 0.0)
+            assert abs(fd - ad) <= 1e-6 * (1.0 + abs(ad)), (k, pos, fd, ad)
