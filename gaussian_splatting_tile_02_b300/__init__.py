@@ -27,7 +27,7 @@ from .native import GsCamera, GsGaussians, GsGaussiansGrad, GsProjected, GsProje
 __all__ = ["GsCamera", "camera_struct", "gaussians_to_device", "gaussians_struct", "preprocess",
            "bin_keys", "sort_pairs", "tile_ranges", "rasterize", "Renderer", "read_status",
            "key_bits", "tiles_xy", "lib", "render_from_host", "rasterize_backward", "preprocess_backward",
-           "alloc_param_grads", "BatchRenderer"]
+           "alloc_param_grads", "BatchRenderer", "densify_stats", "densify"]
 
 
 def _torch():
@@ -232,6 +232,50 @@ def preprocess_backward(g: dict, cam: dict, p: dict, pgrad: dict, stream=None) -
                                        ctypes.byref(_ggrad_struct(out)), _stream_ptr(stream)),
           "gs_preprocess_backward")
     return out
+
+
+# ------------------------------------------------------------------------------ densify / prune
+
+def densify_stats(grad_mean2d, tiles_touched, accum, count, stream=None) -> None:
+    """accum += |dL/d(u, v)|, count += 1 for Gaussians that touched a tile."""
+    n = int(accum.shape[0])
+    check(lib().gs_densify_stats(_ptr(grad_mean2d), _ptr(tiles_touched), n, _ptr(accum), _ptr(count),
+                                 _stream_ptr(stream)), "gs_densify_stats")
+
+
+def densify(g: dict, accum, count, xi, grad_threshold: float = 2e-4, scale_threshold: float = 0.01,
+            prune_opacity: float = 0.005, capacity: int | None = None, stream=None) -> dict:
+    """Clone / split / prune (section "Densation et taille"). Returns the new
+    device parameter dict (n = new count; synchronises to read it) and
+    ``action`` (uint8 per input Gaussian: 0 keep, 1 clone, 2 split, 3 prune)."""
+    torch = _torch()
+    n = int(g["n"])
+    dev = g["means"].device
+    cap = 2 * n if capacity is None else int(capacity)
+    k3 = (int(g["sh_degree"]) + 1) ** 2
+    out = {"means": torch.empty((max(cap, 1), 3), dtype=torch.float32, device=dev),
+           "quats": torch.empty((max(cap, 1), 4), dtype=torch.float32, device=dev),
+           "log_scales": torch.empty((max(cap, 1), 3), dtype=torch.float32, device=dev),
+           "opacity_logits": torch.empty(max(cap, 1), dtype=torch.float32, device=dev),
+           "sh": torch.empty((max(cap, 1), k3, 3), dtype=torch.float32, device=dev)}
+    o = native.GsGaussiansOut()
+    for k in _FIELDS:
+        setattr(o, k, _ptr(out[k]))
+    o.n = cap
+    o.sh_degree = int(g["sh_degree"])
+    new_n = torch.zeros(1, dtype=torch.int64, device=dev)
+    action = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+    wsb = int(lib().gs_densify_workspace_bytes(n))
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    check(lib().gs_densify(ctypes.byref(gaussians_struct(g)), _ptr(accum), _ptr(count), _ptr(xi),
+                           float(grad_threshold), float(scale_threshold), float(prune_opacity), ctypes.byref(o),
+                           _ptr(new_n), _ptr(action), _ptr(ws), wsb, _stream_ptr(stream)), "gs_densify")
+    st, flags, _ = read_status(ws, stream)
+    check(st, "gs_densify (capacity)")
+    m = int(new_n.item())
+    res = {k: v[:m] for k, v in out.items()}
+    res.update(n=m, sh_degree=int(g["sh_degree"]), action=action[:n])
+    return res
 
 
 def read_status(ws, stream=None) -> tuple:

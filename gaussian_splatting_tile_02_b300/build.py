@@ -9,7 +9,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libgs_b300.so")
-SOURCES = ["api.cu", "preprocess.cu", "binning.cu", "sort.cu", "rasterize.cu", "backward.cu", "splat2d.cu",
+SOURCES = ["api.cu", "preprocess.cu", "binning.cu", "sort.cu", "rasterize.cu", "backward.cu", "splat2d.cu", "densify.cu",
            "bin_static.cu"]
 HEADERS = ["gs_internal.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

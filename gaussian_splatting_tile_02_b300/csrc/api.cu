@@ -575,6 +575,37 @@ gs_status gs_rasterize_2d_backward(const float* covs, int64_t n, int32_t width, 
     return cuda_status(e);
 }
 
+gs_status gs_densify_stats(const float* grad_mean2d, const uint32_t* tiles_touched, int64_t n, float* accum,
+                           uint32_t* count, void* stream) {
+    if (n < 0 || n > kMaxGaussians) return GS_ERR_INVALID_ARG;
+    if (n > 0 && (!grad_mean2d || !tiles_touched || !accum || !count || !aligned(grad_mean2d, 8)))
+        return GS_ERR_INVALID_ARG;
+    return cuda_status(launch_densify_stats(grad_mean2d, tiles_touched, n, accum, count, (cudaStream_t)stream));
+}
+
+size_t gs_densify_workspace_bytes(int64_t n) {
+    if (n < 0 || n > kMaxGaussians) return 0;
+    return densify_scratch_bytes(n);
+}
+
+gs_status gs_densify(const gs_gaussians* in, const float* accum, const uint32_t* count, const float* xi,
+                     float grad_threshold, float scale_threshold, float prune_opacity, const gs_gaussians_out* out,
+                     uint64_t* out_count, uint8_t* action, void* ws, size_t ws_bytes, void* stream) {
+    if (!gaussians_ok(in) || !out || !out_count) return GS_ERR_INVALID_ARG;
+    if (out->sh_degree != in->sh_degree || out->n < 0 || out->n > kMaxGaussians) return GS_ERR_INVALID_ARG;
+    if (in->n > 0 && (!accum || !count || !xi)) return GS_ERR_INVALID_ARG;
+    if (out->n > 0 && (!out->means || !out->quats || !out->log_scales || !out->opacity_logits || !out->sh))
+        return GS_ERR_INVALID_ARG;
+    if (!(prune_opacity > 0.0f && prune_opacity < 1.0f) || !(scale_threshold > 0.0f) || !isfinite(grad_threshold))
+        return GS_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < densify_scratch_bytes(in->n)) return GS_ERR_WORKSPACE;
+    const double t = prune_opacity;
+    const float logit_thr = (float)log(t / (1.0 - t));
+    const float log_scale_thr = (float)log((double)scale_threshold);
+    return cuda_status(launch_densify(*in, *out, out->n, accum, count, xi, grad_threshold, log_scale_thr, logit_thr,
+                                      action, out_count, ws, (cudaStream_t)stream));
+}
+
 size_t gs_render_batch_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity,
                                        int32_t views) {
     if (views < 1 || views > GS_MAX_BATCH_VIEWS) return 0;

@@ -123,6 +123,14 @@ cudaError_t launch_preprocess2d(const float* means, const float* covs, const flo
 cudaError_t launch_conic_to_cov_grad(const float* covs, const uint32_t* tiles_touched, const float* g_conic,
                                      int64_t n, float* g_covs, cudaStream_t s);
 
+size_t densify_scratch_bytes(int64_t n);
+cudaError_t launch_densify_stats(const float* grad_mean2d, const uint32_t* tiles_touched, int64_t n, float* accum,
+                                 uint32_t* count, cudaStream_t s);
+cudaError_t launch_densify(const gs_gaussians& in, const gs_gaussians_out& out, int64_t capacity, const float* accum,
+                           const uint32_t* count, const float* xi, float grad_threshold, float log_scale_threshold,
+                           float logit_threshold, uint8_t* action, uint64_t* out_count, void* scratch,
+                           cudaStream_t s);
+
 // at most this many views per batched preprocess launch
 constexpr int kMaxBatchViews = 8;
 // cams[views], outs[views]: one projected record per view

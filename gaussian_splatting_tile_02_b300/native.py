@@ -42,6 +42,11 @@ class GsGaussiansGrad(ctypes.Structure):
                 ("opacity_logits", c_void_p), ("sh", c_void_p)]
 
 
+class GsGaussiansOut(ctypes.Structure):
+    _fields_ = [("means", c_void_p), ("quats", c_void_p), ("log_scales", c_void_p),
+                ("opacity_logits", c_void_p), ("sh", c_void_p), ("n", ctypes.c_int64), ("sh_degree", ctypes.c_int32)]
+
+
 GS_OK, GS_ERR_INVALID_ARG, GS_ERR_CAPACITY, GS_ERR_CUDA, GS_ERR_TIMEOUT, GS_ERR_WORKSPACE = range(6)
 GS_FLAG_CAPACITY, GS_FLAG_TIMEOUT = 1, 2
 
@@ -96,6 +101,11 @@ _SIGNATURES = {
     "gs_rasterize_2d_backward": (ctypes.c_int, [c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                                 ctypes.c_int64, c_void_p, ctypes.c_size_t, c_void_p, c_void_p,
                                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "gs_densify_stats": (ctypes.c_int, [c_void_p, c_void_p, ctypes.c_int64, c_void_p, c_void_p, c_void_p]),
+    "gs_densify_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64]),
+    "gs_densify": (ctypes.c_int, [ctypes.POINTER(GsGaussians), c_void_p, c_void_p, c_void_p, ctypes.c_float,
+                                  ctypes.c_float, ctypes.c_float, ctypes.POINTER(GsGaussiansOut), c_void_p, c_void_p,
+                                  c_void_p, ctypes.c_size_t, c_void_p]),
     "gs_rasterize_backward": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, c_void_p, c_void_p,
                                              ctypes.POINTER(GsCamera), c_void_p, c_void_p, c_void_p, c_void_p,
                                              ctypes.POINTER(GsProjectedGrad), c_void_p]),

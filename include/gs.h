@@ -407,6 +407,57 @@ gs_status gs_rasterize_2d_backward(const float* covs, int64_t n, int32_t width, 
                                    const float* grad_image, float* grad_means, float* grad_covs,
                                    float* grad_colours, float* grad_opacities, void* stream);
 
+/* ---------------------------------------------------------------- densify / prune
+ * Section "Densation et taille": every N iterations, clone a Gaussian whose
+ * gradient magnitude is high but whose scale is small, split a large one with
+ * a high gradient into two smaller ones, prune those whose opacity fell below
+ * a threshold.
+ *
+ * gs_densify_stats: accumulates, for every Gaussian that touched a tile in
+ * the frame (projected->tiles_touched > 0), |dL/d(u, v)| into accum[n] and 1
+ * into count[n] (device; zero them at the start of a densification period).
+ * grad_mean2d: the gs_projected_grad mean2d of the frame's backward [n][2]. */
+gs_status gs_densify_stats(const float* grad_mean2d, const uint32_t* tiles_touched, int64_t n,
+                           float* accum, uint32_t* count, void* stream);
+
+/* Writable parameter arrays (layouts as gs_gaussians) with room for n
+ * Gaussians. */
+typedef struct gs_gaussians_out {
+    float* means;
+    float* quats;
+    float* log_scales;
+    float* opacity_logits;
+    float* sh;
+    int64_t n;
+    int32_t sh_degree;
+} gs_gaussians_out;
+
+/* The densification step, as one stable compaction of `in` into `out`:
+ *   prune  o < prune_opacity  (o = sigmoid(logit))
+ *   else, with g = accum / count (0 if count = 0):
+ *   clone  g >= grad_threshold and max(exp(log_scale)) <= scale_threshold:
+ *          the Gaussian and an exact copy right after it
+ *   split  g >= grad_threshold and max scale > scale_threshold: two children
+ *          at mu + R S xi_c (c = 0, 1) with log_scales - log(1.6), the other
+ *          parameters copied; xi: device float [in->n][2][3] standard normal
+ *          samples supplied by the caller (only split Gaussians read theirs)
+ *   keep   otherwise.
+ * Survivors keep the input order; children replace their parent. The tests
+ * are taken on logit < log(t/(1-t)) and max log_scale > log(scale_threshold)
+ * (thresholds mapped on the host, in double, then rounded to float), so the
+ * decisions are exact. out->n is the capacity (2 * in->n always suffices);
+ * out->sh_degree must equal in->sh_degree. *out_count (device uint64) gets
+ * the new count; if it exceeds the capacity GS_FLAG_CAPACITY is set in the
+ * workspace header and the out arrays are unspecified. action (device uint8
+ * [in->n], nullable): 0 keep, 1 clone, 2 split, 3 prune.
+ * ws: >= gs_densify_workspace_bytes(in->n); the first 256 bytes are the status
+ * header read by gs_read_status. */
+size_t gs_densify_workspace_bytes(int64_t n);
+gs_status gs_densify(const gs_gaussians* in, const float* accum, const uint32_t* count,
+                     const float* xi, float grad_threshold, float scale_threshold,
+                     float prune_opacity, const gs_gaussians_out* out, uint64_t* out_count,
+                     uint8_t* action, void* ws, size_t ws_bytes, void* stream);
+
 /* Reads the status header at the start of a gs_bin, gs_sort or gs_render
  * workspace. SYNCHRONISES `stream`. flags/num_keys may be NULL. Returns
  * GS_ERR_TIMEOUT, GS_ERR_CAPACITY or GS_OK from the flags. num_keys is the

@@ -405,3 +405,53 @@ def dense_rasterise_2d(means, covs, colours, opacities, depths, width: int, heig
         out += (T * a)[..., None] * col[gi][None, None, :]
         T = T * (1.0 - a)
     return out
+
+
+# --------------------------------------------------------------------------- densify / prune
+# Section "Densation et taille": clone a Gaussian whose gradient magnitude is
+# high but whose scale is small, split a large one with a high gradient into
+# two smaller ones, prune those whose opacity fell below a threshold.
+
+def densify(params: dict, accum, count, xi, grad_threshold: float, scale_threshold: float,
+            prune_opacity: float) -> dict:
+    """The densification step on host arrays. Decisions in float32 on the
+    logit and the log-scales against thresholds mapped in float64 (o < t iff
+    logit < log(t/(1-t)); max s > t iff max log s > log t), gradient g = accum /
+    count (float32 division, 0 if count = 0). Split children at mu + R S xi_c,
+    log-scales - log(1.6) (float64 arithmetic). Returns the new arrays
+    (float64) and ``action`` (0 keep, 1 clone, 2 split, 3 prune)."""
+    f = np.float32
+    lg = np.asarray(params["opacity_logits"], f)
+    ls = np.asarray(params["log_scales"], f)
+    acc = np.asarray(accum, f)
+    cnt = np.asarray(count, np.uint32)
+    logit_thr = f(np.log(prune_opacity / (1.0 - prune_opacity)))
+    ls_thr = f(np.log(scale_threshold))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        avg = np.where(cnt > 0, acc / np.maximum(cnt, 1).astype(f), f(0))
+    high = (cnt > 0) & (avg >= f(grad_threshold))
+    big = ls.max(axis=1) > ls_thr
+    action = np.where(lg < logit_thr, 3, np.where(high, np.where(big, 2, 1), 0)).astype(np.uint8)
+    q = np.asarray(params["quats"], np.float64)
+    q = q / np.linalg.norm(q, axis=1, keepdims=True)
+    w, x, y, z = q.T
+    R = np.stack([np.stack([1 - 2 * (y * y + z * z), 2 * (x * y - w * z), 2 * (x * z + w * y)], 1),
+                  np.stack([2 * (x * y + w * z), 1 - 2 * (x * x + z * z), 2 * (y * z - w * x)], 1),
+                  np.stack([2 * (x * z - w * y), 2 * (y * z + w * x), 1 - 2 * (x * x + y * y)], 1)], 1)
+    s = np.exp(ls.astype(np.float64))
+    out = {k: [] for k in PARAMS}
+    src = []
+    for gi, act in enumerate(action):
+        if act == 3:
+            continue
+        copies = 1 if act == 0 else 2
+        for c in range(copies):
+            src.append(gi)
+            for k in PARAMS:
+                out[k].append(np.asarray(params[k][gi], np.float64))
+            if act == 2:
+                out["means"][-1] = np.asarray(params["means"][gi], np.float64) + R[gi] @ (s[gi] * np.asarray(xi[gi, c], np.float64))
+                out["log_scales"][-1] = ls[gi].astype(np.float64) - np.log(1.6)
+    res = {k: np.asarray(v) for k, v in out.items()}
+    res.update(action=action, source=np.asarray(src, np.int64))
+    return res

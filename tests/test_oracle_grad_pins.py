@@ -202,3 +202,30 @@ def test_2d_gradients_match_central_differences():
             fd = (vals[0] - vals[1]) / (2 * h)
             ad = r[k][pos] + (r[k][(pos[0], pos[2], pos[1])] if k == "covs" and pos[1] != pos[2] else 0.0)
             assert abs(fd - ad) <= 1e-6 * (1.0 + abs(ad)), (k, pos, fd, ad)
+
+
+def test_densify_rules_on_hand_made_cases():
+    """One Gaussian per rule: prune (o < 0.005), keep (low gradient), clone (high
+    gradient, small), split (high gradient, large) with xi = 0 and xi = e_x;
+    and the boundaries: gradient exactly at the threshold counts as high,
+    opacity exactly at the threshold is kept."""
+    logit = lambda o: np.float32(np.log(o / (1 - o)))
+    t = np.log(np.float32(0.005) / (1 - np.float32(0.005)))
+    p = {"means": np.float32([[0, 0, 0], [1, 0, 0], [2, 0, 0], [3, 0, 0], [4, 0, 0], [5, 0, 0]]),
+         "quats": np.float32([[1, 0, 0, 0]] * 6),
+         "log_scales": np.float32([[-5, -5, -5], [-5, -5, -5], [-5, -6, -7], [-1, -3, -3], [-5, -5, -5],
+                                   [np.log(0.2), -3, -3]]),
+         "opacity_logits": np.float32([logit(0.001), logit(0.5), logit(0.5), logit(0.5), np.float32(t) + 1e-3, 2.0]),
+         "sh": np.zeros((6, 1, 3), np.float32)}
+    accum = np.float32([1.0, 1e-5, 4e-4, 1.0, 0.0, 2e-4])
+    count = np.uint32([1, 1, 2, 1, 0, 1])
+    xi = np.zeros((6, 2, 3), np.float32)
+    xi[5, 1] = [1, 0, 0]
+    r = gs_grad.densify(p, accum, count, xi, 2e-4, 0.01, 0.005)
+    assert list(r["action"]) == [3, 0, 1, 2, 0, 2]
+    assert list(r["source"]) == [1, 2, 2, 3, 3, 4, 5, 5]
+    # split with xi = 0: children at the parent's centre; xi = e_x: + s_x e_x
+    np.testing.assert_allclose(r["means"][3], [3, 0, 0], atol=1e-12)
+    np.testing.assert_allclose(r["means"][7], [5 + 0.2, 0, 0], rtol=1e-6)
+    np.testing.assert_allclose(r["log_scales"][6], np.float32([np.log(0.2), -3, -3]) - np.log(1.6), rtol=1e-12)
+    np.testing.assert_array_equal(r["means"][1], r["means"][2])   # clone = exact copy
