@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-batch", action="store_true")
+    ap.add_argument("--no-densify", action="store_true")
+    ap.add_argument("--no-toy", action="store_true")
     ap.add_argument("--batch-streams", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     return ap.parse_args()
@@ -211,6 +213,19 @@ def backward_summary(bwd, n, hbm_peak, fp32_peak):
             "rasterize_backward": {"ms": ras_ms, "bound": "alu", "walked_entries": walked,
                                    "ops_lower_bound": OPS_PER_EVAL * walked, "Top/s": ras_tops,
                                    "frac": ras_tops / fp32_peak}}
+
+
+def densify_summary(dens, sh_degree, hbm_peak):
+    """Densification step, per input Gaussian: the decision pass reads the
+    logit and log-scales (16 B) and the statistics (8 B); the scatter reads
+    the parameters once and the split samples (24 B), and writes the
+    parameters once per output copy."""
+    if dens is None:
+        return None
+    p = 4 * (3 + 4 + 3 + 1 + 3 * (sh_degree + 1) ** 2)
+    nbytes = dens["n_in"] * (16 + 8 + p + 24) + dens["n_out"] * p
+    return {"ms": dens["ms"], "n_in": dens["n_in"], "n_out": dens["n_out"], "bound": "hbm", "bytes": nbytes,
+            "GB/s": nbytes / (dens["ms"] * 1e-3) / 1e9, "frac": nbytes / (dens["ms"] * 1e-3) / 1e9 / hbm_peak}
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -462,6 +477,63 @@ def run_ours(args, rank, local_rank, world):
                      "sequential_ms": seq_ms, "sequential_views_per_s": len(bcams) * 1e3 / seq_ms,
                      "speedup": seq_ms / bat_ms}
             del br, single
+        # --- densification step on this scene (synthetic statistics): one
+        # stable compaction pass over the parameters
+        dens = None
+        if not args.no_densify:
+            n_g = int(g["n"])
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(7)
+            acc = torch.rand(n_g, device=dev, generator=gen) * 4e-4
+            cnt = torch.ones(n_g, dtype=torch.int32, device=dev)
+            xi = torch.randn((n_g, 2, 3), device=dev, generator=gen)
+            with torch.cuda.stream(stream):
+                n_new = gs.densify(g, acc, cnt, xi, 2e-4, 0.01, 0.005, stream=stream)["n"]
+                # the C call alone, into preallocated arrays (no host reads)
+                k3 = (cfg.sh_degree + 1) ** 2
+                ob = {"means": torch.empty((2 * n_g, 3), device=dev), "quats": torch.empty((2 * n_g, 4), device=dev),
+                      "log_scales": torch.empty((2 * n_g, 3), device=dev),
+                      "opacity_logits": torch.empty(2 * n_g, device=dev),
+                      "sh": torch.empty((2 * n_g, k3, 3), device=dev)}
+                o = native.GsGaussiansOut()
+                for k, v in ob.items():
+                    setattr(o, k, v.data_ptr())
+                o.n, o.sh_degree = 2 * n_g, cfg.sh_degree
+                new_n = torch.zeros(1, dtype=torch.int64, device=dev)
+                dwsb = int(L.gs_densify_workspace_bytes(n_g))
+                dws = torch.empty(dwsb, dtype=torch.uint8, device=dev)
+                gstruct = gs.gaussians_struct(g)
+
+                def densify_call():
+                    native.check(L.gs_densify(ctypes.byref(gstruct), acc.data_ptr(), cnt.data_ptr(), xi.data_ptr(),
+                                              2e-4, 0.01, 0.005, ctypes.byref(o), new_n.data_ptr(), None,
+                                              dws.data_ptr(), dwsb, sp), "gs_densify")
+                for _ in range(3):
+                    densify_call()
+                d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                nd = 10
+                stream.synchronize()
+                torch.cuda._sleep(int(40e6))
+                d0.record(stream)
+                for _ in range(nd):
+                    densify_call()
+                d1.record(stream)
+            torch.cuda.synchronize(dev)
+            assert int(new_n.item()) == n_new
+            dens = {"ms": d0.elapsed_time(d1) / nd, "n_in": n_g, "n_out": n_new}
+            del acc, cnt, xi, ob, dws
+        # --- the pages' 2D toy fit on the tile kernels (64 splats, 64x64, 200 Adam steps)
+        toy = None
+        if not args.no_toy:
+            from gaussian_splatting_tile_02_b300 import splat2d
+            splat2d.fit(steps=5)
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            fit = splat2d.fit(steps=200)
+            torch.cuda.synchronize(dev)
+            toy = {"steps": 200, "seconds": time.perf_counter() - t0, "mse_first": fit["losses"][0],
+                   "mse_final": fit["final_mse"]}
+            toy["steps_per_s"] = 200 / toy["seconds"]
     clocks = sampler.summary()
 
     # --- algorithmic work of the last frame (from its outputs)
@@ -543,6 +615,8 @@ def run_ours(args, rank, local_rank, world):
         "hbm_peak_gbs": hbm_peak,
         "backward": backward_summary(bwd, int(g["n"]), hbm_peak, fp32_peak),
         "batch": batch,
+        "densify": densify_summary(dens, cfg.sh_degree, hbm_peak),
+        "toy2d": toy,
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

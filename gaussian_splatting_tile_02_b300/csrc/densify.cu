@@ -127,16 +127,9 @@ __global__ void __launch_bounds__(1024) densify_scan_kernel(const DensArgs a, in
     }
 }
 
-__device__ __forceinline__ void copy_gaussian(const gs_gaussians& in, int64_t g, const gs_gaussians_out& out,
-                                              int64_t o, int nk3) {
-    for (int i = 0; i < 3; i++) out.means[3 * o + i] = in.means[3 * g + i];
-    for (int i = 0; i < 4; i++) out.quats[4 * o + i] = in.quats[4 * g + i];
-    for (int i = 0; i < 3; i++) out.log_scales[3 * o + i] = in.log_scales[3 * g + i];
-    out.opacity_logits[o] = in.opacity_logits[g];
-    for (int i = 0; i < nk3; i++) out.sh[(int64_t)nk3 * o + i] = in.sh[(int64_t)nk3 * g + i];
-}
-
-// scatter: block offset + rank inside the block
+// scatter: block offset + rank inside the block; then each warp copies its
+// 32 Gaussians one after another with all lanes (coalesced rows), and the
+// owner of a split Gaussian writes its children's centres and scales
 __global__ void __launch_bounds__(kDensThreads) densify_scatter_kernel(const DensArgs a) {
     __shared__ uint32_t s_warp[kDensThreads / 32];
     const int64_t g = (int64_t)blockIdx.x * kDensThreads + threadIdx.x;
@@ -152,13 +145,28 @@ __global__ void __launch_bounds__(kDensThreads) densify_scatter_kernel(const Den
     __syncthreads();
     uint32_t before = 0;
     for (int i = 0; i < w; i++) before += s_warp[i];
-    if (g >= a.in.n || slots == 0) return;
     const unsigned long long o = a.block_sums[blockIdx.x] + before + x - slots;
-    if (o + slots > (unsigned long long)a.capacity) return;   // flagged by the scan
+    const bool fits = slots > 0 && o + slots <= (unsigned long long)a.capacity;   // overflow is flagged by the scan
     const int nk3 = (a.in.sh_degree + 1) * (a.in.sh_degree + 1) * 3;
-    copy_gaussian(a.in, g, a.out, (int64_t)o, nk3);
-    if (slots == 1) return;
-    copy_gaussian(a.in, g, a.out, (int64_t)o + 1, nk3);
+    const int64_t gw = g - lane;   // the warp's first Gaussian
+    uint32_t todo = __ballot_sync(0xffffffffu, fits);
+    while (todo) {
+        const int j = __ffs(todo) - 1;
+        todo &= todo - 1;
+        const int64_t gj = gw + j;
+        const int64_t oj = (int64_t)__shfl_sync(0xffffffffu, (unsigned long long)o, j);
+        const uint32_t sj = __shfl_sync(0xffffffffu, slots, j);
+        for (uint32_t c = 0; c < sj; c++) {
+            const int64_t oc = oj + c;
+            for (int k = lane; k < nk3; k += 32) a.out.sh[(int64_t)nk3 * oc + k] = a.in.sh[(int64_t)nk3 * gj + k];
+            if (lane < 3) a.out.means[3 * oc + lane] = a.in.means[3 * gj + lane];
+            else if (lane < 7) a.out.quats[4 * oc + lane - 3] = a.in.quats[4 * gj + lane - 3];
+            else if (lane < 10) a.out.log_scales[3 * oc + lane - 7] = a.in.log_scales[3 * gj + lane - 7];
+            else if (lane == 10) a.out.opacity_logits[oc] = a.in.opacity_logits[gj];
+        }
+    }
+    __syncwarp();
+    if (!fits || slots == 1) return;
     const float* ls = a.in.log_scales + 3 * g;
     const float m = fmaxf(fmaxf(ls[0], ls[1]), ls[2]);
     if (!(m > a.log_scale_threshold)) return;   // clone: two identical copies
@@ -169,14 +177,14 @@ __global__ void __launch_bounds__(kDensThreads) densify_scatter_kernel(const Den
     const float R[9] = {1.f - 2.f * (y0 * y0 + z0 * z0), 2.f * (x0 * y0 - w0 * z0), 2.f * (x0 * z0 + w0 * y0),
                         2.f * (x0 * y0 + w0 * z0), 1.f - 2.f * (x0 * x0 + z0 * z0), 2.f * (y0 * z0 - w0 * x0),
                         2.f * (x0 * z0 - w0 * y0), 2.f * (y0 * z0 + w0 * x0), 1.f - 2.f * (x0 * x0 + y0 * y0)};
-    const float s[3] = {expf(ls[0]), expf(ls[1]), expf(ls[2])};
+    const float sc[3] = {expf(ls[0]), expf(ls[1]), expf(ls[2])};
     constexpr float kLog16 = 0.47000362924573558f;   // log(1.6)
     for (int c = 0; c < 2; c++) {
         const float* e = a.xi + 6 * g + 3 * c;
         const int64_t oc = (int64_t)o + c;
         for (int i = 0; i < 3; i++)
-            a.out.means[3 * oc + i] =
-                a.in.means[3 * g + i] + R[3 * i] * s[0] * e[0] + R[3 * i + 1] * s[1] * e[1] + R[3 * i + 2] * s[2] * e[2];
+            a.out.means[3 * oc + i] = a.in.means[3 * g + i] + R[3 * i] * sc[0] * e[0] + R[3 * i + 1] * sc[1] * e[1] +
+                                      R[3 * i + 2] * sc[2] * e[2];
         for (int i = 0; i < 3; i++) a.out.log_scales[3 * oc + i] = ls[i] - kLog16;
     }
 }
