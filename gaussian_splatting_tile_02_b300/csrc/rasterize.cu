@@ -52,7 +52,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // count per bucket, a prefix over the 33 buckets, then a scatter through
 // per-bucket cursors; the shared-memory atomics are aggregated per warp over
 // lanes with the same bucket.
-constexpr int kOrderThreads = 1024, kOrderItems = 4;
+constexpr int kOrderThreads = 1024, kOrderItems = 8;
 __global__ void __launch_bounds__(kOrderThreads) tile_order_kernel(const uint2* __restrict__ ranges, int tiles,
                                                                    uint32_t* __restrict__ order) {
     __shared__ uint32_t s_cnt[33];
@@ -66,30 +66,14 @@ __global__ void __launch_bounds__(kOrderThreads) tile_order_kernel(const uint2* 
         const uint32_t len = r.y - r.x;
         return len ? 32u - (uint32_t)__clz(len) : 0u;
     };
-    for (int t0 = 0; t0 < tiles; t0 += kOrderItems * kOrderThreads) {
-        uint32_t b[kOrderItems];
-#pragma unroll
-        for (int i = 0; i < kOrderItems; i++) b[i] = bucket(t0 + i * kOrderThreads + threadIdx.x);
+    auto count = [&](const uint32_t (&b)[kOrderItems]) {
 #pragma unroll
         for (int i = 0; i < kOrderItems; i++) {
             const uint32_t peers = __match_any_sync(0xffffffffu, b[i]);
             if (b[i] != 0xffffffffu && (peers & lt) == 0) atomicAdd(&s_cnt[b[i]], (uint32_t)__popc(peers));
         }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t run = 0;
-        for (int k = 32; k >= 0; k--) {
-            const uint32_t c = s_cnt[k];
-            s_cnt[k] = run;
-            run += c;
-        }
-    }
-    __syncthreads();
-    for (int t0 = 0; t0 < tiles; t0 += kOrderItems * kOrderThreads) {
-        uint32_t b[kOrderItems];
-#pragma unroll
-        for (int i = 0; i < kOrderItems; i++) b[i] = bucket(t0 + i * kOrderThreads + threadIdx.x);
+    };
+    auto scatter = [&](const uint32_t (&b)[kOrderItems], int t0) {
 #pragma unroll
         for (int i = 0; i < kOrderItems; i++) {
             const uint32_t peers = __match_any_sync(0xffffffffu, b[i]);
@@ -97,9 +81,43 @@ __global__ void __launch_bounds__(kOrderThreads) tile_order_kernel(const uint2* 
             uint32_t base = 0;
             if (b[i] != 0xffffffffu && lane == leader) base = atomicAdd(&s_cnt[b[i]], (uint32_t)__popc(peers));
             base = __shfl_sync(0xffffffffu, base, leader);
-            if (b[i] != 0xffffffffu)
-                order[base + __popc(peers & lt)] = (uint32_t)(t0 + i * kOrderThreads + threadIdx.x);
+            if (b[i] != 0xffffffffu) order[base + __popc(peers & lt)] = (uint32_t)(t0 + i * kOrderThreads + threadIdx.x);
         }
+    };
+    auto prefix = [&]() {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t run = 0;
+            for (int k = 32; k >= 0; k--) {
+                const uint32_t c = s_cnt[k];
+                s_cnt[k] = run;
+                run += c;
+            }
+        }
+        __syncthreads();
+    };
+    constexpr int kChunk = kOrderItems * kOrderThreads;
+    uint32_t b[kOrderItems];
+    if (tiles <= kChunk) {
+        // every tile in one pass: the buckets stay in registers between the
+        // count and the scatter (one round of loads)
+#pragma unroll
+        for (int i = 0; i < kOrderItems; i++) b[i] = bucket(i * kOrderThreads + threadIdx.x);
+        count(b);
+        prefix();
+        scatter(b, 0);
+        return;
+    }
+    for (int t0 = 0; t0 < tiles; t0 += kChunk) {
+#pragma unroll
+        for (int i = 0; i < kOrderItems; i++) b[i] = bucket(t0 + i * kOrderThreads + threadIdx.x);
+        count(b);
+    }
+    prefix();
+    for (int t0 = 0; t0 < tiles; t0 += kChunk) {
+#pragma unroll
+        for (int i = 0; i < kOrderItems; i++) b[i] = bucket(t0 + i * kOrderThreads + threadIdx.x);
+        scatter(b, t0);
     }
 }
 
