@@ -203,7 +203,8 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
 gs_status render_impl(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, void* ws, size_t ws_bytes,
                       float* image, float* final_T, uint32_t* n_contrib, void* stream, void* const* events) {
     if (!gaussians_ok(g) || !camera_ok(cam) || !image) return GS_ERR_INVALID_ARG;
-    if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
+    // the depth order sorts n keys: its look-back counts keep 30 bits
+    if (g->n > kMaxKeyCapacity || key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
     const RenderLayout L = render_layout(g->n, cam->width, cam->height, key_capacity);
     if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GS_ERR_WORKSPACE;
     return cuda_status(view_pipeline(g, cam, key_capacity, static_cast<char*>(ws), L, image, final_T, n_contrib,
@@ -526,7 +527,7 @@ gs_status gs_rasterize_2d(const float* means, const float* covs, const float* co
                           const float* depths, int64_t n, int32_t width, int32_t height, int64_t key_capacity,
                           void* ws, size_t ws_bytes, float* image, float* final_T, uint32_t* n_contrib,
                           void* stream) {
-    if (n < 0 || n > kMaxGaussians || width < 1 || height < 1 || width > 32768 || height > 32768 || !image)
+    if (n < 0 || n > kMaxKeyCapacity || width < 1 || height < 1 || width > 32768 || height > 32768 || !image)
         return GS_ERR_INVALID_ARG;
     if (n > 0 && (!means || !covs || !colours || !opacities || !depths || !aligned(means, 8)))
         return GS_ERR_INVALID_ARG;
@@ -616,6 +617,7 @@ gs_status gs_render_batch(const gs_gaussians* g, const gs_camera* cams, int32_t 
                           void* ws, size_t ws_bytes, float* images, float* final_T, uint32_t* n_contrib,
                           void* const* streams, int32_t n_streams) {
     if (!gaussians_ok(g) || !cams || views < 1 || views > GS_MAX_BATCH_VIEWS || !images) return GS_ERR_INVALID_ARG;
+    if (g->n > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
     if (!streams || n_streams < 1 || n_streams > kMaxBatchStreams) return GS_ERR_INVALID_ARG;
     if (key_capacity < 0 || key_capacity > kMaxKeyCapacity) return GS_ERR_INVALID_ARG;
     for (int v = 0; v < views; v++) {

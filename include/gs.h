@@ -263,6 +263,8 @@ gs_status gs_rasterize(const gs_projected* projected, int64_t n, const uint32_t*
  * key_capacity bounds the (Gaussian, tile) pairs of the frame; if the frame
  * needs more, GS_FLAG_CAPACITY is set, the image is unspecified and
  * gs_read_status reports the count needed. */
+/* Limits: n and key_capacity at most 2^30 - 1 (the radix sort's look-back
+ * words keep 30-bit counts); GS_ERR_INVALID_ARG above. */
 size_t gs_render_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity);
 gs_status gs_render(const gs_gaussians* gaussians, const gs_camera* camera, int64_t key_capacity,
                     void* ws, size_t ws_bytes, float* image, float* final_T,

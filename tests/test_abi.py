@@ -91,6 +91,33 @@ def test_host_validation_rejects_bad_arguments():
     assert L.gs_render(ctypes.byref(g3), ctypes.byref(cam), 10, 256, 8, 256, None, None, None) == \
         native.GS_ERR_WORKSPACE
     assert L.gs_read_status(None, None, None, None) == native.GS_ERR_WORKSPACE
+    # render / batch / 2D: n beyond the depth sort's 30-bit counts (checked before any pointer use)
+    g4 = native.GsGaussians()
+    g4.n, g4.sh_degree = 1 << 30, 0
+    g4.means = g4.log_scales = g4.opacity_logits = g4.sh = g4.quats = 1 << 20
+    assert L.gs_render(ctypes.byref(g4), ctypes.byref(cam), 10, 1 << 20, 1 << 40, 256, None, None, None) == \
+        native.GS_ERR_INVALID_ARG
+    cams = (native.GsCamera * 1)(cam)
+    streams = (ctypes.c_void_p * 1)(None)
+    assert L.gs_render_batch(ctypes.byref(g4), cams, 1, 10, 1 << 20, 1 << 40, 256, None, None, streams, 1) == \
+        native.GS_ERR_INVALID_ARG
+    assert L.gs_rasterize_2d(256, 256, 256, 256, 256, 1 << 30, 64, 64, 10, 1 << 20, 1 << 40, 256, None, None,
+                             None) == native.GS_ERR_INVALID_ARG
+    # batch: views out of range, too many streams; backward / densify: null outputs
+    g3.n = 0
+    assert L.gs_render_batch(ctypes.byref(g3), cams, 0, 10, 1 << 20, 1 << 40, 256, None, None, streams, 1) == \
+        native.GS_ERR_INVALID_ARG
+    many = (ctypes.c_void_p * 9)(*([None] * 9))
+    assert L.gs_render_batch(ctypes.byref(g3), cams, 1, 10, 1 << 20, 1 << 40, 256, None, None, many, 9) == \
+        native.GS_ERR_INVALID_ARG
+    assert L.gs_render_backward(ctypes.byref(g3), ctypes.byref(cam), 10, 1 << 20, 1 << 40, None, None, None,
+                                None, None) == native.GS_ERR_INVALID_ARG
+    assert L.gs_densify(ctypes.byref(g3), None, None, None, 2e-4, 0.01, 0.005, None, None, None, None, 0,
+                        None) == native.GS_ERR_INVALID_ARG
+    out = native.GsGaussiansOut()
+    out.n, out.sh_degree = 0, 0
+    assert L.gs_densify(ctypes.byref(g3), None, None, None, 2e-4, 0.01, 1.5, ctypes.byref(out), 256, None, 256,
+                        1 << 20, None) == native.GS_ERR_INVALID_ARG
 
 
 def test_key_bits():
