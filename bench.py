@@ -561,17 +561,17 @@ def run_ours(args, rank, local_rank, world):
     K = K_keys
     tile_bits = max(1, (tx * ty - 1).bit_length())
     tpasses = (tile_bits + 7) // 8
-    # preprocess; depth keys, sort bases, 4 depth passes; 5 binning kernels;
-    # sort bases + tile passes; ranges; tile order + rasterize
-    launches_per_frame = 1 + (1 + 1 + 4) + 5 + (1 + tpasses) + 1 + 2
+    # preprocess (which also writes the depth keys); sort bases, 4 depth passes;
+    # 5 binning kernels; sort bases + tile passes; ranges; tile order + rasterize
+    launches_per_frame = 1 + (1 + 4) + 5 + (1 + tpasses) + 1 + 2
     ras_ms = st_ms["rasterize"]
     clk = clocks.get("sm_mhz") or SM_MAX_MHZ
     fp32_peak = SM_COUNT * FP32_LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12     # T lane-ops/s at max clock
     ras_ops = OPS_PER_EVAL * evals
     ras_achieved = ras_ops / (ras_ms * 1e-3) / 1e12
     stage_bytes = {
-        "preprocess": (PARAM_BYTES_PER_G + PROJ_BYTES_PER_G) * n,
-        "depth_order": 16 * n + 4 * 16 * n,
+        "preprocess": (PARAM_BYTES_PER_G + PROJ_BYTES_PER_G + 8) * n,   # + the depth keys and indices
+        "depth_order": 4 * 16 * n,
         "bin": 24 * n + 8 * K,
         "tile_sort": tpasses * 16 * K,
         "ranges": 4 * K + 8 * tx * ty,

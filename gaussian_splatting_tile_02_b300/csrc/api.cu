@@ -141,12 +141,27 @@ gs_projected view_projected(char* w, const RenderLayout& L) {
 namespace gs {
 namespace {
 
-// Steps 2-5 of one view (and step 1 unless the caller already ran it into
-// this view's workspace), on stream s. events: null, or 7 handles recorded at
-// the stage boundaries.
+// How the depth-order input of a view comes about.
+enum class Step1 {
+    kProject,      // run the projection here; it also writes the depth keys and their histograms
+    kKeysReady,    // the caller projected into this workspace and wrote the keys and histograms
+    kRecordOnly,   // the caller wrote the record only (2D splats): derive the keys here
+};
+
+// The depth-order keys of a view's workspace.
+DepthKeysOut view_depth_keys(char* w, const RenderLayout& L) {
+    DepthKeysOut dk;
+    dk.keys = reinterpret_cast<uint32_t*>(w + L.dkeys);
+    dk.vals = reinterpret_cast<uint32_t*>(w + L.order);
+    dk.hist = sort_histogram_of(w + L.sort);
+    return dk;
+}
+
+// Steps 2-5 of one view (step 1 as `step1` says), on stream s. events: null,
+// or 7 handles recorded at the stage boundaries.
 cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, char* w,
                           const RenderLayout& L, float* image, float* final_T, uint32_t* n_contrib, cudaStream_t s,
-                          void* const* events, bool run_preprocess) {
+                          void* const* events, Step1 step1) {
     auto* header = reinterpret_cast<StatusHeader*>(w + L.header);
     auto* num_keys = reinterpret_cast<uint64_t*>(w + L.num_keys);
     gs_projected p = view_projected(w, L);
@@ -171,12 +186,18 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
     auto mark = [&](int i) {
         return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
     };
+    const DepthKeysOut dk = view_depth_keys(w, L);
     cudaError_t e = mark(0);
     if (e == cudaSuccess) e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
-    if (e == cudaSuccess && run_preprocess) e = launch_preprocess(*g, cc, p, s);
+    if (e == cudaSuccess && step1 == Step1::kProject) {
+        e = sort_prepare_histogram(sort_ws, s);
+        if (e == cudaSuccess) e = launch_preprocess(*g, cc, p, s, &dk);
+    }
     if (e == cudaSuccess) e = mark(1);
-    if (e == cudaSuccess) e = sort_prepare_histogram(sort_ws, s);
-    if (e == cudaSuccess) e = launch_depth_keys(p, g->n, dkeys, order, hist, s);
+    if (e == cudaSuccess && step1 == Step1::kRecordOnly) {
+        e = sort_prepare_histogram(sort_ws, s);
+        if (e == cudaSuccess) e = launch_depth_keys(p, g->n, dkeys, order, hist, s);
+    }
     if (e == cudaSuccess)
         e = launch_sort32(dkeys, order, dkeys_alt, order_alt, nullptr, g->n, 32, header, sort_ws, g_spin_limit, s,
                           true);
@@ -208,7 +229,7 @@ gs_status render_impl(const gs_gaussians* g, const gs_camera* cam, int64_t key_c
     const RenderLayout L = render_layout(g->n, cam->width, cam->height, key_capacity);
     if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GS_ERR_WORKSPACE;
     return cuda_status(view_pipeline(g, cam, key_capacity, static_cast<char*>(ws), L, image, final_T, n_contrib,
-                                     (cudaStream_t)stream, events, true));
+                                     (cudaStream_t)stream, events, Step1::kProject));
 }
 
 // Fork/join events for gs_render_batch, created once per device on first use
@@ -543,7 +564,8 @@ gs_status gs_rasterize_2d(const float* means, const float* covs, const float* co
     if (launch_preprocess2d(means, covs, colours, opacities, depths, n, width, height, view_projected(w, L), s) !=
         cudaSuccess)
         return GS_ERR_CUDA;
-    return cuda_status(view_pipeline(&g, &cam, key_capacity, w, L, image, final_T, n_contrib, s, nullptr, false));
+    return cuda_status(
+        view_pipeline(&g, &cam, key_capacity, w, L, image, final_T, n_contrib, s, nullptr, Step1::kRecordOnly));
 }
 
 gs_status gs_rasterize_2d_backward(const float* covs, int64_t n, int32_t width, int32_t height, int64_t key_capacity,
@@ -637,11 +659,15 @@ gs_status gs_render_batch(const gs_gaussians* g, const gs_camera* cams, int32_t 
         const int nv = views - v0 < kMaxBatchViews ? views - v0 : kMaxBatchViews;
         CamConst cc[kMaxBatchViews];
         gs_projected pr[kMaxBatchViews];
+        DepthKeysOut dk[kMaxBatchViews];
         for (int i = 0; i < nv; i++) {
+            char* wv = w0 + (size_t)(v0 + i) * stride;
             cc[i] = make_cam_const(cams[v0 + i]);
-            pr[i] = view_projected(w0 + (size_t)(v0 + i) * stride, L);
+            pr[i] = view_projected(wv, L);
+            dk[i] = view_depth_keys(wv, L);
+            if (sort_prepare_histogram(wv + L.sort, s0) != cudaSuccess) return GS_ERR_CUDA;
         }
-        if (launch_preprocess_batch(*g, cc, pr, nv, s0) != cudaSuccess) return GS_ERR_CUDA;
+        if (launch_preprocess_batch(*g, cc, pr, dk, nv, s0) != cudaSuccess) return GS_ERR_CUDA;
     }
     // steps 2-5 per view, round-robin over the streams, forked from and joined into streams[0]
     if (n_streams > 1) {
@@ -653,7 +679,8 @@ gs_status gs_render_batch(const gs_gaussians* g, const gs_camera* cams, int32_t 
         cudaStream_t s = (cudaStream_t)streams[v % n_streams];
         const cudaError_t e = view_pipeline(g, cams + v, key_capacity, w0 + (size_t)v * stride, L,
                                             images + (size_t)v * pix * 3, final_T ? final_T + (size_t)v * pix : nullptr,
-                                            n_contrib ? n_contrib + (size_t)v * pix : nullptr, s, nullptr, false);
+                                            n_contrib ? n_contrib + (size_t)v * pix : nullptr, s, nullptr,
+                                            Step1::kKeysReady);
         if (e != cudaSuccess) return GS_ERR_CUDA;
     }
     for (int i = 1; i < n_streams; i++) {

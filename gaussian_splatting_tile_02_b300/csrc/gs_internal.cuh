@@ -75,8 +75,16 @@ __device__ __forceinline__ void raise_flag(StatusHeader* h, uint32_t flag, uint3
 // ---------------------------------------------------------------- launchers
 
 // preprocess.cu
-cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const gs_projected& out,
-                              cudaStream_t s);
+// Depth-order sort input written by the projection step (nullable): keys
+// (depth bits, or 0xffffffff without tiles), values (indices), and the keys'
+// 8-bit digit histograms [4][256], accumulated (zeroed by the caller).
+struct DepthKeysOut {
+    uint32_t* keys;
+    uint32_t* vals;
+    uint32_t* hist;
+};
+cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const gs_projected& out, cudaStream_t s,
+                              const DepthKeysOut* dk = nullptr);
 
 // binning.cu
 size_t bin_scratch_bytes(int64_t n);
@@ -134,8 +142,8 @@ cudaError_t launch_densify(const gs_gaussians& in, const gs_gaussians_out& out, 
 // at most this many views per batched preprocess launch
 constexpr int kMaxBatchViews = 8;
 // cams[views], outs[views]: one projected record per view
-cudaError_t launch_preprocess_batch(const gs_gaussians& g, const CamConst* cams, const gs_projected* outs, int views,
-                                    cudaStream_t s);
+cudaError_t launch_preprocess_batch(const gs_gaussians& g, const CamConst* cams, const gs_projected* outs,
+                                    const DepthKeysOut* dks, int views, cudaStream_t s);
 cudaError_t launch_rasterize_backward(const gs_projected& p, int64_t n, const uint32_t* sorted_vals,
                                       const uint32_t* ranges, const uint32_t* tile_order, const CamConst& cam,
                                       const float* final_T, const uint32_t* n_contrib, const float* grad_image,

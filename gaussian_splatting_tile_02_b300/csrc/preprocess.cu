@@ -35,6 +35,9 @@
 #include <cuda_fp16.h>
 #include <float.h>
 
+#include <map>
+#include <mutex>
+
 #include "gs_internal.cuh"
 
 namespace gs {
@@ -201,11 +204,18 @@ struct PreArgs {
     int32_t* radius;
     uint32_t* tiles_touched;
     ushort4* rect;
+    // depth-order sort input, nullable: key = depth bits for Gaussians with
+    // tiles (depth > near > 0, so the bits order like the depths), 0xffffffff
+    // for the others (sorted last); value = index; digit histograms of the
+    // keys ([4][256], accumulated)
+    uint32_t* dkeys;
+    uint32_t* dvals;
+    uint32_t* dhist;
 };
 
-// One Gaussian seen by one camera.
+// One Gaussian seen by one camera; returns its depth-order key.
 template <int D>
-__device__ __forceinline__ void preprocess_one(const PreArgs& a, int64_t g) {
+__device__ __forceinline__ uint32_t preprocess_one(const PreArgs& a, int64_t g) {
     const CamConst& C = a.cam;
     const float m0 = __ldg(a.means + 3 * g), m1 = __ldg(a.means + 3 * g + 1), m2 = __ldg(a.means + 3 * g + 2);
 
@@ -227,7 +237,7 @@ __device__ __forceinline__ void preprocess_one(const PreArgs& a, int64_t g) {
         if (a.radius) a.radius[g] = 0;
         a.tiles_touched[g] = 0;
         a.rect[g] = make_ushort4(0, 0, 0, 0);
-        return;
+        return 0xffffffffu;
     }
     const float rn = sq(n2);
     const float w = dv(q.x, rn), x = dv(q.y, rn), y = dv(q.z, rn), zq = dv(q.w, rn);
@@ -281,7 +291,7 @@ __device__ __forceinline__ void preprocess_one(const PreArgs& a, int64_t g) {
         if (a.radius) a.radius[g] = 0;
         a.tiles_touched[g] = 0;
         a.rect[g] = make_ushort4(0, 0, 0, 0);
-        return;
+        return 0xffffffffu;
     }
     float x0 = ceilf(sub(u, rf)), x1 = floorf(add(u, rf));
     float y0 = ceilf(sub(v, rf)), y1 = floorf(add(v, rf));
@@ -376,12 +386,56 @@ __device__ __forceinline__ void preprocess_one(const PreArgs& a, int64_t g) {
         rec[1] = make_float4(k1, k2, k3, log2f(o));
         rec[2] = make_float4(col.x, col.y, col.z, __uint_as_float(*reinterpret_cast<const uint32_t*>(&h)));
     }
+    return touched ? __float_as_uint(z) : 0xffffffffu;
 }
 
+// The depth-order key of Gaussian g into the sort input and the block's digit
+// histograms (8-bit digits of the 32-bit key, [4][256] in shared memory).
+// The two high digits take few values across a warp (depths of nearby
+// magnitude share their exponent bits), so they are counted once per distinct
+// value per warp; the two low ones are near-uniform and counted per key.
+// Called by whole warps (inactive lanes pass valid = false).
+__device__ __forceinline__ void emit_depth_key(const PreArgs& a, int64_t g, uint32_t key, uint32_t* s_hist,
+                                               bool valid = true) {
+    if (valid) {
+        a.dkeys[g] = key;
+        a.dvals[g] = (uint32_t)g;
+        atomicAdd(&s_hist[key & 255u], 1u);
+        atomicAdd(&s_hist[256 + ((key >> 8) & 255u)], 1u);
+    }
+    const uint32_t lt = (1u << (threadIdx.x & 31)) - 1u;
+    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+    for (int p = 2; p < 4; p++) {
+        const uint32_t d = (key >> (8 * p)) & 255u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? d : 0xffffffffu) & vmask;
+        if (valid && (peers & lt) == 0) atomicAdd(&s_hist[p * 256 + d], (uint32_t)__popc(peers));
+    }
+}
+__device__ __forceinline__ void flush_depth_hist(const uint32_t* s_hist, uint32_t* hist) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x)
+        if (s_hist[i]) atomicAdd(&hist[i], s_hist[i]);
+}
+
+// Grid-stride over the Gaussians with as many blocks as fit on the GPU at
+// once, so that the per-block digit histograms of the depth keys are flushed
+// by few blocks.
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
-    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (g < a.n) preprocess_one<D>(a, g);
+    __shared__ uint32_t s_hist[4 * 256];
+    if (a.dkeys)
+        for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) s_hist[i] = 0;
+    __syncthreads();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    // warp-uniform trip count (the key emission works on whole warps)
+    for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); g0 < a.n; g0 += stride) {
+        const int64_t g = g0 + (threadIdx.x & 31);
+        const bool valid = g < a.n;
+        const uint32_t key = valid ? preprocess_one<D>(a, g) : 0u;
+        if (a.dkeys) emit_depth_key(a, g, key, s_hist, valid);
+    }
+    if (a.dkeys) flush_depth_hist(s_hist, a.dhist);
 }
 
 // Several cameras in one pass over the parameters: each thread projects its
@@ -395,12 +449,24 @@ struct PreBatchArgs {
 
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_batch_kernel(const PreBatchArgs a) {
-    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (g >= a.v[0].n) return;
-    for (int i = 0; i < a.views; i++) preprocess_one<D>(a.v[i], g);
+    __shared__ uint32_t s_hist[kMaxBatchViews * 4 * 256];   // per view
+    const int nv = a.views;
+    for (int k = threadIdx.x; k < nv * 1024; k += blockDim.x) s_hist[k] = 0;
+    __syncthreads();
+    const int64_t n = a.v[0].n, stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); g0 < n; g0 += stride) {
+        const int64_t g = g0 + (threadIdx.x & 31);
+        const bool valid = g < n;
+        for (int i = 0; i < nv; i++) {
+            const uint32_t key = valid ? preprocess_one<D>(a.v[i], g) : 0u;
+            if (a.v[i].dkeys) emit_depth_key(a.v[i], g, key, s_hist + i * 1024, valid);
+        }
+    }
+    for (int i = 0; i < nv; i++)
+        if (a.v[i].dkeys) flush_depth_hist(s_hist + i * 1024, a.v[i].dhist);
 }
 
-PreArgs pre_args(const gs_gaussians& g, const CamConst& cam, const gs_projected& out) {
+PreArgs pre_args(const gs_gaussians& g, const CamConst& cam, const gs_projected& out, const DepthKeysOut* dk) {
     PreArgs a;
     a.means = g.means;
     a.quats = reinterpret_cast<const float4*>(g.quats);
@@ -417,38 +483,63 @@ PreArgs pre_args(const gs_gaussians& g, const CamConst& cam, const gs_projected&
     a.radius = out.radius;
     a.tiles_touched = out.tiles_touched;
     a.rect = reinterpret_cast<ushort4*>(out.rect);
+    a.dkeys = dk ? dk->keys : nullptr;
+    a.dvals = dk ? dk->vals : nullptr;
+    a.dhist = dk ? dk->hist : nullptr;
     return a;
+}
+
+// blocks of 256 that fit on the GPU at once for this kernel (occupancy
+// computed once per kernel; every instantiation has its own cache entry)
+template <typename K>
+unsigned resident_blocks(K kernel, int64_t n) {
+    static std::mutex mu;
+    static std::map<const void*, int64_t> cache;
+    int64_t cap = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(reinterpret_cast<const void*>(kernel));
+        if (it == cache.end()) {
+            int dev = 0, sms = 0, per_sm = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+            it = cache.emplace(reinterpret_cast<const void*>(kernel),
+                               (int64_t)(per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 148)).first;
+        }
+        cap = it->second;
+    }
+    const int64_t need = (n + 255) / 256;
+    return (unsigned)(need < cap ? need : cap);
 }
 
 }  // namespace
 
-cudaError_t launch_preprocess_batch(const gs_gaussians& g, const CamConst* cams, const gs_projected* outs, int views,
-                                    cudaStream_t s) {
+cudaError_t launch_preprocess_batch(const gs_gaussians& g, const CamConst* cams, const gs_projected* outs,
+                                    const DepthKeysOut* dks, int views, cudaStream_t s) {
     if (g.n == 0 || views <= 0) return cudaSuccess;
     if (views > kMaxBatchViews) return cudaErrorInvalidValue;
     PreBatchArgs a;
-    for (int i = 0; i < views; i++) a.v[i] = pre_args(g, cams[i], outs[i]);
+    for (int i = 0; i < views; i++) a.v[i] = pre_args(g, cams[i], outs[i], dks ? dks + i : nullptr);
     a.views = views;
-    const unsigned blocks = (unsigned)((g.n + 255) / 256);
     switch (g.sh_degree) {
-        case 0: preprocess_batch_kernel<0><<<blocks, 256, 0, s>>>(a); break;
-        case 1: preprocess_batch_kernel<1><<<blocks, 256, 0, s>>>(a); break;
-        case 2: preprocess_batch_kernel<2><<<blocks, 256, 0, s>>>(a); break;
-        default: preprocess_batch_kernel<3><<<blocks, 256, 0, s>>>(a); break;
+        case 0: preprocess_batch_kernel<0><<<resident_blocks(preprocess_batch_kernel<0>, g.n), 256, 0, s>>>(a); break;
+        case 1: preprocess_batch_kernel<1><<<resident_blocks(preprocess_batch_kernel<1>, g.n), 256, 0, s>>>(a); break;
+        case 2: preprocess_batch_kernel<2><<<resident_blocks(preprocess_batch_kernel<2>, g.n), 256, 0, s>>>(a); break;
+        default: preprocess_batch_kernel<3><<<resident_blocks(preprocess_batch_kernel<3>, g.n), 256, 0, s>>>(a); break;
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const gs_projected& out,
-                              cudaStream_t s) {
+                              cudaStream_t s, const DepthKeysOut* dk) {
     if (g.n == 0) return cudaSuccess;
-    const PreArgs a = pre_args(g, cam, out);
-    const unsigned blocks = (unsigned)((g.n + 255) / 256);
+    const PreArgs a = pre_args(g, cam, out, dk);
     switch (g.sh_degree) {
-        case 0: preprocess_kernel<0><<<blocks, 256, 0, s>>>(a); break;
-        case 1: preprocess_kernel<1><<<blocks, 256, 0, s>>>(a); break;
-        case 2: preprocess_kernel<2><<<blocks, 256, 0, s>>>(a); break;
-        default: preprocess_kernel<3><<<blocks, 256, 0, s>>>(a); break;
+        case 0: preprocess_kernel<0><<<resident_blocks(preprocess_kernel<0>, g.n), 256, 0, s>>>(a); break;
+        case 1: preprocess_kernel<1><<<resident_blocks(preprocess_kernel<1>, g.n), 256, 0, s>>>(a); break;
+        case 2: preprocess_kernel<2><<<resident_blocks(preprocess_kernel<2>, g.n), 256, 0, s>>>(a); break;
+        default: preprocess_kernel<3><<<resident_blocks(preprocess_kernel<3>, g.n), 256, 0, s>>>(a); break;
     }
     return cudaGetLastError();
 }
