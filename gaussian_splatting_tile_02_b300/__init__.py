@@ -27,7 +27,7 @@ from .native import GsCamera, GsGaussians, GsGaussiansGrad, GsProjected, GsProje
 __all__ = ["GsCamera", "camera_struct", "gaussians_to_device", "gaussians_struct", "preprocess",
            "bin_keys", "sort_pairs", "tile_ranges", "rasterize", "Renderer", "read_status",
            "key_bits", "tiles_xy", "lib", "render_from_host", "rasterize_backward", "preprocess_backward",
-           "alloc_param_grads", "BatchRenderer", "densify_stats", "densify"]
+           "alloc_param_grads", "BatchRenderer", "densify_stats", "densify", "HostPipeline"]
 
 
 def _torch():
@@ -394,6 +394,50 @@ class BatchRenderer:
     def status(self, view: int, stream=None) -> tuple:
         """(status, flags, num_keys) of one view; synchronises the stream."""
         return read_status(self.ws[view * self.view_ws_bytes:], stream)
+
+
+class HostPipeline:
+    """Frames from pinned host parameters with the copies overlapped
+    (gs_render_from_host_async): two device parameter sets, and render,
+    upload and read-back streams, so that frame k + 1's upload runs during
+    frame k's render and image read-back."""
+
+    def __init__(self, renderer: Renderer):
+        torch = _torch()
+        self.r = renderer
+        g = renderer.g
+        dev = g["means"].device
+        self.sets = [{k: torch.empty_like(g[k]) for k in _FIELDS} for _ in range(2)]
+        structs = []
+        for d in self.sets:
+            d.update(n=g["n"], sh_degree=g["sh_degree"])
+            structs.append(gaussians_struct(d))
+        self._sets = (GsGaussians * 2)(*structs)
+        self.streams = [torch.cuda.Stream(device=dev) for _ in range(3)]
+        self.events = [torch.cuda.Event() for _ in range(6)]
+        for e in self.events:
+            e.record(self.streams[0])   # creates the underlying CUDA events
+        torch.cuda.synchronize(dev)
+        self._streams = (ctypes.c_void_p * 3)(*[s.cuda_stream for s in self.streams])
+        self._events = (ctypes.c_void_p * 6)(*[e.cuda_event for e in self.events])
+        self.frame = 0
+
+    def submit(self, host: dict, cam: dict, host_image) -> None:
+        hs = GsGaussians()
+        for k in _FIELDS:
+            setattr(hs, k, host[k].data_ptr())
+        hs.n = int(self.r.g["n"])
+        hs.sh_degree = int(self.r.g["sh_degree"])
+        check(lib().gs_render_from_host_async(ctypes.byref(hs), self._sets, self.frame,
+                                              ctypes.byref(camera_struct(cam)), self.r.key_capacity,
+                                              _ptr(self.r.ws), self.r.ws_bytes, _ptr(self.r.image),
+                                              host_image.data_ptr(), self._streams, self._events),
+              "gs_render_from_host_async")
+        self.frame += 1
+
+    def synchronize(self) -> None:
+        for s in self.streams:
+            s.synchronize()
 
 
 def render_from_host(host: dict, renderer: Renderer, cam: dict, host_image, stream=None) -> None:

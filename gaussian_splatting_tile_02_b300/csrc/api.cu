@@ -690,6 +690,54 @@ gs_status gs_render_batch(const gs_gaussians* g, const gs_camera* cams, int32_t 
     return GS_OK;
 }
 
+gs_status gs_render_from_host_async(const gs_gaussians* hg, const gs_gaussians* device_sets, int64_t frame,
+                                    const gs_camera* cam, int64_t key_capacity, void* ws, size_t ws_bytes,
+                                    float* device_image, float* host_image, void* const* streams,
+                                    void* const* events) {
+    if (!hg || !device_sets || frame < 0 || !streams || !events || !host_image || !device_image)
+        return GS_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; i++)
+        if (!streams[i]) return GS_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; i++)
+        if (!events[i]) return GS_ERR_INVALID_ARG;
+    const int set = (int)(frame & 1);
+    const gs_gaussians* dg = device_sets + set;
+    if (hg->n != dg->n || hg->sh_degree != dg->sh_degree || !gaussians_ok(dg) || !camera_ok(cam))
+        return GS_ERR_INVALID_ARG;
+    if (dg->n > 0 && (!hg->means || !hg->quats || !hg->log_scales || !hg->opacity_logits || !hg->sh))
+        return GS_ERR_INVALID_ARG;
+    cudaStream_t s_render = (cudaStream_t)streams[0], s_h2d = (cudaStream_t)streams[1],
+                 s_d2h = (cudaStream_t)streams[2];
+    cudaEvent_t h2d_done = (cudaEvent_t)events[set], render_done = (cudaEvent_t)events[2 + set],
+                img_ready = (cudaEvent_t)events[4], img_copied = (cudaEvent_t)events[5];
+    const size_t n = (size_t)dg->n, nk = (size_t)((dg->sh_degree + 1) * (dg->sh_degree + 1));
+    struct { const void* src; const void* dst; size_t bytes; } cp[5] = {
+        {hg->means, dg->means, 12 * n}, {hg->quats, dg->quats, 16 * n}, {hg->log_scales, dg->log_scales, 12 * n},
+        {hg->opacity_logits, dg->opacity_logits, 4 * n}, {hg->sh, dg->sh, 12 * nk * n}};
+    // 1. parameters into this frame's device set, once the frame two back has
+    //    finished rendering from it
+    if (frame >= 2 && cudaStreamWaitEvent(s_h2d, render_done, 0) != cudaSuccess) return GS_ERR_CUDA;
+    for (auto& c : cp) {
+        if (c.bytes == 0) continue;
+        if (cudaMemcpyAsync(const_cast<void*>(c.dst), c.src, c.bytes, cudaMemcpyHostToDevice, s_h2d) != cudaSuccess)
+            return GS_ERR_CUDA;
+    }
+    if (cudaEventRecord(h2d_done, s_h2d) != cudaSuccess) return GS_ERR_CUDA;
+    // 2. render once the copy is in and the previous image has been read back
+    if (cudaStreamWaitEvent(s_render, h2d_done, 0) != cudaSuccess) return GS_ERR_CUDA;
+    if (frame >= 1 && cudaStreamWaitEvent(s_render, img_copied, 0) != cudaSuccess) return GS_ERR_CUDA;
+    gs_status st = gs_render(dg, cam, key_capacity, ws, ws_bytes, device_image, nullptr, nullptr, s_render);
+    if (st != GS_OK) return st;
+    if (cudaEventRecord(render_done, s_render) != cudaSuccess) return GS_ERR_CUDA;
+    if (cudaEventRecord(img_ready, s_render) != cudaSuccess) return GS_ERR_CUDA;
+    // 3. the image back to the host
+    if (cudaStreamWaitEvent(s_d2h, img_ready, 0) != cudaSuccess) return GS_ERR_CUDA;
+    const size_t img = (size_t)cam->width * cam->height * 3 * sizeof(float);
+    if (cudaMemcpyAsync(host_image, device_image, img, cudaMemcpyDeviceToHost, s_d2h) != cudaSuccess)
+        return GS_ERR_CUDA;
+    return cuda_status(cudaEventRecord(img_copied, s_d2h));
+}
+
 gs_status gs_read_status(const void* ws, void* stream, uint32_t* flags, uint64_t* num_keys) {
     if (!ws || !aligned(ws, kAlign)) return GS_ERR_WORKSPACE;
     StatusHeader h;

@@ -106,6 +106,10 @@ _SIGNATURES = {
     "gs_densify": (ctypes.c_int, [ctypes.POINTER(GsGaussians), c_void_p, c_void_p, c_void_p, ctypes.c_float,
                                   ctypes.c_float, ctypes.c_float, ctypes.POINTER(GsGaussiansOut), c_void_p, c_void_p,
                                   c_void_p, ctypes.c_size_t, c_void_p]),
+    "gs_render_from_host_async": (ctypes.c_int, [ctypes.POINTER(GsGaussians), ctypes.POINTER(GsGaussians),
+                                                 ctypes.c_int64, ctypes.POINTER(GsCamera), ctypes.c_int64, c_void_p,
+                                                 ctypes.c_size_t, c_void_p, c_void_p, ctypes.POINTER(c_void_p),
+                                                 ctypes.POINTER(c_void_p)]),
     "gs_rasterize_backward": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, c_void_p, c_void_p,
                                              ctypes.POINTER(GsCamera), c_void_p, c_void_p, c_void_p, c_void_p,
                                              ctypes.POINTER(GsProjectedGrad), c_void_p]),

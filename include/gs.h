@@ -460,6 +460,26 @@ gs_status gs_densify(const gs_gaussians* in, const float* accum, const uint32_t*
                      float prune_opacity, const gs_gaussians_out* out, uint64_t* out_count,
                      uint8_t* action, void* ws, size_t ws_bytes, void* stream);
 
+/* Frames from host memory with the copies overlapped: a two-deep pipeline
+ * over a sequence of calls with frame = 0, 1, 2, ... . Frame k copies the
+ * host parameters into device_sets[k % 2] on streams[1], renders from that set
+ * with gs_render on streams[0] once the copy is in (and the previous frame's
+ * image has been read back), and copies the image to host_image on streams[2]
+ * once it is rendered. So frame k + 1's parameter upload runs during frame
+ * k's render and read-back, and throughput is bound by the upload alone.
+ * device_sets[2]: two device parameter sets with the same n and degree as
+ * host_gaussians. streams[3]: render, upload, read-back (distinct). events[6]:
+ * caller-created cudaEvent_t handles (timing may be disabled), reused across
+ * the calls of one pipeline: upload done per set [0..1], render done per set
+ * [2..3], image ready [4], image read back [5]. host buffers should be
+ * page-locked. No call waits for the GPU; host_image of frame k is complete
+ * once streams[2] has passed that frame (e.g. after a synchronisation). */
+gs_status gs_render_from_host_async(const gs_gaussians* host_gaussians,
+                                    const gs_gaussians* device_sets, int64_t frame,
+                                    const gs_camera* camera, int64_t key_capacity, void* ws,
+                                    size_t ws_bytes, float* device_image, float* host_image,
+                                    void* const* streams, void* const* events);
+
 /* Reads the status header at the start of a gs_bin, gs_sort or gs_render
  * workspace. SYNCHRONISES `stream`. flags/num_keys may be NULL. Returns
  * GS_ERR_TIMEOUT, GS_ERR_CAPACITY or GS_OK from the flags. num_keys is the

@@ -588,3 +588,31 @@ def test_large_frame_near_the_key_limit(oracle_mod):
         err = np.abs(img[y0:y0 + 16, x0:x0 + 16] - ref).max(-1)
         # a decision on a threshold may flip a few pixels by a small amount
         assert (err > 1e-4).mean() <= 0.02 and err.max() < 0.02, (x0, y0, float(err.max()))
+
+
+def test_host_pipeline_frames_equal_single_renders():
+    """gs_render_from_host_async over 7 frames (two device sets, overlapped
+    upload / render / read-back, a different camera and parameters each frame)
+    gives every frame's gs_render image in its host buffer."""
+    base = scenes.make_scene("100k", n=20_000)
+    cams = [scenes.orbit_camera(th, 6.0, 500.0, 640, 480) for th in (0, 40, 80, 120, 160, 200, 240)]
+    frames = []
+    for k in range(len(cams)):
+        s = dict(base, means=(base["means"] + np.float32(0.01 * k)).astype(np.float32))
+        frames.append({f: torch.from_numpy(np.ascontiguousarray(s[f], np.float32)).pin_memory()
+                       for f in ("means", "quats", "log_scales", "opacity_logits", "sh")})
+    g = gs.gaussians_to_device(base)
+    r = gs.Renderer.for_scene(g, cams, headroom=1.5)
+    pipe = gs.HostPipeline(r)
+    outs = [torch.empty((480, 640, 3), dtype=torch.float32).pin_memory() for _ in cams]
+    for k, cam in enumerate(cams):
+        pipe.submit(frames[k], cam, outs[k])
+    pipe.synchronize()
+    assert r.status()[0] == native.GS_OK
+    for k, cam in enumerate(cams):
+        gk = {f: v.cuda() for f, v in frames[k].items()}
+        gk.update(n=g["n"], sh_degree=g["sh_degree"])
+        single = gs.Renderer(gk, 640, 480, r.key_capacity)
+        single.render(cam)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(outs[k].numpy(), single.image.cpu().numpy())
