@@ -153,7 +153,9 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
         if (lane == 0) atomicMax(&s_max, m);
     }
     __syncthreads();
-    const uint32_t len = min(s_max, range.y - range.x);   // list positions [0, len) matter
+    // list positions [0, len) matter (an inverted range -- only a sort cut
+    // short gives one, and it is flagged -- counts as empty)
+    const uint32_t len = range.y > range.x ? min(s_max, range.y - range.x) : 0u;
 
     auto fetch = [&](uint32_t pos, float4& r0, float4& r1, float4& r2) {
         uint32_t g = __ldg(a.sorted_vals + range.x + pos);

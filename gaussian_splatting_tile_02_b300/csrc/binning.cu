@@ -250,7 +250,9 @@ __global__ void gather_rect_kernel(const uint32_t* __restrict__ tiles_touched, c
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
         const uint32_t g = __ldg(order + i);
-        rs[i] = __ldg(tiles_touched + g) ? __ldg(rect + g) : make_ushort4(0xffff, 0, 0, 0);
+        // an index outside the scene can only come from a depth sort that was
+        // cut short (flagged): no tiles, never a read past the arrays
+        rs[i] = (g < n && __ldg(tiles_touched + g)) ? __ldg(rect + g) : make_ushort4(0xffff, 0, 0, 0);
     }
 }
 

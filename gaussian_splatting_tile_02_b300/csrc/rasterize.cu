@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kOrderThreads) tile_order_kernel(const uint2* 
     auto bucket = [&](int t) -> uint32_t {
         if (t >= tiles) return 0xffffffffu;
         const uint2 r = __ldg(ranges + t);
-        const uint32_t len = r.y - r.x;
+        const uint32_t len = r.y > r.x ? r.y - r.x : 0u;
         return len ? 32u - (uint32_t)__clz(len) : 0u;
     };
     auto count = [&](const uint32_t (&b)[kOrderItems]) {
@@ -182,7 +182,9 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
         s_box[buf][threadIdx.x] = make_float4(mx - hx, mx + hx, my - hy, my + hy);
     };
 
-    const uint32_t len = range.y - range.x;
+    // a range with end < start can only come from a sort that was cut short
+    // (its status is flagged): treat it as empty, never read past the list
+    const uint32_t len = range.y > range.x ? range.y - range.x : 0u;
     const uint32_t nbatch = (len + kRastThreads - 1) / kRastThreads;
     if (threadIdx.x < len) {
         float4 r0, r1, r2;

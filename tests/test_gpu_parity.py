@@ -616,3 +616,70 @@ def test_host_pipeline_frames_equal_single_renders():
         single.render(cam)
         torch.cuda.synchronize()
         np.testing.assert_array_equal(outs[k].numpy(), single.image.cpu().numpy())
+
+
+def test_non_finite_inputs_are_culled(oracle_mod):
+    """NaN and infinite centres, NaN and zero quaternions, infinite log-scales:
+    those Gaussians touch no tile (culled, never trapped), the others render as
+    the oracle renders them."""
+    scene = scenes.make_scene("100k", n=3000)
+    cam = scenes.make_cameras("100k")[0]
+    bad = np.arange(0, 3000, 97)
+    kinds = len(bad)
+    for j, i in enumerate(bad):
+        k = j % 6
+        if k == 0:
+            scene["means"][i, 0] = np.nan
+        elif k == 1:
+            scene["means"][i, 2] = np.inf
+        elif k == 2:
+            scene["means"][i] = [np.inf, -np.inf, 1.0]
+        elif k == 3:
+            scene["quats"][i] = np.nan
+        elif k == 4:
+            scene["quats"][i] = 0.0
+        else:
+            scene["log_scales"][i, 1] = np.inf
+    g = gs.gaussians_to_device(scene)
+    out = run_stages(g, cam)
+    tt = out["p"]["tiles_touched"].view(np.uint32)
+    assert kinds > 20 and np.all(tt[bad] == 0)
+    d = oracle_mod.decide_f32(scene, cam)
+    np.testing.assert_array_equal(tt, d["tiles_touched"])
+    ref = oracle_render(oracle_mod, scene, cam)
+    assert out["K"] == ref["num_keys"]
+    assert_image_parity(check_image(oracle_mod, ref, cam, out["image"], out["final_T"], out["n_contrib"]))
+
+
+def test_spin_limit_of_one_reports_timeouts_never_wrong_images():
+    """With every device wait bounded by a single poll, a frame either completes
+    with the right image or reports GS_ERR_TIMEOUT; the next frame with the
+    default bound is right again (the context and the workspace recover)."""
+    scene, g = scene_of("1M")
+    cam = scenes.make_cameras("1M")[0]
+    r = gs.Renderer.for_scene(g, cam)
+    r.render(cam)
+    torch.cuda.synchronize()
+    assert r.status()[0] == native.GS_OK
+    good = r.image.cpu().numpy().copy()
+    L = native.lib()
+    outcomes = []
+    try:
+        L.gs_set_spin_limit(1)
+        for _ in range(6):
+            r.image.zero_()
+            r.render(cam)
+            torch.cuda.synchronize()
+            st, flags, _ = r.status()
+            if st == native.GS_OK:
+                np.testing.assert_array_equal(r.image.cpu().numpy(), good)
+            else:
+                assert st == native.GS_ERR_TIMEOUT and flags & native.GS_FLAG_TIMEOUT
+            outcomes.append(st)
+    finally:
+        L.gs_set_spin_limit(0)
+    print("spin limit 1 outcomes", outcomes)
+    r.render(cam)
+    torch.cuda.synchronize()
+    assert r.status()[0] == native.GS_OK
+    np.testing.assert_array_equal(r.image.cpu().numpy(), good)
