@@ -1,4 +1,6 @@
-"""Builds libgs_b300.so (the C-ABI renderer library) in-tree with nvcc for sm_103a."""
+"""Builds libgs_b300.so (the C-ABI renderer library) in-tree with nvcc for sm_103a,
+and libgs_b300_debug.so, the same sources with the kernels' index checks on
+(GS_DEBUG_CHECKS: failures are counted into a device counter, never trapped)."""
 from __future__ import annotations
 
 import os
@@ -9,6 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libgs_b300.so")
+DEBUG_LIB = os.path.join(HERE, "libgs_b300_debug.so")
 SOURCES = ["api.cu", "preprocess.cu", "binning.cu", "sort.cu", "rasterize.cu", "backward.cu", "splat2d.cu", "densify.cu",
            "bin_static.cu"]
 HEADERS = ["gs_internal.cuh"]
@@ -31,27 +34,29 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra: list | None = None) -> str:
-    if not force and up_to_date():
-        return LIB
-    tmp = LIB + f".{os.getpid()}.tmp"
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *(extra or []), "-I", os.path.join(ROOT, "include"),
+def build(force: bool = False, verbose: bool = False, extra: list | None = None, debug: bool = False) -> str:
+    lib = DEBUG_LIB if debug else LIB
+    if not force and up_to_date(lib):
+        return lib
+    tmp = lib + f".{os.getpid()}.tmp"
+    defs = ["-DGS_DEBUG_CHECKS"] if debug else []
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *defs, *(extra or []), "-I", os.path.join(ROOT, "include"),
            *[os.path.join(CSRC, f) for f in SOURCES], "-o", tmp]
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     force = "--force" in sys.argv
     extra = ["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None
-    print(build(force=force or bool(extra), verbose=True, extra=extra))
+    print(build(force=force or bool(extra), verbose=True, extra=extra, debug="--debug" in sys.argv))

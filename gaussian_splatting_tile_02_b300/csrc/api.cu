@@ -738,6 +738,26 @@ gs_status gs_render_from_host_async(const gs_gaussians* hg, const gs_gaussians* 
     return cuda_status(cudaEventRecord(img_copied, s_d2h));
 }
 
+int32_t gs_debug_checks_enabled(void) {
+#ifdef GS_DEBUG_CHECKS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+gs_status gs_debug_set_check_counter(uint64_t* device_counter) {
+    unsigned long long* p = reinterpret_cast<unsigned long long*>(device_counter);
+    cudaError_t e = set_check_counter_preprocess(p);
+    if (e == cudaSuccess) e = set_check_counter_binning(p);
+    if (e == cudaSuccess) e = set_check_counter_sort(p);
+    if (e == cudaSuccess) e = set_check_counter_rasterize(p);
+    if (e == cudaSuccess) e = set_check_counter_backward(p);
+    if (e == cudaSuccess) e = set_check_counter_splat2d(p);
+    if (e == cudaSuccess) e = set_check_counter_densify(p);
+    return cuda_status(e);
+}
+
 gs_status gs_read_status(const void* ws, void* stream, uint32_t* flags, uint64_t* num_keys) {
     if (!ws || !aligned(ws, kAlign)) return GS_ERR_WORKSPACE;
     StatusHeader h;

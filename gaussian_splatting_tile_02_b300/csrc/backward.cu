@@ -155,10 +155,12 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
     __syncthreads();
     // list positions [0, len) matter (an inverted range -- only a sort cut
     // short gives one, and it is flagged -- counts as empty)
+    GS_CHECK(range.y >= range.x && s_max <= range.y - range.x);
     const uint32_t len = range.y > range.x ? min(s_max, range.y - range.x) : 0u;
 
     auto fetch = [&](uint32_t pos, float4& r0, float4& r1, float4& r2) {
         uint32_t g = __ldg(a.sorted_vals + range.x + pos);
+        GS_CHECK(g < a.n);
         if (g >= a.n) g = 0;   // only a sort cut short (flagged) can give this
         r0 = __ldg(a.raster + 3 * g);
         r1 = __ldg(a.raster + 3 * g + 1);
@@ -604,5 +606,7 @@ cudaError_t launch_preprocess_backward(const gs_gaussians& g, const CamConst& ca
     }
     return cudaGetLastError();
 }
+
+GS_DEFINE_CHECK_SETTER(backward)
 
 }  // namespace gs

@@ -252,6 +252,7 @@ __global__ void gather_rect_kernel(const uint32_t* __restrict__ tiles_touched, c
         const uint32_t g = __ldg(order + i);
         // an index outside the scene can only come from a depth sort that was
         // cut short (flagged): no tiles, never a read past the arrays
+        GS_CHECK(g < n);
         rs[i] = (g < n && __ldg(tiles_touched + g)) ? __ldg(rect + g) : make_ushort4(0xffff, 0, 0, 0);
     }
 }
@@ -381,6 +382,7 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
                 }
                 const uint32_t tile = ty * (uint32_t)tiles_x + tx;
                 const uint32_t si = (uint32_t)(j - S0);
+                GS_CHECK(si < (uint32_t)kKeysPerBlock && j < (unsigned long long)key_capacity && tx <= r.z);
                 s_key[si + (si >> 5)] = tile;
                 s_val[si + (si >> 5)] = s_g[lo];
                 if (hist) {
@@ -516,5 +518,7 @@ cudaError_t launch_depth_keys(const gs_projected& p, int64_t n, uint32_t* keys, 
                                                                             vals, hist);
     return cudaGetLastError();
 }
+
+GS_DEFINE_CHECK_SETTER(binning)
 
 }  // namespace gs

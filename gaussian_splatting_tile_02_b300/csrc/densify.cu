@@ -235,4 +235,6 @@ cudaError_t launch_densify(const gs_gaussians& in, const gs_gaussians_out& out, 
     return cudaGetLastError();
 }
 
+GS_DEFINE_CHECK_SETTER(densify)
+
 }  // namespace gs

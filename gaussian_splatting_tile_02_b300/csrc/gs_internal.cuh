@@ -49,6 +49,36 @@ struct CamConst {
 };
 CamConst make_cam_const(const gs_camera& c);
 
+// ---------------------------------------------------------------- debug checks
+// Built with -DGS_DEBUG_CHECKS (libgs_b300_debug.so), the kernels check their
+// index invariants and count each failure into a caller-given device counter
+// (gs_debug_set_check_counter); they never trap. The counter pointer lives in
+// one __device__ variable per translation unit, set by that unit's setter.
+#ifdef GS_DEBUG_CHECKS
+static __device__ unsigned long long* g_check_counter = nullptr;
+#define GS_CHECK(cond)                                                         \
+    do {                                                                       \
+        if (!(cond) && g_check_counter) atomicAdd(g_check_counter, 1ull);      \
+    } while (0)
+#define GS_DEFINE_CHECK_SETTER(unit)                                           \
+    cudaError_t set_check_counter_##unit(unsigned long long* p) {              \
+        return cudaMemcpyToSymbol(g_check_counter, &p, sizeof(p));             \
+    }
+#else
+#define GS_CHECK(cond) \
+    do {               \
+    } while (0)
+#define GS_DEFINE_CHECK_SETTER(unit) \
+    cudaError_t set_check_counter_##unit(unsigned long long*) { return cudaSuccess; }
+#endif
+cudaError_t set_check_counter_preprocess(unsigned long long* p);
+cudaError_t set_check_counter_binning(unsigned long long* p);
+cudaError_t set_check_counter_sort(unsigned long long* p);
+cudaError_t set_check_counter_rasterize(unsigned long long* p);
+cudaError_t set_check_counter_backward(unsigned long long* p);
+cudaError_t set_check_counter_splat2d(unsigned long long* p);
+cudaError_t set_check_counter_densify(unsigned long long* p);
+
 // Default bound of every device-side spin, in polling iterations.
 extern long long g_spin_limit;
 

@@ -544,4 +544,6 @@ cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const 
     return cudaGetLastError();
 }
 
+GS_DEFINE_CHECK_SETTER(preprocess)
+
 }  // namespace gs

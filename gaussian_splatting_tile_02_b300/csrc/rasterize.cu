@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
     __shared__ float2 w_bj[kRastThreads / 32][32];  // (b, list position + 1 as bits)
 
     const int tile = a.order ? (int)a.order[blockIdx.x] : (int)blockIdx.x;
+    GS_CHECK(tile >= 0 && tile < (int)gridDim.x);
     const int tx = tile % a.tiles_x, ty = tile / a.tiles_x;
     const float tile_x0 = (float)(tx * kTile), tile_y0 = (float)(ty * kTile);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
         uint32_t g = __ldg(a.sorted_vals + idx);
         // an index outside the scene can only come from a sort that was cut
         // short (its status is flagged); never read past the arrays
+        GS_CHECK(g < a.n);
         if (g >= a.n) g = 0;
         r0 = __ldg(a.raster + 3 * g);
         r1 = __ldg(a.raster + 3 * g + 1);
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
 
     // a range with end < start can only come from a sort that was cut short
     // (its status is flagged): treat it as empty, never read past the list
+    GS_CHECK(range.y >= range.x);
     const uint32_t len = range.y > range.x ? range.y - range.x : 0u;
     const uint32_t nbatch = (len + kRastThreads - 1) / kRastThreads;
     if (threadIdx.x < len) {
@@ -309,5 +312,7 @@ cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* s
     rasterize_kernel<<<tiles, kRastThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
+
+GS_DEFINE_CHECK_SETTER(rasterize)
 
 }  // namespace gs

@@ -341,6 +341,7 @@ __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_ker
             const KeyT kk = s_keys[j];
             const uint32_t d = digit_of(kk, shift, dmask);
             const uint32_t o = s_goff[d] + (uint32_t)j - s_dstart[d];
+            GS_CHECK(skip || (int64_t)o < K);
             if (!skip && (int64_t)o < K) {
                 a.keys_out[o] = kk;
                 dest[k] = o;
@@ -380,6 +381,7 @@ __global__ void tile_ranges_kernel(const KeyT* __restrict__ keys, const uint64_t
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < K; i += stride) {
         const uint32_t t = (uint32_t)(keys[i] >> shift);
+        GS_CHECK(t < (uint32_t)n_tiles);
         if (t >= (uint32_t)n_tiles) continue;
         const uint32_t prev = i > 0 ? (uint32_t)(keys[i - 1] >> shift) : 0xffffffffu;
         const uint32_t next = i + 1 < K ? (uint32_t)(keys[i + 1] >> shift) : 0xffffffffu;
@@ -498,5 +500,7 @@ cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations,
     spin_timeout_test_kernel<<<1, 1, 0, s>>>(status, iterations);
     return cudaGetLastError();
 }
+
+GS_DEFINE_CHECK_SETTER(sort)
 
 }  // namespace gs

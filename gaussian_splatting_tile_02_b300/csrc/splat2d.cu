@@ -175,4 +175,6 @@ cudaError_t launch_conic_to_cov_grad(const float* covs, const uint32_t* tiles_to
     return cudaGetLastError();
 }
 
+GS_DEFINE_CHECK_SETTER(splat2d)
+
 }  // namespace gs

@@ -110,6 +110,8 @@ _SIGNATURES = {
                                                  ctypes.c_int64, ctypes.POINTER(GsCamera), ctypes.c_int64, c_void_p,
                                                  ctypes.c_size_t, c_void_p, c_void_p, ctypes.POINTER(c_void_p),
                                                  ctypes.POINTER(c_void_p)]),
+    "gs_debug_checks_enabled": (ctypes.c_int32, []),
+    "gs_debug_set_check_counter": (ctypes.c_int, [c_void_p]),
     "gs_rasterize_backward": (ctypes.c_int, [ctypes.POINTER(GsProjected), ctypes.c_int64, c_void_p, c_void_p,
                                              ctypes.POINTER(GsCamera), c_void_p, c_void_p, c_void_p, c_void_p,
                                              ctypes.POINTER(GsProjectedGrad), c_void_p]),
@@ -151,6 +153,26 @@ def lib() -> ctypes.CDLL:
             fn.argtypes = args
         _lib = L
     return _lib
+
+
+_debug_lib = None
+
+
+def debug_lib() -> ctypes.CDLL:
+    """Load libgs_b300_debug.so: the same library with the kernels' index checks
+    on (gs_debug_set_check_counter), building it in-tree first if needed."""
+    global _debug_lib
+    if _debug_lib is None:
+        path = _build.DEBUG_LIB
+        if not _build.up_to_date(path):
+            _build.build(debug=True)
+        L = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _debug_lib = L
+    return _debug_lib
 
 
 class GsError(RuntimeError):

@@ -480,6 +480,17 @@ gs_status gs_render_from_host_async(const gs_gaussians* host_gaussians,
                                     size_t ws_bytes, float* device_image, float* host_image,
                                     void* const* streams, void* const* events);
 
+/* Debug build (libgs_b300_debug.so, compiled with GS_DEBUG_CHECKS): the
+ * kernels check their index invariants -- tile ranges ordered, list entries
+ * naming a Gaussian of the scene, sort destinations inside the key count,
+ * expansion slots inside the capacity, tile ids inside the image -- and add 1
+ * to *device_counter (device uint64, zeroed by the caller) for each failure,
+ * instead of trapping. gs_debug_set_check_counter sets the counter for the
+ * current device (NULL turns counting off); gs_debug_checks_enabled returns 1
+ * in the debug build and 0 in the release build (where the call does nothing). */
+int32_t gs_debug_checks_enabled(void);
+gs_status gs_debug_set_check_counter(uint64_t* device_counter);
+
 /* Reads the status header at the start of a gs_bin, gs_sort or gs_render
  * workspace. SYNCHRONISES `stream`. flags/num_keys may be NULL. Returns
  * GS_ERR_TIMEOUT, GS_ERR_CAPACITY or GS_OK from the flags. num_keys is the

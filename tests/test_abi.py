@@ -28,6 +28,14 @@ def test_library_builds_and_exports_every_declared_symbol():
         assert hasattr(L, name), name
     assert set(names) == set(native._SIGNATURES), "binding must cover exactly the declared entry points"
     assert L.gs_abi_version() == 2
+    assert L.gs_debug_checks_enabled() == 0
+
+
+def test_debug_build_exports_the_same_symbols():
+    D = native.debug_lib()
+    for name in declared_functions():
+        assert hasattr(D, name), name
+    assert D.gs_debug_checks_enabled() == 1 and D.gs_abi_version() == 2
 
 
 def test_status_strings():
