@@ -577,8 +577,9 @@ def run_ours(args, rank, local_rank, world):
     tile_bits = max(1, (tx * ty - 1).bit_length())
     tpasses = (tile_bits + 7) // 8
     # preprocess (which also writes the depth keys); sort bases, 4 depth passes;
-    # 5 binning kernels; sort bases + tile passes; ranges; tile order + rasterize
-    launches_per_frame = 1 + (1 + 4) + 5 + (1 + tpasses) + 1 + 2
+    # 5 binning kernels; sort bases + tile passes (+ a copy back after an odd
+    # count); ranges; tile order + rasterize
+    launches_per_frame = 1 + (1 + 4) + 5 + (1 + tpasses + tpasses % 2) + 1 + 2
     ras_ms = st_ms["rasterize"]
     clk = clocks.get("sm_mhz") or SM_MAX_MHZ
     fp32_peak = SM_COUNT * FP32_LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12     # T lane-ops/s at max clock

@@ -154,7 +154,11 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
     const int lx = lbx0 + (lane & 7), ly = lby0 + (lane >> 3);
     const int px = tx * kTile + lx, py = ty * kTile + ly;
     const float fbx0 = (float)lbx0, fbx1 = (float)(lbx0 + 7), fby0 = (float)lby0, fby1 = (float)(lby0 + 7);
-    const uint2 range = a.ranges[tile];
+    const uint2 range0 = a.ranges[tile];
+    // a range with end < start can only come from a sort that was cut short
+    // (its status is flagged): treat it as empty, never read past the list
+    GS_CHECK(range0.y >= range0.x);
+    const uint2 range = make_uint2(range0.x, max(range0.x, range0.y));
     const float fpx = (float)lx, fpy = (float)ly, fpy2 = (float)(ly + 4);
 
     float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
@@ -184,10 +188,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
         s_box[buf][threadIdx.x] = make_float4(mx - hx, mx + hx, my - hy, my + hy);
     };
 
-    // a range with end < start can only come from a sort that was cut short
-    // (its status is flagged): treat it as empty, never read past the list
-    GS_CHECK(range.y >= range.x);
-    const uint32_t len = range.y > range.x ? range.y - range.x : 0u;
+    const uint32_t len = range.y - range.x;
     const uint32_t nbatch = (len + kRastThreads - 1) / kRastThreads;
     if (threadIdx.x < len) {
         float4 r0, r1, r2;
