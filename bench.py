@@ -578,7 +578,7 @@ def run_ours(args, rank, local_rank, world):
     tpasses = (tile_bits + 7) // 8
     # preprocess (which also writes the depth keys); sort bases, 4 depth passes;
     # 5 binning kernels; sort bases + tile passes (+ a copy back after an odd
-    # count); ranges; tile order + rasterize
+    # count); ranges + tile order; rasterize
     launches_per_frame = 1 + (1 + 4) + 5 + (1 + tpasses + tpasses % 2) + 1 + 2
     ras_ms = st_ms["rasterize"]
     clk = clocks.get("sm_mhz") or SM_MAX_MHZ
@@ -590,7 +590,7 @@ def run_ours(args, rank, local_rank, world):
         "depth_order": 4 * 16 * n,
         "bin": 24 * n + 8 * K,
         "tile_sort": tpasses * 16 * K,
-        "ranges": 4 * K + 8 * tx * ty,
+        "ranges": 4 * K + 8 * tx * ty + 12 * tx * ty,   # + the launch order: ranges read, order written
     }
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
     stages_out = {}

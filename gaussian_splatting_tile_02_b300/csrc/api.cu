@@ -213,10 +213,11 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
     if (e == cudaSuccess) e = mark(4);
     if (e == cudaSuccess)
         e = launch_tile_ranges32(keys, num_keys, key_capacity, cc.tiles_x * cc.tiles_y, ranges, s);
+    auto* tile_order = reinterpret_cast<uint32_t*>(w + L.tile_order);
+    if (e == cudaSuccess) e = launch_tile_order(ranges, cc.tiles_x * cc.tiles_y, tile_order, s);
     if (e == cudaSuccess) e = mark(5);
     if (e == cudaSuccess)
-        e = launch_rasterize(p, g->n, vals, ranges, reinterpret_cast<uint32_t*>(w + L.tile_order), cc, image, final_T,
-                             n_contrib, s);
+        e = launch_rasterize(p, g->n, vals, ranges, tile_order, cc, image, final_T, n_contrib, s);
     if (e == cudaSuccess) e = mark(6);
     return e;
 }
@@ -348,8 +349,13 @@ gs_status gs_rasterize(const gs_projected* p, int64_t n, const uint32_t* sorted_
         return GS_ERR_INVALID_ARG;
     if (n > 0 && !p->raster) return GS_ERR_INVALID_ARG;
     if (n > 0 && !sorted_vals) return GS_ERR_INVALID_ARG;
-    return cuda_status(launch_rasterize(*p, n, sorted_vals, ranges, tile_order, make_cam_const(*cam), image, final_T,
-                                        n_contrib, (cudaStream_t)stream));
+    const CamConst cc = make_cam_const(*cam);
+    if (tile_order) {
+        const cudaError_t e = launch_tile_order(ranges, cc.tiles_x * cc.tiles_y, tile_order, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return cuda_status(
+        launch_rasterize(*p, n, sorted_vals, ranges, tile_order, cc, image, final_T, n_contrib, (cudaStream_t)stream));
 }
 
 size_t gs_render_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity) {

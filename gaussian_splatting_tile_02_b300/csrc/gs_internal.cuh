@@ -182,10 +182,13 @@ cudaError_t launch_preprocess_backward(const gs_gaussians& g, const CamConst& ca
                                        const gs_projected_grad& gin, const gs_gaussians_grad& gout,
                                        cudaStream_t s);
 
-// tile_order (nullable): [tiles] scratch that receives the heavy-first launch
-// order of the tiles; null launches them in index order (same image)
+// Heavy-first launch order of the tiles from their ranges: tile_order[tiles]
+// receives a permutation of the tile indices, longest lists first.
+cudaError_t launch_tile_order(const uint32_t* ranges, int tiles, uint32_t* tile_order, cudaStream_t s);
+// tile_order (nullable): a launch order written by launch_tile_order; null
+// launches the tiles in index order (same image)
 cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* sorted_vals, const uint32_t* ranges,
-                             uint32_t* tile_order, const CamConst& cam, float* image, float* final_T,
+                             const uint32_t* tile_order, const CamConst& cam, float* image, float* final_T,
                              uint32_t* n_contrib, cudaStream_t s);
 
 }  // namespace gs

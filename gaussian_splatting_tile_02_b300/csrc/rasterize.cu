@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
 }  // namespace
 
 cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* sorted_vals, const uint32_t* ranges,
-                             uint32_t* tile_order, const CamConst& cam, float* image, float* final_T,
+                             const uint32_t* tile_order, const CamConst& cam, float* image, float* final_T,
                              uint32_t* n_contrib, cudaStream_t s) {
     RastArgs a;
     a.raster = reinterpret_cast<const float4*>(p.raster);
@@ -309,8 +309,12 @@ cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* s
     a.n_contrib = n_contrib;
     const unsigned tiles = (unsigned)(cam.tiles_x * cam.tiles_y);
     if (n == 0) a.sorted_vals = nullptr;
-    if (tile_order) tile_order_kernel<<<1, kOrderThreads, 0, s>>>(a.ranges, (int)tiles, tile_order);
     rasterize_kernel<<<tiles, kRastThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tile_order(const uint32_t* ranges, int tiles, uint32_t* tile_order, cudaStream_t s) {
+    tile_order_kernel<<<1, kOrderThreads, 0, s>>>(reinterpret_cast<const uint2*>(ranges), tiles, tile_order);
     return cudaGetLastError();
 }
 
