@@ -230,12 +230,12 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
                 const float4 r = w_r[warp][k];
                 const float4 c = w_c[warp][k];
                 const uint32_t lp = __float_as_uint(c.z);
-                // the forward's exponent, operation for operation
+                // the forward's exponent, operation for operation; the
+                // offsets themselves enter the conic gradients
                 const float dx = q.x - fpx, dy = q.y - fpy, dy2 = q.y - fpy2;
-                const float t1 = q.z * dx;
-                const float t2 = fmaf(r.x, dx, q.w * dy), t22 = fmaf(r.x, dx, q.w * dy2);
-                const float e1 = fmaf(-t1, t1, r.y);
-                const float e = fmaf(-t2, t2, e1), e2 = fmaf(-t22, t22, e1);
+                const float2 A = entry_origin_terms(q.x, q.y, q.z, q.w, r.x);
+                float t1, t2, t22, e, e2;
+                pixel_pair_exponents(A.x, A.y, q.z, q.w, r.x, r.y, -fpx, -fpy, t1, t2, t22, e, e2);
                 const bool c1 = lp < P1.last && e >= kLog2AlphaMin;
                 const bool c2 = lp < P2.last && e2 >= kLog2AlphaMin;
                 if (!__any_sync(0xffffffffu, c1 || c2)) continue;

@@ -34,6 +34,28 @@ __host__ __device__ inline int digit_shift(int key_bits, int p) {
     return 8 * p;
 }
 
+// The compositing exponent of one list entry at a lane's two pixels (x, y)
+// and (x, y + 4), in tile-local coordinates:
+//   log2(alpha) = log2 o - t1^2 - t2^2,  t1 = k1 (mx - x),  t2 = k3 (mx - x) + k2 (my - y).
+// The terms are expanded around the tile origin, A1 = k1 mx and
+// A2 = k3 mx + k2 my once per entry, so that each pixel pair costs seven
+// FMAs; nx = -x and ny = -y are the lane's constants. Compositing and its
+// backward both use exactly this sequence, so they take the same per-entry
+// decisions bit for bit.
+__device__ __forceinline__ float2 entry_origin_terms(float mx, float my, float k1, float k2, float k3) {
+    return make_float2(__fmul_rn(k1, mx), __fmaf_rn(k3, mx, __fmul_rn(k2, my)));
+}
+__device__ __forceinline__ void pixel_pair_exponents(float A1, float A2, float k1, float k2, float k3, float log2o,
+                                                     float nx, float ny, float& t1, float& t2, float& t22,
+                                                     float& e, float& e2) {
+    t1 = __fmaf_rn(k1, nx, A1);
+    t2 = __fmaf_rn(k3, nx, __fmaf_rn(k2, ny, A2));
+    t22 = __fmaf_rn(-4.0f, k2, t2);   // y + 4
+    const float e1 = __fmaf_rn(-t1, t1, log2o);
+    e = __fmaf_rn(-t2, t2, e1);
+    e2 = __fmaf_rn(-t22, t22, e1);
+}
+
 inline int tiles_x(const gs_camera& c) { return (c.width + kTile - 1) / kTile; }
 inline int tiles_y(const gs_camera& c) { return (c.height + kTile - 1) / kTile; }
 

@@ -23,11 +23,12 @@
 //
 // Coordinates are relative to the tile's first pixel: a centre enters as
 // (u - x0) + residual (an exact subtraction, then one rounding at small
-// magnitude), so d = pixel - centre keeps ~1e-6 px where a binary32 centre
-// near x = 1000 carries ~1e-4 px. The quadratic form is a sum of two squares,
+// magnitude), so the centre keeps ~1e-6 px where a binary32 centre near
+// x = 1000 carries ~1e-4 px. The quadratic form is a sum of two squares,
 // log2(alpha) = log2 o - (k1 dx)^2 - (k2 dy + k3 dx)^2, which keeps its
-// accuracy for elongated footprints. Per evaluated (pixel, entry): two
-// subtractions, the form (5 FP32 ops) and a compare; ex2 (MUFU pipe), the
+// accuracy for elongated footprints. Its linear terms are expanded around the
+// tile origin once per batch entry (k1 mx and k3 mx + k2 my), so a lane's two
+// pixels cost seven FMAs per entry and two compares; ex2 (MUFU pipe), the
 // 0.99 cap and the blend only for the pairs past the 1/255 test.
 #include <cuda_fp16.h>
 
@@ -135,7 +136,7 @@ struct RastArgs {
 };
 
 __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastArgs a) {
-    __shared__ float4 s_q[2][kRastThreads];    // (mx, my, k1, k2), centre tile-local
+    __shared__ float4 s_q[2][kRastThreads];    // (A1, A2, k1, k2): origin terms of the exponent
     __shared__ float4 s_r[2][kRastThreads];    // (k3, log2 o, r, g)
     __shared__ float s_b[2][kRastThreads];     // b
     __shared__ float4 s_box[2][kRastThreads];  // (x lo, x hi, y lo, y hi), tile-local
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
     // (its status is flagged): treat it as empty, never read past the list
     GS_CHECK(range0.y >= range0.x);
     const uint2 range = make_uint2(range0.x, max(range0.x, range0.y));
-    const float fpx = (float)lx, fpy = (float)ly, fpy2 = (float)(ly + 4);
+    const float nfpx = -(float)lx, nfpy = -(float)ly;
 
     float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
     float U = 1.0f, D0 = 0.0f, D1 = 0.0f, D2 = 0.0f;   // second pixel
@@ -182,7 +183,8 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
         const uint32_t hb = __float_as_uint(r2.w);
         const __half2 h = *reinterpret_cast<const __half2*>(&hb);
         const float hx = __low2float(h), hy = __high2float(h);
-        s_q[buf][threadIdx.x] = make_float4(mx, my, r1.x, r1.y);   // (mx, my, k1, k2)
+        const float2 A = entry_origin_terms(mx, my, r1.x, r1.y, r1.z);
+        s_q[buf][threadIdx.x] = make_float4(A.x, A.y, r1.x, r1.y);   // (A1, A2, k1, k2)
         s_r[buf][threadIdx.x] = make_float4(r1.z, r1.w, r2.x, r2.y);   // (k3, log2 o, r, g)
         s_b[buf][threadIdx.x] = r2.z;
         s_box[buf][threadIdx.x] = make_float4(mx - hx, mx + hx, my - hy, my + hy);
@@ -233,11 +235,8 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
             for (int k = 0; k < nh; k++) {
                 const float4 q = w_q[warp][k];
                 const float4 r = w_r[warp][k];
-                const float dx = q.x - fpx, dy = q.y - fpy, dy2 = q.y - fpy2;
-                const float t1 = q.z * dx;
-                const float t2 = fmaf(r.x, dx, q.w * dy), t22 = fmaf(r.x, dx, q.w * dy2);
-                const float e1 = fmaf(-t1, t1, r.y);   // shared by the two pixels (same dx)
-                const float e = fmaf(-t2, t2, e1), e2 = fmaf(-t22, t22, e1);
+                float t1, t2, t22, e, e2;
+                pixel_pair_exponents(q.x, q.y, q.z, q.w, r.x, r.y, nfpx, nfpy, t1, t2, t22, e, e2);
                 // alpha = min(0.99, 2^e) < 1/255 is e < log2(1/255) (the same
                 // decision in exact arithmetic; ex2 is only evaluated past it)
                 const bool c = !done && e >= kLog2AlphaMin, c2 = !done2 && e2 >= kLog2AlphaMin;
