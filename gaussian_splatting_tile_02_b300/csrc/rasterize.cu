@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
             }
             __syncwarp();
             const int nh = __popc(m);
-#pragma unroll 2
+#pragma unroll 4
             for (int k = 0; k < nh; k++) {
                 const float4 q = w_q[warp][k];
                 const float4 r = w_r[warp][k];

@@ -373,20 +373,52 @@ __global__ void copy_back_kernel(const KeyT* __restrict__ ks, const uint32_t* __
     }
 }
 
-// ranges from sorted keys whose tile id is (key >> shift)
+// ranges from sorted keys whose tile id is (key >> shift). Each thread takes
+// a run of kRangeItems consecutive keys (16-byte vector loads when the key
+// array is 16-byte aligned) and the key on either side of it, so every key
+// is read about once; a tile's start and end are written where its id
+// differs from the previous and the next key's.
+constexpr int kRangeItems = 8;
+
 template <typename KeyT>
-__global__ void tile_ranges_kernel(const KeyT* __restrict__ keys, const uint64_t* __restrict__ num_keys,
-                                   int64_t cap, int shift, int n_tiles, uint2* __restrict__ ranges) {
+__global__ void __launch_bounds__(256) tile_ranges_kernel(const KeyT* __restrict__ keys,
+                                                          const uint64_t* __restrict__ num_keys, int64_t cap,
+                                                          int shift, int n_tiles, bool vec,
+                                                          uint2* __restrict__ ranges) {
+    static_assert(kRangeItems * sizeof(KeyT) % 16 == 0, "a run is whole 16-byte vectors");
     const int64_t K = key_count(num_keys, cap);
+    const int64_t runs = (K + kRangeItems - 1) / kRangeItems;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < K; i += stride) {
-        const uint32_t t = (uint32_t)(keys[i] >> shift);
-        GS_CHECK(t < (uint32_t)n_tiles);
-        if (t >= (uint32_t)n_tiles) continue;
-        const uint32_t prev = i > 0 ? (uint32_t)(keys[i - 1] >> shift) : 0xffffffffu;
-        const uint32_t next = i + 1 < K ? (uint32_t)(keys[i + 1] >> shift) : 0xffffffffu;
-        if (t != prev) ranges[t].x = (uint32_t)i;
-        if (t != next) ranges[t].y = (uint32_t)(i + 1);
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < runs; c += stride) {
+        const int64_t i0 = c * kRangeItems;
+        const int n = K - i0 < kRangeItems ? (int)(K - i0) : kRangeItems;
+        KeyT k[kRangeItems];
+        if (vec && n == kRangeItems) {
+            constexpr int kVec = kRangeItems * (int)sizeof(KeyT) / 16;
+            const uint4* p = reinterpret_cast<const uint4*>(keys + i0);
+            uint4 v[kVec];
+#pragma unroll
+            for (int j = 0; j < kVec; j++) v[j] = __ldg(p + j);
+            memcpy(k, v, sizeof(k));
+        } else {
+#pragma unroll
+            for (int j = 0; j < kRangeItems; j++) k[j] = j < n ? keys[i0 + j] : (KeyT)0;
+        }
+        uint32_t prev = i0 > 0 ? (uint32_t)(keys[i0 - 1] >> shift) : 0xffffffffu;
+        const uint32_t after = i0 + n < K ? (uint32_t)(keys[i0 + n] >> shift) : 0xffffffffu;
+#pragma unroll
+        for (int j = 0; j < kRangeItems; j++) {
+            if (j < n) {
+                const uint32_t t = (uint32_t)(k[j] >> shift);
+                const uint32_t next = j + 1 < n ? (uint32_t)(k[j + 1] >> shift) : after;
+                GS_CHECK(t < (uint32_t)n_tiles);
+                if (t < (uint32_t)n_tiles) {
+                    if (t != prev) ranges[t].x = (uint32_t)(i0 + j);
+                    if (t != next) ranges[t].y = (uint32_t)(i0 + j + 1);
+                }
+                prev = t;
+            }
+        }
     }
 }
 
@@ -482,8 +514,9 @@ cudaError_t launch_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_
                                uint32_t* ranges, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(ranges, 0, sizeof(uint32_t) * 2 * (size_t)n_tiles, s);
     if (e != cudaSuccess || cap == 0) return e;
-    tile_ranges_kernel<uint64_t><<<grid_for(cap, 256 * 8, 148 * 8), 256, 0, s>>>(
-        sorted_keys, num_keys, cap, 32, n_tiles, reinterpret_cast<uint2*>(ranges));
+    const bool vec = (reinterpret_cast<uintptr_t>(sorted_keys) & 15) == 0;
+    tile_ranges_kernel<uint64_t><<<grid_for(cap, 256 * kRangeItems, 148 * 8), 256, 0, s>>>(
+        sorted_keys, num_keys, cap, 32, n_tiles, vec, reinterpret_cast<uint2*>(ranges));
     return cudaGetLastError();
 }
 
@@ -491,8 +524,9 @@ cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* n
                                  uint32_t* ranges, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(ranges, 0, sizeof(uint32_t) * 2 * (size_t)n_tiles, s);
     if (e != cudaSuccess || cap == 0) return e;
-    tile_ranges_kernel<uint32_t><<<grid_for(cap, 256 * 8, 148 * 8), 256, 0, s>>>(
-        sorted_tiles, num_keys, cap, 0, n_tiles, reinterpret_cast<uint2*>(ranges));
+    const bool vec = (reinterpret_cast<uintptr_t>(sorted_tiles) & 15) == 0;
+    tile_ranges_kernel<uint32_t><<<grid_for(cap, 256 * kRangeItems, 148 * 8), 256, 0, s>>>(
+        sorted_tiles, num_keys, cap, 0, n_tiles, vec, reinterpret_cast<uint2*>(ranges));
     return cudaGetLastError();
 }
 

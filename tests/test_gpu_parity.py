@@ -469,6 +469,41 @@ def test_sort32_random_keys(oracle_mod, count, bits):
     np.testing.assert_array_equal(vd[:count].cpu().numpy().view(np.uint32), vals[sv])
 
 
+@pytest.mark.parametrize("count", [1, 7, 8, 9, 2047, 2049, 100_003, 1_000_001])
+@pytest.mark.parametrize("offset", [0, 1], ids=["aligned", "unaligned"])
+def test_tile_ranges_ragged_counts_and_unaligned_keys(oracle_mod, count, offset):
+    """Step 4 on sorted keys of any count (runs of eight per thread and a
+    ragged last run) and key arrays that are or are not 16-byte aligned (the
+    vector and the scalar loads), for 32-bit tile ids and 64-bit keys, with a
+    capacity above the count on the device; against the oracle's ranges."""
+    cam = scenes.make_cameras("1M")[0]
+    tx, ty = gs.tiles_xy(cam)
+    nt = tx * ty
+    rng = np.random.default_rng(2 * count + offset)
+    tiles = rng.integers(0, nt, size=count).astype(np.uint64)
+    sk = np.sort((tiles << np.uint64(32)) | rng.integers(0, 1 << 32, size=count, dtype=np.uint64))
+    ref = oracle_mod.tile_ranges(sk, nt)
+    L = gs.lib()
+    cs = gs.camera_struct(cam)
+    nk = torch.tensor([count], dtype=torch.int64, device="cuda")
+    cap = count + 5
+    for kind in ("tiles32", "keys64"):
+        if kind == "tiles32":
+            host = (sk >> np.uint64(32)).astype(np.uint32).view(np.int32)
+            buf = torch.zeros(cap + offset, dtype=torch.int32, device="cuda")
+        else:
+            host = sk.view(np.int64)
+            buf = torch.zeros(cap + offset, dtype=torch.int64, device="cuda")
+        buf[offset:offset + count] = torch.from_numpy(host).cuda()
+        ptr = buf.data_ptr() + offset * buf.element_size()
+        assert (ptr % 16 == 0) == (offset == 0)
+        ranges = torch.full((nt, 2), -1, dtype=torch.int32, device="cuda")
+        fn = L.gs_tile_ranges32 if kind == "tiles32" else L.gs_tile_ranges
+        native.check(fn(ptr, nk.data_ptr(), cap, ctypes.byref(cs), ranges.data_ptr(), None), kind)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(ranges.cpu().numpy().view(np.uint32), ref, err_msg=kind)
+
+
 @pytest.mark.parametrize("views,n_streams", [(8, 3), (10, 4), (1, 1)])
 def test_render_batch_equals_single_views(views, n_streams):
     """gs_render_batch (one projection pass for all views, views spread over
