@@ -187,12 +187,12 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
         return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
     };
     const DepthKeysOut dk = view_depth_keys(w, L);
-    cudaError_t e = mark(0);
-    if (e == cudaSuccess) e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
-    if (e == cudaSuccess && step1 == Step1::kProject) {
-        e = sort_prepare_histogram(sort_ws, s);
-        if (e == cudaSuccess) e = launch_preprocess(*g, cc, p, s, &dk);
-    }
+    // the frame's setup (status header, the depth digits' histograms) comes
+    // before the first stage mark, so that stage 1 brackets the projection alone
+    cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
+    if (e == cudaSuccess && step1 == Step1::kProject) e = sort_prepare_histogram(sort_ws, s);
+    if (e == cudaSuccess) e = mark(0);
+    if (e == cudaSuccess && step1 == Step1::kProject) e = launch_preprocess(*g, cc, p, s, &dk);
     if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess && step1 == Step1::kRecordOnly) {
         e = sort_prepare_histogram(sort_ws, s);

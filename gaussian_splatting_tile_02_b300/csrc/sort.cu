@@ -15,9 +15,10 @@
 //                    ever waits on blocks that are already running), ranks
 //                    its keys stably with warp match/popc counters, publishes
 //                    its per-digit counts, and finds its global offsets by
-//                    decoupled look-back over earlier tiles. Keys are then
-//                    reordered in shared memory and written out in
-//                    digit-contiguous runs (coalesced), values likewise.
+//                    decoupled look-back over earlier tiles. Keys and values
+//                    are then reordered in shared memory (together for 32-bit
+//                    keys, one after the other for 64-bit keys) and written
+//                    out in digit-contiguous runs (coalesced).
 //   copy back      : only when the pass count is odd.
 //
 // A look-back status word is (flag << 30 | count), written and read as one
@@ -198,6 +199,11 @@ __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_ker
     __shared__ uint32_t s_goff[kRadix];
     __shared__ uint32_t s_warp_tot[kRadix / 32];
     __shared__ __align__(16) KeyT s_keys[kSortTile];
+    // 32-bit keys: the values get their own staging, so keys and values move
+    // in one round (64-bit keys and their values would not fit the 48 KB of
+    // static shared memory; the values then reuse the key staging afterwards)
+    constexpr bool kJoint = sizeof(KeyT) == 4;
+    __shared__ uint32_t s_vals_joint[kJoint ? kSortTile : 1];
     __shared__ uint32_t s_tile;
     __shared__ int s_timed_out;
 
@@ -320,44 +326,73 @@ __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_ker
     const bool skip = s_timed_out != 0;
 
     // reorder keys in shared memory by (digit, rank)
-    uint32_t loc[kSortItems];
+    if constexpr (kJoint) {
 #pragma unroll
-    for (int i = 0; i < kSortItems; i++) {
-        const int li = warp_base + i * 32 + lane;
-        loc[i] = 0xffffffffu;
-        if (li < n_valid) {
-            const uint32_t d = digit_of(key[i], shift, dmask);
-            loc[i] = s_dstart[d] + s_hist[warp * kRadix + d] + rank[i];
-            s_keys[loc[i]] = key[i];
-        }
-    }
-    __syncthreads();
-    uint32_t dest[kSortItems];
-#pragma unroll
-    for (int k = 0; k < kSortItems; k++) {
-        const int j = k * kSortThreads + tid;
-        dest[k] = 0xffffffffu;
-        if (j < n_valid) {
-            const KeyT kk = s_keys[j];
-            const uint32_t d = digit_of(kk, shift, dmask);
-            const uint32_t o = s_goff[d] + (uint32_t)j - s_dstart[d];
-            GS_CHECK(skip || (int64_t)o < K);
-            if (!skip && (int64_t)o < K) {
-                a.keys_out[o] = kk;
-                dest[k] = o;
+        for (int i = 0; i < kSortItems; i++) {
+            const int li = warp_base + i * 32 + lane;
+            if (li < n_valid) {
+                const uint32_t d = digit_of(key[i], shift, dmask);
+                const uint32_t loc = s_dstart[d] + s_hist[warp * kRadix + d] + rank[i];
+                s_keys[loc] = key[i];
+                s_vals_joint[loc] = val[i];
             }
         }
-    }
-    __syncthreads();
-    uint32_t* s_vals = reinterpret_cast<uint32_t*>(s_keys);
+        __syncthreads();
 #pragma unroll
-    for (int i = 0; i < kSortItems; i++)
-        if (loc[i] != 0xffffffffu) s_vals[loc[i]] = val[i];
-    __syncthreads();
+        for (int k = 0; k < kSortItems; k++) {
+            const int j = k * kSortThreads + tid;
+            if (j < n_valid) {
+                const KeyT kk = s_keys[j];
+                const uint32_t d = digit_of(kk, shift, dmask);
+                const uint32_t o = s_goff[d] + (uint32_t)j - s_dstart[d];
+                GS_CHECK(skip || (int64_t)o < K);
+                if (!skip && (int64_t)o < K) {
+                    a.keys_out[o] = kk;
+                    a.vals_out[o] = s_vals_joint[j];
+                }
+            }
+        }
+    } else {
+        // 64-bit keys: keys first, then the values through the same staging
+        uint32_t loc[kSortItems];
 #pragma unroll
-    for (int k = 0; k < kSortItems; k++) {
-        const int j = k * kSortThreads + tid;
-        if (j < n_valid && dest[k] != 0xffffffffu) a.vals_out[dest[k]] = s_vals[j];
+        for (int i = 0; i < kSortItems; i++) {
+            const int li = warp_base + i * 32 + lane;
+            loc[i] = 0xffffffffu;
+            if (li < n_valid) {
+                const uint32_t d = digit_of(key[i], shift, dmask);
+                loc[i] = s_dstart[d] + s_hist[warp * kRadix + d] + rank[i];
+                s_keys[loc[i]] = key[i];
+            }
+        }
+        __syncthreads();
+        uint32_t dest[kSortItems];
+#pragma unroll
+        for (int k = 0; k < kSortItems; k++) {
+            const int j = k * kSortThreads + tid;
+            dest[k] = 0xffffffffu;
+            if (j < n_valid) {
+                const KeyT kk = s_keys[j];
+                const uint32_t d = digit_of(kk, shift, dmask);
+                const uint32_t o = s_goff[d] + (uint32_t)j - s_dstart[d];
+                GS_CHECK(skip || (int64_t)o < K);
+                if (!skip && (int64_t)o < K) {
+                    a.keys_out[o] = kk;
+                    dest[k] = o;
+                }
+            }
+        }
+        __syncthreads();
+        uint32_t* s_vals = reinterpret_cast<uint32_t*>(s_keys);
+#pragma unroll
+        for (int i = 0; i < kSortItems; i++)
+            if (loc[i] != 0xffffffffu) s_vals[loc[i]] = val[i];
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kSortItems; k++) {
+            const int j = k * kSortThreads + tid;
+            if (j < n_valid && dest[k] != 0xffffffffu) a.vals_out[dest[k]] = s_vals[j];
+        }
     }
 }
 

@@ -273,7 +273,8 @@ gs_status gs_render(const gs_gaussians* gaussians, const gs_camera* camera, int6
 /* gs_render that also records CUDA events at its stage boundaries, for
  * per-stage timing of the very launches a frame makes. events[0..6] are
  * caller-created cudaEvent_t handles (as void*), recorded on `stream`:
- *   0 start, 1 after projection, 2 after the depth order, 3 after binning,
+ *   0 start (after the frame's setup memsets: status header and the depth
+ *   digits' histograms), 1 after projection, 2 after the depth order, 3 after binning,
  *   4 after the tile sort, 5 after the ranges and the tiles' launch order,
  *   6 after compositing (the compositing kernel alone).
  * n_events must be >= GS_RENDER_STAGES + 1. */
