@@ -173,8 +173,9 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0) for r in rows)}
 
 
-def traffic_from_profile(kernel_file: str, profile: str):
-    """Per-launch DRAM bytes recorded in a committed ncu summary, if the kernel source is unchanged."""
+def traffic_from_profile(kernel_file: str, profile: str, workload: str):
+    """Per-launch DRAM bytes recorded in a committed ncu summary, if the summary was taken on
+    this workload and the kernel source is unchanged since."""
     try:
         src = open(os.path.join(ROOT, "gaussian_splatting_tile_02_b300", "csrc", kernel_file), "rb").read()
         sha = hashlib.sha256(src).hexdigest()[:16]
@@ -184,7 +185,7 @@ def traffic_from_profile(kernel_file: str, profile: str):
                 if ":" in line and line.startswith("- "):
                     k, v = line[2:].split(":", 1)
                     rec[k.strip()] = v.strip()
-        if rec.get("source_sha256_16") == sha:
+        if rec.get("source_sha256_16") == sha and rec.get("workload") == workload:
             return float(rec["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -605,7 +606,7 @@ def run_ours(args, rank, local_rank, world):
         roof = {"kernel": "rasterize_kernel", "bound": "alu", "achieved": ras_achieved, "peak": fp32_peak,
                 "unit": "T FP32 lane-ops/s", "frac": ras_achieved / fp32_peak,
                 "peak_kind": f"derived: {SM_COUNT} SMs x {FP32_LANES_PER_SM} FP32 lanes x {SM_MAX_MHZ:.0f} MHz",
-                "traffic": traffic_from_profile("rasterize.cu", "rasterize_1M.md"),
+                "traffic": traffic_from_profile("rasterize.cu", "rasterize_1M.md", args.config),
                 "units": f"{evals} pixel-Gaussian evaluations x {OPS_PER_EVAL} FP32 ops"}
     else:
         d = stages_out[dominant]
