@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -173,19 +174,30 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0) for r in rows)}
 
 
-def traffic_from_profile(kernel_file: str, profile: str, workload: str):
+def code_hash(files) -> str:
+    """sha256 (16 hex digits) of the code of the given csrc files, comments and whitespace
+    removed, so that a comment edit does not void counters taken on the same code."""
+    h = hashlib.sha256()
+    for name in files:
+        src = open(os.path.join(ROOT, "gaussian_splatting_tile_02_b300", "csrc", name)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
+        h.update(b"\0")
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(profile: str, workload: str):
     """Per-launch DRAM bytes recorded in a committed ncu summary, if the summary was taken on
-    this workload and the kernel source is unchanged since."""
+    this workload and the code of the files it names is unchanged since."""
     try:
-        src = open(os.path.join(ROOT, "gaussian_splatting_tile_02_b300", "csrc", kernel_file), "rb").read()
-        sha = hashlib.sha256(src).hexdigest()[:16]
         rec = {}
         with open(os.path.join(ROOT, "profiles", profile)) as f:
             for line in f:
                 if ":" in line and line.startswith("- "):
                     k, v = line[2:].split(":", 1)
                     rec[k.strip()] = v.strip()
-        if rec.get("source_sha256_16") == sha and rec.get("workload") == workload:
+        if rec.get("workload") == workload and rec.get("code_sha256_16") == code_hash(rec["code_files"].split()):
             return float(rec["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -606,7 +618,7 @@ def run_ours(args, rank, local_rank, world):
         roof = {"kernel": "rasterize_kernel", "bound": "alu", "achieved": ras_achieved, "peak": fp32_peak,
                 "unit": "T FP32 lane-ops/s", "frac": ras_achieved / fp32_peak,
                 "peak_kind": f"derived: {SM_COUNT} SMs x {FP32_LANES_PER_SM} FP32 lanes x {SM_MAX_MHZ:.0f} MHz",
-                "traffic": traffic_from_profile("rasterize.cu", "rasterize_1M.md", args.config),
+                "traffic": traffic_from_profile("rasterize_1M.md", args.config),
                 "units": f"{evals} pixel-Gaussian evaluations x {OPS_PER_EVAL} FP32 ops"}
     else:
         d = stages_out[dominant]

@@ -210,8 +210,8 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
 
         const uint32_t cnt = min((uint32_t)kRastThreads, range.y - base);
         // groups of 32 batch entries: ballot the ones whose box meets this
-        // warp's 8x4 pixel block, copy those records into the warp's list, then
-        // evaluate the list in order for the warp's 32 pixels
+        // warp's 8x8 pixel block, copy those records into the warp's list, then
+        // evaluate the list in order for the warp's 64 pixels
 #pragma unroll 1
         for (int i = 0; i < kRastThreads / 32; i++) {
             if (__all_sync(0xffffffffu, done && done2)) break;

@@ -58,19 +58,22 @@ def test_single_rank_helpers():
     assert [bench.rank_view(2, r, 4) for r in range(4)] == [2, 3, 0, 1]
 
 
-def test_traffic_figure_only_for_its_workload_and_source(tmp_path, monkeypatch):
+def test_traffic_figure_only_for_its_workload_and_code(tmp_path, monkeypatch):
     """roofline.traffic comes from a committed ncu summary only for the workload the
-    counters were taken on and only while the kernel source still has the recorded hash."""
-    import hashlib
+    counters were taken on and only while the code of the named files is unchanged;
+    comments and whitespace do not count as code."""
     csrc = tmp_path / "gaussian_splatting_tile_02_b300" / "csrc"
     csrc.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
-    (csrc / "k.cu").write_bytes(b"kernel source")
-    sha = hashlib.sha256(b"kernel source").hexdigest()[:16]
-    (tmp_path / "profiles" / "k.md").write_text(
-        f"# k\n- workload: 1M\n- source_sha256_16: {sha}\n- dram_bytes_per_launch: 1234\n")
+    (csrc / "k.cu").write_text("int f() { return 1; }  // one\n")
+    (csrc / "h.cuh").write_text("/* helper */ int g();\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.traffic_from_profile("k.cu", "k.md", "1M") == 1234.0
-    assert bench.traffic_from_profile("k.cu", "k.md", "5M") is None
-    (csrc / "k.cu").write_bytes(b"kernel source, changed")
-    assert bench.traffic_from_profile("k.cu", "k.md", "1M") is None
+    h = bench.code_hash(["k.cu", "h.cuh"])
+    (tmp_path / "profiles" / "k.md").write_text(
+        f"# k\n- workload: 1M\n- code_files: k.cu h.cuh\n- code_sha256_16: {h}\n- dram_bytes_per_launch: 1234\n")
+    assert bench.traffic_from_profile("k.md", "1M") == 1234.0
+    assert bench.traffic_from_profile("k.md", "5M") is None
+    (csrc / "k.cu").write_text("int f() {\n    return 1;   // a reworded comment\n}\n")
+    assert bench.traffic_from_profile("k.md", "1M") == 1234.0
+    (csrc / "h.cuh").write_text("/* helper */ int g(int);\n")
+    assert bench.traffic_from_profile("k.md", "1M") is None
