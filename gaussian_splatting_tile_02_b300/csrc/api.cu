@@ -254,7 +254,13 @@ cudaError_t batch_events(BatchEvents** out) {
         e = cudaEventCreateWithFlags(&be.fork, cudaEventDisableTiming);
         for (int i = 0; e == cudaSuccess && i < kMaxBatchStreams; i++)
             e = cudaEventCreateWithFlags(&be.join[i], cudaEventDisableTiming);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) {
+            // release whatever was created; the next call tries again
+            if (be.fork) cudaEventDestroy(be.fork);
+            for (int i = 0; i < kMaxBatchStreams; i++)
+                if (be.join[i]) cudaEventDestroy(be.join[i]);
+            return e;
+        }
         it = g_batch_events.emplace(dev, be).first;
     }
     *out = &it->second;

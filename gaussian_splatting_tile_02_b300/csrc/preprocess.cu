@@ -36,6 +36,7 @@
 #include <float.h>
 
 #include <map>
+#include <utility>
 #include <mutex>
 
 #include "gs_internal.cuh"
@@ -489,23 +490,26 @@ PreArgs pre_args(const gs_gaussians& g, const CamConst& cam, const gs_projected&
     return a;
 }
 
-// blocks of 256 that fit on the GPU at once for this kernel (occupancy
-// computed once per kernel; every instantiation has its own cache entry)
+// blocks of 256 that fit on the current GPU at once for this kernel
+// (occupancy computed once per device and kernel; every instantiation has its
+// own cache entry). Only the grid size depends on it: the kernels are
+// grid-stride loops.
 template <typename K>
 unsigned resident_blocks(K kernel, int64_t n) {
     static std::mutex mu;
-    static std::map<const void*, int64_t> cache;
+    static std::map<std::pair<int, const void*>, int64_t> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    const auto key = std::make_pair(dev, reinterpret_cast<const void*>(kernel));
     int64_t cap = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
-        auto it = cache.find(reinterpret_cast<const void*>(kernel));
+        auto it = cache.find(key);
         if (it == cache.end()) {
-            int dev = 0, sms = 0, per_sm = 0;
-            cudaGetDevice(&dev);
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
-            it = cache.emplace(reinterpret_cast<const void*>(kernel),
-                               (int64_t)(per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 148)).first;
+            int sms = 0, per_sm = 0;
+            if (dev < 0 || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0) != cudaSuccess) per_sm = 0;
+            it = cache.emplace(key, (int64_t)(per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 148)).first;
         }
         cap = it->second;
     }
