@@ -120,6 +120,11 @@ typedef struct gs_projected {
     float* raster;
 } gs_projected;
 
+/* gs_status_string: a static, NUL-terminated English description of a
+ * gs_status value ("unknown status" for any other number); never NULL, never
+ * to be freed. gs_abi_version: GS_ABI_VERSION of the library that was loaded,
+ * so a caller can refuse a library built from another version of this header.
+ * Neither touches the GPU. */
 const char* gs_status_string(int32_t status);
 int32_t gs_abi_version(void);
 
@@ -218,7 +223,11 @@ gs_status gs_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_keys,
  * gs_sort32: gs_sort for 32-bit keys (key_bits 1..32). num_keys may be NULL,
  * in which case key_capacity is the key count. ws: >= gs_sort_workspace_bytes.
  *
- * gs_tile_ranges32: step 4 for sorted 32-bit tile-id keys. */
+ * gs_tile_ranges32: step 4 (as gs_tile_ranges) for sorted 32-bit tile-id
+ * keys: sorted_tiles is device uint32 [key_capacity], of which the first
+ * min(*num_keys, key_capacity) are read; any 4-byte alignment (16-byte
+ * aligned arrays are read with vector loads). ranges: device uint32
+ * [tiles_y * tiles_x][2], 8-byte aligned. */
 size_t gs_depth_order_workspace_bytes(int64_t n);
 size_t gs_bin_ordered_workspace_bytes(int64_t n, int64_t key_capacity);
 gs_status gs_depth_order(const gs_projected* projected, int64_t n, uint32_t* order, void* ws,
