@@ -62,7 +62,9 @@ def sh_basis_t(d):
 
     Bands 0-2 with the signs printed in eval_sh_degree_3 ("Étape 6"); band 3
     from the closed forms of the real harmonics with the band-1 sign pattern
-    (odd m negative). Normalisations from their closed forms."""
+    (odd m negative). Normalisations from their closed forms. Band 3's signs
+    are parity unpinned (the pages print no band-3 code); this basis is pinned
+    equal to the C oracle's."""
     torch = _torch()
     x, y, z = d[:, 0], d[:, 1], d[:, 2]
     pi = math.pi

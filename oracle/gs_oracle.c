@@ -133,7 +133,10 @@ void or_covariance3d(int64_t n, const float *quats, const float *log_scales, dou
  * +C2 xy, +C2 yz, +C2' (2z^2-x^2-y^2), +C2 xz, +C2'' (x^2-y^2).
  * Band 3 is left out of the printed code; it is taken here from the closed
  * forms of the real harmonics with the band-1 pattern (odd m negative). The
- * normalisation constants are computed from their closed forms, not typed in. */
+ * normalisation constants are computed from their closed forms, not typed in.
+ * Parity unpinned for band 3's signs: the pages print no band-3 code, so only
+ * its orthonormality, harmonicity and parity Y(-d) = (-1)^l Y(d) are pinned; its
+ * sign convention is a reading. */
 void or_sh_basis(double x, double y, double z, double *Y /* [16] */) {
     const double pi = 3.14159265358979323846;
     const double c0 = sqrt(1.0 / (4.0 * pi));
