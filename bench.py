@@ -28,6 +28,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -71,6 +72,9 @@ def parse():
     ap.add_argument("--no-toy", action="store_true")
     ap.add_argument("--batch-streams", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the raw nvidia-smi samples of the timed region in this file "
+                         "(a {rank} field is filled in); by default they go to a temporary file")
     return ap.parse_args()
 
 
@@ -117,14 +121,20 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, path=None):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.keep = path is not None
+        if path is None:
+            fd, path = tempfile.mkstemp(prefix=f"gs_clocks_{gpu_index}_", suffix=".csv")
+            os.close(fd)
+        self.path = path
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            d = os.path.dirname(self.path)
+            if d:
+                os.makedirs(d, exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -153,6 +163,11 @@ class ClockSampler:
                     rows.append(parts)
         except Exception:
             pass
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         def num(x):
@@ -324,7 +339,7 @@ def run_ours(args, rank, local_rank, world):
             stream.synchronize()
 
     hbm_peak, peak_kind, peaks = measured_peaks()
-    sampler = ClockSampler(local_rank)
+    sampler = ClockSampler(local_rank, args.clocks_csv.format(rank=rank) if args.clocks_csv else None)
     with sampler:
         time.sleep(0.3)
         # --- main timed region: K whole frames

@@ -77,3 +77,25 @@ def test_traffic_figure_only_for_its_workload_and_code(tmp_path, monkeypatch):
     assert bench.traffic_from_profile("k.md", "1M") == 1234.0
     (csrc / "h.cuh").write_text("/* helper */ int g(int);\n")
     assert bench.traffic_from_profile("k.md", "1M") is None
+
+
+def test_clock_summary_median_under_load_and_reasons(tmp_path):
+    """The clocks record of the JSON line: median SM clock over the samples taken under load,
+    the throttle reasons seen active, and the raw file kept only when asked for."""
+    rows = [
+        "0, 1200, 2032, 150.0, 0, Not Active, Not Active, Not Active, Not Active, Not Active",
+        "0, 2032, 2032, 400.0, 97, Active, Not Active, Not Active, Not Active, Active",
+        "0, 2010, 2032, 420.0, 99, Not Active, Not Active, Not Active, Not Active, Not Active",
+        "0, 1990, 2032, 430.0, 98, Not Active, Not Active, Not Active, Not Active, Not Active",
+    ]
+    kept = tmp_path / "clocks.csv"
+    kept.write_text("\n".join(rows) + "\n")
+    s = bench.ClockSampler(0, str(kept)).summary()
+    assert s["sm_mhz"] == 2010 and s["sm_max_mhz"] == 2032
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 4 and s["samples_under_load"] == 3
+    assert s["power_w_max"] == 430.0 and kept.exists()
+    temp = bench.ClockSampler(0)
+    with open(temp.path, "w") as f:
+        f.write("\n".join(rows) + "\n")
+    assert temp.summary()["sm_mhz"] == 2010
+    assert not os.path.exists(temp.path)
