@@ -189,6 +189,16 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0) for r in rows)}
 
 
+def frame_launches(tiles: int) -> int:
+    """Kernels one gs_render frame launches for an image of `tiles` 16x16 tiles: preprocess
+    (which also writes the depth keys); sort bases and 4 depth passes; 5 binning kernels;
+    sort bases and one pass per 8 tile-id bits, plus a copy back after an odd pass count;
+    ranges; tile order; rasterize."""
+    tile_bits = max(1, (tiles - 1).bit_length())
+    passes = (tile_bits + 7) // 8
+    return 1 + (1 + 4) + 5 + (1 + passes + passes % 2) + 1 + 1 + 1
+
+
 def code_hash(files) -> str:
     """sha256 (16 hex digits) of the code of the given csrc files, comments and whitespace
     removed, so that a comment edit does not void counters taken on the same code."""
@@ -604,10 +614,7 @@ def run_ours(args, rank, local_rank, world):
     K = K_keys
     tile_bits = max(1, (tx * ty - 1).bit_length())
     tpasses = (tile_bits + 7) // 8
-    # preprocess (which also writes the depth keys); sort bases, 4 depth passes;
-    # 5 binning kernels; sort bases + tile passes (+ a copy back after an odd
-    # count); ranges + tile order; rasterize
-    launches_per_frame = 1 + (1 + 4) + 5 + (1 + tpasses + tpasses % 2) + 1 + 2
+    launches_per_frame = frame_launches(tx * ty)
     ras_ms = st_ms["rasterize"]
     clk = clocks.get("sm_mhz") or SM_MAX_MHZ
     fp32_peak = SM_COUNT * FP32_LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12     # T lane-ops/s at max clock

@@ -99,3 +99,13 @@ def test_clock_summary_median_under_load_and_reasons(tmp_path):
         f.write("\n".join(rows) + "\n")
     assert temp.summary()["sm_mhz"] == 2010
     assert not os.path.exists(temp.path)
+
+
+def test_frame_launch_count():
+    """gpu_launches per frame: 17 at 1920x1080 (8160 tiles, 13 bits, two passes) and at
+    64x64 (16 tiles, one pass and a copy back); 19 at 8192x4320 (138240 tiles, three passes
+    and a copy back)."""
+    assert bench.frame_launches(120 * 68) == 17
+    assert bench.frame_launches(4 * 4) == 17
+    assert bench.frame_launches(512 * 270) == 19
+    assert bench.frame_launches(240 * 135) == 17   # 3840x2160: 15 bits, two passes
