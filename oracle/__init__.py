@@ -11,7 +11,9 @@ rectangles) in the precision the pages' own code uses. The arithmetic lives in
 assembles the stages. It never imports the CUDA package.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
-(closed forms, invariants, brute force, the printed constants) except the sign
+(closed forms, invariants, brute force, the printed constants; the
+threshold-flip helper ``composite_pixel_flipped`` by closed-form pixels in
+``tests/test_oracle_flip_pins.py``) except the sign
 convention of SH band 3, which the pages leave out: band 3 is parity
 unpinned (its orthonormality and harmonicity are pinned, its signs are a
 reading).

@@ -618,7 +618,11 @@ void or_composite(const or_camera *cam, const double *mean2d, const double *coni
     }
 }
 
-/* One pixel of the tiled composite with the given decisions inverted. */
+/* One pixel of the tiled composite with the given decisions inverted: each
+ * (list position, decision type) in the flip list inverts the skip test or the
+ * stop test taken at that position of the pixel's tile list; positions the walk
+ * never reaches change nothing. Pinned on hand-made pixels with closed forms
+ * (tests/test_oracle_flip_pins.py). */
 void or_composite_pixel_flipped(const or_camera *cam, int32_t x, int32_t y, const double *mean2d,
                                 const double *conic, const double *opacity, const double *rgb,
                                 const uint32_t *sorted_vals, const uint32_t *ranges,

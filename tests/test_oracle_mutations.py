@@ -19,6 +19,7 @@ import pytest
 import oracle
 from oracle import gs_grad
 
+import test_oracle_flip_pins as fpins
 import test_oracle_grad_pins as gpins
 import test_oracle_pins as pins
 
@@ -44,6 +45,17 @@ C_MUTATIONS = [
      [(pins.test_decision_program_second_build, {"name": "100k", "n": 30000})]),
     ("no skip below 1/255", "int skip = alpha < OR_ALPHA_MIN;", "int skip = alpha < 0.0;",
      [(pins.test_skip_below_one_over_255, {})]),
+    # the threshold-flip helper behind the GPU image check's "several results are correct" rule
+    ("flip type ignored by the skip decision", "if (flip_pos[f] == j && flip_type[f] == OR_EV_SKIP) skip = !skip;",
+     "if (flip_pos[f] == j) skip = !skip;",
+     [(fpins.test_flips_the_walk_never_takes_change_nothing, {}),
+      (fpins.test_stop_flip_at_the_crossing_takes_the_next_layer, {})]),
+    ("stop flip one list position late", "if (flip_pos[f] == j && flip_type[f] == OR_EV_STOP) stop = !stop;",
+     "if (flip_pos[f] == j + 1 && flip_type[f] == OR_EV_STOP) stop = !stop;",
+     [(fpins.test_stop_flip_at_the_crossing_takes_the_next_layer, {}), (fpins.test_two_flips_closed_form, {})]),
+    # (the wrong column stays inside the 640x480 tile grid: y / 16 < 30 < 40 tiles per row)
+    ("flipped pixel's tile column taken from y", "const int64_t tile = (int64_t)(y / 16) * TX + (x / 16);",
+     "const int64_t tile = (int64_t)(y / 16) * TX + (y / 16);", [(fpins.test_no_flip_equals_the_composite, {})]),
 ]
 
 
