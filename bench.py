@@ -124,6 +124,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int, path=None):
         self.gpu = gpu_index
         self.proc = None
+        self.fh = None
         self.keep = path is not None
         if path is None:
             fd, path = tempfile.mkstemp(prefix=f"gs_clocks_{gpu_index}_", suffix=".csv")
@@ -150,7 +151,9 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        if self.fh is not None:
             self.fh.close()
+            self.fh = None
 
     def summary(self):
         rows = []

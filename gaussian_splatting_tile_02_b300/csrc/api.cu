@@ -234,7 +234,10 @@ gs_status render_impl(const gs_gaussians* g, const gs_camera* cam, int64_t key_c
 }
 
 // Fork/join events for gs_render_batch, created once per device on first use
-// (timing disabled, so recording them costs no timestamp).
+// (timing disabled, so recording them costs no timestamp). g_batch_mutex is
+// held by gs_render_batch from the lookup through its last join wait, so two
+// host threads batching on one device cannot re-record each other's fork or
+// join events between a record and the waits that depend on it.
 constexpr int kMaxBatchStreams = 8;
 struct BatchEvents {
     cudaEvent_t fork = nullptr;
@@ -243,11 +246,11 @@ struct BatchEvents {
 std::mutex g_batch_mutex;
 std::map<int, BatchEvents> g_batch_events;
 
+// The calling thread must hold g_batch_mutex.
 cudaError_t batch_events(BatchEvents** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(g_batch_mutex);
     auto it = g_batch_events.find(dev);
     if (it == g_batch_events.end()) {
         BatchEvents be;
@@ -661,6 +664,8 @@ gs_status gs_render_batch(const gs_gaussians* g, const gs_camera* cams, int32_t 
     const RenderLayout L = render_layout(g->n, cams[0].width, cams[0].height, key_capacity);
     const size_t stride = L.total;
     if (!ws || !aligned(ws, kAlign) || ws_bytes < stride * (size_t)views) return GS_ERR_WORKSPACE;
+    // held until the last join wait is enqueued (the calls below only enqueue work)
+    std::lock_guard<std::mutex> lock(g_batch_mutex);
     BatchEvents* ev = nullptr;
     if (batch_events(&ev) != cudaSuccess) return GS_ERR_CUDA;
     char* w0 = static_cast<char*>(ws);
@@ -781,6 +786,16 @@ gs_status gs_read_status(const void* ws, void* stream, uint32_t* flags, uint64_t
     if (h.flags & GS_FLAG_TIMEOUT) return GS_ERR_TIMEOUT;
     if (h.flags & GS_FLAG_CAPACITY) return GS_ERR_CAPACITY;
     return GS_OK;
+}
+
+size_t gs_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity) {
+    return gs_render_workspace_bytes(n, width, height, key_capacity);
+}
+
+gs_status gs_last_device_status(const void* ws) {
+    if (!ws || !aligned(ws, kAlign)) return GS_ERR_WORKSPACE;
+    if (cudaDeviceSynchronize() != cudaSuccess) return GS_ERR_CUDA;
+    return gs_read_status(ws, nullptr, nullptr, nullptr);
 }
 
 gs_status gs_test_spin_timeout(void* ws, int64_t iterations, void* stream) {

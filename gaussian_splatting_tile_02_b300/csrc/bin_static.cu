@@ -11,8 +11,10 @@
 //
 // The array is 256 + 8 * (16,777,216 / 2048) = 65,792 bytes and lives on
 // every device that loads this library until the process exits. Its device
-// address is looked up once per device (cudaGetSymbolAddress, with that
-// device current) on the first call made on that device.
+// address is looked up with cudaGetSymbolAddress, with the device current:
+// on every call whose stream is not being captured (so that an address made
+// stale by cudaDeviceReset is replaced), and taken from the per-device cache
+// while the stream is being captured (so a first call must precede capture).
 #include <mutex>
 
 #include "gs_internal.cuh"
@@ -31,14 +33,19 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_dev_ptr[kMaxDevices] = {};
 
-// Device address of g_bin_scratch on the current device (looked up once per device).
-cudaError_t static_scratch(void** out) {
+// Device address of g_bin_scratch on the current device: looked up again on
+// every call outside stream capture, from the cache during capture.
+cudaError_t static_scratch(cudaStream_t s, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_dev_ptr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone || !g_dev_ptr[dev]) {
+        if (cap != cudaStreamCaptureStatusNone) return cudaErrorStreamCaptureUnsupported;
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_bin_scratch);
         if (e != cudaSuccess) return e;
@@ -66,9 +73,9 @@ extern "C" gs_status gs_bin_static(const gs_projected* p, int64_t n, const gs_ca
         return GS_ERR_INVALID_ARG;
     if ((uintptr_t)num_keys % 8 != 0) return GS_ERR_INVALID_ARG;
 
-    void* base = nullptr;
-    if (static_scratch(&base) != cudaSuccess) return GS_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
+    void* base = nullptr;
+    if (static_scratch(s, &base) != cudaSuccess) return GS_ERR_CUDA;
     auto* header = static_cast<StatusHeader*>(base);
     // the array keeps the previous call's contents: the header's flags must start at zero
     // (the partial sums are fully rewritten by every call)

@@ -123,6 +123,8 @@ _SIGNATURES = {
                                           ctypes.POINTER(GsGaussiansGrad), c_void_p]),
     "gs_read_status": (ctypes.c_int, [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_uint32),
                                       ctypes.POINTER(ctypes.c_uint64)]),
+    "gs_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64]),
+    "gs_last_device_status": (ctypes.c_int, [c_void_p]),
     "gs_set_spin_limit": (None, [ctypes.c_int64]),
     "gs_test_spin_timeout": (ctypes.c_int, [c_void_p, ctypes.c_int64, c_void_p]),
 }

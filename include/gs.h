@@ -25,6 +25,14 @@
  *     stated). Images are HWC float32.
  *   - Tiles are 16x16 pixels, tiles_x = ceil(width/16), tiles_y =
  *     ceil(height/16), tile id = ty * tiles_x + tx.
+ *   - Host threads: entry points may be called from several host threads on
+ *     different workspaces. gs_render_batch enqueues under one process-wide
+ *     lock (its fork/join events are shared per device); gs_set_spin_limit is
+ *     not thread-safe.
+ *   - cudaDeviceReset: gs_render_batch keeps per-device fork/join events that
+ *     a reset destroys; do not call it on a device after resetting that device
+ *     in the same process. (gs_bin_static looks its scratch address up again
+ *     on every call made outside stream capture.)
  */
 #ifndef GS_B300_H
 #define GS_B300_H
@@ -507,6 +515,16 @@ gs_status gs_debug_set_check_counter(uint64_t* device_counter);
  * GS_ERR_TIMEOUT, GS_ERR_CAPACITY or GS_OK from the flags. num_keys is the
  * key count of the last gs_bin/gs_render on that workspace. */
 gs_status gs_read_status(const void* ws, void* stream, uint32_t* flags, uint64_t* num_keys);
+
+/* The boundary's names for two of the calls above:
+ *   gs_workspace_bytes(n, width, height, key_capacity) ==
+ *       gs_render_workspace_bytes(n, width, height, key_capacity);
+ *   gs_last_device_status(ws): the flags of a gs_render / gs_bin / gs_sort
+ *       workspace as gs_read_status returns them, after a cudaDeviceSynchronize
+ *       (so the work of every stream of the device is included). SYNCHRONISES
+ *       the device. */
+size_t gs_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity);
+gs_status gs_last_device_status(const void* ws);
 
 /* Upper bound on the wait of every device-side spin (look-back of the radix
  * sort), in polling iterations; <= 0 restores the default (about a second).

@@ -55,6 +55,15 @@ def test_workspace_sizes():
     assert L.gs_sort_workspace_bytes(0) > 0 and L.gs_bin_workspace_bytes(0) > 0
     # 256-byte status header + aligned scratch
     assert L.gs_sort_workspace_bytes(1 << 20) % 256 == 0
+    # the boundary's name for the render workspace size
+    for args in ((1000, 64, 64, 5000), (10**6, 1920, 1080, 3 * 10**6), (0, 1, 1, 0), (-1, 64, 64, 10)):
+        assert L.gs_workspace_bytes(*args) == L.gs_render_workspace_bytes(*args)
+
+
+def test_last_device_status_rejects_a_missing_or_misaligned_workspace():
+    L = native.lib()
+    assert L.gs_last_device_status(None) == native.GS_ERR_WORKSPACE
+    assert L.gs_last_device_status(256 + 8) == native.GS_ERR_WORKSPACE
 
 
 def _cam(**over):

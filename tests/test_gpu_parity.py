@@ -316,6 +316,11 @@ def test_capacity_overflow_reports_count(oracle_mod):
     torch.cuda.synchronize()
     st, flags, nk = r.status()
     assert st == native.GS_ERR_CAPACITY and nk == K
+    # the boundary's status call (synchronises the device) reads the same flags
+    assert gs.lib().gs_last_device_status(r.ws.data_ptr()) == native.GS_ERR_CAPACITY
+    r_ok = gs.Renderer(g, cam["width"], cam["height"], K)
+    r_ok.render(cam)
+    assert gs.lib().gs_last_device_status(r_ok.ws.data_ptr()) == native.GS_OK
 
 
 @pytest.mark.parametrize("count,bits", [(0, 40), (1, 40), (4096, 45), (4097, 45), (12289, 20), (100_000, 64),

@@ -101,6 +101,19 @@ def test_clock_summary_median_under_load_and_reasons(tmp_path):
     assert not os.path.exists(temp.path)
 
 
+def test_clock_sampler_closes_its_file_when_the_sampler_cannot_start(tmp_path, monkeypatch):
+    """nvidia-smi missing: Popen raises inside __enter__; the record file is still closed on exit
+    and the summary reports no samples."""
+    def no_smi(*a, **k):
+        raise FileNotFoundError("nvidia-smi")
+    monkeypatch.setattr(bench.subprocess, "Popen", no_smi)
+    sampler = bench.ClockSampler(0, str(tmp_path / "c.csv"))
+    with sampler:
+        assert sampler.proc is None and sampler.fh is not None
+    assert sampler.fh is None
+    assert sampler.summary()["samples"] == 0
+
+
 def test_frame_launch_count():
     """gpu_launches per frame: 17 at 1920x1080 (8160 tiles, 13 bits, two passes) and at
     64x64 (16 tiles, one pass and a copy back); 19 at 8192x4320 (138240 tiles, three passes
