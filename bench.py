@@ -14,6 +14,12 @@ copied from pinned host memory and the image read back inside the timed
 region. Under torchrun each rank renders its own replica (independent frames:
 replicas only, no collective on the data path).
 
+The FP32 roofline of the compositing step is taken against the FMA rate that
+gs_fp32_peak_probe measures on the same GPU in the same run (scalar and packed
+FMA chains; the higher rate). The `configs` block repeats the frame and stage
+measurement for every view of every workload (tiny, 100k, 1M, 5M x 4 views,
+stress x 8 views) with the per-view and mean figures; it runs at N=1 only.
+
 --impl reference times the CPU oracle (the plain fp64 renderer) on the host
 cores on the same workload.
 """
@@ -38,16 +44,21 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6400.0
-SM_COUNT = 148
-FP32_LANES_PER_SM = 128
-SM_MAX_MHZ = 2032.0
-# algorithmic FP32 work per (pixel, Gaussian) evaluation: dx, dy (2), the
-# exponent with the conic pre-scaled (5), min with 0.99 (1), the 1/255 test (1)
+# FP32 work per evaluated (pixel, Gaussian) pair, counted two ways:
+# - the method's count: dx, dy, the quadratic form with its cross term, the -1/2 scale, the
+#   opacity product, the 0.99 cap and the 1/255 test, 15 flops (an FMA is 2), against the
+#   measured FMA rate x 2 flops;
+FLOPS_PER_EVAL = 15
+# - the kernel's count: dx, dy (2), the exponent with the conic pre-scaled (5), min with 0.99
+#   (1), the 1/255 test (1), 9 FP32 lane operations, against the measured FMA rate (one
+#   operation per lane and cycle).
 OPS_PER_EVAL = 9
-# per contribution: alpha*T, three colour FMAs, T update, the 1e-4 test
-OPS_PER_CONTRIB = 6
 PARAM_BYTES_PER_G = 12 + 16 + 12 + 4 + 192       # SH degree 3
-PROJ_BYTES_PER_G = 8 + 16 + 12 + 4 + 4 + 4 + 8
+# what the projection writes per Gaussian: the method's record (mean2d 8, conic + opacity 16,
+# rgb 12, depth 4, radius 4, tiles touched 4 = 48 B) ...
+PROJ_BYTES_METHOD = 8 + 16 + 12 + 4 + 4 + 4
+# ... and this implementation's (depth 4, tiles touched 4, tile rectangle 8, the 48-byte raster record)
+PROJ_BYTES_PER_G = 4 + 4 + 8 + 48
 
 
 def metric_name(cfg) -> str:
@@ -72,6 +83,10 @@ def parse():
     ap.add_argument("--no-toy", action="store_true")
     ap.add_argument("--batch-streams", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-single-thread", action="store_true", help="skip the one-thread oracle frame")
+    ap.add_argument("--configs", default="tiny,100k,1M,5M,stress",
+                    help="workloads of the configs block (every view of each); empty for none")
+    ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--clocks-csv", default=None,
                     help="keep the raw nvidia-smi samples of the timed region in this file "
                          "(a {rank} field is filled in); by default they go to a temporary file")
@@ -309,6 +324,201 @@ def run_reference(args, rank, world):
 
 # ----------------------------------------------------------------------------- our arm
 
+def fp32_peak_probe(torch, L, native, stream, dev):
+    """The measured FMA rate of this GPU: gs_fp32_peak_probe (16 independent FMA chains per
+    thread, 8 blocks of 256 threads per SM), scalar and packed, best of 5 timed launches each."""
+    import ctypes
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks = sms * 8
+    sink = torch.zeros(blocks * 256, device=dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    iters = 1 << 16
+    out = {"sms": sms, "blocks": blocks, "threads": 256, "chains": 16, "iterations": iters}
+    for packed in (0, 1):
+        n = ctypes.c_int64(0)
+
+        def launch():
+            native.check(L.gs_fp32_peak_probe(blocks, iters, packed, sink.data_ptr(), ctypes.byref(n), sp),
+                         "gs_fp32_peak_probe")
+        best = None
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                launch()
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                launch()
+                b.record(stream)
+                b.synchronize()
+                ms = a.elapsed_time(b)
+                best = ms if best is None else min(best, ms)
+        out["packed_f32x2" if packed else "scalar"] = {"ms": best, "fmas": n.value,
+                                                      "fma_per_s": n.value / (best * 1e-3)}
+    fma = max(out["scalar"]["fma_per_s"], out["packed_f32x2"]["fma_per_s"])
+    out["fma_per_s"] = fma
+    out["TFLOP/s"] = 2 * fma / 1e12          # an FMA is 2 flops
+    out["T_lane_ops/s"] = fma / 1e12         # one FMA per lane and cycle
+    del sink
+    return out
+
+
+def param_bytes(sh_degree: int) -> int:
+    return 4 * (3 + 4 + 3 + 1 + 3 * (sh_degree + 1) ** 2)
+
+
+def evaluation_count(torch, gs, g, cam, final_T, n_contrib, dev) -> int:
+    """The rasterizer's algorithmic count: over pixels, the list entries walked before T < 1e-4
+    (all of the tile's list, or n_contrib for a pixel that stopped). The per-tile list lengths
+    are recounted from the per-Gaussian tile rectangles (the sorted order is the oracle-checked
+    one) with a 2D difference array."""
+    tx, ty = gs.tiles_xy(cam)
+    p_dev = gs.preprocess(g, cam)
+    rect = p_dev["rect"].to(torch.int64) & 0xFFFF
+    tt = p_dev["tiles_touched"].to(torch.int64)
+    has = torch.nonzero(tt > 0).flatten()
+    diff = torch.zeros((ty + 1, tx + 1), dtype=torch.int64, device=dev)
+    rr = rect[has]
+    ones = torch.ones(rr.shape[0], dtype=torch.int64, device=dev)
+    diff.index_put_((rr[:, 1], rr[:, 0]), ones, accumulate=True)
+    diff.index_put_((rr[:, 1], rr[:, 2] + 1), -ones, accumulate=True)
+    diff.index_put_((rr[:, 3] + 1, rr[:, 0]), -ones, accumulate=True)
+    diff.index_put_((rr[:, 3] + 1, rr[:, 2] + 1), ones, accumulate=True)
+    cover = diff.cumsum(0).cumsum(1)[:ty, :tx]
+    lens = cover.cpu().numpy()
+    L_pix = np.kron(lens, np.ones((16, 16), np.int64))[: cam["height"], : cam["width"]]
+    nc = n_contrib.cpu().numpy().astype(np.int64)
+    Tf = final_T.cpu().numpy()
+    del p_dev
+    return int(np.where(Tf < 1e-4, nc, L_pix).sum())
+
+
+STAGE_NAMES = ["preprocess", "depth_order", "bin", "tile_sort", "ranges", "rasterize"]
+
+
+def measure_view(torch, gs, native, g, cam, r, stream, dev, steps, warmup, use_graph, world=1):
+    """One view: K graph-replayed frames of gs_render (the frame time), K more through
+    gs_render_profiled (per-stage CUDA-event times of the very launches a frame makes), and one
+    frame with the per-pixel outputs (the rasterizer's evaluation count)."""
+    import ctypes
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            r.render(cam, stream=stream, aux=False)
+        stream.synchronize()
+        st, flags, k = r.status(stream)
+        if st != native.GS_OK:
+            raise RuntimeError(f"render status {st} flags {flags} keys {k}")
+        graph = None
+        if use_graph:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                r.render(cam, stream=stream, aux=False)
+            for _ in range(3):
+                graph.replay()
+            stream.synchronize()
+    # --- the timed region: K whole frames, a barrier and a device synchronisation on both sides
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(40e6))
+        e0.record(stream)
+        for _ in range(steps):
+            if graph is not None:
+                graph.replay()
+            else:
+                r.render(cam, stream=stream, aux=False)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    frame_ms = e0.elapsed_time(e1) / steps
+    del graph
+
+    # --- per-stage times
+    L = gs.lib()
+    cs = gs.camera_struct(cam)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    n_stage = max(3, min(steps, 20))
+
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(STAGE_NAMES) + 1)]
+        for ev in evs:
+            ev.record(stream)   # creates the underlying CUDA event
+        arr = (ctypes.c_void_p * len(evs))(*[ctypes.c_void_p(ev.cuda_event) for ev in evs])
+        return evs, arr
+
+    def profiled(arr):
+        native.check(L.gs_render_profiled(ctypes.byref(r._gs), ctypes.byref(cs), r.key_capacity,
+                                          r.ws.data_ptr(), r.ws_bytes, r.image.data_ptr(), None, None, sp,
+                                          arr, len(arr)), "gs_render_profiled")
+
+    st_ms = {k: 0.0 for k in STAGE_NAMES}
+    with torch.cuda.stream(stream):
+        pool = [new_events() for _ in range(n_stage)]
+        for evs, arr in pool[:3]:
+            profiled(arr)
+        stream.synchronize()
+        # a fixed-length device sleep first, so the host queues frames ahead of the GPU
+        # and no stage time includes host launch latency
+        torch.cuda._sleep(int(40e6))
+        for evs, arr in pool:
+            profiled(arr)
+    torch.cuda.synchronize(dev)
+    for evs, _ in pool:
+        for i, k in enumerate(STAGE_NAMES):
+            st_ms[k] += evs[i].elapsed_time(evs[i + 1]) / n_stage
+    # --- one frame with the per-pixel outputs, for the evaluation count
+    with torch.cuda.stream(stream):
+        r.render(cam, stream=stream, aux=True)
+    torch.cuda.synchronize(dev)
+    st, flags, K = r.status(stream)
+    if st != native.GS_OK:
+        raise RuntimeError(f"render status {st} flags {flags} keys {K}")
+    evals = evaluation_count(torch, gs, g, cam, r.final_T, r.n_contrib, dev)
+    return {"frame_ms": frame_ms, "stage_ms": st_ms, "stage_steps": n_stage, "keys": int(K),
+            "evaluations": evals, "graph": use_graph}
+
+
+def stage_summary(st_ms, n, sh_degree, K, tiles_x, tiles_y, evals, hbm_peak, fp32):
+    """Per-stage achieved rates and roofline fractions. HBM-bound stages: algorithmic bytes per
+    unit (preprocess also in the method's count: parameters read + the 48-byte projected record
+    written). Rasterize: evaluations x 15 flops (the method's count) against the measured FMA
+    rate x 2, and evaluations x 9 FP32 lane operations (the kernel's count) against the measured
+    FMA rate."""
+    tile_bits = max(1, (tiles_x * tiles_y - 1).bit_length())
+    tpasses = (tile_bits + 7) // 8
+    pb = param_bytes(sh_degree)
+    stage_bytes = {
+        "preprocess": (pb + PROJ_BYTES_PER_G + 8) * n,   # + the depth keys and indices
+        "depth_order": 4 * 16 * n,
+        "bin": 24 * n + 8 * K,
+        "tile_sort": tpasses * 16 * K,
+        "ranges": 4 * K + 8 * tiles_x * tiles_y + 12 * tiles_x * tiles_y,   # + the launch order
+    }
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
+    out = {}
+    for k, b in stage_bytes.items():
+        out[k] = {"ms": st_ms[k], "bound": "hbm", "GB/s": gbs(b, st_ms[k]), "frac": gbs(b, st_ms[k]) / hbm_peak,
+                  "bytes": b}
+    mb = (pb + PROJ_BYTES_METHOD) * n
+    out["preprocess"].update({"bytes_method": mb, "GB/s_method": gbs(mb, st_ms["preprocess"]),
+                              "frac_method": gbs(mb, st_ms["preprocess"]) / hbm_peak})
+    ras_ms = st_ms["rasterize"]
+    flops = FLOPS_PER_EVAL * evals
+    lane_ops = OPS_PER_EVAL * evals
+    tf = flops / (ras_ms * 1e-3) / 1e12 if ras_ms > 0 else 0.0
+    lo = lane_ops / (ras_ms * 1e-3) / 1e12 if ras_ms > 0 else 0.0
+    out["rasterize"] = {"ms": ras_ms, "bound": "alu", "evaluations": evals,
+                        "flops": flops, "TFLOP/s": tf, "frac": tf / fp32["TFLOP/s"],
+                        "lane_ops": lane_ops, "T_lane_ops/s": lo, "frac_lane_ops": lo / fp32["T_lane_ops/s"]}
+    return out
+
+
 def run_ours(args, rank, local_rank, world):
     import torch
     import gaussian_splatting_tile_02_b300 as gs
@@ -326,95 +536,28 @@ def run_ours(args, rank, local_rank, world):
     g = gs.gaussians_to_device(scene, dev)
     r = gs.Renderer.for_scene(g, cam, headroom=1.1)
     stream = torch.cuda.Stream(device=dev)
-    K_keys = gs.Renderer.count_keys(g, cam)
+    L = gs.lib()
+    sp = None
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-
-    # --- warm-up and optional graph capture
-    with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            r.render(cam, stream=stream, aux=False)
-        stream.synchronize()
-        st, flags, k = r.status(stream)
-        if st != native.GS_OK:
-            raise RuntimeError(f"render status {st} flags {flags} keys {k}")
-        graph = None
-        if not args.no_graph:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                r.render(cam, stream=stream, aux=False)
-            for _ in range(3):
-                graph.replay()
-            stream.synchronize()
-
     hbm_peak, peak_kind, peaks = measured_peaks()
     sampler = ClockSampler(local_rank, args.clocks_csv.format(rank=rank) if args.clocks_csv else None)
     with sampler:
         time.sleep(0.3)
-        # --- main timed region: K whole frames
-        barrier()
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            torch.cuda._sleep(int(40e6))
-            e0.record(stream)
-            for _ in range(args.steps):
-                if graph is not None:
-                    graph.replay()
-                else:
-                    r.render(cam, stream=stream, aux=False)
-            e1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
-        frame_ms = e0.elapsed_time(e1) / args.steps
-        frame_ms_max = max_over_ranks(frame_ms, world, dev)
-
-        # --- per-stage times: K more frames through gs_render_profiled, which records
-        # CUDA events at the stage boundaries of the very launches a frame makes
-        stage_names = ["preprocess", "depth_order", "bin", "tile_sort", "ranges", "rasterize"]
-        st_ms = {k: 0.0 for k in stage_names}
-        import ctypes
-        L = gs.lib()
-        cs = gs.camera_struct(cam)
-        sp = ctypes.c_void_p(stream.cuda_stream)
-
-        def new_events():
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
-            for ev in evs:
-                ev.record(stream)   # creates the underlying CUDA event
-            arr = (ctypes.c_void_p * len(evs))(*[ctypes.c_void_p(ev.cuda_event) for ev in evs])
-            return evs, arr
-
-        def profiled(arr):
-            native.check(L.gs_render_profiled(ctypes.byref(r._gs), ctypes.byref(cs), r.key_capacity,
-                                              r.ws.data_ptr(), r.ws_bytes, r.image.data_ptr(), None, None, sp,
-                                              arr, len(arr)), "gs_render_profiled")
-
-        with torch.cuda.stream(stream):
-            pool = [new_events() for _ in range(args.steps)]
-            for evs, arr in pool[:3]:
-                profiled(arr)
-            stream.synchronize()
-            # a fixed-length device sleep first, so the host queues frames ahead of the GPU
-            # and no stage time includes host launch latency
-            torch.cuda._sleep(int(40e6))
-            for evs, arr in pool:
-                profiled(arr)
-        torch.cuda.synchronize(dev)
-        for evs, _ in pool:
-            for i, k in enumerate(stage_names):
-                st_ms[k] += evs[i].elapsed_time(evs[i + 1]) / args.steps
+        # --- the FP32 rate the compositing kernel is measured against
+        fp32 = fp32_peak_probe(torch, L, native, stream, dev)
+        # --- the headline workload (timed region inside, max over ranks)
+        head = measure_view(torch, gs, native, g, cam, r, stream, dev, args.steps, args.warmup,
+                            not args.no_graph, world)
+        frame_ms_max = max_over_ranks(head["frame_ms"], world, dev)
+        st_ms = head["stage_ms"]
         stage_total = sum(st_ms.values())
-        # one frame with the per-pixel outputs, for the rasterizer's evaluation count
-        with torch.cuda.stream(stream):
-            r.render(cam, stream=stream, aux=True)
-        torch.cuda.synchronize(dev)
-        fT, ncon = r.final_T, r.n_contrib
-        ranges = torch.empty(0)
+        import ctypes
+        sp = ctypes.c_void_p(stream.cuda_stream)
         tx, ty = gs.tiles_xy(cam)
 
         # --- end to end from host memory
@@ -590,61 +733,63 @@ def run_ours(args, rank, local_rank, world):
             toy = {"steps": 200, "seconds": time.perf_counter() - t0, "mse_first": fit["losses"][0],
                    "mse_final": fit["final_mse"]}
             toy["steps_per_s"] = 200 / toy["seconds"]
+        # --- every workload of the benchmark, each view (one GPU only)
+        configs = None
+        if world == 1 and not args.no_configs:
+            configs = {}
+            names = [c for c in args.configs.split(",") if c]
+            for name in names:
+                if name == args.config and len(cams) == 1:
+                    cfg_n, views = cfg, [(0, cam, head)]
+                    g_n = g
+                else:
+                    cfg_n = scenes.CONFIGS[name]
+                    sc = scenes.make_scene(cfg_n)
+                    cams_n = scenes.make_cameras(cfg_n)
+                    g_n = gs.gaussians_to_device(sc, dev)
+                    del sc
+                    r_n = gs.Renderer.for_scene(g_n, cams_n, headroom=1.1)
+                    views = []
+                    for v, c in enumerate(cams_n):
+                        views.append((v, c, measure_view(torch, gs, native, g_n, c, r_n, stream, dev, args.steps,
+                                                         args.warmup, not args.no_graph)))
+                    del r_n
+                recs = []
+                for v, c, m in views:
+                    ctx, cty = gs.tiles_xy(c)
+                    recs.append({"view": v, "frame_ms": m["frame_ms"], "fps": 1e3 / m["frame_ms"], "keys": m["keys"],
+                                 "stages": stage_summary(m["stage_ms"], cfg_n.n, cfg_n.sh_degree, m["keys"], ctx, cty,
+                                                         m["evaluations"], hbm_peak, fp32)})
+                mean_ms = statistics.mean(x["frame_ms"] for x in recs)
+                mean_st = {}
+                for k in recs[0]["stages"]:
+                    mean_st[k] = {kk: statistics.mean(x["stages"][k][kk] for x in recs)
+                                  for kk in recs[0]["stages"][k] if isinstance(recs[0]["stages"][k][kk], (int, float))}
+                configs[name] = {"workload": cfg_n.description, "n": cfg_n.n, "width": cfg_n.width,
+                                 "height": cfg_n.height, "sh_degree": cfg_n.sh_degree, "steps": args.steps,
+                                 "views": recs,
+                                 "mean": {"frame_ms": mean_ms, "fps": 1e3 / mean_ms, "stages": mean_st}}
+                if g_n is not g:
+                    del g_n
+                torch.cuda.empty_cache()
     clocks = sampler.summary()
 
-    # --- algorithmic work of the last frame (from its outputs)
-    # per-tile list lengths: the sorted order is the oracle-checked one, so the
-    # ranges can be recounted from the per-Gaussian tile rectangles on the device
-    p_dev = gs.preprocess(g, cam)
-    rect = p_dev["rect"].to(torch.int64) & 0xFFFF
-    tt = p_dev["tiles_touched"].to(torch.int64)
-    has = torch.nonzero(tt > 0).flatten()
-    # rectangle coverage counts per tile via a 2D difference array
-    diff = torch.zeros((ty + 1, tx + 1), dtype=torch.int64, device=dev)
-    rr = rect[has]
-    ones = torch.ones(rr.shape[0], dtype=torch.int64, device=dev)
-    diff.index_put_((rr[:, 1], rr[:, 0]), ones, accumulate=True)
-    diff.index_put_((rr[:, 1], rr[:, 2] + 1), -ones, accumulate=True)
-    diff.index_put_((rr[:, 3] + 1, rr[:, 0]), -ones, accumulate=True)
-    diff.index_put_((rr[:, 3] + 1, rr[:, 2] + 1), ones, accumulate=True)
-    cover = diff.cumsum(0).cumsum(1)[:ty, :tx]
-    lens = cover.cpu().numpy()
-    L_pix = np.kron(lens, np.ones((16, 16), np.int64))[: cam["height"], : cam["width"]]
-    nc = ncon.cpu().numpy().astype(np.int64)
-    Tf = fT.cpu().numpy()
-    evals = int(np.where(Tf < 1e-4, nc, L_pix).sum())
     n = int(g["n"])
-    K = K_keys
-    tile_bits = max(1, (tx * ty - 1).bit_length())
-    tpasses = (tile_bits + 7) // 8
+    K = head["keys"]
+    stages_out = stage_summary(st_ms, n, cfg.sh_degree, K, tx, ty, head["evaluations"], hbm_peak, fp32)
     launches_per_frame = frame_launches(tx * ty)
-    ras_ms = st_ms["rasterize"]
-    clk = clocks.get("sm_mhz") or SM_MAX_MHZ
-    fp32_peak = SM_COUNT * FP32_LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12     # T lane-ops/s at max clock
-    ras_ops = OPS_PER_EVAL * evals
-    ras_achieved = ras_ops / (ras_ms * 1e-3) / 1e12
-    stage_bytes = {
-        "preprocess": (PARAM_BYTES_PER_G + PROJ_BYTES_PER_G + 8) * n,   # + the depth keys and indices
-        "depth_order": 4 * 16 * n,
-        "bin": 24 * n + 8 * K,
-        "tile_sort": tpasses * 16 * K,
-        "ranges": 4 * K + 8 * tx * ty + 12 * tx * ty,   # + the launch order: ranges read, order written
-    }
-    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
-    stages_out = {}
-    for k, b in stage_bytes.items():
-        stages_out[k] = {"ms": st_ms[k], "bound": "hbm", "GB/s": gbs(b, st_ms[k]),
-                         "frac": gbs(b, st_ms[k]) / hbm_peak, "bytes": b}
-    stages_out["rasterize"] = {"ms": ras_ms, "bound": "alu", "Top/s": ras_achieved, "frac": ras_achieved / fp32_peak,
-                               "evaluations": evals, "ops": ras_ops,
-                               "frac_at_sampled_clock": ras_achieved / (fp32_peak * clk / SM_MAX_MHZ)}
+    ras = stages_out["rasterize"]
+    evals = head["evaluations"]
     dominant = max(stages_out, key=lambda k: stages_out[k]["ms"])
     if dominant == "rasterize":
-        roof = {"kernel": "rasterize_kernel", "bound": "alu", "achieved": ras_achieved, "peak": fp32_peak,
-                "unit": "T FP32 lane-ops/s", "frac": ras_achieved / fp32_peak,
-                "peak_kind": f"derived: {SM_COUNT} SMs x {FP32_LANES_PER_SM} FP32 lanes x {SM_MAX_MHZ:.0f} MHz",
+        roof = {"kernel": "rasterize_kernel", "bound": "alu", "achieved": ras["TFLOP/s"], "peak": fp32["TFLOP/s"],
+                "unit": "TFLOP/s", "frac": ras["frac"],
+                "peak_kind": "measured: FFMA probe (gs_fp32_peak_probe), 2 flops per FMA, of measured",
                 "traffic": traffic_from_profile("rasterize_1M.md", args.config),
-                "units": f"{evals} pixel-Gaussian evaluations x {OPS_PER_EVAL} FP32 ops"}
+                "units": f"{evals} pixel-Gaussian evaluations x {FLOPS_PER_EVAL} flops",
+                "lane_ops": {"achieved": ras["T_lane_ops/s"], "peak": fp32["T_lane_ops/s"], "frac": ras["frac_lane_ops"],
+                             "unit": "T FP32 lane-ops/s",
+                             "units": f"{evals} evaluations x {OPS_PER_EVAL} FP32 lane operations"}}
     else:
         d = stages_out[dominant]
         roof = {"kernel": dominant, "bound": "hbm", "achieved": d["GB/s"], "peak": hbm_peak, "unit": "GB/s",
@@ -657,7 +802,7 @@ def run_ours(args, rank, local_rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": cfg.description, "n": cfg.n, "width": cfg.width, "height": cfg.height,
                    "sh_degree": cfg.sh_degree, "view": args.view, "keys": K, "key_capacity": r.key_capacity,
-                   "graph": graph is not None,
+                   "graph": not args.no_graph,
                    "l2": "inputs larger than L2: 236 MB of Gaussian parameters per frame (L2 126 MB)",
                    "parallelism": f"replicas x{world}"},
         "clocks": clocks,
@@ -667,10 +812,12 @@ def run_ours(args, rank, local_rank, world):
         "stages": stages_out,
         "stage_sum_ms": stage_total,
         "hbm_peak_gbs": hbm_peak,
-        "backward": backward_summary(bwd, int(g["n"]), hbm_peak, fp32_peak),
+        "fp32_peak_measured": fp32,
+        "backward": backward_summary(bwd, int(g["n"]), hbm_peak, fp32["T_lane_ops/s"]),
         "batch": batch,
         "densify": densify_summary(dens, cfg.sh_degree, hbm_peak),
         "toy2d": toy,
+        "configs": configs,
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -687,6 +834,16 @@ def run_ours(args, rank, local_rank, world):
         dt = time.perf_counter() - t0
         result["cpu_baseline"] = {"value": frames / dt, "unit": "frames/s", "cores": cores, "kind": "oracle",
                                   "sample": f"{frames} full frame(s) of this workload, all stages, fp64"}
+        if not args.no_single_thread:
+            # the same oracle on one thread, one full frame
+            oracle.set_threads(1)
+            t0 = time.perf_counter()
+            oracle.render(scene, cam)
+            dt1 = time.perf_counter() - t0
+            oracle.set_threads(cores)
+            result["cpu_baseline"]["single_thread"] = {
+                "value": 1.0 / dt1, "unit": "frames/s", "cores": 1,
+                "sample": "1 full frame of this workload, all stages, fp64, one thread"}
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -288,6 +288,21 @@ def read_status(ws, stream=None) -> tuple:
 
 # ------------------------------------------------------------------------------ whole frame
 
+def workspace_lists(ws, n: int, width: int, height: int, key_capacity: int, num_keys: int) -> tuple:
+    """(sorted_vals [num_keys] int32, ranges [tiles, 2] int32): views into a gs_render workspace
+    tensor (uint8) of the frame's per-tile lists, located by gs_render_workspace_lists."""
+    vp, rp = ctypes.c_void_p(), ctypes.c_void_p()
+    check(lib().gs_render_workspace_lists(_ptr(ws), int(n), int(width), int(height), int(key_capacity),
+                                          ctypes.byref(vp), ctypes.byref(rp)), "gs_render_workspace_lists")
+    base = ws.data_ptr()
+    num_keys = min(int(num_keys), int(key_capacity))
+    tx, ty = (int(width) + 15) // 16, (int(height) + 15) // 16
+    vo, ro = vp.value - base, rp.value - base
+    vals = ws[vo: vo + 4 * int(num_keys)].view(_torch().int32)
+    ranges = ws[ro: ro + 8 * tx * ty].view(_torch().int32).view(tx * ty, 2)
+    return vals, ranges
+
+
 class Renderer:
     """Owns a device copy of a scene and a gs_render workspace sized for it."""
 
@@ -332,6 +347,11 @@ class Renderer:
 
     def status(self, stream=None) -> tuple:
         return read_status(self.ws, stream)
+
+    def lists(self, stream=None) -> tuple:
+        """(sorted_vals [K], ranges [tiles, 2]) of the last frame (synchronises the stream)."""
+        K = self.status(stream)[2]
+        return workspace_lists(self.ws, int(self.g["n"]), self.width, self.height, self.key_capacity, K)
 
     def render_backward(self, cam: dict, grad_image, grads: dict | None = None, stream=None) -> dict:
         """Parameter gradients of sum(grad_image * image) for the frame last
@@ -394,6 +414,12 @@ class BatchRenderer:
     def status(self, view: int, stream=None) -> tuple:
         """(status, flags, num_keys) of one view; synchronises the stream."""
         return read_status(self.ws[view * self.view_ws_bytes:], stream)
+
+    def lists(self, view: int, stream=None) -> tuple:
+        """(sorted_vals [K], ranges [tiles, 2]) of one view of the last batch (synchronises the stream)."""
+        K = self.status(view, stream)[2]
+        w = self.ws[view * self.view_ws_bytes: (view + 1) * self.view_ws_bytes]
+        return workspace_lists(w, int(self.g["n"]), self.width, self.height, self.key_capacity, K)
 
 
 class HostPipeline:

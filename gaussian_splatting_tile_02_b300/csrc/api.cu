@@ -377,6 +377,17 @@ gs_status gs_render(const gs_gaussians* g, const gs_camera* cam, int64_t key_cap
     return render_impl(g, cam, key_capacity, ws, ws_bytes, image, final_T, n_contrib, stream, nullptr);
 }
 
+gs_status gs_render_workspace_lists(const void* ws, int64_t n, int32_t width, int32_t height, int64_t key_capacity,
+                                    const uint32_t** sorted_vals, const uint32_t** ranges) {
+    if (!ws || !aligned(ws, kAlign)) return GS_ERR_WORKSPACE;
+    if (n < 0 || width < 1 || height < 1 || key_capacity < 0 || !sorted_vals || !ranges) return GS_ERR_INVALID_ARG;
+    const RenderLayout L = render_layout(n, width, height, key_capacity);
+    const char* w = static_cast<const char*>(ws);
+    *sorted_vals = reinterpret_cast<const uint32_t*>(w + L.vals);
+    *ranges = reinterpret_cast<const uint32_t*>(w + L.ranges);
+    return GS_OK;
+}
+
 gs_status gs_render_profiled(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, void* ws,
                              size_t ws_bytes, float* image, float* final_T, uint32_t* n_contrib, void* stream,
                              void* const* events, int32_t n_events) {

@@ -287,6 +287,19 @@ gs_status gs_render(const gs_gaussians* gaussians, const gs_camera* camera, int6
                     void* ws, size_t ws_bytes, float* image, float* final_T,
                     uint32_t* n_contrib, void* stream);
 
+/* Where a gs_render (or one view of gs_render_batch) workspace keeps the
+ * frame's per-tile lists: *sorted_vals receives the device address of the
+ * Gaussian indices sorted by (tile, depth bits, index) -- its first K entries
+ * are valid after a frame, K as gs_read_status reports it -- and *ranges that
+ * of the tile ranges (uint32 [tiles_y * tiles_x][2], [start, end) into the
+ * sorted list). n, width, height and key_capacity must be those the workspace
+ * was sized with (gs_render_workspace_bytes). Host-only arithmetic on ws; no
+ * CUDA call. The lists are the ones the pages' step "Depth-sort per tile"
+ * produces (section "Rastérisation, non rayée"). */
+gs_status gs_render_workspace_lists(const void* ws, int64_t n, int32_t width, int32_t height,
+                                    int64_t key_capacity, const uint32_t** sorted_vals,
+                                    const uint32_t** ranges);
+
 /* gs_render that also records CUDA events at its stage boundaries, for
  * per-stage timing of the very launches a frame makes. events[0..6] are
  * caller-created cudaEvent_t handles (as void*), recorded on `stream`:
@@ -525,6 +538,18 @@ gs_status gs_read_status(const void* ws, void* stream, uint32_t* flags, uint64_t
  *       the device. */
 size_t gs_workspace_bytes(int64_t n, int32_t width, int32_t height, int64_t key_capacity);
 gs_status gs_last_device_status(const void* ws);
+
+/* FP32 peak probe (a measurement utility; the pages have no counterpart). The
+ * compositing step is bound by FP32 issue, so its roofline needs the rate of
+ * fused multiply-adds the device sustains. This launches `blocks` blocks of
+ * 256 threads; each thread runs 16 independent FMA chains for `iterations`
+ * steps, as one fma.rn.f32 per chain and step, or with packed != 0 as one
+ * fma.rn.f32x2 per pair of chains. *fma_count (host, may be NULL) receives the
+ * number of FMAs the launch executes (2 flops each). Time it with events on
+ * `stream`. sink: device float[blocks * 256], never written in practice.
+ * 1 <= blocks <= 2^20, iterations >= 1. */
+gs_status gs_fp32_peak_probe(int32_t blocks, int32_t iterations, int32_t packed, float* sink,
+                             int64_t* fma_count, void* stream);
 
 /* Upper bound on the wait of every device-side spin (look-back of the radix
  * sort), in polling iterations; <= 0 restores the default (about a second).

@@ -60,6 +60,35 @@ def test_workspace_sizes():
         assert L.gs_workspace_bytes(*args) == L.gs_render_workspace_bytes(*args)
 
 
+def test_workspace_lists_lie_inside_the_workspace():
+    """gs_render_workspace_lists is host arithmetic: the sorted list and the ranges sit inside
+    the workspace, 256-byte aligned, apart from each other, with room for capacity and tiles."""
+    L = native.lib()
+    base = 1 << 30
+    for n, w, h, cap in ((1000, 64, 64, 5000), (10**6, 1920, 1080, 3 * 10**6), (0, 1, 1, 0)):
+        size = L.gs_render_workspace_bytes(n, w, h, cap)
+        vp, rp = ctypes.c_void_p(), ctypes.c_void_p()
+        assert L.gs_render_workspace_lists(base, n, w, h, cap, ctypes.byref(vp), ctypes.byref(rp)) == native.GS_OK
+        tiles = ((w + 15) // 16) * ((h + 15) // 16)
+        v, r = vp.value - base, rp.value - base
+        assert v % 256 == 0 and r % 256 == 0
+        assert 0 < v and v + 4 * cap <= size and 0 < r and r + 8 * tiles <= size
+        assert v + 4 * cap <= r or r + 8 * tiles <= v
+    vp, rp = ctypes.c_void_p(), ctypes.c_void_p()
+    assert L.gs_render_workspace_lists(None, 10, 64, 64, 10, ctypes.byref(vp), ctypes.byref(rp)) == \
+        native.GS_ERR_WORKSPACE
+    assert L.gs_render_workspace_lists(base, -1, 64, 64, 10, ctypes.byref(vp), ctypes.byref(rp)) == \
+        native.GS_ERR_INVALID_ARG
+
+
+def test_fp32_peak_probe_rejects_bad_arguments():
+    L = native.lib()
+    n = ctypes.c_int64(0)
+    assert L.gs_fp32_peak_probe(0, 10, 0, 256, ctypes.byref(n), None) == native.GS_ERR_INVALID_ARG
+    assert L.gs_fp32_peak_probe(4, 0, 0, 256, ctypes.byref(n), None) == native.GS_ERR_INVALID_ARG
+    assert L.gs_fp32_peak_probe(4, 10, 1, None, ctypes.byref(n), None) == native.GS_ERR_INVALID_ARG
+
+
 def test_last_device_status_rejects_a_missing_or_misaligned_workspace():
     L = native.lib()
     assert L.gs_last_device_status(None) == native.GS_ERR_WORKSPACE

@@ -29,15 +29,36 @@ def cuda_only():
 
 
 _SCENES = {}
+_BATCH = {}
 
 
 def scene_of(name, n=None):
     key = (name, n)
     if key not in _SCENES:
         _SCENES.clear()
+        _BATCH.clear()
         s = scenes.make_scene(name, n=n)
         _SCENES[key] = (s, gs.gaussians_to_device(s))
     return _SCENES[key]
+
+
+def batch_of(name):
+    """gs_render_batch of every view of a full-size workload, rendered once and kept on the
+    device while that workload's parametrized cases run (the views share one projection pass
+    and run on four streams)."""
+    if name not in _BATCH:
+        _BATCH.clear()
+        _, g = scene_of(name)
+        br = gs.BatchRenderer.for_scene(g, scenes.make_cameras(name), headroom=1.05, n_streams=4)
+        br.render(aux=True)
+        torch.cuda.synchronize()
+        _BATCH[name] = br
+    return _BATCH[name]
+
+
+# the multi-view workloads, whose views are also rendered by gs_render_batch and checked
+# against the same oracle frame
+BATCH_WORKLOADS = ("5M", "stress")
 
 
 def run_stages(g, cam, capacity=None):
@@ -137,6 +158,8 @@ CASES = [("tiny", 0), ("100k", 0), ("1M", 0)] + [("5M", i) for i in range(4)] + 
 
 @pytest.mark.parametrize("name,view", CASES, ids=[f"{n}-v{v}" for n, v in CASES])
 def test_full_path_parity(oracle_mod, name, view):
+    """The staged path, stage by stage, against the oracle; for the multi-view workloads also
+    the batched call's view (gs_render_batch) against the same oracle frame."""
     scene, g = scene_of(name)
     cam = scenes.make_cameras(name)[view]
     out = run_stages(g, cam)
@@ -148,6 +171,19 @@ def test_full_path_parity(oracle_mod, name, view):
     stats = check_image(oracle_mod, ref, cam, out["image"], out["final_T"], out["n_contrib"])
     print(name, view, "K", out["K"], stats)
     assert_image_parity(stats)
+    if name in BATCH_WORKLOADS:
+        # the batched call (gs_render_batch, all views of the workload in one call) against the
+        # oracle, element by element: its per-tile lists, ranges and image for this view
+        br = batch_of(name)
+        st, flags, K = br.status(view)
+        assert st == native.GS_OK and K == ref["num_keys"], (st, flags, K)
+        vals, ranges = br.lists(view)
+        np.testing.assert_array_equal(vals.cpu().numpy().view(np.uint32), ref["sorted_vals"])
+        np.testing.assert_array_equal(ranges.cpu().numpy().view(np.uint32), ref["ranges"])
+        bstats = check_image(oracle_mod, ref, cam, br.images[view].cpu().numpy(), br.final_T[view].cpu().numpy(),
+                             br.n_contrib[view].cpu().numpy())
+        print(name, view, "batch", bstats)
+        assert_image_parity(bstats)
 
 
 def test_render_equals_stages_and_graph_replay(oracle_mod):
@@ -160,6 +196,9 @@ def test_render_equals_stages_and_graph_replay(oracle_mod):
     torch.cuda.synchronize()
     st, flags, K = r.status()
     assert st == native.GS_OK and K == out["K"]
+    vals, ranges = r.lists()
+    np.testing.assert_array_equal(vals.cpu().numpy().view(np.uint32), out["sorted_vals"])
+    np.testing.assert_array_equal(ranges.cpu().numpy().view(np.uint32), out["ranges"])
     np.testing.assert_array_equal(r.image.cpu().numpy(), out["image"])
     np.testing.assert_array_equal(r.final_T.cpu().numpy(), out["final_T"])
     np.testing.assert_array_equal(r.n_contrib.cpu().numpy(), out["n_contrib"])
@@ -346,6 +385,27 @@ def test_sort_random_keys(oracle_mod, count, bits):
     sk, sv = oracle_mod.sort_pairs(keys, np.arange(count, dtype=np.uint32))   # stable: ties by position
     np.testing.assert_array_equal(kd[:count].cpu().numpy().view(np.uint64), sk)
     np.testing.assert_array_equal(vd[:count].cpu().numpy().view(np.uint32), vals[sv])
+
+
+def test_fp32_peak_probe_runs_and_counts_its_fmas():
+    """The FP32 peak probe: both forms run, report blocks x 256 threads x iterations x 16 FMAs,
+    and leave the sink untouched; a longer run takes longer (the work is not dropped)."""
+    L = native.lib()
+    sink = torch.full((8 * 256,), 7.0, device="cuda")
+    for packed in (0, 1):
+        times = []
+        for iters in (1 << 12, 1 << 15):
+            n = ctypes.c_int64(0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            native.check(L.gs_fp32_peak_probe(8, iters, packed, sink.data_ptr(), ctypes.byref(n), None), "probe")
+            a.record()
+            native.check(L.gs_fp32_peak_probe(8, iters, packed, sink.data_ptr(), ctypes.byref(n), None), "probe")
+            b.record()
+            torch.cuda.synchronize()
+            assert n.value == 8 * 256 * iters * 16
+            times.append(a.elapsed_time(b))
+        assert times[1] > 3 * times[0], times
+    assert (sink == 7.0).all()
 
 
 def test_bounded_wait_times_out():
