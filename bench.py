@@ -207,14 +207,21 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0) for r in rows)}
 
 
+def sort_launches(key_bits: int) -> int:
+    """Kernels of one 32-bit sort: the digit bases, one pass per 8-bit digit, a copy back after
+    an odd pass count."""
+    passes = (key_bits + 7) // 8
+    return 1 + passes + passes % 2
+
+
 def frame_launches(tiles: int) -> int:
     """Kernels one gs_render frame launches for an image of `tiles` 16x16 tiles: preprocess
-    (which also writes the depth keys); sort bases and 4 depth passes; 5 binning kernels;
-    sort bases and one pass per 8 tile-id bits, plus a copy back after an odd pass count;
-    ranges; tile order; rasterize."""
+    (which also writes the depth keys); the depth sort (4 passes); 5 binning kernels; the
+    tile-id sort; ranges; the tile order (count and scatter kernels up to 186 blocks of 256
+    tiles, one kernel beyond); rasterize."""
     tile_bits = max(1, (tiles - 1).bit_length())
-    passes = (tile_bits + 7) // 8
-    return 1 + (1 + 4) + 5 + (1 + passes + passes % 2) + 1 + 1 + 1
+    order = 2 if -(-tiles // 256) <= 186 else 1
+    return 1 + sort_launches(32) + 5 + sort_launches(tile_bits) + 1 + order + 1
 
 
 def code_hash(files) -> str:

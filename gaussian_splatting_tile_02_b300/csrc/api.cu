@@ -114,7 +114,7 @@ RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
     L.vals_alt = take(4 * uc);
     L.sort = take(sort_scratch_bytes(cap > n ? cap : n));
     L.ranges = take(8 * tiles);
-    L.tile_order = take(4 * tiles);
+    L.tile_order = take(tile_order_scratch_bytes((int)tiles));
     L.pgrad = take(36 * un);   // backward: dL/d(u, v), dL/d(conic), dL/do, dL/dc
     L.total = o;
     return L;
@@ -192,7 +192,7 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
     cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
     if (e == cudaSuccess && step1 == Step1::kProject) e = sort_prepare_histogram(sort_ws, s);
     if (e == cudaSuccess) e = mark(0);
-    if (e == cudaSuccess && step1 == Step1::kProject) e = launch_preprocess(*g, cc, p, s, &dk);
+    if (e == cudaSuccess && step1 == Step1::kProject) e = launch_preprocess(*g, cc, p, s, &dk, header);
     if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess && step1 == Step1::kRecordOnly) {
         e = sort_prepare_histogram(sort_ws, s);
@@ -213,8 +213,8 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
     if (e == cudaSuccess) e = mark(4);
     if (e == cudaSuccess)
         e = launch_tile_ranges32(keys, num_keys, key_capacity, cc.tiles_x * cc.tiles_y, ranges, s);
-    auto* tile_order = reinterpret_cast<uint32_t*>(w + L.tile_order);
-    if (e == cudaSuccess) e = launch_tile_order(ranges, cc.tiles_x * cc.tiles_y, tile_order, s);
+    uint32_t* tile_order = nullptr;
+    if (e == cudaSuccess) e = launch_tile_order_multi(ranges, cc.tiles_x * cc.tiles_y, w + L.tile_order, &tile_order, s);
     if (e == cudaSuccess) e = mark(5);
     if (e == cudaSuccess)
         e = launch_rasterize(p, g->n, vals, ranges, tile_order, cc, image, final_T, n_contrib, s);

@@ -124,6 +124,51 @@ __device__ __forceinline__ void raise_flag(StatusHeader* h, uint32_t flag, uint3
     if (flag == GS_FLAG_TIMEOUT) atomicMax(&h->timeout_site, site);
 }
 
+// ---------------------------------------------------------------- bulk copies
+// One-dimensional bulk copies from global to shared memory (cp.async.bulk,
+// the TMA unit's untiled form), completed on a shared-memory mbarrier that
+// counts the bytes still to land. Source and destination 16-byte aligned, size
+// a multiple of 16 bytes. The copies read this GPU's own memory only.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// makes an initialised barrier visible to the copy engine (then a __syncthreads)
+__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+// orders this thread's earlier shared-memory accesses before later bulk copies into them
+__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Bound on the wait for a bulk copy to land, in polls. A copy from valid global
+// memory always lands, so this bound is fixed and generous (it is not the
+// adjustable bound on waits for other blocks' progress): a block never leaves
+// while its copies are in flight unless the copy engine has failed.
+constexpr long long kBulkWaitLimit = 1ll << 24;
+// Waits for the phase of the given parity to complete; false once `limit` polls ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit) {
+    for (long long it = 0; it < limit; it++)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
 // ---------------------------------------------------------------- launchers
 
 // preprocess.cu
@@ -135,8 +180,11 @@ struct DepthKeysOut {
     uint32_t* vals;
     uint32_t* hist;
 };
+// status (nullable): with a status header the parameters are staged through
+// shared memory by bulk copies when their arrays allow it (16-byte aligned);
+// a bulk copy that did not land within kBulkWaitLimit polls sets GS_FLAG_TIMEOUT.
 cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const gs_projected& out, cudaStream_t s,
-                              const DepthKeysOut* dk = nullptr);
+                              const DepthKeysOut* dk = nullptr, StatusHeader* status = nullptr);
 
 // binning.cu
 size_t bin_scratch_bytes(int64_t n);
@@ -207,6 +255,11 @@ cudaError_t launch_preprocess_backward(const gs_gaussians& g, const CamConst& ca
 // Heavy-first launch order of the tiles from their ranges: tile_order[tiles]
 // receives a permutation of the tile indices, longest lists first.
 cudaError_t launch_tile_order(const uint32_t* ranges, int tiles, uint32_t* tile_order, cudaStream_t s);
+// The same order from many blocks, into scratch of tile_order_scratch_bytes(tiles)
+// bytes (the order itself first, *tile_order points at it).
+size_t tile_order_scratch_bytes(int tiles);
+cudaError_t launch_tile_order_multi(const uint32_t* ranges, int tiles, void* scratch, uint32_t** tile_order,
+                                    cudaStream_t s);
 // tile_order (nullable): a launch order written by launch_tile_order; null
 // launches the tiles in index order (same image)
 cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* sorted_vals, const uint32_t* ranges,

@@ -141,20 +141,8 @@ constexpr float kY3e = 1.4453057213202769f;
 // -x; band 2 all +); band 3 (not printed) uses the band-1 pattern, odd m
 // negative.
 template <int D>
-__device__ __forceinline__ float3 eval_sh(const float* __restrict__ c, float x, float y, float z) {
+__device__ __forceinline__ float3 eval_sh(const float* co, float x, float y, float z) {
     constexpr int NK = (D + 1) * (D + 1);
-    float co[NK * 3];
-    if constexpr (D == 3 || D == 1) {
-        const float4* c4 = reinterpret_cast<const float4*>(c);
-#pragma unroll
-        for (int i = 0; i < NK * 3 / 4; i++) {
-            float4 q = __ldg(c4 + i);
-            co[4 * i] = q.x; co[4 * i + 1] = q.y; co[4 * i + 2] = q.z; co[4 * i + 3] = q.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < NK * 3; i++) co[i] = __ldg(c + i);
-    }
     float Y[NK];
     Y[0] = kY0;
     if constexpr (D >= 1) {
@@ -189,6 +177,25 @@ __device__ __forceinline__ float3 eval_sh(const float* __restrict__ c, float x, 
     return make_float3(fmaxf(r, 0.0f), fmaxf(g, 0.0f), fmaxf(b, 0.0f));
 }
 
+// The (D + 1)^2 x 3 SH coefficients of one Gaussian into registers, from
+// global memory (read-only path) or from a shared-memory stage; rows of
+// 12 or 48 floats (D = 1, 3) as float4 loads.
+template <int D, bool kShared>
+__device__ __forceinline__ void load_sh(const float* __restrict__ c, float* co) {
+    constexpr int NK3 = (D + 1) * (D + 1) * 3;
+    if constexpr (D == 3 || D == 1) {
+        const float4* c4 = reinterpret_cast<const float4*>(c);
+#pragma unroll
+        for (int i = 0; i < NK3 / 4; i++) {
+            const float4 q = kShared ? c4[i] : __ldg(c4 + i);
+            co[4 * i] = q.x; co[4 * i + 1] = q.y; co[4 * i + 2] = q.z; co[4 * i + 3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < NK3; i++) co[i] = kShared ? c[i] : __ldg(c + i);
+    }
+}
+
 struct PreArgs {
     const float* means;
     const float4* quats;
@@ -212,13 +219,50 @@ struct PreArgs {
     uint32_t* dkeys;
     uint32_t* dvals;
     uint32_t* dhist;
+    // staged kernel only: where a bulk copy that did not land is reported
+    StatusHeader* header;
+};
+
+// Where preprocess_one reads a Gaussian's parameters: the caller's arrays in
+// global memory, or a block's shared-memory stage of them (same layouts,
+// indexed from the stage's first Gaussian).
+struct GlobalIn {
+    const PreArgs& a;
+    int64_t g;
+    __device__ float mean(int k) const { return __ldg(a.means + 3 * g + k); }
+    __device__ float4 quat() const { return __ldg(a.quats + g); }
+    __device__ float log_scale(int k) const { return __ldg(a.log_scales + 3 * g + k); }
+    __device__ float logit() const { return __ldg(a.logits + g); }
+    template <int D>
+    __device__ void sh(float* co) const {
+        load_sh<D, false>(a.sh + g * (D + 1) * (D + 1) * 3, co);
+    }
+};
+struct SharedIn {
+    const float* means;
+    const float4* quats;
+    const float* log_scales;
+    const float* logits;
+    const float* shs;
+    int i;
+    uint64_t* sh_bar;     // the SH rows land on their own barrier, waited for here
+    uint32_t parity;
+    __device__ float mean(int k) const { return means[3 * i + k]; }
+    __device__ float4 quat() const { return quats[i]; }
+    __device__ float log_scale(int k) const { return log_scales[3 * i + k]; }
+    __device__ float logit() const { return logits[i]; }
+    template <int D>
+    __device__ void sh(float* co) const {
+        mbar_wait_bounded(sh_bar, parity, kBulkWaitLimit);   // a failure is recorded by the block after the chunk
+        load_sh<D, true>(shs + i * (D + 1) * (D + 1) * 3, co);
+    }
 };
 
 // One Gaussian seen by one camera; returns its depth-order key.
-template <int D>
-__device__ __forceinline__ uint32_t preprocess_one(const PreArgs& a, int64_t g) {
+template <int D, typename In>
+__device__ __forceinline__ uint32_t preprocess_one(const PreArgs& a, int64_t g, const In& in) {
     const CamConst& C = a.cam;
-    const float m0 = __ldg(a.means + 3 * g), m1 = __ldg(a.means + 3 * g + 1), m2 = __ldg(a.means + 3 * g + 2);
+    const float m0 = in.mean(0), m1 = in.mean(1), m2 = in.mean(2);
 
     float p[3];
 #pragma unroll
@@ -230,7 +274,7 @@ __device__ __forceinline__ uint32_t preprocess_one(const PreArgs& a, int64_t g) 
     bool ok = z > C.near_z;
     float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
     if (ok) {
-        q = __ldg(a.quats + g);
+        q = in.quat();
     }
     const float n2 = add(add(add(mul(q.x, q.x), mul(q.y, q.y)), mul(q.z, q.z)), mul(q.w, q.w));
     ok = ok && n2 > 0.0f && n2 <= FLT_MAX;
@@ -259,7 +303,7 @@ __device__ __forceinline__ uint32_t preprocess_one(const PreArgs& a, int64_t g) 
     }
     float s[3];
 #pragma unroll
-    for (int k = 0; k < 3; k++) s[k] = exp32(__ldg(a.log_scales + 3 * g + k));
+    for (int k = 0; k < 3; k++) s[k] = exp32(in.log_scale(k));
     float Arot[9], B[9];   // Arot = W R (the Gaussian's axes in camera space), B = Arot S
 #pragma unroll
     for (int i = 0; i < 3; i++)
@@ -332,7 +376,7 @@ __device__ __forceinline__ uint32_t preprocess_one(const PreArgs& a, int64_t g) 
         if (!(det_acc > 0.0f) || !isfinite(det_acc)) det_acc = det;
     }
     const float inv_det = 1.0f / det_acc;
-    const float logit = __ldg(a.logits + g);
+    const float logit = in.logit();
     const float o = 1.0f / (1.0f + expf(-logit));
     const float conA = cc * inv_det, conB = -cb * inv_det, conC = ca * inv_det;
     if (a.conic_opacity) a.conic_opacity[g] = make_float4(conA, conB, conC, o);
@@ -340,8 +384,9 @@ __device__ __forceinline__ uint32_t preprocess_one(const PreArgs& a, int64_t g) 
     float dx = m0 - C.campos[0], dy = m1 - C.campos[1], dz = m2 - C.campos[2];
     const float il = rsqrtf(dx * dx + dy * dy + dz * dz);
     dx *= il; dy *= il; dz *= il;
-    constexpr int NK3 = (D + 1) * (D + 1) * 3;
-    const float3 col = eval_sh<D>(a.sh + g * NK3, dx, dy, dz);
+    float co[(D + 1) * (D + 1) * 3];
+    in.template sh<D>(co);
+    const float3 col = eval_sh<D>(co, dx, dy, dz);
     if (a.rgb) {
         a.rgb[3 * g] = col.x;
         a.rgb[3 * g + 1] = col.y;
@@ -433,8 +478,101 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
     for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); g0 < a.n; g0 += stride) {
         const int64_t g = g0 + (threadIdx.x & 31);
         const bool valid = g < a.n;
-        const uint32_t key = valid ? preprocess_one<D>(a, g) : 0u;
+        const uint32_t key = valid ? preprocess_one<D>(a, g, GlobalIn{a, g}) : 0u;
         if (a.dkeys) emit_depth_key(a, g, key, s_hist, valid);
+    }
+    if (a.dkeys) flush_depth_hist(s_hist, a.dhist);
+}
+
+// The same projection with the parameters staged through shared memory.
+// Persistent blocks (six per SM) take chunks of kStage Gaussians in turn; for
+// each chunk one thread issues five bulk copies (means, quaternions,
+// log-scales, logits, SH rows: 236 B per Gaussian at degree 3, 30 KB per
+// chunk). The first four land on one mbarrier and the SH rows on a second, so
+// the decision program starts on the 44 B per Gaussian it needs while the
+// 192 B of SH rows are still on their way; every thread then projects its
+// Gaussian from the stage. With three chunks in flight per SM the HBM stream
+// does not wait on per-thread load latency. A chunk that is not whole (the
+// tail) is read from global memory directly. Waits are bounded (kBulkWaitLimit
+// polls): a copy that did not land in time sets GS_FLAG_TIMEOUT, and the block
+// waits once more (again bounded) for its copy before it leaves.
+constexpr int kStage = 128;
+template <int D>
+constexpr int stage_bytes() {
+    return kStage * (12 + 16 + 12 + 4 + (D + 1) * (D + 1) * 12);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kStage, 6) preprocess_staged_kernel(const PreArgs a) {
+    extern __shared__ __align__(16) unsigned char s_stage[];
+    __shared__ uint32_t s_hist[4 * 256];
+    __shared__ __align__(8) uint64_t s_bar[2];   // means..logits, SH rows
+    constexpr int NK3 = (D + 1) * (D + 1) * 3;
+    float* s_means = reinterpret_cast<float*>(s_stage);
+    float4* s_quats = reinterpret_cast<float4*>(s_stage + kStage * 12);
+    float* s_ls = reinterpret_cast<float*>(s_stage + kStage * 28);
+    float* s_logits = reinterpret_cast<float*>(s_stage + kStage * 40);
+    float* s_sh = reinterpret_cast<float*>(s_stage + kStage * 44);
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        mbar_init(&s_bar[0], 1);
+        mbar_init(&s_bar[1], 1);
+        mbar_init_fence();
+    }
+    if (a.dkeys)
+        for (int i = tid; i < 4 * 256; i += kStage) s_hist[i] = 0;
+    __syncthreads();
+    const int64_t chunks = (a.n + kStage - 1) / kStage, whole = a.n / kStage;
+    auto issue = [&](int64_t c) {   // one thread, whole chunks only
+        const int64_t g0 = c * kStage;
+        mbar_arrive_expect_tx(&s_bar[0], (uint32_t)(kStage * 44));
+        mbar_arrive_expect_tx(&s_bar[1], (uint32_t)(kStage * NK3 * 4));
+        bulk_copy_g2s(s_means, a.means + 3 * g0, kStage * 12, &s_bar[0]);
+        bulk_copy_g2s(s_quats, a.quats + g0, kStage * 16, &s_bar[0]);
+        bulk_copy_g2s(s_ls, a.log_scales + 3 * g0, kStage * 12, &s_bar[0]);
+        bulk_copy_g2s(s_logits, a.logits + g0, kStage * 4, &s_bar[0]);
+        bulk_copy_g2s(s_sh, a.sh + NK3 * g0, kStage * NK3 * 4, &s_bar[1]);
+    };
+    uint32_t parity = 0;
+    int64_t c = blockIdx.x;
+    if (tid == 0 && c < whole) issue(c);
+    for (; c < chunks; c += gridDim.x) {
+        const bool staged = c < whole;   // the same for the whole block
+        if (staged) {
+            const bool landed = mbar_wait_bounded(&s_bar[0], parity, kBulkWaitLimit);
+            if (__syncthreads_or(!landed)) {
+                if (tid == 0) raise_flag(a.header, GS_FLAG_TIMEOUT, 3u);
+                mbar_wait_bounded(&s_bar[0], parity, kBulkWaitLimit);
+                mbar_wait_bounded(&s_bar[1], parity, kBulkWaitLimit);
+                return;
+            }
+        }
+        const int64_t g = c * kStage + tid;
+        const bool valid = g < a.n;
+        uint32_t key = 0u;
+        if (valid) {
+            if (staged)
+                key = preprocess_one<D>(a, g, SharedIn{s_means, s_quats, s_ls, s_logits, s_sh, tid, &s_bar[1], parity});
+            else
+                key = preprocess_one<D>(a, g, GlobalIn{a, g});
+        }
+        if (a.dkeys) emit_depth_key(a, g, key, s_hist, valid);
+        if (staged) {
+            // the SH rows have landed (culled Gaussians never read them) before the stage is reused
+            const bool landed = mbar_wait_bounded(&s_bar[1], parity, kBulkWaitLimit);
+            parity ^= 1u;
+            if (__syncthreads_or(!landed)) {
+                if (tid == 0) raise_flag(a.header, GS_FLAG_TIMEOUT, 3u);
+                mbar_wait_bounded(&s_bar[1], parity ^ 1u, kBulkWaitLimit);
+                return;
+            }
+        }
+        __syncthreads();   // every read of the stage is done before the next copy lands in it
+        const int64_t next = c + gridDim.x;
+        if (tid == 0 && next < whole) {
+            fence_proxy_async_shared();
+            issue(next);
+        }
     }
     if (a.dkeys) flush_depth_hist(s_hist, a.dhist);
 }
@@ -459,7 +597,7 @@ __global__ void __launch_bounds__(256) preprocess_batch_kernel(const PreBatchArg
         const int64_t g = g0 + (threadIdx.x & 31);
         const bool valid = g < n;
         for (int i = 0; i < nv; i++) {
-            const uint32_t key = valid ? preprocess_one<D>(a.v[i], g) : 0u;
+            const uint32_t key = valid ? preprocess_one<D>(a.v[i], g, GlobalIn{a.v[i], g}) : 0u;
             if (a.v[i].dkeys) emit_depth_key(a.v[i], g, key, s_hist + i * 1024, valid);
         }
     }
@@ -487,7 +625,42 @@ PreArgs pre_args(const gs_gaussians& g, const CamConst& cam, const gs_projected&
     a.dkeys = dk ? dk->keys : nullptr;
     a.dvals = dk ? dk->vals : nullptr;
     a.dhist = dk ? dk->hist : nullptr;
+    a.header = nullptr;
     return a;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Grid of the staged kernel: its resident blocks (three per SM), with the
+// dynamic shared memory of its stage allowed once per device.
+template <int D>
+cudaError_t launch_staged(const PreArgs& a, cudaStream_t s) {
+    static std::mutex mu;
+    static std::map<int, int64_t> grid;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int64_t cap = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = grid.find(dev);
+        if (it == grid.end()) {
+            e = cudaFuncSetAttribute(preprocess_staged_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     stage_bytes<D>());
+            if (e != cudaSuccess) return e;
+            int sms = 0, per_sm = 0;
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, preprocess_staged_kernel<D>, kStage,
+                                                              stage_bytes<D>());
+            if (e != cudaSuccess) return e;
+            it = grid.emplace(dev, (int64_t)(per_sm > 0 ? per_sm : 1) * sms).first;
+        }
+        cap = it->second;
+    }
+    const int64_t need = (a.n + kStage - 1) / kStage;
+    preprocess_staged_kernel<D><<<(unsigned)(need < cap ? need : cap), kStage, stage_bytes<D>(), s>>>(a);
+    return cudaGetLastError();
 }
 
 // blocks of 256 that fit on the current GPU at once for this kernel
@@ -536,9 +709,19 @@ cudaError_t launch_preprocess_batch(const gs_gaussians& g, const CamConst* cams,
 }
 
 cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const gs_projected& out,
-                              cudaStream_t s, const DepthKeysOut* dk) {
+                              cudaStream_t s, const DepthKeysOut* dk, StatusHeader* status) {
     if (g.n == 0) return cudaSuccess;
-    const PreArgs a = pre_args(g, cam, out, dk);
+    PreArgs a = pre_args(g, cam, out, dk);
+    if (status && aligned16(g.means) && aligned16(g.quats) && aligned16(g.log_scales) &&
+        aligned16(g.opacity_logits) && aligned16(g.sh)) {
+        a.header = status;
+        switch (g.sh_degree) {
+            case 0: return launch_staged<0>(a, s);
+            case 1: return launch_staged<1>(a, s);
+            case 2: return launch_staged<2>(a, s);
+            default: return launch_staged<3>(a, s);
+        }
+    }
     switch (g.sh_degree) {
         case 0: preprocess_kernel<0><<<resident_blocks(preprocess_kernel<0>, g.n), 256, 0, s>>>(a); break;
         case 1: preprocess_kernel<1><<<resident_blocks(preprocess_kernel<1>, g.n), 256, 0, s>>>(a); break;

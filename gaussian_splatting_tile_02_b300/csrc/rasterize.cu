@@ -49,77 +49,199 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // Launch order of the tiles: longest lists first, bucketed by floor(log2
 // length) (order within a bucket unspecified), so that the heaviest tiles
-// start in the first wave instead of trailing the last one. One block: a
-// count per bucket, a prefix over the 33 buckets, then a scatter through
-// per-bucket cursors; the shared-memory atomics are aggregated per warp over
-// lanes with the same bucket.
-constexpr int kOrderThreads = 1024, kOrderItems = 8;
+// start in the first wave instead of trailing the last one. One block: the
+// tiles are counted into shared counters per (bucket, warp), one exclusive
+// scan over those pairs in launch order (bucket descending, then warp) turns
+// the counters into start positions, and a second round hands out each tile's
+// position. Rows are kept in launch order: row clz(len) holds bucket
+// 32 - clz(len), row 32 the empty tiles. Most tiles of a frame share one or
+// two buckets, so a warp's lanes are first grouped by row with six ballots
+// (the row's bits) and one lane per group updates the counter.
+constexpr int kOrderThreads = 1024, kOrderItems = 8, kOrderRows = 33;
+
+// lanes of the warp holding the same 6-bit value v (63 = none)
+__device__ __forceinline__ uint32_t same_row_lanes(uint32_t v) {
+    uint32_t m = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < 6; b++) {
+        const uint32_t bit = (v >> b) & 1u;
+        const uint32_t bal = __ballot_sync(0xffffffffu, bit);
+        m &= bit ? bal : ~bal;
+    }
+    return m;
+}
+
 __global__ void __launch_bounds__(kOrderThreads) tile_order_kernel(const uint2* __restrict__ ranges, int tiles,
                                                                    uint32_t* __restrict__ order) {
-    __shared__ uint32_t s_cnt[33];
-    const int lane = threadIdx.x & 31;
+    __shared__ uint32_t s_cnt[kOrderRows][32];   // [row][warp]
+    __shared__ uint32_t s_row[kOrderRows];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t lt = (1u << lane) - 1u;
-    if (threadIdx.x < 33) s_cnt[threadIdx.x] = 0;
+    for (int i = threadIdx.x; i < kOrderRows * 32; i += kOrderThreads) s_cnt[i >> 5][i & 31] = 0;
     __syncthreads();
-    auto bucket = [&](int t) -> uint32_t {
-        if (t >= tiles) return 0xffffffffu;
+    auto row_of = [&](int t) -> uint32_t {
+        if (t >= tiles) return 63u;
         const uint2 r = __ldg(ranges + t);
         const uint32_t len = r.y > r.x ? r.y - r.x : 0u;
-        return len ? 32u - (uint32_t)__clz(len) : 0u;
-    };
-    auto count = [&](const uint32_t (&b)[kOrderItems]) {
-#pragma unroll
-        for (int i = 0; i < kOrderItems; i++) {
-            const uint32_t peers = __match_any_sync(0xffffffffu, b[i]);
-            if (b[i] != 0xffffffffu && (peers & lt) == 0) atomicAdd(&s_cnt[b[i]], (uint32_t)__popc(peers));
-        }
-    };
-    auto scatter = [&](const uint32_t (&b)[kOrderItems], int t0) {
-#pragma unroll
-        for (int i = 0; i < kOrderItems; i++) {
-            const uint32_t peers = __match_any_sync(0xffffffffu, b[i]);
-            const int leader = __ffs(peers) - 1;
-            uint32_t base = 0;
-            if (b[i] != 0xffffffffu && lane == leader) base = atomicAdd(&s_cnt[b[i]], (uint32_t)__popc(peers));
-            base = __shfl_sync(0xffffffffu, base, leader);
-            if (b[i] != 0xffffffffu) order[base + __popc(peers & lt)] = (uint32_t)(t0 + i * kOrderThreads + threadIdx.x);
-        }
-    };
-    auto prefix = [&]() {
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            uint32_t run = 0;
-            for (int k = 32; k >= 0; k--) {
-                const uint32_t c = s_cnt[k];
-                s_cnt[k] = run;
-                run += c;
-            }
-        }
-        __syncthreads();
+        return len ? (uint32_t)__clz(len) : 32u;
     };
     constexpr int kChunk = kOrderItems * kOrderThreads;
-    uint32_t b[kOrderItems];
-    if (tiles <= kChunk) {
-        // every tile in one pass: the buckets stay in registers between the
-        // count and the scatter (one round of loads)
-#pragma unroll
-        for (int i = 0; i < kOrderItems; i++) b[i] = bucket(i * kOrderThreads + threadIdx.x);
-        count(b);
-        prefix();
-        scatter(b, 0);
-        return;
-    }
+    const bool one_chunk = tiles <= kChunk;
+    uint32_t rw[kOrderItems];
     for (int t0 = 0; t0 < tiles; t0 += kChunk) {
 #pragma unroll
-        for (int i = 0; i < kOrderItems; i++) b[i] = bucket(t0 + i * kOrderThreads + threadIdx.x);
-        count(b);
+        for (int i = 0; i < kOrderItems; i++) rw[i] = row_of(t0 + i * kOrderThreads + (int)threadIdx.x);
+#pragma unroll
+        for (int i = 0; i < kOrderItems; i++) {
+            const uint32_t m = same_row_lanes(rw[i]);
+            if (rw[i] != 63u && (m & lt) == 0) s_cnt[rw[i]][warp] += (uint32_t)__popc(m);
+            __syncwarp();
+        }
     }
-    prefix();
+    __syncthreads();
+    // exclusive scan over (row, warp): warp w scans row w (warp 0 also row 32)
+    for (int row = warp; row < kOrderRows; row += 32) {
+        const uint32_t c = s_cnt[row][lane];
+        uint32_t v = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+        }
+        s_cnt[row][lane] = v - c;
+        if (lane == 31) s_row[row] = v;
+    }
+    __syncthreads();
+    for (int row = warp; row < kOrderRows; row += 32) {
+        uint32_t before = 0;
+        for (int k = lane; k < row; k += 32) before += s_row[k];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+        s_cnt[row][lane] += before;
+    }
+    __syncthreads();
     for (int t0 = 0; t0 < tiles; t0 += kChunk) {
 #pragma unroll
-        for (int i = 0; i < kOrderItems; i++) b[i] = bucket(t0 + i * kOrderThreads + threadIdx.x);
-        scatter(b, t0);
+        for (int i = 0; i < kOrderItems; i++) {
+            const int t = t0 + i * kOrderThreads + (int)threadIdx.x;
+            const uint32_t r = one_chunk ? rw[i] : row_of(t);
+            const uint32_t m = same_row_lanes(r);
+            const int leader = __ffs(m) - 1;
+            uint32_t base = 0;
+            if (r != 63u && lane == leader) {
+                base = s_cnt[r][warp];
+                s_cnt[r][warp] = base + (uint32_t)__popc(m);
+            }
+            base = __shfl_sync(0xffffffffu, base, leader);
+            if (r != 63u) order[base + __popc(m & lt)] = (uint32_t)t;
+            __syncwarp();
+        }
     }
+}
+
+// The same launch order from many blocks (the render path, where the frame's
+// workspace has room for the table): one thread per tile.
+//   tile_order_count_kernel  : per block, the tiles of each row (bucket); the
+//                              last block to finish turns the [block][row]
+//                              table into start positions, in launch order
+//                              (row ascending, then block).
+//   tile_order_scatter_kernel: each tile's position = its (block, row) start +
+//                              the tiles of that row in earlier warps + its
+//                              rank among its warp's lanes of the same row.
+constexpr int kOrderMultiThreads = 256, kOrderMultiWarps = kOrderMultiThreads / 32;
+// the last block scans the [block][row] table with at most kOrderMaxPer entries per
+// thread: up to 24 * 256 / 33 = 186 blocks of 256 tiles (47,616 tiles; 3840x2160 has
+// 32,400); larger grids use the one-block order
+constexpr int kOrderMaxPer = 24;
+constexpr int kOrderMaxBlocks = kOrderMaxPer * kOrderMultiThreads / kOrderRows;
+
+__device__ __forceinline__ uint32_t tile_row(const uint2* __restrict__ ranges, int tiles, int t) {
+    if (t >= tiles) return 63u;
+    const uint2 r = __ldg(ranges + t);
+    const uint32_t len = r.y > r.x ? r.y - r.x : 0u;
+    return len ? (uint32_t)__clz(len) : 32u;
+}
+
+__global__ void __launch_bounds__(kOrderMultiThreads) tile_order_count_kernel(const uint2* __restrict__ ranges,
+                                                                              int tiles, uint32_t* __restrict__ table,
+                                                                              uint32_t* __restrict__ done) {
+    __shared__ uint32_t s_cnt[kOrderRows][kOrderMultiWarps];
+    __shared__ uint32_t s_wt[kOrderMultiWarps];
+    __shared__ bool s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < kOrderRows * kOrderMultiWarps; i += kOrderMultiThreads)
+        s_cnt[i / kOrderMultiWarps][i % kOrderMultiWarps] = 0;
+    __syncthreads();
+    const uint32_t row = tile_row(ranges, tiles, blockIdx.x * kOrderMultiThreads + tid);
+    const uint32_t m = same_row_lanes(row);
+    if (row != 63u && (m & ((1u << lane) - 1u)) == 0) s_cnt[row][warp] = (uint32_t)__popc(m);
+    __syncthreads();
+    const int nb = gridDim.x;
+    if (tid < kOrderRows) {
+        uint32_t t = 0;
+#pragma unroll
+        for (int w = 0; w < kOrderMultiWarps; w++) t += s_cnt[tid][w];
+        table[blockIdx.x * kOrderRows + tid] = t;
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(done, 1u) == (uint32_t)nb - 1u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // exclusive scan over f = row * nb + block (launch order) of the table: each thread
+    // takes a run of `per` consecutive f (its loads all issued at once), then one block scan
+    const int total = kOrderRows * nb;
+    const int per = (total + kOrderMultiThreads - 1) / kOrderMultiThreads;
+    // (launch_tile_order_multi keeps total within kOrderMaxPer runs per thread)
+    uint32_t x[kOrderMaxPer];
+    uint32_t sum = 0;
+    const int f0 = tid * per;
+#pragma unroll
+    for (int k = 0; k < kOrderMaxPer; k++) {
+        const int f = f0 + k;
+        x[k] = (k < per && f < total) ? ld_volatile_u32(table + (f % nb) * kOrderRows + f / nb) : 0u;
+        sum += x[k];
+    }
+    uint32_t v = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    if (lane == 31) s_wt[warp] = v;
+    __syncthreads();
+    uint32_t run = v - sum;
+    for (int w = 0; w < warp; w++) run += s_wt[w];
+#pragma unroll
+    for (int k = 0; k < kOrderMaxPer; k++) {
+        const int f = f0 + k;
+        if (k < per && f < total) {
+            table[(f % nb) * kOrderRows + f / nb] = run;
+            run += x[k];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kOrderMultiThreads) tile_order_scatter_kernel(const uint2* __restrict__ ranges,
+                                                                                int tiles,
+                                                                                const uint32_t* __restrict__ table,
+                                                                                uint32_t* __restrict__ order) {
+    __shared__ uint32_t s_cnt[kOrderRows][kOrderMultiWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < kOrderRows * kOrderMultiWarps; i += kOrderMultiThreads)
+        s_cnt[i / kOrderMultiWarps][i % kOrderMultiWarps] = 0;
+    __syncthreads();
+    const int t = blockIdx.x * kOrderMultiThreads + tid;
+    const uint32_t row = tile_row(ranges, tiles, t);
+    const uint32_t lt = (1u << lane) - 1u;
+    const uint32_t m = same_row_lanes(row);
+    if (row != 63u && (m & lt) == 0) s_cnt[row][warp] = (uint32_t)__popc(m);
+    __syncthreads();
+    if (row == 63u) return;
+    uint32_t pos = table[blockIdx.x * kOrderRows + row] + (uint32_t)__popc(m & lt);
+    for (int w = 0; w < warp; w++) pos += s_cnt[row][w];
+    order[pos] = (uint32_t)t;
 }
 
 struct RastArgs {
@@ -135,6 +257,9 @@ struct RastArgs {
     uint32_t* n_contrib;
 };
 
+// kAux: the per-pixel list position of the last contributor is tracked (for
+// n_contrib); without it the blend is the same arithmetic minus that bookkeeping.
+template <bool kAux>
 __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastArgs a) {
     __shared__ float4 s_q[2][kRastThreads];    // (A1, A2, k1, k2): origin terms of the exponent
     __shared__ float4 s_r[2][kRastThreads];    // (k3, log2 o, r, g)
@@ -227,7 +352,10 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
                 const int pos = __popc(m & lt_mask);
                 w_q[warp][pos] = s_q[buf][j];
                 w_r[warp][pos] = s_r[buf][j];
-                w_bj[warp][pos] = make_float2(s_b[buf][j], __uint_as_float(base - range.x + j + 1));
+                if constexpr (kAux)
+                    w_bj[warp][pos] = make_float2(s_b[buf][j], __uint_as_float(base - range.x + j + 1));
+                else
+                    w_bj[warp][pos].x = s_b[buf][j];
             }
             __syncwarp();
             const int nh = __popc(m);
@@ -241,7 +369,11 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
                 // decision in exact arithmetic; ex2 is only evaluated past it)
                 const bool c = !done && e >= kLog2AlphaMin, c2 = !done2 && e2 >= kLog2AlphaMin;
                 if (!(c || c2)) continue;
-                const float2 bj = w_bj[warp][k];
+                float2 bj;
+                if constexpr (kAux)
+                    bj = w_bj[warp][k];
+                else
+                    bj.x = w_bj[warp][k].x;
                 if (c) {
                     const float alpha = fminf(0.99f, fast_exp2(e));
                     const float w = alpha * T;
@@ -249,7 +381,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
                     C1 += w * r.w;
                     C2 += w * bj.x;
                     T -= w;
-                    last = __float_as_uint(bj.y);
+                    if constexpr (kAux) last = __float_as_uint(bj.y);
                     if (T < 1e-4f) done = true;
                 }
                 if (c2) {
@@ -259,7 +391,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
                     D1 += w * r.w;
                     D2 += w * bj.x;
                     U -= w;
-                    last2 = __float_as_uint(bj.y);
+                    if constexpr (kAux) last2 = __float_as_uint(bj.y);
                     if (U < 1e-4f) done2 = true;
                 }
             }
@@ -274,7 +406,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
         a.image[3 * p + 1] = C1 + T * a.bg1;
         a.image[3 * p + 2] = C2 + T * a.bg2;
         if (a.final_T) a.final_T[p] = T;
-        if (a.n_contrib) a.n_contrib[p] = last;
+        if (kAux && a.n_contrib) a.n_contrib[p] = last;
     }
     if (px < a.width && py + 4 < a.height) {
         const int64_t p = (int64_t)(py + 4) * a.width + px;
@@ -282,7 +414,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
         a.image[3 * p + 1] = D1 + U * a.bg1;
         a.image[3 * p + 2] = D2 + U * a.bg2;
         if (a.final_T) a.final_T[p] = U;
-        if (a.n_contrib) a.n_contrib[p] = last2;
+        if (kAux && a.n_contrib) a.n_contrib[p] = last2;
     }
 }
 
@@ -308,7 +440,33 @@ cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* s
     a.n_contrib = n_contrib;
     const unsigned tiles = (unsigned)(cam.tiles_x * cam.tiles_y);
     if (n == 0) a.sorted_vals = nullptr;
-    rasterize_kernel<<<tiles, kRastThreads, 0, s>>>(a);
+    if (n_contrib)
+        rasterize_kernel<true><<<tiles, kRastThreads, 0, s>>>(a);
+    else
+        rasterize_kernel<false><<<tiles, kRastThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+size_t tile_order_scratch_bytes(int tiles) {
+    const size_t nb = (size_t)(tiles + kOrderMultiThreads - 1) / kOrderMultiThreads;
+    return align_up(4 * (size_t)tiles) + align_up(4 * kOrderRows * nb) + align_up(4);
+}
+
+cudaError_t launch_tile_order_multi(const uint32_t* ranges, int tiles, void* scratch, uint32_t** tile_order,
+                                    cudaStream_t s) {
+    char* w = static_cast<char*>(scratch);
+    uint32_t* order = reinterpret_cast<uint32_t*>(w);
+    const size_t nb = (size_t)(tiles + kOrderMultiThreads - 1) / kOrderMultiThreads;
+    uint32_t* table = reinterpret_cast<uint32_t*>(w + align_up(4 * (size_t)tiles));
+    uint32_t* done = reinterpret_cast<uint32_t*>(w + align_up(4 * (size_t)tiles) + align_up(4 * kOrderRows * nb));
+    *tile_order = order;
+    if (tiles <= 0) return cudaSuccess;
+    if (nb > (size_t)kOrderMaxBlocks) return launch_tile_order(ranges, tiles, order, s);
+    cudaError_t e = cudaMemsetAsync(done, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    const uint2* r = reinterpret_cast<const uint2*>(ranges);
+    tile_order_count_kernel<<<(unsigned)nb, kOrderMultiThreads, 0, s>>>(r, tiles, table, done);
+    tile_order_scatter_kernel<<<(unsigned)nb, kOrderMultiThreads, 0, s>>>(r, tiles, table, order);
     return cudaGetLastError();
 }
 

@@ -14,8 +14,9 @@
 //                    keys (tile ids from an atomic counter, so a block only
 //                    ever waits on blocks that are already running), ranks
 //                    its keys stably with warp match/popc counters, publishes
-//                    its per-digit counts, and finds its global offsets by
-//                    decoupled look-back over earlier tiles. Keys and values
+//                    its per-digit counts (before the ranking when the whole
+//                    pass is one wave of resident blocks), and finds its global
+//                    offsets by decoupled look-back over earlier tiles. Keys and values
 //                    are then reordered in shared memory (together for 32-bit
 //                    keys, one after the other for 64-bit keys) and written
 //                    out in digit-contiguous runs (coalesced).
@@ -27,6 +28,9 @@
 // that runs out sets GS_FLAG_TIMEOUT in the workspace header and the block
 // still publishes a status so that no other block waits on it. All stores are
 // bounds-checked against the key count.
+#include <map>
+#include <mutex>
+
 #include "gs_internal.cuh"
 
 #ifndef GS_SORT_THREADS
@@ -192,7 +196,12 @@ struct PassArgs {
     long long spin_limit;
 };
 
-template <typename KeyT>
+// kEarly: the tile's digit counts are taken (shared atomics) and published as
+// its aggregate before the ranking, so that later tiles' look-back finds them
+// sooner. That pays when every tile of the pass is resident at once (a single
+// wave, where each tile's look-back walks back over tiles started at the same
+// moment); with several waves the extra counting costs more than it saves.
+template <typename KeyT, bool kEarly>
 __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_kernel(const PassArgs<KeyT> a) {
     __shared__ uint16_t s_hist[kSortWarps * kRadix];  // per-warp digit counters -> offsets
     __shared__ uint32_t s_dstart[kRadix];
@@ -206,6 +215,7 @@ __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_ker
     __shared__ uint32_t s_vals_joint[kJoint ? kSortTile : 1];
     __shared__ uint32_t s_tile;
     __shared__ int s_timed_out;
+    __shared__ uint32_t s_early[kEarly ? kRadix : 1];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
@@ -213,6 +223,7 @@ __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_ker
         s_timed_out = 0;
     }
     for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) s_hist[i] = 0;
+    if (kEarly && tid < kRadix) s_early[tid] = 0;
     __syncthreads();
     const int64_t K = key_count(a.num_keys, a.cap);
     const uint32_t tile = s_tile;
@@ -238,6 +249,16 @@ __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_ker
     for (int i = 0; i < kSortItems; i++) {
         const int li = warp_base + i * 32 + lane;
         val[i] = li < n_valid ? a.vals_in[start + li] : 0u;
+    }
+
+    if constexpr (kEarly) {
+#pragma unroll
+        for (int i = 0; i < kSortItems; i++) {
+            const int li = warp_base + i * 32 + lane;
+            if (li < n_valid) atomicAdd(&s_early[digit_of(key[i], shift, dmask)], 1u);
+        }
+        __syncthreads();
+        if (tid < kRadix && tile != 0) st_relaxed_u32(a.status + (int64_t)tile * kRadix + tid, kFlagAgg | s_early[tid]);
     }
 
     // stable rank within the warp: position order is (i, lane)
@@ -275,7 +296,7 @@ __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_ker
             st_relaxed_u32(row + d, kFlagIncl | sum);
             s_goff[d] = a.bases[d];
         } else {
-            st_relaxed_u32(row + d, kFlagAgg | sum);
+            if (!kEarly) st_relaxed_u32(row + d, kFlagAgg | sum);
             // look back in windows of kLookback earlier tiles: the window's
             // loads are issued together, then consumed nearest first until an
             // inclusive prefix is met (a not-yet-published one is waited for)
@@ -396,6 +417,208 @@ __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_ker
     }
 }
 
+// Persistent pass for 32-bit keys, used when a pass spans several waves of
+// blocks (large key counts): each block claims tiles from the pass's counter
+// and, while it ranks and scatters one tile, the bulk-copy engine already
+// brings the next tile's keys and values into the other half of a
+// double-buffered shared-memory stage (cp.async.bulk on an mbarrier), so the
+// loads of one tile overlap the latency-bound phases of the previous one. The
+// tile's digit counts are published before the ranking, as in the single-wave
+// case. The ranking, look-back and scatter are those of onesweep_kernel. Tiles
+// are claimed in increasing order and a block only claims its next tile while
+// it holds a lower one, so every tile a look-back waits on is being processed.
+// A bulk copy that did not land within kBulkWaitLimit polls sets
+// GS_FLAG_TIMEOUT; the block then waits (bounded) for both of its copies and
+// leaves.
+constexpr int kPipeBytes = (6 * kSortTile) * 4 + kSortWarps * kRadix * 2;
+__global__ void __launch_bounds__(kSortThreads, 2) onesweep_pipe_kernel(const PassArgs<uint32_t> a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint32_t* s_kin = reinterpret_cast<uint32_t*>(smem);          // [2][kSortTile]
+    uint32_t* s_vin = s_kin + 2 * kSortTile;                       // [2][kSortTile]
+    uint32_t* s_keys = s_vin + 2 * kSortTile;                      // [kSortTile] sorted staging
+    uint32_t* s_vals = s_keys + kSortTile;                         // [kSortTile]
+    uint16_t* s_hist = reinterpret_cast<uint16_t*>(s_vals + kSortTile);   // [kSortWarps][kRadix]
+    __shared__ uint32_t s_dstart[kRadix];
+    __shared__ uint32_t s_goff[kRadix];
+    __shared__ uint32_t s_warp_tot[kRadix / 32];
+    __shared__ uint32_t s_early[kRadix];
+    __shared__ uint32_t s_tile[2];
+    __shared__ int s_timed_out;
+    __shared__ __align__(8) uint64_t s_bar[2];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t K = key_count(a.num_keys, a.cap);
+    const int64_t ntiles = (K + kSortTile - 1) / kSortTile;
+    const int shift = a.shift;
+    const uint32_t dmask = (1u << a.digit_bits) - 1u;
+    auto whole = [&](int64_t t) { return (t + 1) * kSortTile <= K; };
+    auto issue = [&](int64_t t, int b) {
+        mbar_arrive_expect_tx(&s_bar[b], 2u * kSortTile * 4u);
+        bulk_copy_g2s(s_kin + b * kSortTile, a.keys_in + t * kSortTile, kSortTile * 4, &s_bar[b]);
+        bulk_copy_g2s(s_vin + b * kSortTile, a.vals_in + t * kSortTile, kSortTile * 4, &s_bar[b]);
+    };
+    if (tid == 0) {
+        mbar_init(&s_bar[0], 1);
+        mbar_init(&s_bar[1], 1);
+        mbar_init_fence();
+        s_tile[0] = atomicAdd(a.counter, 1u);
+    }
+    __syncthreads();
+    if (tid == 0 && (int64_t)s_tile[0] < ntiles && whole(s_tile[0])) issue(s_tile[0], 0);
+    uint32_t parity = 0;   // bit b: parity of the next phase of s_bar[b]
+    int buf = 0;
+    while (true) {
+        const int64_t tile = s_tile[buf];
+        if (tile >= ntiles) break;
+        if (tid == 0) {
+            const uint32_t nt = atomicAdd(a.counter, 1u);
+            s_tile[buf ^ 1] = nt;
+            if ((int64_t)nt < ntiles && whole(nt)) {
+                fence_proxy_async_shared();
+                issue(nt, buf ^ 1);
+            }
+            s_timed_out = 0;
+        }
+        for (int i = tid; i < kSortWarps * kRadix / 2; i += kSortThreads) reinterpret_cast<uint32_t*>(s_hist)[i] = 0;
+        if (tid < kRadix) s_early[tid] = 0;
+        const int64_t start = tile * kSortTile;
+        const int n_valid = (int)(K - start < kSortTile ? K - start : kSortTile);
+        uint32_t* kin = s_kin + buf * kSortTile;
+        uint32_t* vin = s_vin + buf * kSortTile;
+        bool landed = true;
+        if (whole(tile)) {
+            landed = mbar_wait_bounded(&s_bar[buf], (parity >> buf) & 1u, kBulkWaitLimit);
+            parity ^= 1u << buf;
+        } else {
+            for (int i = tid; i < n_valid; i += kSortThreads) {
+                kin[i] = a.keys_in[start + i];
+                vin[i] = a.vals_in[start + i];
+            }
+        }
+        if (__syncthreads_or(!landed)) {
+            if (tid == 0) raise_flag(a.header, GS_FLAG_TIMEOUT, 4u);
+            mbar_wait_bounded(&s_bar[buf], ((parity >> buf) & 1u) ^ 1u, kBulkWaitLimit);
+            mbar_wait_bounded(&s_bar[buf ^ 1], (parity >> (buf ^ 1)) & 1u, kBulkWaitLimit);
+            return;
+        }
+        if (a.status_clear && tid < kRadix) a.status_clear[tile * kRadix + tid] = 0;
+
+        const int warp_base = warp * (kSortItems * 32);
+        uint32_t key[kSortItems];
+#pragma unroll
+        for (int i = 0; i < kSortItems; i++) {
+            const int li = warp_base + i * 32 + lane;
+            key[i] = li < n_valid ? kin[li] : 0u;
+            if (li < n_valid) atomicAdd(&s_early[digit_of(key[i], shift, dmask)], 1u);
+        }
+        __syncthreads();
+        if (tid < kRadix && tile != 0) st_relaxed_u32(a.status + tile * kRadix + tid, kFlagAgg | s_early[tid]);
+
+        uint16_t* wh = s_hist + warp * kRadix;
+        const uint32_t lt = lanemask_lt();
+        uint32_t rank[kSortItems];
+#pragma unroll
+        for (int i = 0; i < kSortItems; i++) {
+            const int li = warp_base + i * 32 + lane;
+            const bool v = li < n_valid;
+            const uint32_t d = digit_of(key[i], shift, dmask);
+            const uint32_t peers = __match_any_sync(0xffffffffu, v ? d : 0xffffu) & __ballot_sync(0xffffffffu, v);
+            uint32_t r = 0;
+            if (v) r = wh[d] + __popc(peers & lt);
+            __syncwarp();
+            if (v && (peers & lt) == 0) wh[d] = (uint16_t)(wh[d] + __popc(peers));
+            __syncwarp();
+            rank[i] = r;
+        }
+        __syncthreads();
+        uint32_t sum = 0;
+        if (tid < kRadix) {
+            const int d = tid;
+#pragma unroll
+            for (int w = 0; w < kSortWarps; w++) {
+                const uint32_t c = s_hist[w * kRadix + d];
+                s_hist[w * kRadix + d] = (uint16_t)sum;
+                sum += c;
+            }
+            uint32_t* row = a.status + tile * kRadix;
+            if (tile == 0) {
+                st_relaxed_u32(row + d, kFlagIncl | sum);
+                s_goff[d] = a.bases[d];
+            } else {
+                uint32_t excl = 0;
+                bool ok = true, found = false;
+                for (int64_t j = tile - 1; j >= 0 && ok && !found; j -= kLookback) {
+                    uint32_t v[kLookback];
+#pragma unroll
+                    for (int k = 0; k < kLookback; k++)
+                        v[k] = j - k >= 0 ? ld_relaxed_u32(a.status + (j - k) * kRadix + d) : 0u;
+#pragma unroll
+                    for (int k = 0; k < kLookback; k++) {
+                        if (found || !ok || j - k < 0) break;
+                        uint32_t x = v[k];
+                        if (!(x & (kFlagAgg | kFlagIncl)) &&
+                            !bounded_wait(a.status + (j - k) * kRadix + d, x, a.spin_limit, a.header)) {
+                            ok = false;
+                            break;
+                        }
+                        excl += x & kValueMask;
+                        if (x & kFlagIncl) found = true;
+                    }
+                }
+                if (!ok) {
+                    raise_flag(a.header, GS_FLAG_TIMEOUT, 1u);
+                    s_timed_out = 1;
+                }
+                st_relaxed_u32(row + d, kFlagIncl | ((excl + sum) & kValueMask));
+                s_goff[d] = a.bases[d] + excl;
+            }
+            uint32_t v = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += t;
+            }
+            if (lane == 31) s_warp_tot[warp] = v;
+            sum = v - sum;
+        }
+        __syncthreads();
+        if (tid < kRadix) {
+            uint32_t add = 0;
+            for (int w = 0; w < warp; w++) add += s_warp_tot[w];
+            s_dstart[tid] = sum + add;
+        }
+        __syncthreads();
+        const bool skip = s_timed_out != 0;
+#pragma unroll
+        for (int i = 0; i < kSortItems; i++) {
+            const int li = warp_base + i * 32 + lane;
+            if (li < n_valid) {
+                const uint32_t d = digit_of(key[i], shift, dmask);
+                const uint32_t loc = s_dstart[d] + s_hist[warp * kRadix + d] + rank[i];
+                s_keys[loc] = key[i];
+                s_vals[loc] = vin[li];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kSortItems; k++) {
+            const int j = k * kSortThreads + tid;
+            if (j < n_valid) {
+                const uint32_t kk = s_keys[j];
+                const uint32_t d = digit_of(kk, shift, dmask);
+                const uint32_t o = s_goff[d] + (uint32_t)j - s_dstart[d];
+                GS_CHECK(skip || (int64_t)o < K);
+                if (!skip && (int64_t)o < K) {
+                    a.keys_out[o] = kk;
+                    a.vals_out[o] = s_vals[j];
+                }
+            }
+        }
+        __syncthreads();
+        buf ^= 1;
+    }
+}
+
 template <typename KeyT>
 __global__ void copy_back_kernel(const KeyT* __restrict__ ks, const uint32_t* __restrict__ vs,
                                  KeyT* __restrict__ kd, uint32_t* __restrict__ vd,
@@ -469,6 +692,45 @@ int grid_for(int64_t work, int threads, int max_blocks) {
     return (int)(b < max_blocks ? b : max_blocks);
 }
 
+// Blocks of the pass kernel resident on the current GPU at once, and the grid
+// of the persistent pass (its resident blocks; 0 where it cannot run), with
+// its dynamic shared memory allowed. Computed once per device and key width.
+struct PassShapes {
+    unsigned resident;      // blocks of onesweep_kernel resident at once
+    unsigned pipe_blocks;   // grid of onesweep_pipe_kernel (0: not available)
+};
+
+template <typename KeyT>
+cudaError_t resident_tiles(PassShapes* out) {
+    static std::mutex mu;
+    static std::map<int, PassShapes> cache;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it == cache.end()) {
+        int sms = 0, per_sm = 0, pipe_per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, onesweep_kernel<KeyT, false>, kSortThreads, 0);
+        if (e != cudaSuccess) return e;
+        if (sizeof(KeyT) == 4) {
+            e = cudaFuncSetAttribute(onesweep_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeBytes);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&pipe_per_sm, onesweep_pipe_kernel, kSortThreads,
+                                                                  kPipeBytes);
+            if (e != cudaSuccess) return e;
+        }
+        PassShapes ps;
+        ps.resident = (unsigned)(sms * per_sm);
+        ps.pipe_blocks = (unsigned)(sms * pipe_per_sm);
+        it = cache.emplace(dev, ps).first;
+    }
+    *out = it->second;
+    return cudaSuccess;
+}
+
 // hist_ready: the digit histograms were already accumulated into the
 // scratch's histogram array (zeroed by sort_prepare_histogram) by the kernel
 // that produced the keys.
@@ -488,10 +750,14 @@ cudaError_t launch_sort_t(KeyT* keys, uint32_t* vals, KeyT* keys_alt, uint32_t* 
     }
     e = cudaMemsetAsync(sc.counters, 0, sizeof(uint32_t) * kMaxPasses, s);
     if (e != cudaSuccess) return e;
+    const unsigned tiles = (unsigned)sc.max_tiles;
+    PassShapes shapes;
+    e = resident_tiles<KeyT>(&shapes);
+    if (e != cudaSuccess) return e;
+    const unsigned resident = shapes.resident, pipe_blocks = shapes.pipe_blocks;
     const int clear_blocks = grid_for(2 * sc.max_tiles * kRadix, kRadix * 8, 148 * 2);
     sort_bases_kernel<<<passes + clear_blocks, kRadix, 0, s>>>(sc.hist, passes, num_keys, cap, sc.lookback,
                                                               sc.max_tiles);
-    const unsigned tiles = (unsigned)sc.max_tiles;
     for (int p = 0; p < passes; p++) {
         PassArgs<KeyT> a;
         const bool even = (p % 2) == 0;
@@ -510,7 +776,19 @@ cudaError_t launch_sort_t(KeyT* keys, uint32_t* vals, KeyT* keys_alt, uint32_t* 
         a.status_clear = p >= 1 ? sc.lookback + (int64_t)((p + 1) % 2) * sc.max_tiles * kRadix : nullptr;
         a.header = status;
         a.spin_limit = spin_limit;
-        onesweep_kernel<KeyT><<<tiles, kSortThreads, 0, s>>>(a);
+        bool piped = false;
+        if constexpr (sizeof(KeyT) == 4) {
+            // three waves or more, and arrays the bulk copies can read
+            piped = pipe_blocks > 0 && tiles >= 3u * resident && ((uintptr_t)a.keys_in & 15) == 0 &&
+                    ((uintptr_t)a.vals_in & 15) == 0;
+            if (piped) onesweep_pipe_kernel<<<pipe_blocks, kSortThreads, kPipeBytes, s>>>(a);
+        }
+        if (!piped) {
+            if (tiles <= resident)
+                onesweep_kernel<KeyT, true><<<tiles, kSortThreads, 0, s>>>(a);
+            else
+                onesweep_kernel<KeyT, false><<<tiles, kSortThreads, 0, s>>>(a);
+        }
     }
     if (passes % 2 == 1)
         copy_back_kernel<KeyT><<<grid_for(cap, 256 * 8, 148 * 8), 256, 0, s>>>(keys_alt, vals_alt, keys, vals,

@@ -115,10 +115,10 @@ def test_clock_sampler_closes_its_file_when_the_sampler_cannot_start(tmp_path, m
 
 
 def test_frame_launch_count():
-    """gpu_launches per frame: 17 at 1920x1080 (8160 tiles, 13 bits, two passes) and at
+    """gpu_launches per frame: 18 at 1920x1080 (8160 tiles, 13-bit tile ids, two passes) and at
     64x64 (16 tiles, one pass and a copy back); 19 at 8192x4320 (138240 tiles, three passes
-    and a copy back)."""
-    assert bench.frame_launches(120 * 68) == 17
-    assert bench.frame_launches(4 * 4) == 17
+    and a copy back, and the one-kernel tile order beyond 186 blocks of tiles)."""
+    assert bench.frame_launches(120 * 68) == 18
+    assert bench.frame_launches(4 * 4) == 18
     assert bench.frame_launches(512 * 270) == 19
-    assert bench.frame_launches(240 * 135) == 17   # 3840x2160: 15 bits, two passes
+    assert bench.frame_launches(240 * 135) == 18   # 3840x2160: 15 bits, two passes, 127 order blocks
