@@ -214,14 +214,24 @@ def sort_launches(key_bits: int) -> int:
     return 1 + passes + passes % 2
 
 
-def frame_launches(tiles: int) -> int:
+def tile_depth_launches(key_capacity: int) -> int:
+    """Kernels of a tile-first frame's per-tile depth sort: one per list-size class the key
+    capacity allows (up to 512, 2048 and 8192 entries, and longer)."""
+    if key_capacity <= 1:
+        return 0
+    return 1 + (key_capacity > 512) + (key_capacity > 2048) + (key_capacity > 8192)
+
+
+def frame_launches(tiles: int, tile_first: bool = False, key_capacity: int = 1 << 20) -> int:
     """Kernels one gs_render frame launches for an image of `tiles` 16x16 tiles: preprocess
-    (which also writes the depth keys); the depth sort (4 passes); 5 binning kernels; the
-    tile-id sort; ranges; the tile order (count and scatter kernels up to 186 blocks of 256
-    tiles, one kernel beyond); rasterize."""
+    (which, depth-first, also writes the depth keys); depth-first, the depth sort (4 passes);
+    5 binning kernels; the tile-id sort; ranges; the tile order (count and scatter kernels up
+    to 186 blocks of 256 tiles, one kernel beyond); tile-first, the per-tile depth sort
+    (tile_depth_launches); rasterize."""
     tile_bits = max(1, (tiles - 1).bit_length())
     order = 2 if -(-tiles // 256) <= 186 else 1
-    return 1 + sort_launches(32) + 5 + sort_launches(tile_bits) + 1 + order + 1
+    depth = tile_depth_launches(key_capacity) if tile_first else sort_launches(32)
+    return 1 + depth + 5 + sort_launches(tile_bits) + 1 + order + 1
 
 
 def code_hash(files) -> str:
@@ -400,6 +410,8 @@ def evaluation_count(torch, gs, g, cam, final_T, n_contrib, dev) -> int:
 
 
 STAGE_NAMES = ["preprocess", "depth_order", "bin", "tile_sort", "ranges", "rasterize"]
+# the event order of a tile-first frame: the depth sort runs per tile, after the ranges
+STAGE_NAMES_TILE_FIRST = ["preprocess", "bin", "tile_sort", "ranges", "depth_order", "rasterize"]
 
 
 def measure_view(torch, gs, native, g, cam, r, stream, dev, steps, warmup, use_graph, world=1):
@@ -464,6 +476,8 @@ def measure_view(torch, gs, native, g, cam, r, stream, dev, steps, warmup, use_g
                                           r.ws.data_ptr(), r.ws_bytes, r.image.data_ptr(), None, None, sp,
                                           arr, len(arr)), "gs_render_profiled")
 
+    tile_first = bool(L.gs_render_tile_first(int(g["n"]), int(cam["width"]), int(cam["height"]), r.key_capacity))
+    names = STAGE_NAMES_TILE_FIRST if tile_first else STAGE_NAMES
     st_ms = {k: 0.0 for k in STAGE_NAMES}
     with torch.cuda.stream(stream):
         pool = [new_events() for _ in range(n_stage)]
@@ -477,7 +491,7 @@ def measure_view(torch, gs, native, g, cam, r, stream, dev, steps, warmup, use_g
             profiled(arr)
     torch.cuda.synchronize(dev)
     for evs, _ in pool:
-        for i, k in enumerate(STAGE_NAMES):
+        for i, k in enumerate(names):
             st_ms[k] += evs[i].elapsed_time(evs[i + 1]) / n_stage
     # --- one frame with the per-pixel outputs, for the evaluation count
     with torch.cuda.stream(stream):
@@ -488,10 +502,10 @@ def measure_view(torch, gs, native, g, cam, r, stream, dev, steps, warmup, use_g
         raise RuntimeError(f"render status {st} flags {flags} keys {K}")
     evals = evaluation_count(torch, gs, g, cam, r.final_T, r.n_contrib, dev)
     return {"frame_ms": frame_ms, "stage_ms": st_ms, "stage_steps": n_stage, "keys": int(K),
-            "evaluations": evals, "graph": use_graph}
+            "evaluations": evals, "graph": use_graph, "tile_first": tile_first}
 
 
-def stage_summary(st_ms, n, sh_degree, K, tiles_x, tiles_y, evals, hbm_peak, fp32):
+def stage_summary(st_ms, n, sh_degree, K, tiles_x, tiles_y, evals, hbm_peak, fp32, tile_first=False):
     """Per-stage achieved rates and roofline fractions. HBM-bound stages: algorithmic bytes per
     unit (preprocess also in the method's count: parameters read + the 48-byte projected record
     written). Rasterize: evaluations x 15 flops (the method's count) against the measured FMA
@@ -501,8 +515,11 @@ def stage_summary(st_ms, n, sh_degree, K, tiles_x, tiles_y, evals, hbm_peak, fp3
     tpasses = (tile_bits + 7) // 8
     pb = param_bytes(sh_degree)
     stage_bytes = {
-        "preprocess": (pb + PROJ_BYTES_PER_G + 8) * n,   # + the depth keys and indices
-        "depth_order": 4 * 16 * n,
+        # (depth-first: + the depth keys and indices)
+        "preprocess": (pb + PROJ_BYTES_PER_G + (0 if tile_first else 8)) * n,
+        # depth-first: the keys and indices written, 4 passes of 16 B; tile-first: each list entry
+        # read, its depth gathered and the entry written back (12 B)
+        "depth_order": 12 * K if tile_first else 4 * 16 * n,
         "bin": 24 * n + 8 * K,
         "tile_sort": tpasses * 16 * K,
         "ranges": 4 * K + 8 * tiles_x * tiles_y + 12 * tiles_x * tiles_y,   # + the launch order
@@ -765,8 +782,9 @@ def run_ours(args, rank, local_rank, world):
                 for v, c, m in views:
                     ctx, cty = gs.tiles_xy(c)
                     recs.append({"view": v, "frame_ms": m["frame_ms"], "fps": 1e3 / m["frame_ms"], "keys": m["keys"],
+                                 "tile_first": m["tile_first"],
                                  "stages": stage_summary(m["stage_ms"], cfg_n.n, cfg_n.sh_degree, m["keys"], ctx, cty,
-                                                         m["evaluations"], hbm_peak, fp32)})
+                                                         m["evaluations"], hbm_peak, fp32, m["tile_first"])})
                 mean_ms = statistics.mean(x["frame_ms"] for x in recs)
                 mean_st = {}
                 for k in recs[0]["stages"]:
@@ -783,8 +801,9 @@ def run_ours(args, rank, local_rank, world):
 
     n = int(g["n"])
     K = head["keys"]
-    stages_out = stage_summary(st_ms, n, cfg.sh_degree, K, tx, ty, head["evaluations"], hbm_peak, fp32)
-    launches_per_frame = frame_launches(tx * ty)
+    stages_out = stage_summary(st_ms, n, cfg.sh_degree, K, tx, ty, head["evaluations"], hbm_peak, fp32,
+                               head["tile_first"])
+    launches_per_frame = frame_launches(tx * ty, head["tile_first"], r.key_capacity)
     ras = stages_out["rasterize"]
     evals = head["evaluations"]
     dominant = max(stages_out, key=lambda k: stages_out[k]["ms"])
@@ -810,6 +829,7 @@ def run_ours(args, rank, local_rank, world):
         "config": {"workload": cfg.description, "n": cfg.n, "width": cfg.width, "height": cfg.height,
                    "sh_degree": cfg.sh_degree, "view": args.view, "keys": K, "key_capacity": r.key_capacity,
                    "graph": not args.no_graph,
+                   "steps_order": "tile-first" if head["tile_first"] else "depth-first",
                    "l2": "inputs larger than L2: 236 MB of Gaussian parameters per frame (L2 126 MB)",
                    "parallelism": f"replicas x{world}"},
         "clocks": clocks,

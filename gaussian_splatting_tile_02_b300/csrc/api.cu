@@ -3,6 +3,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 
@@ -84,7 +85,7 @@ int tile_bits_for(const gs_camera& c) {
 // gs_render workspace layout
 struct RenderLayout {
     size_t header, raster, depth, touched, rect, dkeys, dkeys_alt, order, order_alt, bin,
-        keys, vals, keys_alt, vals_alt, sort, ranges, tile_order, pgrad, num_keys, total;
+        keys, vals, keys_alt, vals_alt, sort, ranges, tile_order, tdepth, pgrad, num_keys, total;
 };
 
 RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
@@ -115,6 +116,7 @@ RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
     L.sort = take(sort_scratch_bytes(cap > n ? cap : n));
     L.ranges = take(8 * tiles);
     L.tile_order = take(tile_order_scratch_bytes((int)tiles));
+    L.tdepth = take(tile_depth_scratch_bytes((int)tiles));
     L.pgrad = take(36 * un);   // backward: dL/d(u, v), dL/d(conic), dL/do, dL/dc
     L.total = o;
     return L;
@@ -157,8 +159,30 @@ DepthKeysOut view_depth_keys(char* w, const RenderLayout& L) {
     return dk;
 }
 
+// The order of steps 2-4 for a frame. Tile-first (bin in index order, stable
+// sort by tile, then each tile's list by depth) when the key capacity is at
+// most kTileFirstMaxKeys: below about a million pairs the four global passes
+// of the depth sort are short, latency-bound launches, and the per-tile sorts
+// (shared memory, one block per list) cost less. Above it the per-tile sorts
+// cost more than the depth sort of the Gaussians they replace, and the frame
+// is depth-first (depth order of the Gaussians, bin in that order, stable sort
+// by tile). Both give the same lists bit for bit. gs_set_steps_order can pin
+// either order.
+#ifndef GS_TILE_FIRST_MAX_KEYS
+#define GS_TILE_FIRST_MAX_KEYS (1 << 20)
+#endif
+constexpr int64_t kTileFirstMaxKeys = GS_TILE_FIRST_MAX_KEYS;
+std::atomic<int32_t> g_steps_order{0};   // 0 automatic, 1 depth-first, 2 tile-first
+bool tile_first(int64_t key_capacity, Step1 step1) {
+    if (step1 == Step1::kRecordOnly) return false;
+    const int32_t o = g_steps_order.load(std::memory_order_relaxed);
+    if (o != 0) return o == 2;
+    return key_capacity <= kTileFirstMaxKeys;
+}
+
 // Steps 2-5 of one view (step 1 as `step1` says), on stream s. events: null,
-// or 7 handles recorded at the stage boundaries.
+// or 7 handles recorded at the stage boundaries (see gs_render_profiled for
+// their order in each order of the steps).
 cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, char* w,
                           const RenderLayout& L, float* image, float* final_T, uint32_t* n_contrib, cudaStream_t s,
                           void* const* events, Step1 step1) {
@@ -187,6 +211,36 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
         return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
     };
     const DepthKeysOut dk = view_depth_keys(w, L);
+    const int n_tiles = cc.tiles_x * cc.tiles_y;
+    if (tile_first(key_capacity, step1)) {
+        // bin in index order, stable sort by tile, then each tile's list by (depth bits, index)
+        cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
+        if (e == cudaSuccess) e = mark(0);
+        if (e == cudaSuccess && step1 == Step1::kProject) e = launch_preprocess(*g, cc, p, s, nullptr, header);
+        if (e == cudaSuccess) e = mark(1);
+        if (e == cudaSuccess) e = sort_prepare_histogram(sort_ws, s);
+        if (e == cudaSuccess)
+            e = launch_bin_ordered(p, nullptr, g->n, cc, nullptr, keys, vals, key_capacity, num_keys, header,
+                                   w + L.bin, s, hist, tbits);
+        if (e == cudaSuccess) e = mark(2);
+        if (e == cudaSuccess)
+            e = launch_sort32(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, tbits, header, sort_ws,
+                              g_spin_limit, s, true);
+        if (e == cudaSuccess) e = mark(3);
+        if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s);
+        uint32_t* tile_order = nullptr;
+        if (e == cudaSuccess) e = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, s);
+        if (e == cudaSuccess) e = mark(4);
+        // the tile ids are not read again: their array is the long lists' key scratch
+        if (e == cudaSuccess)
+            e = launch_tile_depth_sort(ranges, tile_order, n_tiles, p.depth, g->n, key_capacity, vals, keys,
+                                       keys_alt, vals_alt, w + L.tdepth, s);
+        if (e == cudaSuccess) e = mark(5);
+        if (e == cudaSuccess)
+            e = launch_rasterize(p, g->n, vals, ranges, tile_order, cc, image, final_T, n_contrib, s);
+        if (e == cudaSuccess) e = mark(6);
+        return e;
+    }
     // the frame's setup (status header, the depth digits' histograms) comes
     // before the first stage mark, so that stage 1 brackets the projection alone
     cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
@@ -211,10 +265,9 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
         e = launch_sort32(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, tbits, header, sort_ws,
                           g_spin_limit, s, true);
     if (e == cudaSuccess) e = mark(4);
-    if (e == cudaSuccess)
-        e = launch_tile_ranges32(keys, num_keys, key_capacity, cc.tiles_x * cc.tiles_y, ranges, s);
+    if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s);
     uint32_t* tile_order = nullptr;
-    if (e == cudaSuccess) e = launch_tile_order_multi(ranges, cc.tiles_x * cc.tiles_y, w + L.tile_order, &tile_order, s);
+    if (e == cudaSuccess) e = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, s);
     if (e == cudaSuccess) e = mark(5);
     if (e == cudaSuccess)
         e = launch_rasterize(p, g->n, vals, ranges, tile_order, cc, image, final_T, n_contrib, s);
@@ -375,6 +428,18 @@ size_t gs_render_workspace_bytes(int64_t n, int32_t width, int32_t height, int64
 gs_status gs_render(const gs_gaussians* g, const gs_camera* cam, int64_t key_capacity, void* ws, size_t ws_bytes,
                     float* image, float* final_T, uint32_t* n_contrib, void* stream) {
     return render_impl(g, cam, key_capacity, ws, ws_bytes, image, final_T, n_contrib, stream, nullptr);
+}
+
+int32_t gs_render_tile_first(int64_t n, int32_t width, int32_t height, int64_t key_capacity) {
+    (void)n;
+    if (width < 1 || height < 1 || key_capacity < 0) return 0;
+    return tile_first(key_capacity, Step1::kProject) ? 1 : 0;
+}
+
+gs_status gs_set_steps_order(int32_t order) {
+    if (order < 0 || order > 2) return GS_ERR_INVALID_ARG;
+    g_steps_order.store(order, std::memory_order_relaxed);
+    return GS_OK;
 }
 
 gs_status gs_render_workspace_lists(const void* ws, int64_t n, int32_t width, int32_t height, int64_t key_capacity,
@@ -783,6 +848,7 @@ gs_status gs_debug_set_check_counter(uint64_t* device_counter) {
     if (e == cudaSuccess) e = set_check_counter_backward(p);
     if (e == cudaSuccess) e = set_check_counter_splat2d(p);
     if (e == cudaSuccess) e = set_check_counter_densify(p);
+    if (e == cudaSuccess) e = set_check_counter_tiledepth(p);
     return cuda_status(e);
 }
 

@@ -25,10 +25,13 @@
 // the forward kernel, so every skip decision and every alpha is bit-identical.
 // The tile, warp and lane layout, the per-warp ballot of entries whose alpha
 // box meets the warp's 8x8 block, and the list staging are the forward's; the
-// list is walked from the last contributor of the tile backwards. Per entry,
-// the warp sums its lanes' contributions (a reduce-scatter of the 9 values
-// over the lanes) and nine lanes add them to the Gaussian's gradient with one
-// global atomic instruction.
+// list is walked from the last contributor of the tile backwards. A lane's two
+// pixels are carried as pairs in packed fp32 arithmetic (PTX .f32x2): a pixel
+// that does not take the entry blends alpha = 0, which leaves its T and its
+// suffix colour a unchanged and adds no gradient, so both pixels run the same
+// instructions without branching. Per entry, the warp sums its lanes'
+// contributions (a reduce-scatter of the 9 values over the lanes) and nine
+// lanes add them to the Gaussian's gradient with one global atomic instruction.
 //
 // Step 1 backward (preprocess_backward_kernel): one thread per Gaussian maps
 // dL/d(u, v), dL/d(conic), dL/do, dL/dc to the parameters through
@@ -52,6 +55,37 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+typedef unsigned long long f2x;   // two fp32 in one 64-bit register pair (PTX .f32x2)
+__device__ __forceinline__ f2x pk2(float lo, float hi) {
+    f2x r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 up2(f2x v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ f2x mul2(f2x a, f2x b) {
+    f2x r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2x fma2(f2x a, f2x b, f2x c) {
+    f2x r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ f2x sub2(f2x a, f2x b) {
+    f2x r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float hsum(f2x v) {
+    const float2 p = up2(v);
+    return p.x + p.y;
 }
 
 // Sums 9 per-lane values over the warp as a reduce-scatter: at each butterfly
@@ -145,6 +179,8 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
     PixelState P1, P2;
     load_pixel(px, py, P1);
     load_pixel(px, py + 4, P2);
+    f2x TT = pk2(P1.T, P2.T), AA0 = pk2(P1.a0, P2.a0), AA1 = pk2(P1.a1, P2.a1), AA2 = pk2(P1.a2, P2.a2);
+    const f2x GG0 = pk2(P1.g0, P2.g0), GG1 = pk2(P1.g1, P2.g1), GG2 = pk2(P1.g2, P2.g2);
 
     if (threadIdx.x == 0) s_max = 0;
     __syncthreads();
@@ -239,33 +275,36 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
                 const bool c1 = lp < P1.last && e >= kLog2AlphaMin;
                 const bool c2 = lp < P2.last && e2 >= kLog2AlphaMin;
                 if (!__any_sync(0xffffffffu, c1 || c2)) continue;
-                float gu = 0.f, gv = 0.f, gA = 0.f, gB = 0.f, gC = 0.f, go = 0.f, gr = 0.f, gg = 0.f, gb = 0.f;
-                auto accumulate = [&](PixelState& S, float ee, float tt2, float ddy) {
-                    const float raw = fast_exp2(ee);
-                    const float alpha = fminf(0.99f, raw);
-                    const float Ti = __fdividef(S.T, 1.0f - alpha);   // 1 - alpha >= 0.01
-                    const float w = alpha * Ti;
-                    gr += w * S.g0;
-                    gg += w * S.g1;
-                    gb += w * S.g2;
-                    const float dLda = Ti * ((r.z - S.a0) * S.g0 + (r.w - S.a1) * S.g1 + (c.x - S.a2) * S.g2);
-                    S.a0 = alpha * r.z + (1.0f - alpha) * S.a0;
-                    S.a1 = alpha * r.w + (1.0f - alpha) * S.a1;
-                    S.a2 = alpha * c.x + (1.0f - alpha) * S.a2;
-                    S.T = Ti;
-                    if (raw < 0.99f) {
-                        const float dLds = -dLda * alpha;   // dL/dsigma
-                        // d = pixel - centre = -(dx, ddy); sigma = (t1^2 + t2^2) / log2(e)
-                        gu += dLds * kTwoOverLog2e * (q.z * t1 + r.x * tt2);
-                        gv += dLds * kTwoOverLog2e * (q.w * tt2);
-                        gA += dLds * 0.5f * dx * dx;
-                        gB += dLds * dx * ddy;
-                        gC += dLds * 0.5f * ddy * ddy;
-                        go += dLda * alpha * c.y;
-                    }
-                };
-                if (c1) accumulate(P1, e, t2, dy);
-                if (c2) accumulate(P2, e2, t22, dy2);
+                // both pixels in pairs; a pixel that does not take this entry blends alpha = 0,
+                // which leaves its state as it is and adds nothing
+                const float raw1 = c1 ? fast_exp2(e) : 0.0f, raw2 = c2 ? fast_exp2(e2) : 0.0f;
+                const float al1 = fminf(0.99f, raw1), al2 = fminf(0.99f, raw2);
+                const f2x AL = pk2(al1, al2);
+                const float2 tt = up2(TT);
+                const float ti1 = c1 ? __fdividef(tt.x, 1.0f - al1) : tt.x;   // 1 - alpha >= 0.01
+                const float ti2 = c2 ? __fdividef(tt.y, 1.0f - al2) : tt.y;
+                const f2x TI = pk2(ti1, ti2);
+                const f2x W = mul2(AL, TI);
+                const f2x D0 = sub2(pk2(r.z, r.z), AA0), D1 = sub2(pk2(r.w, r.w), AA1), D2 = sub2(pk2(c.x, c.x), AA2);
+                const f2x DLDA = mul2(TI, fma2(D2, GG2, fma2(D1, GG1, mul2(D0, GG0))));
+                AA0 = fma2(AL, D0, AA0);
+                AA1 = fma2(AL, D1, AA1);
+                AA2 = fma2(AL, D2, AA2);
+                TT = TI;
+                // below the 0.99 cap: dL/dsigma = -alpha dL/dalpha
+                const f2x ADA = mul2(DLDA, AL);
+                const f2x DLDS = mul2(ADA, pk2(raw1 < 0.99f ? -1.0f : 0.0f, raw2 < 0.99f ? -1.0f : 0.0f));
+                const f2x TT2 = pk2(t2, t22), DDY = pk2(dy, dy2);
+                const float zt1 = q.z * t1;
+                const f2x KD = mul2(DLDS, pk2(kTwoOverLog2e, kTwoOverLog2e));
+                const float gu = hsum(mul2(KD, fma2(pk2(r.x, r.x), TT2, pk2(zt1, zt1))));
+                const float gv = hsum(mul2(KD, mul2(pk2(q.w, q.w), TT2)));
+                const float hdx2 = 0.5f * dx * dx;
+                const float gA = hsum(mul2(DLDS, pk2(hdx2, hdx2)));
+                const float gB = hsum(mul2(DLDS, mul2(pk2(dx, dx), DDY)));
+                const float gC = hsum(mul2(DLDS, mul2(pk2(0.5f, 0.5f), mul2(DDY, DDY))));
+                const float go = hsum(mul2(ADA, pk2(raw1 < 0.99f ? c.y : 0.0f, raw2 < 0.99f ? c.y : 0.0f)));
+                const float gr = hsum(mul2(W, GG0)), gg = hsum(mul2(W, GG1)), gb = hsum(mul2(W, GG2));
                 const float part[9] = {gu, gv, gA, gB, gC, go, gr, gg, gb};
                 const float sum = warp_reduce_scatter9(part, lane);
                 const int slot = slot_of(lane);

@@ -244,12 +244,13 @@ constexpr int kExpandThreads = 256;
 constexpr int kWindow = 1024;   // positions staged per step
 
 // Rectangles in list order (coalesced reads for the three kernels below); a
-// Gaussian without tiles gets the marker x0 = 0xffff.
+// Gaussian without tiles gets the marker x0 = 0xffff. The list is the given
+// order, or the index order when order is null.
 __global__ void gather_rect_kernel(const uint32_t* __restrict__ tiles_touched, const ushort4* __restrict__ rect,
                                    const uint32_t* __restrict__ order, int64_t n, ushort4* __restrict__ rs) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const uint32_t g = __ldg(order + i);
+        const uint32_t g = at(order, i);
         // an index outside the scene can only come from a depth sort that was
         // cut short (flagged): no tiles, never a read past the arrays
         GS_CHECK(g < n);
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
         wn = wn < n - p ? wn : n - p;
         for (int i = threadIdx.x; i < wn; i += kExpandThreads) {
             s_first[i] = __ldg(first_slot + p + i);
-            s_g[i] = __ldg(order + p + i);
+            s_g[i] = at(order, p + i);
             s_rect[i] = __ldg(rs + p + i);
         }
         if (threadIdx.x == 0)

@@ -223,6 +223,18 @@ cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* n
                                  int64_t key_capacity, int n_tiles, uint32_t* ranges, cudaStream_t s);
 cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations, cudaStream_t s);
 
+// tiledepth.cu: each tile's list (Gaussians in index order, [ranges.x, ranges.y) of vals)
+// sorted by (depth bits, index) in place, tiles in the given launch order (nullable).
+// keys_a, keys_b, vals_b: scratch of the key capacity (lists longer than a block's
+// shared-memory sort go through them); scratch: tile_depth_scratch_bytes(tiles).
+// One kernel per list-size class that the key capacity allows (tile_depth_sort_launches).
+size_t tile_depth_scratch_bytes(int tiles);
+cudaError_t launch_tile_depth_sort(const uint32_t* ranges, const uint32_t* tile_order, int tiles, const float* depth,
+                                   int64_t n, int64_t key_capacity, uint32_t* vals, uint32_t* keys_a,
+                                   uint32_t* keys_b, uint32_t* vals_b, void* scratch, cudaStream_t s);
+int tile_depth_sort_launches(int64_t key_capacity);
+cudaError_t set_check_counter_tiledepth(unsigned long long* p);
+
 // rasterize.cu
 // 2D splats: their per-Gaussian record into p (depth, tiles_touched, rect, raster)
 cudaError_t launch_preprocess2d(const float* means, const float* covs, const float* colours, const float* opacities,

@@ -82,6 +82,7 @@ _SIGNATURES = {
                                     ctypes.POINTER(GsCamera), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "gs_render_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                                     ctypes.c_int64]),
+    "gs_render_tile_first": (ctypes.c_int32, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64]),
     "gs_render_workspace_lists": (ctypes.c_int, [c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                                  ctypes.c_int64, ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p)]),
     "gs_render": (ctypes.c_int, [ctypes.POINTER(GsGaussians), ctypes.POINTER(GsCamera), ctypes.c_int64,
@@ -130,6 +131,7 @@ _SIGNATURES = {
     "gs_fp32_peak_probe": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, c_void_p,
                                           ctypes.POINTER(ctypes.c_int64), c_void_p]),
     "gs_set_spin_limit": (None, [ctypes.c_int64]),
+    "gs_set_steps_order": (ctypes.c_int32, [ctypes.c_int32]),
     "gs_test_spin_timeout": (ctypes.c_int, [c_void_p, ctypes.c_int64, c_void_p]),
 }
 

@@ -269,10 +269,14 @@ gs_status gs_rasterize(const gs_projected* projected, int64_t n, const uint32_t*
                        const uint32_t* ranges, const gs_camera* camera, float* image,
                        float* final_T, uint32_t* n_contrib, uint32_t* tile_order, void* stream);
 
-/* The whole frame: step 1, the depth-first steps 2-4 (gs_depth_order,
- * gs_bin_ordered, gs_sort32, gs_tile_ranges32) and step 5, chained on
- * `stream` with no host synchronisation (so the call can be captured into a
- * CUDA graph). The image equals the one of the staged path
+/* The whole frame: step 1, steps 2-4 in one of two orders, and step 5, chained
+ * on `stream` with no host synchronisation (so the call can be captured into a
+ * CUDA graph). Depth-first (gs_depth_order, gs_bin_ordered, gs_sort32,
+ * gs_tile_ranges32): the Gaussians are sorted by depth, binned in that order
+ * and stably sorted by tile. Tile-first, for short tile lists (see
+ * gs_render_tile_first): binned in index order, stably sorted by tile, then
+ * each tile's list is sorted by (depth bits, index) on its own. Both give the
+ * same per-tile lists bit for bit. The image equals the one of the staged path
  * gs_preprocess/gs_bin/gs_sort/gs_tile_ranges/gs_rasterize bit for bit. All
  * intermediates live in ws (device, 256-byte aligned, at least
  * gs_render_workspace_bytes(n, width, height, key_capacity) bytes); the first
@@ -286,6 +290,20 @@ size_t gs_render_workspace_bytes(int64_t n, int32_t width, int32_t height, int64
 gs_status gs_render(const gs_gaussians* gaussians, const gs_camera* camera, int64_t key_capacity,
                     void* ws, size_t ws_bytes, float* image, float* final_T,
                     uint32_t* n_contrib, void* stream);
+
+/* 1 if gs_render takes the tile-first order of steps 2-4 for these sizes, 0 if
+ * depth-first: tile-first when key_capacity is at most 2^20 pairs (the
+ * frame's four global depth-sort passes would be short, latency-bound
+ * launches), unless gs_set_steps_order pins an order. Host-only arithmetic
+ * (no CUDA call). */
+int32_t gs_render_tile_first(int64_t n, int32_t width, int32_t height, int64_t key_capacity);
+
+/* Pins the order of steps 2-4 for gs_render, gs_render_profiled and
+ * gs_render_batch frames enqueued after the call: 0 automatic (the default,
+ * gs_render_tile_first), 1 depth-first, 2 tile-first. Either order gives the
+ * same lists and image bit for bit; the pin is for tests and measurement.
+ * Process-wide; GS_ERR_INVALID_ARG for other values. */
+gs_status gs_set_steps_order(int32_t order);
 
 /* Where a gs_render (or one view of gs_render_batch) workspace keeps the
  * frame's per-tile lists: *sorted_vals receives the device address of the
@@ -302,11 +320,16 @@ gs_status gs_render_workspace_lists(const void* ws, int64_t n, int32_t width, in
 
 /* gs_render that also records CUDA events at its stage boundaries, for
  * per-stage timing of the very launches a frame makes. events[0..6] are
- * caller-created cudaEvent_t handles (as void*), recorded on `stream`:
- *   0 start (after the frame's setup memsets: status header and the depth
- *   digits' histograms), 1 after projection, 2 after the depth order, 3 after binning,
- *   4 after the tile sort, 5 after the ranges and the tiles' launch order,
- *   6 after compositing (the compositing kernel alone).
+ * caller-created cudaEvent_t handles (as void*), recorded on `stream`, in the
+ * order of the steps the frame takes (gs_render_tile_first):
+ *   depth-first: 0 start (after the frame's setup memsets: status header and
+ *   the depth digits' histograms), 1 after projection, 2 after the depth order
+ *   of the Gaussians, 3 after binning, 4 after the tile sort, 5 after the
+ *   ranges and the tiles' launch order, 6 after compositing (the compositing
+ *   kernel alone);
+ *   tile-first: 0 start, 1 after projection, 2 after binning, 3 after the tile
+ *   sort, 4 after the ranges and the tiles' launch order, 5 after the per-tile
+ *   depth sort, 6 after compositing.
  * n_events must be >= GS_RENDER_STAGES + 1. */
 #define GS_RENDER_STAGES 6
 gs_status gs_render_profiled(const gs_gaussians* gaussians, const gs_camera* camera,

@@ -81,6 +81,28 @@ def test_workspace_lists_lie_inside_the_workspace():
         native.GS_ERR_INVALID_ARG
 
 
+def test_render_order_of_the_steps():
+    """Tile-first when the key capacity is at most 2^20 pairs, unless an order is pinned."""
+    L = native.lib()
+    assert L.gs_render_tile_first(10**6, 1920, 1080, 1 << 20) == 1
+    assert L.gs_render_tile_first(10**6, 1920, 1080, (1 << 20) + 1) == 0
+    assert L.gs_render_tile_first(10**6, 1920, 1080, 3 * 10**6) == 0
+    assert L.gs_render_tile_first(10**5, 1920, 1080, 400_000) == 1
+    assert L.gs_render_tile_first(256, 64, 64, 2000) == 1
+    assert L.gs_render_tile_first(10, 0, 64, 10) == 0
+    try:
+        assert L.gs_set_steps_order(1) == native.GS_OK
+        assert L.gs_render_tile_first(256, 64, 64, 2000) == 0
+        assert L.gs_set_steps_order(2) == native.GS_OK
+        assert L.gs_render_tile_first(10**6, 1920, 1080, 3 * 10**6) == 1
+        assert L.gs_set_steps_order(3) == native.GS_ERR_INVALID_ARG
+        assert L.gs_set_steps_order(-1) == native.GS_ERR_INVALID_ARG
+        assert L.gs_render_tile_first(10**6, 1920, 1080, 3 * 10**6) == 1
+    finally:
+        assert L.gs_set_steps_order(0) == native.GS_OK
+    assert L.gs_render_tile_first(10**6, 1920, 1080, 3 * 10**6) == 0
+
+
 def test_fp32_peak_probe_rejects_bad_arguments():
     L = native.lib()
     n = ctypes.c_int64(0)

@@ -224,6 +224,63 @@ def test_render_equals_stages_and_graph_replay(oracle_mod):
     assert_image_parity(check_image(oracle_mod, ref, cam, out["image"], out["final_T"], out["n_contrib"]))
 
 
+@pytest.mark.parametrize("name,n,view", [("tiny", None, 0), ("100k", None, 0), ("stress", 100_000, 2)])
+def test_tile_first_and_depth_first_orders_agree(oracle_mod, name, n, view):
+    """gs_render bins in index order and sorts each tile's list by depth (tile-first), or sorts
+    all Gaussians by depth first (depth-first); both orders, pinned in turn, must give the
+    staged path's sorted lists, ranges and image bit for bit. The 100k-Gaussian stress scene
+    has lists in every size class of the per-tile sort: up to 512 entries (128-thread blocks),
+    up to 2048 and up to 8192 (256- and 1024-thread blocks) and longer (the chunked sort)."""
+    scene, g = scene_of(name, n)
+    cam = scenes.make_cameras(name)[view]
+    out = run_stages(g, cam)
+    K = out["K"]
+    L = gs.lib()
+    lens = (out["ranges"][:, 1].astype(np.int64) - out["ranges"][:, 0])
+    if name == "stress":
+        for lo, hi in ((1, 512), (512, 2048), (2048, 8192), (8192, 1 << 40)):
+            assert ((lens > lo) & (lens <= hi)).any(), (lo, hi)
+    try:
+        for order in (2, 1):
+            assert L.gs_set_steps_order(order) == native.GS_OK
+            assert L.gs_render_tile_first(int(g["n"]), cam["width"], cam["height"], K + 64) == (order == 2)
+            r = gs.Renderer(g, cam["width"], cam["height"], K + 64)
+            r.render(cam)
+            torch.cuda.synchronize()
+            st, flags, k = r.status()
+            assert st == native.GS_OK and k == K, (order, st, flags, k)
+            vals, ranges = r.lists()
+            np.testing.assert_array_equal(vals.cpu().numpy().view(np.uint32)[:K], out["sorted_vals"])
+            np.testing.assert_array_equal(ranges.cpu().numpy().view(np.uint32), out["ranges"])
+            np.testing.assert_array_equal(r.image.cpu().numpy(), out["image"])
+            np.testing.assert_array_equal(r.final_T.cpu().numpy(), out["final_T"])
+            np.testing.assert_array_equal(r.n_contrib.cpu().numpy(), out["n_contrib"])
+            del r
+    finally:
+        L.gs_set_steps_order(0)
+
+
+def test_batch_views_agree_in_both_orders():
+    """gs_render_batch with the order of steps 2-4 pinned tile-first and depth-first: every
+    view's image, final T and n_contrib are equal bit for bit."""
+    scene, g = scene_of("stress", 100_000)
+    cams = scenes.make_cameras("stress")[:3]
+    L = gs.lib()
+    outs = []
+    try:
+        for order in (2, 1):
+            assert L.gs_set_steps_order(order) == native.GS_OK
+            b = gs.BatchRenderer.for_scene(g, cams, headroom=1.1, n_streams=2)
+            b.render(aux=True)
+            torch.cuda.synchronize()
+            outs.append([t.cpu().numpy().copy() for t in (b.images, b.final_T, b.n_contrib)])
+            del b
+    finally:
+        L.gs_set_steps_order(0)
+    for x, y in zip(*outs):
+        np.testing.assert_array_equal(x, y)
+
+
 def test_tile_order_is_heavy_first_and_leaves_image_unchanged():
     """The heavy-first launch order is a permutation of the tiles with
     non-increasing floor(log2 length); the image, final T and n_contrib do not

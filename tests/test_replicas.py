@@ -122,3 +122,11 @@ def test_frame_launch_count():
     assert bench.frame_launches(4 * 4) == 18
     assert bench.frame_launches(512 * 270) == 19
     assert bench.frame_launches(240 * 135) == 18   # 3840x2160: 15 bits, two passes, 127 order blocks
+    # tile-first frames sort each tile's list instead of all Gaussians by depth: one kernel per
+    # list-size class the key capacity allows (up to 512, 2048, 8192 entries, and longer)
+    assert bench.frame_launches(120 * 68, tile_first=True, key_capacity=400_000) == 17
+    assert bench.frame_launches(120 * 68, tile_first=True, key_capacity=8192) == 16
+    assert bench.frame_launches(4 * 4, tile_first=True, key_capacity=2000) == 15
+    assert bench.frame_launches(4 * 4, tile_first=True, key_capacity=512) == 14
+    assert [bench.tile_depth_launches(c) for c in (0, 1, 2, 512, 513, 2048, 2049, 8192, 8193)] == \
+        [0, 0, 1, 1, 2, 2, 3, 3, 4]
