@@ -12,6 +12,7 @@
 namespace gs {
 
 long long g_spin_limit = 1ll << 22;   // ~1 s of polling with backoff
+std::atomic<int> g_programmatic_launch{1};
 constexpr long long kDefaultSpin = 1ll << 22;
 constexpr int64_t kMaxKeyCapacity = (1ll << 30) - 1;   // look-back status words keep 30 bits
 constexpr int64_t kMaxGaussians = (1ll << 32) - 1;     // values are uint32 indices
@@ -82,10 +83,14 @@ int tile_bits_for(const gs_camera& c) {
     return b > 0 ? b : 1;
 }
 
-// gs_render workspace layout
+// gs_render workspace layout. The buffers a frame must find zeroed sit at
+// the start, [header, zero_end), so one memset at the frame's start clears
+// them all and no memset separates two kernels of the frame (each kernel is
+// then launched as a programmatic dependent of the one before it).
 struct RenderLayout {
-    size_t header, raster, depth, touched, rect, dkeys, dkeys_alt, order, order_alt, bin,
-        keys, vals, keys_alt, vals_alt, sort, ranges, tile_order, tdepth, pgrad, num_keys, total;
+    size_t header, num_keys, depth_head, ranges, order_done, td_counts, tile_head, zero_end, raster, depth,
+        touched, rect, dkeys, dkeys_alt, order, order_alt, bin, keys, vals, keys_alt, vals_alt, depth_lb, tile_lb,
+        tile_order, tdepth, pgrad, total;
 };
 
 RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
@@ -100,6 +105,12 @@ RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
     const size_t tiles = (size_t)((w + kTile - 1) / kTile) * (size_t)((h + kTile - 1) / kTile);
     L.header = take(sizeof(StatusHeader));
     L.num_keys = take(sizeof(uint64_t));
+    L.depth_head = take(sort_head_bytes());      // the depth sort's digit histograms and counters
+    L.ranges = take(8 * tiles);
+    L.order_done = take(sizeof(uint32_t));       // the tile order's finished-block counter
+    L.td_counts = take(3 * sizeof(uint32_t));    // the per-tile depth sort's list lengths
+    L.tile_head = take(sort_head_bytes());       // the tile sort's digit histograms and counters
+    L.zero_end = o;
     L.raster = take(48 * un);
     L.depth = take(4 * un);
     L.touched = take(4 * un);
@@ -113,8 +124,8 @@ RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
     L.vals = take(4 * uc);
     L.keys_alt = take(4 * uc);
     L.vals_alt = take(4 * uc);
-    L.sort = take(sort_scratch_bytes(cap > n ? cap : n));
-    L.ranges = take(8 * tiles);
+    L.depth_lb = take(sort_lookback_bytes(n));
+    L.tile_lb = take(sort_lookback_bytes(cap));
     L.tile_order = take(tile_order_scratch_bytes((int)tiles));
     L.tdepth = take(tile_depth_scratch_bytes((int)tiles));
     L.pgrad = take(36 * un);   // backward: dL/d(u, v), dL/d(conic), dL/do, dL/dc
@@ -155,7 +166,7 @@ DepthKeysOut view_depth_keys(char* w, const RenderLayout& L) {
     DepthKeysOut dk;
     dk.keys = reinterpret_cast<uint32_t*>(w + L.dkeys);
     dk.vals = reinterpret_cast<uint32_t*>(w + L.order);
-    dk.hist = sort_histogram_of(w + L.sort);
+    dk.hist = sort_histogram_of(w + L.depth_head);
     return dk;
 }
 
@@ -200,74 +211,74 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
     auto* ranges = reinterpret_cast<uint32_t*>(w + L.ranges);
     const CamConst cc = make_cam_const(*cam);
 
-    // depth order first, then (tile, index) pairs in that order, then a stable
-    // sort by tile: the same per-tile (depth, index) order as sorting the
-    // 64-bit tile|depth keys, with far fewer key bits moved
-    // (the producers of both key lists also count their sort digits)
-    void* sort_ws = w + L.sort;
-    uint32_t* hist = sort_histogram_of(sort_ws);
     const int tbits = tile_bits_for(*cam);
     auto mark = [&](int i) {
         return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
     };
-    const DepthKeysOut dk = view_depth_keys(w, L);
+    uint32_t* tile_hist = sort_histogram_of(w + L.tile_head);
     const int n_tiles = cc.tiles_x * cc.tiles_y;
+    // the frame's setup, before the first stage mark (so that stage 1 brackets
+    // the projection alone): one memset of the buffers the frame finds zeroed;
+    // a batch view keeps the depth histograms its projection filled
+    cudaError_t e;
+    if (step1 == Step1::kKeysReady) {
+        e = cudaMemsetAsync(w + L.header, 0, L.depth_head - L.header, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(w + L.ranges, 0, L.zero_end - L.ranges, s);
+    } else {
+        e = cudaMemsetAsync(w + L.header, 0, L.zero_end - L.header, s);
+    }
+    if (e == cudaSuccess) e = mark(0);
+    uint32_t* tile_order = nullptr;
+    auto* order_done = reinterpret_cast<uint32_t*>(w + L.order_done);
     if (tile_first(key_capacity, step1)) {
         // bin in index order, stable sort by tile, then each tile's list by (depth bits, index)
-        cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
-        if (e == cudaSuccess) e = mark(0);
         if (e == cudaSuccess && step1 == Step1::kProject) e = launch_preprocess(*g, cc, p, s, nullptr, header);
         if (e == cudaSuccess) e = mark(1);
-        if (e == cudaSuccess) e = sort_prepare_histogram(sort_ws, s);
         if (e == cudaSuccess)
             e = launch_bin_ordered(p, nullptr, g->n, cc, nullptr, keys, vals, key_capacity, num_keys, header,
-                                   w + L.bin, s, hist, tbits);
+                                   w + L.bin, s, tile_hist, tbits);
         if (e == cudaSuccess) e = mark(2);
         if (e == cudaSuccess)
-            e = launch_sort32(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, tbits, header, sort_ws,
-                              g_spin_limit, s, true);
+            e = launch_sort32_split(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, tbits, header,
+                                    w + L.tile_head, w + L.tile_lb, g_spin_limit, s, true);
         if (e == cudaSuccess) e = mark(3);
-        if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s);
-        uint32_t* tile_order = nullptr;
-        if (e == cudaSuccess) e = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, s);
+        if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s, true);
+        if (e == cudaSuccess)
+            e = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, s, order_done);
         if (e == cudaSuccess) e = mark(4);
         // the tile ids are not read again: their array is the long lists' key scratch
         if (e == cudaSuccess)
             e = launch_tile_depth_sort(ranges, tile_order, n_tiles, p.depth, g->n, key_capacity, vals, keys,
-                                       keys_alt, vals_alt, w + L.tdepth, s);
+                                       keys_alt, vals_alt, reinterpret_cast<uint32_t*>(w + L.td_counts),
+                                       w + L.tdepth, s);
         if (e == cudaSuccess) e = mark(5);
         if (e == cudaSuccess)
             e = launch_rasterize(p, g->n, vals, ranges, tile_order, cc, image, final_T, n_contrib, s);
         if (e == cudaSuccess) e = mark(6);
         return e;
     }
-    // the frame's setup (status header, the depth digits' histograms) comes
-    // before the first stage mark, so that stage 1 brackets the projection alone
-    cudaError_t e = cudaMemsetAsync(header, 0, sizeof(StatusHeader), s);
-    if (e == cudaSuccess && step1 == Step1::kProject) e = sort_prepare_histogram(sort_ws, s);
-    if (e == cudaSuccess) e = mark(0);
+    // depth order first, then (tile, index) pairs in that order, then a stable
+    // sort by tile: the same per-tile (depth, index) order as sorting the
+    // 64-bit tile|depth keys, with far fewer key bits moved
+    // (the producers of both key lists also count their sort digits)
+    const DepthKeysOut dk = view_depth_keys(w, L);
     if (e == cudaSuccess && step1 == Step1::kProject) e = launch_preprocess(*g, cc, p, s, &dk, header);
     if (e == cudaSuccess) e = mark(1);
-    if (e == cudaSuccess && step1 == Step1::kRecordOnly) {
-        e = sort_prepare_histogram(sort_ws, s);
-        if (e == cudaSuccess) e = launch_depth_keys(p, g->n, dkeys, order, hist, s);
-    }
+    if (e == cudaSuccess && step1 == Step1::kRecordOnly) e = launch_depth_keys(p, g->n, dkeys, order, dk.hist, s);
     if (e == cudaSuccess)
-        e = launch_sort32(dkeys, order, dkeys_alt, order_alt, nullptr, g->n, 32, header, sort_ws, g_spin_limit, s,
-                          true);
+        e = launch_sort32_split(dkeys, order, dkeys_alt, order_alt, nullptr, g->n, 32, header, w + L.depth_head,
+                                w + L.depth_lb, g_spin_limit, s, true);
     if (e == cudaSuccess) e = mark(2);
-    if (e == cudaSuccess) e = sort_prepare_histogram(sort_ws, s);
     if (e == cudaSuccess)
         e = launch_bin_ordered(p, order, g->n, cc, nullptr, keys, vals, key_capacity, num_keys, header, w + L.bin, s,
-                               hist, tbits);
+                               tile_hist, tbits);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess)
-        e = launch_sort32(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, tbits, header, sort_ws,
-                          g_spin_limit, s, true);
+        e = launch_sort32_split(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, tbits, header,
+                                w + L.tile_head, w + L.tile_lb, g_spin_limit, s, true);
     if (e == cudaSuccess) e = mark(4);
-    if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s);
-    uint32_t* tile_order = nullptr;
-    if (e == cudaSuccess) e = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, s);
+    if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s, true);
+    if (e == cudaSuccess) e = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, s, order_done);
     if (e == cudaSuccess) e = mark(5);
     if (e == cudaSuccess)
         e = launch_rasterize(p, g->n, vals, ranges, tile_order, cc, image, final_T, n_contrib, s);
@@ -435,6 +446,8 @@ int32_t gs_render_tile_first(int64_t n, int32_t width, int32_t height, int64_t k
     if (width < 1 || height < 1 || key_capacity < 0) return 0;
     return tile_first(key_capacity, Step1::kProject) ? 1 : 0;
 }
+
+void gs_set_programmatic_launch(int32_t on) { g_programmatic_launch.store(on ? 1 : 0, std::memory_order_relaxed); }
 
 gs_status gs_set_steps_order(int32_t order) {
     if (order < 0 || order > 2) return GS_ERR_INVALID_ARG;
@@ -758,7 +771,7 @@ gs_status gs_render_batch(const gs_gaussians* g, const gs_camera* cams, int32_t 
             cc[i] = make_cam_const(cams[v0 + i]);
             pr[i] = view_projected(wv, L);
             dk[i] = view_depth_keys(wv, L);
-            if (sort_prepare_histogram(wv + L.sort, s0) != cudaSuccess) return GS_ERR_CUDA;
+            if (sort_prepare_histogram(wv + L.depth_head, s0) != cudaSuccess) return GS_ERR_CUDA;
         }
         if (launch_preprocess_batch(*g, cc, pr, dk, nv, s0) != cudaSuccess) return GS_ERR_CUDA;
     }

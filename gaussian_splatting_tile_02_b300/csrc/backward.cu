@@ -138,6 +138,7 @@ struct PixelState {
 };
 
 __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const BwdArgs a) {
+    grid_dependency_begin();
     __shared__ float4 s_q[2][kBwdThreads];    // (mx, my, k1, k2), centre tile-local
     __shared__ float4 s_r[2][kBwdThreads];    // (k3, log2 o, r, g)
     __shared__ float2 s_c[2][kBwdThreads];    // (b, 1/o)
@@ -562,6 +563,7 @@ constexpr int kPreBwdThreads = 128;
 
 template <int D>
 __global__ void __launch_bounds__(kPreBwdThreads) preprocess_backward_kernel(const PreBwdArgs a) {
+    grid_dependency_begin();
     constexpr int NK = (D + 1) * (D + 1);
     constexpr int NC = NK * 3, NS = NC + 1;
     __shared__ float s_sh[kPreBwdThreads * NS];
@@ -610,7 +612,7 @@ cudaError_t launch_rasterize_backward(const gs_projected& p, int64_t n, const ui
     a.g_opacity = grad.opacity;
     a.g_rgb = grad.rgb;
     const unsigned tiles = (unsigned)(cam.tiles_x * cam.tiles_y);
-    rasterize_backward_kernel<<<tiles, kBwdThreads, 0, s>>>(a);
+    launch_k(rasterize_backward_kernel, tiles, kBwdThreads, 0, s, a);
     return cudaGetLastError();
 }
 
@@ -638,10 +640,10 @@ cudaError_t launch_preprocess_backward(const gs_gaussians& g, const CamConst& ca
     a.d_sh = gout.sh;
     const unsigned blocks = (unsigned)((g.n + kPreBwdThreads - 1) / kPreBwdThreads);
     switch (g.sh_degree) {
-        case 0: preprocess_backward_kernel<0><<<blocks, kPreBwdThreads, 0, s>>>(a); break;
-        case 1: preprocess_backward_kernel<1><<<blocks, kPreBwdThreads, 0, s>>>(a); break;
-        case 2: preprocess_backward_kernel<2><<<blocks, kPreBwdThreads, 0, s>>>(a); break;
-        default: preprocess_backward_kernel<3><<<blocks, kPreBwdThreads, 0, s>>>(a); break;
+        case 0: launch_k(preprocess_backward_kernel<0>, blocks, kPreBwdThreads, 0, s, a); break;
+        case 1: launch_k(preprocess_backward_kernel<1>, blocks, kPreBwdThreads, 0, s, a); break;
+        case 2: launch_k(preprocess_backward_kernel<2>, blocks, kPreBwdThreads, 0, s, a); break;
+        default: launch_k(preprocess_backward_kernel<3>, blocks, kPreBwdThreads, 0, s, a); break;
     }
     return cudaGetLastError();
 }

@@ -80,6 +80,7 @@ __device__ __forceinline__ uint32_t at(const uint32_t* __restrict__ order, int64
 __global__ void __launch_bounds__(kBinThreads) bin_reduce_kernel(const uint32_t* __restrict__ tiles_touched,
                                                                  const uint32_t* __restrict__ order, int64_t n,
                                                                  unsigned long long* __restrict__ block_sums) {
+    grid_dependency_begin();
     __shared__ unsigned long long warp_tot[kBinThreads / 32];
     __shared__ unsigned long long total;
     const int64_t base = (int64_t)blockIdx.x * kBinChunk + (int64_t)threadIdx.x * kBinItems;
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_reduce_kernel(const uint32_t*
 __global__ void __launch_bounds__(1024) bin_scan_sums_kernel(unsigned long long* __restrict__ sums, int nb,
                                                              int64_t key_capacity, uint64_t* __restrict__ num_keys,
                                                              StatusHeader* __restrict__ status) {
+    grid_dependency_begin();
     __shared__ unsigned long long warp_tot[32];
     __shared__ unsigned long long carry;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_duplicate_kernel(
     const uint32_t* __restrict__ order, int64_t n, int tiles_x, const unsigned long long* __restrict__ block_prefix,
     int64_t key_capacity, uint32_t* __restrict__ offsets, KeyT* __restrict__ keys, uint32_t* __restrict__ vals,
     uint32_t* __restrict__ hist, int key_bits) {
+    grid_dependency_begin();
     __shared__ uint32_t s_dhist[kHistPasses * 256];
     __shared__ unsigned long long warp_tot[kBinThreads / 32];
     __shared__ unsigned long long total;
@@ -248,6 +251,7 @@ constexpr int kWindow = 1024;   // positions staged per step
 // order, or the index order when order is null.
 __global__ void gather_rect_kernel(const uint32_t* __restrict__ tiles_touched, const ushort4* __restrict__ rect,
                                    const uint32_t* __restrict__ order, int64_t n, ushort4* __restrict__ rs) {
+    grid_dependency_begin();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
         const uint32_t g = at(order, i);
@@ -264,6 +268,7 @@ __device__ __forceinline__ uint32_t rect_tiles(const ushort4 r) {
 
 __global__ void __launch_bounds__(kBinThreads) bin_reduce_rect_kernel(const ushort4* __restrict__ rs, int64_t n,
                                                                       unsigned long long* __restrict__ block_sums) {
+    grid_dependency_begin();
     __shared__ unsigned long long warp_tot[kBinThreads / 32];
     __shared__ unsigned long long total;
     const int64_t base = (int64_t)blockIdx.x * kBinChunk + (int64_t)threadIdx.x * kBinItems;
@@ -279,6 +284,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_offsets_kernel(
     const ushort4* __restrict__ rs, int64_t n,
     const unsigned long long* __restrict__ block_prefix, int64_t key_capacity, uint32_t* __restrict__ first_slot,
     uint32_t* __restrict__ owner, uint32_t* __restrict__ offsets) {
+    grid_dependency_begin();
     __shared__ unsigned long long warp_tot[kBinThreads / 32];
     __shared__ unsigned long long total;
     const int64_t chunk0 = (int64_t)blockIdx.x * kBinChunk;
@@ -316,6 +322,7 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
     const uint32_t* __restrict__ first_slot, const uint32_t* __restrict__ owner,
     const uint64_t* __restrict__ num_keys, int64_t key_capacity, uint32_t* __restrict__ keys,
     uint32_t* __restrict__ vals, uint32_t* __restrict__ hist, int key_bits) {
+    grid_dependency_begin();
     __shared__ uint32_t s_first[kWindow];
     __shared__ ushort4 s_rect[kWindow];
     __shared__ uint32_t s_g[kWindow];
@@ -424,6 +431,7 @@ __global__ void __launch_bounds__(256) depth_keys_kernel(const float* __restrict
                                                          const uint32_t* __restrict__ tiles_touched, int64_t n,
                                                          uint32_t* __restrict__ keys, uint32_t* __restrict__ vals,
                                                          uint32_t* __restrict__ hist) {
+    grid_dependency_begin();
     __shared__ uint32_t s_dhist[kHistPasses * 256];
     if (hist)
         for (int i = threadIdx.x; i < kHistPasses * 256; i += blockDim.x) s_dhist[i] = 0;
@@ -460,11 +468,11 @@ cudaError_t launch_bin_t(const gs_projected& p, const uint32_t* order, int64_t n
     }
     const int nb = (int)((n + kBinChunk - 1) / kBinChunk);
     auto* sums = static_cast<unsigned long long*>(scratch);
-    bin_reduce_kernel<<<nb, kBinThreads, 0, s>>>(p.tiles_touched, order, n, sums);
-    bin_scan_sums_kernel<<<1, 1024, 0, s>>>(sums, nb, key_capacity, num_keys, status);
-    bin_duplicate_kernel<KeyT><<<nb, kBinThreads, 0, s>>>(p.tiles_touched, reinterpret_cast<const ushort4*>(p.rect),
-                                                          p.depth, order, n, cam.tiles_x, sums, key_capacity,
-                                                          offsets, keys, vals, hist, key_bits);
+    launch_k(bin_reduce_kernel, nb, kBinThreads, 0, s, p.tiles_touched, order, n, sums);
+    launch_k(bin_scan_sums_kernel, 1, 1024, 0, s, sums, nb, key_capacity, num_keys, status);
+    launch_k(bin_duplicate_kernel<KeyT>, nb, kBinThreads, 0, s, p.tiles_touched,
+             reinterpret_cast<const ushort4*>(p.rect), p.depth, order, n, cam.tiles_x, sums, key_capacity, offsets,
+             keys, vals, hist, key_bits);
     return cudaGetLastError();
 }
 
@@ -498,15 +506,15 @@ cudaError_t launch_bin_ordered(const gs_projected& p, const uint32_t* order, int
     auto* owner = reinterpret_cast<uint32_t*>(w + bin_scratch_bytes(n) + align_up(4 * (size_t)n));
     auto* rs = reinterpret_cast<ushort4*>(w + bin_scratch_bytes(n) + align_up(4 * (size_t)n) + align_up(4 * blocks_b));
     const int64_t gb = (n + 255) / 256;
-    gather_rect_kernel<<<(unsigned)(gb < 148 * 16 ? gb : 148 * 16), 256, 0, s>>>(
-        p.tiles_touched, reinterpret_cast<const ushort4*>(p.rect), order, n, rs);
-    bin_reduce_rect_kernel<<<nb, kBinThreads, 0, s>>>(rs, n, sums);
-    bin_scan_sums_kernel<<<1, 1024, 0, s>>>(sums, nb, key_capacity, num_keys, status);
-    bin_offsets_kernel<<<nb, kBinThreads, 0, s>>>(rs, n, sums, key_capacity, first_slot, owner, offsets);
+    launch_k(gather_rect_kernel, (unsigned)(gb < 148 * 16 ? gb : 148 * 16), 256, 0, s,
+             p.tiles_touched, reinterpret_cast<const ushort4*>(p.rect), order, n, rs);
+    launch_k(bin_reduce_rect_kernel, nb, kBinThreads, 0, s, rs, n, sums);
+    launch_k(bin_scan_sums_kernel, 1, 1024, 0, s, sums, nb, key_capacity, num_keys, status);
+    launch_k(bin_offsets_kernel, nb, kBinThreads, 0, s, rs, n, sums, key_capacity, first_slot, owner, offsets);
     if (key_capacity > 0) {
         const unsigned blocks = (unsigned)((key_capacity + kKeysPerBlock - 1) / kKeysPerBlock);
-        bin_expand_kernel<<<blocks, kExpandThreads, 0, s>>>(rs, order, n, cam.tiles_x, first_slot, owner, num_keys,
-                                                            key_capacity, tile_keys, vals, hist, key_bits);
+        launch_k(bin_expand_kernel, blocks, kExpandThreads, 0, s, rs, order, n, cam.tiles_x, first_slot, owner,
+                 num_keys, key_capacity, tile_keys, vals, hist, key_bits);
     }
     return cudaGetLastError();
 }
@@ -515,8 +523,8 @@ cudaError_t launch_depth_keys(const gs_projected& p, int64_t n, uint32_t* keys, 
                               cudaStream_t s) {
     if (n == 0) return cudaSuccess;
     int64_t b = (n + 1023) / 1024;
-    depth_keys_kernel<<<(unsigned)(b < 148 * 4 ? b : 148 * 4), 256, 0, s>>>(p.depth, p.tiles_touched, n, keys,
-                                                                            vals, hist);
+    launch_k(depth_keys_kernel, (unsigned)(b < 148 * 4 ? b : 148 * 4), 256, 0, s, p.depth, p.tiles_touched, n, keys,
+             vals, hist);
     return cudaGetLastError();
 }
 

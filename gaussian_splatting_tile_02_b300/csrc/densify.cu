@@ -30,6 +30,7 @@ constexpr int kDensThreads = 256;
 __global__ void __launch_bounds__(256) densify_stats_kernel(const float2* __restrict__ grad_mean2d,
                                                             const uint32_t* __restrict__ tiles_touched, int64_t n,
                                                             float* __restrict__ accum, uint32_t* __restrict__ count) {
+    grid_dependency_begin();
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= n || tiles_touched[g] == 0) return;
     const float2 d = grad_mean2d[g];
@@ -68,6 +69,7 @@ __device__ __forceinline__ int decide(const DensArgs& a, int64_t g) {
 
 // per block: slot counts and their block total
 __global__ void __launch_bounds__(kDensThreads) densify_count_kernel(const DensArgs a) {
+    grid_dependency_begin();
     __shared__ unsigned long long s_sum;
     if (threadIdx.x == 0) s_sum = 0;
     __syncthreads();
@@ -88,6 +90,7 @@ __global__ void __launch_bounds__(kDensThreads) densify_count_kernel(const DensA
 // exclusive scan of the block totals (one block), the new count and the
 // capacity flag
 __global__ void __launch_bounds__(1024) densify_scan_kernel(const DensArgs a, int nb) {
+    grid_dependency_begin();
     __shared__ unsigned long long s_carry;
     __shared__ unsigned long long s_warp[32];
     if (threadIdx.x == 0) s_carry = 0;
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(1024) densify_scan_kernel(const DensArgs a, in
 // 32 Gaussians one after another with all lanes (coalesced rows), and the
 // owner of a split Gaussian writes its children's centres and scales
 __global__ void __launch_bounds__(kDensThreads) densify_scatter_kernel(const DensArgs a) {
+    grid_dependency_begin();
     __shared__ uint32_t s_warp[kDensThreads / 32];
     const int64_t g = (int64_t)blockIdx.x * kDensThreads + threadIdx.x;
     const uint32_t slots = g < a.in.n ? a.slots[g] : 0u;
@@ -199,8 +203,8 @@ size_t densify_scratch_bytes(int64_t n) {
 cudaError_t launch_densify_stats(const float* grad_mean2d, const uint32_t* tiles_touched, int64_t n, float* accum,
                                  uint32_t* count, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    densify_stats_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(reinterpret_cast<const float2*>(grad_mean2d),
-                                                                    tiles_touched, n, accum, count);
+    launch_k(densify_stats_kernel, (unsigned)((n + 255) / 256), 256, 0, s, reinterpret_cast<const float2*>(grad_mean2d),
+             tiles_touched, n, accum, count);
     return cudaGetLastError();
 }
 
@@ -229,9 +233,9 @@ cudaError_t launch_densify(const gs_gaussians& in, const gs_gaussians_out& out, 
     cudaError_t e = cudaMemsetAsync(a.header, 0, sizeof(StatusHeader), s);
     if (e != cudaSuccess) return e;
     if (in.n == 0) return cudaMemsetAsync(out_count, 0, sizeof(uint64_t), s);
-    densify_count_kernel<<<nb, kDensThreads, 0, s>>>(a);
-    densify_scan_kernel<<<1, 1024, 0, s>>>(a, nb);
-    densify_scatter_kernel<<<nb, kDensThreads, 0, s>>>(a);
+    launch_k(densify_count_kernel, nb, kDensThreads, 0, s, a);
+    launch_k(densify_scan_kernel, 1, 1024, 0, s, a, nb);
+    launch_k(densify_scatter_kernel, nb, kDensThreads, 0, s, a);
     return cudaGetLastError();
 }
 

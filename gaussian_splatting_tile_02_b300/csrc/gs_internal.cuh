@@ -4,11 +4,42 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "gs.h"
 
 namespace gs {
 
 constexpr int kTile = 16;
+
+// Programmatic dependent launch. Every kernel is launched through launch_k,
+// with the programmatic-serialisation attribute (unless switched off by
+// gs_set_programmatic_launch): the launch of a kernel then overlaps the end of
+// the kernel before it on the stream instead of following it. So every
+// kernel begins with grid_dependency_begin(), before any global memory
+// access: it returns once the preceding kernel has completed and its writes
+// are visible. A kernel launched without the attribute (or after a memset or
+// an event) finds it a no-op. No kernel signals its dependents early: an
+// early signal let the next kernel's blocks take SM slots during the last
+// wave, and graph-replayed 5M frames got 9% slower.
+__device__ __forceinline__ void grid_dependency_begin() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+extern std::atomic<int> g_programmatic_launch;
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_programmatic_launch.load(std::memory_order_relaxed) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // Status header at the start of every workspace (256 bytes reserved).
 struct StatusHeader {
@@ -20,7 +51,7 @@ struct StatusHeader {
 static_assert(sizeof(StatusHeader) == 256, "status header is 256 bytes");
 
 constexpr size_t kAlign = 256;
-__host__ __device__ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
 // Radix digits of a key_bits-bit key: ceil(key_bits / 8) LSD passes of 8-bit
 // digits from the least significant end, the last one narrower (13 bits ->
@@ -205,6 +236,14 @@ cudaError_t launch_depth_keys(const gs_projected& p, int64_t n, uint32_t* keys, 
 
 // sort.cu
 size_t sort_scratch_bytes(int64_t key_capacity);
+// The scratch of one sort in two parts: the head (digit histograms, which the
+// producer of the keys fills when hist_ready, and the passes' tile counters,
+// which the bases kernel clears) and the look-back rows.
+size_t sort_head_bytes();
+size_t sort_lookback_bytes(int64_t key_capacity);
+cudaError_t launch_sort32_split(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
+                                const uint64_t* num_keys, int64_t key_capacity, int key_bits, StatusHeader* status,
+                                void* head, void* lookback, long long spin_limit, cudaStream_t s, bool hist_ready);
 cudaError_t launch_sort(uint64_t* keys, uint32_t* vals, uint64_t* keys_alt, uint32_t* vals_alt,
                         const uint64_t* num_keys, int64_t key_capacity, int key_bits,
                         StatusHeader* status, void* scratch, long long spin_limit, cudaStream_t s);
@@ -219,8 +258,10 @@ uint32_t* sort_histogram_of(void* scratch);
 cudaError_t sort_prepare_histogram(void* scratch, cudaStream_t s);
 cudaError_t launch_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_keys,
                                int64_t key_capacity, int n_tiles, uint32_t* ranges, cudaStream_t s);
+// ranges_zeroed: the caller cleared the ranges already (otherwise a memset does)
 cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* num_keys,
-                                 int64_t key_capacity, int n_tiles, uint32_t* ranges, cudaStream_t s);
+                                 int64_t key_capacity, int n_tiles, uint32_t* ranges, cudaStream_t s,
+                                 bool ranges_zeroed = false);
 cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations, cudaStream_t s);
 
 // tiledepth.cu: each tile's list (Gaussians in index order, [ranges.x, ranges.y) of vals)
@@ -228,10 +269,12 @@ cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations,
 // keys_a, keys_b, vals_b: scratch of the key capacity (lists longer than a block's
 // shared-memory sort go through them); scratch: tile_depth_scratch_bytes(tiles).
 // One kernel per list-size class that the key capacity allows (tile_depth_sort_launches).
+// counts: three uint32 the caller has zeroed.
 size_t tile_depth_scratch_bytes(int tiles);
 cudaError_t launch_tile_depth_sort(const uint32_t* ranges, const uint32_t* tile_order, int tiles, const float* depth,
                                    int64_t n, int64_t key_capacity, uint32_t* vals, uint32_t* keys_a,
-                                   uint32_t* keys_b, uint32_t* vals_b, void* scratch, cudaStream_t s);
+                                   uint32_t* keys_b, uint32_t* vals_b, uint32_t* counts, void* scratch,
+                                   cudaStream_t s);
 int tile_depth_sort_launches(int64_t key_capacity);
 cudaError_t set_check_counter_tiledepth(unsigned long long* p);
 
@@ -268,10 +311,11 @@ cudaError_t launch_preprocess_backward(const gs_gaussians& g, const CamConst& ca
 // receives a permutation of the tile indices, longest lists first.
 cudaError_t launch_tile_order(const uint32_t* ranges, int tiles, uint32_t* tile_order, cudaStream_t s);
 // The same order from many blocks, into scratch of tile_order_scratch_bytes(tiles)
-// bytes (the order itself first, *tile_order points at it).
+// bytes (the order itself first, *tile_order points at it). done: a uint32 the
+// caller has zeroed, or null (the scratch's own, cleared by a memset).
 size_t tile_order_scratch_bytes(int tiles);
 cudaError_t launch_tile_order_multi(const uint32_t* ranges, int tiles, void* scratch, uint32_t** tile_order,
-                                    cudaStream_t s);
+                                    cudaStream_t s, uint32_t* done = nullptr);
 // tile_order (nullable): a launch order written by launch_tile_order; null
 // launches the tiles in index order (same image)
 cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* sorted_vals, const uint32_t* ranges,

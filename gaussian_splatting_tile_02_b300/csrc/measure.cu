@@ -18,6 +18,7 @@ constexpr int kPeakThreads = 256;
 constexpr int kChains = 16;
 
 __global__ void __launch_bounds__(kPeakThreads) ffma_peak_kernel(int iterations, float seed, float* sink) {
+    grid_dependency_begin();
     float a[kChains];
 #pragma unroll
     for (int i = 0; i < kChains; i++) a[i] = seed + 1e-3f * (float)(threadIdx.x + i);
@@ -33,6 +34,7 @@ __global__ void __launch_bounds__(kPeakThreads) ffma_peak_kernel(int iterations,
 }
 
 __global__ void __launch_bounds__(kPeakThreads) ffma2_peak_kernel(int iterations, float seed, float* sink) {
+    grid_dependency_begin();
     unsigned long long a[kChains / 2];
 #pragma unroll
     for (int i = 0; i < kChains / 2; i++) {
@@ -71,9 +73,9 @@ extern "C" gs_status gs_fp32_peak_probe(int32_t blocks, int32_t iterations, int3
     // seed -1: the sum of 16 chains that start near -1 and move slowly towards +0.83 stays far
     // from -1 for any run length a caller can time, so nothing is stored
     if (packed)
-        ffma2_peak_kernel<<<blocks, kPeakThreads, 0, s>>>(iterations, -1.0f, sink);
+        launch_k(ffma2_peak_kernel, blocks, kPeakThreads, 0, s, iterations, -1.0f, sink);
     else
-        ffma_peak_kernel<<<blocks, kPeakThreads, 0, s>>>(iterations, -1.0f, sink);
+        launch_k(ffma_peak_kernel, blocks, kPeakThreads, 0, s, iterations, -1.0f, sink);
     if (fma_count) *fma_count = (int64_t)blocks * kPeakThreads * (int64_t)iterations * kChains;
     return cudaGetLastError() == cudaSuccess ? GS_OK : GS_ERR_CUDA;
 }

@@ -469,6 +469,7 @@ __device__ __forceinline__ void flush_depth_hist(const uint32_t* s_hist, uint32_
 // by few blocks.
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const PreArgs a) {
+    grid_dependency_begin();
     __shared__ uint32_t s_hist[4 * 256];
     if (a.dkeys)
         for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) s_hist[i] = 0;
@@ -504,6 +505,7 @@ constexpr int stage_bytes() {
 
 template <int D>
 __global__ void __launch_bounds__(kStage, 6) preprocess_staged_kernel(const PreArgs a) {
+    grid_dependency_begin();
     extern __shared__ __align__(16) unsigned char s_stage[];
     __shared__ uint32_t s_hist[4 * 256];
     __shared__ __align__(8) uint64_t s_bar[2];   // means..logits, SH rows
@@ -588,6 +590,7 @@ struct PreBatchArgs {
 
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_batch_kernel(const PreBatchArgs a) {
+    grid_dependency_begin();
     __shared__ uint32_t s_hist[kMaxBatchViews * 4 * 256];   // per view
     const int nv = a.views;
     for (int k = threadIdx.x; k < nv * 1024; k += blockDim.x) s_hist[k] = 0;
@@ -659,7 +662,7 @@ cudaError_t launch_staged(const PreArgs& a, cudaStream_t s) {
         cap = it->second;
     }
     const int64_t need = (a.n + kStage - 1) / kStage;
-    preprocess_staged_kernel<D><<<(unsigned)(need < cap ? need : cap), kStage, stage_bytes<D>(), s>>>(a);
+    launch_k(preprocess_staged_kernel<D>, (unsigned)(need < cap ? need : cap), kStage, stage_bytes<D>(), s, a);
     return cudaGetLastError();
 }
 
@@ -700,10 +703,18 @@ cudaError_t launch_preprocess_batch(const gs_gaussians& g, const CamConst* cams,
     for (int i = 0; i < views; i++) a.v[i] = pre_args(g, cams[i], outs[i], dks ? dks + i : nullptr);
     a.views = views;
     switch (g.sh_degree) {
-        case 0: preprocess_batch_kernel<0><<<resident_blocks(preprocess_batch_kernel<0>, g.n), 256, 0, s>>>(a); break;
-        case 1: preprocess_batch_kernel<1><<<resident_blocks(preprocess_batch_kernel<1>, g.n), 256, 0, s>>>(a); break;
-        case 2: preprocess_batch_kernel<2><<<resident_blocks(preprocess_batch_kernel<2>, g.n), 256, 0, s>>>(a); break;
-        default: preprocess_batch_kernel<3><<<resident_blocks(preprocess_batch_kernel<3>, g.n), 256, 0, s>>>(a); break;
+        case 0:
+            launch_k(preprocess_batch_kernel<0>, resident_blocks(preprocess_batch_kernel<0>, g.n), 256, 0, s, a);
+            break;
+        case 1:
+            launch_k(preprocess_batch_kernel<1>, resident_blocks(preprocess_batch_kernel<1>, g.n), 256, 0, s, a);
+            break;
+        case 2:
+            launch_k(preprocess_batch_kernel<2>, resident_blocks(preprocess_batch_kernel<2>, g.n), 256, 0, s, a);
+            break;
+        default:
+            launch_k(preprocess_batch_kernel<3>, resident_blocks(preprocess_batch_kernel<3>, g.n), 256, 0, s, a);
+            break;
     }
     return cudaGetLastError();
 }
@@ -723,10 +734,18 @@ cudaError_t launch_preprocess(const gs_gaussians& g, const CamConst& cam, const 
         }
     }
     switch (g.sh_degree) {
-        case 0: preprocess_kernel<0><<<resident_blocks(preprocess_kernel<0>, g.n), 256, 0, s>>>(a); break;
-        case 1: preprocess_kernel<1><<<resident_blocks(preprocess_kernel<1>, g.n), 256, 0, s>>>(a); break;
-        case 2: preprocess_kernel<2><<<resident_blocks(preprocess_kernel<2>, g.n), 256, 0, s>>>(a); break;
-        default: preprocess_kernel<3><<<resident_blocks(preprocess_kernel<3>, g.n), 256, 0, s>>>(a); break;
+        case 0:
+            launch_k(preprocess_kernel<0>, resident_blocks(preprocess_kernel<0>, g.n), 256, 0, s, a);
+            break;
+        case 1:
+            launch_k(preprocess_kernel<1>, resident_blocks(preprocess_kernel<1>, g.n), 256, 0, s, a);
+            break;
+        case 2:
+            launch_k(preprocess_kernel<2>, resident_blocks(preprocess_kernel<2>, g.n), 256, 0, s, a);
+            break;
+        default:
+            launch_k(preprocess_kernel<3>, resident_blocks(preprocess_kernel<3>, g.n), 256, 0, s, a);
+            break;
     }
     return cudaGetLastError();
 }

@@ -73,6 +73,7 @@ __device__ __forceinline__ uint32_t same_row_lanes(uint32_t v) {
 
 __global__ void __launch_bounds__(kOrderThreads) tile_order_kernel(const uint2* __restrict__ ranges, int tiles,
                                                                    uint32_t* __restrict__ order) {
+    grid_dependency_begin();
     __shared__ uint32_t s_cnt[kOrderRows][32];   // [row][warp]
     __shared__ uint32_t s_row[kOrderRows];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -165,6 +166,7 @@ __device__ __forceinline__ uint32_t tile_row(const uint2* __restrict__ ranges, i
 __global__ void __launch_bounds__(kOrderMultiThreads) tile_order_count_kernel(const uint2* __restrict__ ranges,
                                                                               int tiles, uint32_t* __restrict__ table,
                                                                               uint32_t* __restrict__ done) {
+    grid_dependency_begin();
     __shared__ uint32_t s_cnt[kOrderRows][kOrderMultiWarps];
     __shared__ uint32_t s_wt[kOrderMultiWarps];
     __shared__ bool s_last;
@@ -227,6 +229,7 @@ __global__ void __launch_bounds__(kOrderMultiThreads) tile_order_scatter_kernel(
                                                                                 int tiles,
                                                                                 const uint32_t* __restrict__ table,
                                                                                 uint32_t* __restrict__ order) {
+    grid_dependency_begin();
     __shared__ uint32_t s_cnt[kOrderRows][kOrderMultiWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < kOrderRows * kOrderMultiWarps; i += kOrderMultiThreads)
@@ -261,6 +264,7 @@ struct RastArgs {
 // n_contrib); without it the blend is the same arithmetic minus that bookkeeping.
 template <bool kAux>
 __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastArgs a) {
+    grid_dependency_begin();
     __shared__ float4 s_q[2][kRastThreads];    // (A1, A2, k1, k2): origin terms of the exponent
     __shared__ float4 s_r[2][kRastThreads];    // (k3, log2 o, r, g)
     __shared__ float s_b[2][kRastThreads];     // b
@@ -441,9 +445,9 @@ cudaError_t launch_rasterize(const gs_projected& p, int64_t n, const uint32_t* s
     const unsigned tiles = (unsigned)(cam.tiles_x * cam.tiles_y);
     if (n == 0) a.sorted_vals = nullptr;
     if (n_contrib)
-        rasterize_kernel<true><<<tiles, kRastThreads, 0, s>>>(a);
+        launch_k(rasterize_kernel<true>, tiles, kRastThreads, 0, s, a);
     else
-        rasterize_kernel<false><<<tiles, kRastThreads, 0, s>>>(a);
+        launch_k(rasterize_kernel<false>, tiles, kRastThreads, 0, s, a);
     return cudaGetLastError();
 }
 
@@ -453,7 +457,7 @@ size_t tile_order_scratch_bytes(int tiles) {
 }
 
 cudaError_t launch_tile_order_multi(const uint32_t* ranges, int tiles, void* scratch, uint32_t** tile_order,
-                                    cudaStream_t s) {
+                                    cudaStream_t s, uint32_t* done_zeroed) {
     char* w = static_cast<char*>(scratch);
     uint32_t* order = reinterpret_cast<uint32_t*>(w);
     const size_t nb = (size_t)(tiles + kOrderMultiThreads - 1) / kOrderMultiThreads;
@@ -462,16 +466,20 @@ cudaError_t launch_tile_order_multi(const uint32_t* ranges, int tiles, void* scr
     *tile_order = order;
     if (tiles <= 0) return cudaSuccess;
     if (nb > (size_t)kOrderMaxBlocks) return launch_tile_order(ranges, tiles, order, s);
-    cudaError_t e = cudaMemsetAsync(done, 0, sizeof(uint32_t), s);
-    if (e != cudaSuccess) return e;
+    if (done_zeroed) {
+        done = done_zeroed;
+    } else {
+        const cudaError_t e = cudaMemsetAsync(done, 0, sizeof(uint32_t), s);
+        if (e != cudaSuccess) return e;
+    }
     const uint2* r = reinterpret_cast<const uint2*>(ranges);
-    tile_order_count_kernel<<<(unsigned)nb, kOrderMultiThreads, 0, s>>>(r, tiles, table, done);
-    tile_order_scatter_kernel<<<(unsigned)nb, kOrderMultiThreads, 0, s>>>(r, tiles, table, order);
+    launch_k(tile_order_count_kernel, (unsigned)nb, kOrderMultiThreads, 0, s, r, tiles, table, done);
+    launch_k(tile_order_scatter_kernel, (unsigned)nb, kOrderMultiThreads, 0, s, r, tiles, table, order);
     return cudaGetLastError();
 }
 
 cudaError_t launch_tile_order(const uint32_t* ranges, int tiles, uint32_t* tile_order, cudaStream_t s) {
-    tile_order_kernel<<<1, kOrderThreads, 0, s>>>(reinterpret_cast<const uint2*>(ranges), tiles, tile_order);
+    launch_k(tile_order_kernel, 1, kOrderThreads, 0, s, reinterpret_cast<const uint2*>(ranges), tiles, tile_order);
     return cudaGetLastError();
 }
 

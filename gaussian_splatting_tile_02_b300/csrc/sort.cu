@@ -71,14 +71,15 @@ struct SortScratch {
 
 __host__ __device__ inline int64_t sort_max_tiles(int64_t cap) { return (cap + kSortTile - 1) / kSortTile; }
 
-SortScratch carve(void* scratch, int64_t cap) {
+constexpr size_t kHeadBytes = align_up(sizeof(uint32_t) * kMaxPasses * kRadix) + align_up(sizeof(uint32_t) * kMaxPasses);
+
+// head: the histograms, then the counters; lookback: the look-back rows
+SortScratch carve(void* head, void* lookback, int64_t cap) {
     SortScratch s;
-    char* p = static_cast<char*>(scratch);
+    char* p = static_cast<char*>(head);
     s.hist = reinterpret_cast<uint32_t*>(p);
-    p += align_up(sizeof(uint32_t) * kMaxPasses * kRadix);
-    s.counters = reinterpret_cast<uint32_t*>(p);
-    p += align_up(sizeof(uint32_t) * kMaxPasses);
-    s.lookback = reinterpret_cast<uint32_t*>(p);
+    s.counters = reinterpret_cast<uint32_t*>(p + align_up(sizeof(uint32_t) * kMaxPasses * kRadix));
+    s.lookback = static_cast<uint32_t*>(lookback);
     s.max_tiles = sort_max_tiles(cap > 0 ? cap : 1);
     return s;
 }
@@ -127,6 +128,7 @@ template <typename KeyT>
 __global__ void __launch_bounds__(256) sort_histogram_kernel(const KeyT* __restrict__ keys,
                                                              const uint64_t* __restrict__ num_keys, int64_t cap,
                                                              int passes, int key_bits, uint32_t* __restrict__ hist) {
+    grid_dependency_begin();
     __shared__ uint32_t s_hist[kMaxPasses * kRadix];
     for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x) s_hist[i] = 0;
     __syncthreads();
@@ -144,13 +146,17 @@ __global__ void __launch_bounds__(256) sort_histogram_kernel(const KeyT* __restr
         if (s_hist[i]) atomicAdd(&hist[i], s_hist[i]);
 }
 
-// Blocks [0, passes): exclusive scan of one digit histogram -> digit bases.
-// The other blocks clear the look-back rows the passes will use (both
-// ping-pong arrays), for the tiles of this sort only.
+// Blocks [0, passes): exclusive scan of one digit histogram -> digit bases;
+// block 0 also clears the passes' tile-id counters. The other blocks clear the
+// look-back rows the passes will use (both ping-pong arrays), for the tiles of
+// this sort only.
 __global__ void __launch_bounds__(kRadix) sort_bases_kernel(uint32_t* __restrict__ hist, int passes,
                                                             const uint64_t* __restrict__ num_keys, int64_t cap,
-                                                            uint32_t* __restrict__ lookback, int64_t max_tiles) {
+                                                            uint32_t* __restrict__ lookback, int64_t max_tiles,
+                                                            uint32_t* __restrict__ counters) {
+    grid_dependency_begin();
     __shared__ uint32_t warp_tot[kRadix / 32];
+    if (blockIdx.x == 0 && threadIdx.x < kMaxPasses) counters[threadIdx.x] = 0;
     if ((int)blockIdx.x >= passes) {
         const int64_t K = key_count(num_keys, cap);
         const int64_t words = (K + kSortTile - 1) / kSortTile * kRadix;
@@ -203,6 +209,7 @@ struct PassArgs {
 // moment); with several waves the extra counting costs more than it saves.
 template <typename KeyT, bool kEarly>
 __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_kernel(const PassArgs<KeyT> a) {
+    grid_dependency_begin();
     __shared__ uint16_t s_hist[kSortWarps * kRadix];  // per-warp digit counters -> offsets
     __shared__ uint32_t s_dstart[kRadix];
     __shared__ uint32_t s_goff[kRadix];
@@ -432,6 +439,7 @@ __global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) onesweep_ker
 // leaves.
 constexpr int kPipeBytes = (6 * kSortTile) * 4 + kSortWarps * kRadix * 2;
 __global__ void __launch_bounds__(kSortThreads, 2) onesweep_pipe_kernel(const PassArgs<uint32_t> a) {
+    grid_dependency_begin();
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* s_kin = reinterpret_cast<uint32_t*>(smem);          // [2][kSortTile]
     uint32_t* s_vin = s_kin + 2 * kSortTile;                       // [2][kSortTile]
@@ -623,6 +631,7 @@ template <typename KeyT>
 __global__ void copy_back_kernel(const KeyT* __restrict__ ks, const uint32_t* __restrict__ vs,
                                  KeyT* __restrict__ kd, uint32_t* __restrict__ vd,
                                  const uint64_t* __restrict__ num_keys, int64_t cap) {
+    grid_dependency_begin();
     const int64_t K = key_count(num_keys, cap);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < K; i += stride) {
@@ -643,6 +652,7 @@ __global__ void __launch_bounds__(256) tile_ranges_kernel(const KeyT* __restrict
                                                           const uint64_t* __restrict__ num_keys, int64_t cap,
                                                           int shift, int n_tiles, bool vec,
                                                           uint2* __restrict__ ranges) {
+    grid_dependency_begin();
     static_assert(kRangeItems * sizeof(KeyT) % 16 == 0, "a run is whole 16-byte vectors");
     const int64_t K = key_count(num_keys, cap);
     const int64_t runs = (K + kRangeItems - 1) / kRangeItems;
@@ -681,6 +691,7 @@ __global__ void __launch_bounds__(256) tile_ranges_kernel(const KeyT* __restrict
 }
 
 __global__ void spin_timeout_test_kernel(StatusHeader* h, long long iterations) {
+    grid_dependency_begin();
     uint32_t v;
     // pad[0] of the header is never written by anyone: the wait must run out
     if (!bounded_wait(&h->pad[0], v, iterations, h)) raise_flag(h, GS_FLAG_TIMEOUT, 2u);
@@ -736,28 +747,26 @@ cudaError_t resident_tiles(PassShapes* out) {
 // that produced the keys.
 template <typename KeyT>
 cudaError_t launch_sort_t(KeyT* keys, uint32_t* vals, KeyT* keys_alt, uint32_t* vals_alt, const uint64_t* num_keys,
-                          int64_t cap, int key_bits, StatusHeader* status, void* scratch, long long spin_limit,
-                          cudaStream_t s, bool hist_ready) {
+                          int64_t cap, int key_bits, StatusHeader* status, void* head, void* lookback,
+                          long long spin_limit, cudaStream_t s, bool hist_ready) {
     if (cap == 0) return cudaSuccess;
-    const SortScratch sc = carve(scratch, cap);
+    const SortScratch sc = carve(head, lookback, cap);
     const int passes = (key_bits + 7) / 8;
     cudaError_t e;
     if (!hist_ready) {
         e = cudaMemsetAsync(sc.hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, s);
         if (e != cudaSuccess) return e;
-        sort_histogram_kernel<KeyT><<<grid_for(cap, 256 * 16, 148 * 8), 256, 0, s>>>(keys, num_keys, cap, passes,
-                                                                                     key_bits, sc.hist);
+        launch_k(sort_histogram_kernel<KeyT>, grid_for(cap, 256 * 16, 148 * 8), 256, 0, s, keys, num_keys, cap, passes,
+                 key_bits, sc.hist);
     }
-    e = cudaMemsetAsync(sc.counters, 0, sizeof(uint32_t) * kMaxPasses, s);
-    if (e != cudaSuccess) return e;
     const unsigned tiles = (unsigned)sc.max_tiles;
     PassShapes shapes;
     e = resident_tiles<KeyT>(&shapes);
     if (e != cudaSuccess) return e;
     const unsigned resident = shapes.resident, pipe_blocks = shapes.pipe_blocks;
     const int clear_blocks = grid_for(2 * sc.max_tiles * kRadix, kRadix * 8, 148 * 2);
-    sort_bases_kernel<<<passes + clear_blocks, kRadix, 0, s>>>(sc.hist, passes, num_keys, cap, sc.lookback,
-                                                              sc.max_tiles);
+    launch_k(sort_bases_kernel, passes + clear_blocks, kRadix, 0, s, sc.hist, passes, num_keys, cap, sc.lookback,
+             sc.max_tiles, sc.counters);
     for (int p = 0; p < passes; p++) {
         PassArgs<KeyT> a;
         const bool even = (p % 2) == 0;
@@ -781,39 +790,47 @@ cudaError_t launch_sort_t(KeyT* keys, uint32_t* vals, KeyT* keys_alt, uint32_t* 
             // three waves or more, and arrays the bulk copies can read
             piped = pipe_blocks > 0 && tiles >= 3u * resident && ((uintptr_t)a.keys_in & 15) == 0 &&
                     ((uintptr_t)a.vals_in & 15) == 0;
-            if (piped) onesweep_pipe_kernel<<<pipe_blocks, kSortThreads, kPipeBytes, s>>>(a);
+            if (piped) launch_k(onesweep_pipe_kernel, pipe_blocks, kSortThreads, kPipeBytes, s, a);
         }
         if (!piped) {
             if (tiles <= resident)
-                onesweep_kernel<KeyT, true><<<tiles, kSortThreads, 0, s>>>(a);
+                launch_k(onesweep_kernel<KeyT, true>, tiles, kSortThreads, 0, s, a);
             else
-                onesweep_kernel<KeyT, false><<<tiles, kSortThreads, 0, s>>>(a);
+                launch_k(onesweep_kernel<KeyT, false>, tiles, kSortThreads, 0, s, a);
         }
     }
     if (passes % 2 == 1)
-        copy_back_kernel<KeyT><<<grid_for(cap, 256 * 8, 148 * 8), 256, 0, s>>>(keys_alt, vals_alt, keys, vals,
-                                                                               num_keys, cap);
+        launch_k(copy_back_kernel<KeyT>, grid_for(cap, 256 * 8, 148 * 8), 256, 0, s, keys_alt, vals_alt, keys, vals,
+                 num_keys, cap);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t sort_scratch_bytes(int64_t cap) {
-    return align_up(sizeof(uint32_t) * kMaxPasses * kRadix) + align_up(sizeof(uint32_t) * kMaxPasses) +
-           align_up(sizeof(uint32_t) * 2 * (size_t)sort_max_tiles(cap > 0 ? cap : 1) * kRadix);
+size_t sort_head_bytes() { return kHeadBytes; }
+size_t sort_lookback_bytes(int64_t cap) {
+    return align_up(sizeof(uint32_t) * 2 * (size_t)sort_max_tiles(cap > 0 ? cap : 1) * kRadix);
 }
+size_t sort_scratch_bytes(int64_t cap) { return sort_head_bytes() + sort_lookback_bytes(cap); }
 
 cudaError_t launch_sort(uint64_t* keys, uint32_t* vals, uint64_t* keys_alt, uint32_t* vals_alt,
                         const uint64_t* num_keys, int64_t cap, int key_bits, StatusHeader* status, void* scratch,
                         long long spin_limit, cudaStream_t s) {
     return launch_sort_t<uint64_t>(keys, vals, keys_alt, vals_alt, num_keys, cap, key_bits, status, scratch,
-                                   spin_limit, s, false);
+                                   static_cast<char*>(scratch) + kHeadBytes, spin_limit, s, false);
 }
 
 cudaError_t launch_sort32(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
                           const uint64_t* num_keys, int64_t cap, int key_bits, StatusHeader* status, void* scratch,
                           long long spin_limit, cudaStream_t s, bool hist_ready) {
     return launch_sort_t<uint32_t>(keys, vals, keys_alt, vals_alt, num_keys, cap, key_bits, status, scratch,
+                                   static_cast<char*>(scratch) + kHeadBytes, spin_limit, s, hist_ready);
+}
+
+cudaError_t launch_sort32_split(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
+                                const uint64_t* num_keys, int64_t cap, int key_bits, StatusHeader* status, void* head,
+                                void* lookback, long long spin_limit, cudaStream_t s, bool hist_ready) {
+    return launch_sort_t<uint32_t>(keys, vals, keys_alt, vals_alt, num_keys, cap, key_bits, status, head, lookback,
                                    spin_limit, s, hist_ready);
 }
 
@@ -828,23 +845,23 @@ cudaError_t launch_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_
     cudaError_t e = cudaMemsetAsync(ranges, 0, sizeof(uint32_t) * 2 * (size_t)n_tiles, s);
     if (e != cudaSuccess || cap == 0) return e;
     const bool vec = (reinterpret_cast<uintptr_t>(sorted_keys) & 15) == 0;
-    tile_ranges_kernel<uint64_t><<<grid_for(cap, 256 * kRangeItems, 148 * 8), 256, 0, s>>>(
-        sorted_keys, num_keys, cap, 32, n_tiles, vec, reinterpret_cast<uint2*>(ranges));
+    launch_k(tile_ranges_kernel<uint64_t>, grid_for(cap, 256 * kRangeItems, 148 * 8), 256, 0, s,
+             sorted_keys, num_keys, cap, 32, n_tiles, vec, reinterpret_cast<uint2*>(ranges));
     return cudaGetLastError();
 }
 
 cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* num_keys, int64_t cap, int n_tiles,
-                                 uint32_t* ranges, cudaStream_t s) {
-    cudaError_t e = cudaMemsetAsync(ranges, 0, sizeof(uint32_t) * 2 * (size_t)n_tiles, s);
+                                 uint32_t* ranges, cudaStream_t s, bool ranges_zeroed) {
+    cudaError_t e = ranges_zeroed ? cudaSuccess : cudaMemsetAsync(ranges, 0, sizeof(uint32_t) * 2 * (size_t)n_tiles, s);
     if (e != cudaSuccess || cap == 0) return e;
     const bool vec = (reinterpret_cast<uintptr_t>(sorted_tiles) & 15) == 0;
-    tile_ranges_kernel<uint32_t><<<grid_for(cap, 256 * kRangeItems, 148 * 8), 256, 0, s>>>(
-        sorted_tiles, num_keys, cap, 0, n_tiles, vec, reinterpret_cast<uint2*>(ranges));
+    launch_k(tile_ranges_kernel<uint32_t>, grid_for(cap, 256 * kRangeItems, 148 * 8), 256, 0, s,
+             sorted_tiles, num_keys, cap, 0, n_tiles, vec, reinterpret_cast<uint2*>(ranges));
     return cudaGetLastError();
 }
 
 cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations, cudaStream_t s) {
-    spin_timeout_test_kernel<<<1, 1, 0, s>>>(status, iterations);
+    launch_k(spin_timeout_test_kernel, 1, 1, 0, s, status, iterations);
     return cudaGetLastError();
 }
 

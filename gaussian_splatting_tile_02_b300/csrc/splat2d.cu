@@ -56,6 +56,7 @@ struct Pre2dArgs {
 };
 
 __global__ void __launch_bounds__(256) preprocess2d_kernel(const Pre2dArgs a) {
+    grid_dependency_begin();
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= a.n) return;
     const float2 m = a.means[g];
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(256) conic_to_cov_grad_kernel(const float* __r
                                                                 const uint32_t* __restrict__ tiles_touched,
                                                                 const float* __restrict__ g_conic, int64_t n,
                                                                 float* __restrict__ g_covs) {
+    grid_dependency_begin();
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= n) return;
     float* out = g_covs + 4 * g;
@@ -164,14 +166,14 @@ cudaError_t launch_preprocess2d(const float* means, const float* covs, const flo
     a.tiles_touched = p.tiles_touched;
     a.rect = reinterpret_cast<ushort4*>(p.rect);
     a.raster = reinterpret_cast<float4*>(p.raster);
-    preprocess2d_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a);
+    launch_k(preprocess2d_kernel, (unsigned)((n + 255) / 256), 256, 0, s, a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_conic_to_cov_grad(const float* covs, const uint32_t* tiles_touched, const float* g_conic,
                                      int64_t n, float* g_covs, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    conic_to_cov_grad_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(covs, tiles_touched, g_conic, n, g_covs);
+    launch_k(conic_to_cov_grad_kernel, (unsigned)((n + 255) / 256), 256, 0, s, covs, tiles_touched, g_conic, n, g_covs);
     return cudaGetLastError();
 }
 

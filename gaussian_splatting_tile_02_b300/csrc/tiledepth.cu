@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(kSmallT) tile_sort_small_kernel(const uint2* _
                                                                   const uint32_t* __restrict__ order,
                                                                   const float* __restrict__ depth, uint32_t n,
                                                                   uint32_t* __restrict__ vals, TileLists lists) {
+    grid_dependency_begin();
     __shared__ BlockSortSmem<kSmallT, kSmallI> sm;
     const uint32_t tile = order ? order[blockIdx.x] : blockIdx.x;
     const uint2 r = ranges[tile];
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(T) tile_sort_list_kernel(const uint2* __restri
                                                            const uint32_t* __restrict__ list,
                                                            const float* __restrict__ depth, uint32_t n,
                                                            uint32_t* __restrict__ vals) {
+    grid_dependency_begin();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     auto& sm = *reinterpret_cast<BlockSortSmem<T, I>*>(smem_raw);
     const uint32_t count = *count_p;
@@ -224,6 +226,7 @@ __global__ void __launch_bounds__(kLTThreads) long_tile_sort_kernel(const uint2*
                                                                     uint32_t* __restrict__ keys_a,
                                                                     uint32_t* __restrict__ keys_b,
                                                                     uint32_t* __restrict__ vals_b) {
+    grid_dependency_begin();
     __shared__ uint16_t s_wh[kLTWarps * kRadixTD];   // per-warp digit counters of a chunk
     __shared__ uint32_t s_off[kRadixTD];             // next output slot of each digit (list-relative)
     __shared__ uint32_t s_dstart[kRadixTD];          // a digit's first slot in the chunk's staging
@@ -398,37 +401,36 @@ cudaError_t list_grids(ListGrids* out) {
 
 }  // namespace
 
-size_t tile_depth_scratch_bytes(int tiles) { return align_up(16) + 3 * align_up(4 * (size_t)(tiles > 0 ? tiles : 1)); }
+size_t tile_depth_scratch_bytes(int tiles) { return 3 * align_up(4 * (size_t)(tiles > 0 ? tiles : 1)); }
 
 cudaError_t launch_tile_depth_sort(const uint32_t* ranges, const uint32_t* tile_order, int tiles, const float* depth,
                                    int64_t n, int64_t key_capacity, uint32_t* vals, uint32_t* keys_a,
-                                   uint32_t* keys_b, uint32_t* vals_b, void* scratch, cudaStream_t s) {
+                                   uint32_t* keys_b, uint32_t* vals_b, uint32_t* counts, void* scratch,
+                                   cudaStream_t s) {
     if (tiles <= 0 || n <= 0 || key_capacity <= 1) return cudaSuccess;
     char* w = static_cast<char*>(scratch);
     const size_t stride = align_up(4 * (size_t)tiles);
     TileLists lists;
-    lists.count = reinterpret_cast<uint32_t*>(w);
-    lists.mid = reinterpret_cast<uint32_t*>(w + align_up(16));
-    lists.big = reinterpret_cast<uint32_t*>(w + align_up(16) + stride);
-    lists.huge = reinterpret_cast<uint32_t*>(w + align_up(16) + 2 * stride);
+    lists.count = counts;
+    lists.mid = reinterpret_cast<uint32_t*>(w);
+    lists.big = reinterpret_cast<uint32_t*>(w + stride);
+    lists.huge = reinterpret_cast<uint32_t*>(w + 2 * stride);
     ListGrids grids;
     cudaError_t e = list_grids(&grids);
     if (e != cudaSuccess) return e;
     // no list is longer than the key capacity: the classes above it are not launched
-    e = cudaMemsetAsync(lists.count, 0, 3 * sizeof(uint32_t), s);
-    if (e != cudaSuccess) return e;
     const uint2* r = reinterpret_cast<const uint2*>(ranges);
     const uint32_t un = (uint32_t)n;
-    tile_sort_small_kernel<<<(unsigned)tiles, kSmallT, 0, s>>>(r, tile_order, depth, un, vals, lists);
+    launch_k(tile_sort_small_kernel, (unsigned)tiles, kSmallT, 0, s, r, tile_order, depth, un, vals, lists);
     if (key_capacity > kSmallCap)
-        tile_sort_list_kernel<kMidT, kMidI><<<grids.mid, kMidT, sizeof(BlockSortSmem<kMidT, kMidI>), s>>>(
-            r, lists.count, lists.mid, depth, un, vals);
+        launch_k(tile_sort_list_kernel<kMidT, kMidI>, grids.mid, kMidT, sizeof(BlockSortSmem<kMidT, kMidI>), s,
+                 r, lists.count, lists.mid, depth, un, vals);
     if (key_capacity > kMidCap)
-        tile_sort_list_kernel<kBigT, kBigI><<<grids.big, kBigT, sizeof(BlockSortSmem<kBigT, kBigI>), s>>>(
-            r, lists.count + 1, lists.big, depth, un, vals);
+        launch_k(tile_sort_list_kernel<kBigT, kBigI>, grids.big, kBigT, sizeof(BlockSortSmem<kBigT, kBigI>), s,
+                 r, lists.count + 1, lists.big, depth, un, vals);
     if (key_capacity > kBigCap)
-        long_tile_sort_kernel<<<148, kLTThreads, 0, s>>>(r, lists.count + 2, lists.huge, depth, un, vals, keys_a,
-                                                         keys_b, vals_b);
+        launch_k(long_tile_sort_kernel, 148, kLTThreads, 0, s, r, lists.count + 2, lists.huge, depth, un, vals, keys_a,
+                 keys_b, vals_b);
     return cudaGetLastError();
 }
 

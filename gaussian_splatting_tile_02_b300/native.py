@@ -132,6 +132,7 @@ _SIGNATURES = {
                                           ctypes.POINTER(ctypes.c_int64), c_void_p]),
     "gs_set_spin_limit": (None, [ctypes.c_int64]),
     "gs_set_steps_order": (ctypes.c_int32, [ctypes.c_int32]),
+    "gs_set_programmatic_launch": (None, [ctypes.c_int32]),
     "gs_test_spin_timeout": (ctypes.c_int, [c_void_p, ctypes.c_int64, c_void_p]),
 }
 

@@ -298,6 +298,16 @@ gs_status gs_render(const gs_gaussians* gaussians, const gs_camera* camera, int6
  * (no CUDA call). */
 int32_t gs_render_tile_first(int64_t n, int32_t width, int32_t height, int64_t key_capacity);
 
+/* Programmatic dependent launch (on by default): every kernel is launched
+ * with the programmatic-serialisation attribute, so that its launch overlaps
+ * the end of the kernel before it on the stream (inside a CUDA graph the
+ * dependencies become programmatic edges); each kernel waits in hardware for
+ * its predecessor's completion before it touches memory, so results are the
+ * same bit for bit either way. 0 turns the attribute off for launches made
+ * after the call (for measurement and tests). Process-wide; not thread-safe
+ * against concurrent launches. */
+void gs_set_programmatic_launch(int32_t on);
+
 /* Pins the order of steps 2-4 for gs_render, gs_render_profiled and
  * gs_render_batch frames enqueued after the call: 0 automatic (the default,
  * gs_render_tile_first), 1 depth-first, 2 tile-first. Either order gives the

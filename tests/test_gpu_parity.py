@@ -281,6 +281,51 @@ def test_batch_views_agree_in_both_orders():
         np.testing.assert_array_equal(x, y)
 
 
+@pytest.mark.parametrize("name,n,view", [("tiny", None, 0), ("100k", None, 0), ("stress", 100_000, 2)])
+def test_programmatic_launch_changes_nothing(name, n, view):
+    """Every kernel waits for its predecessor before touching memory, so frames launched as
+    programmatic dependents (eager and replayed from a CUDA graph, where the dependencies
+    become programmatic edges) equal frames launched plainly, bit for bit, in both orders of
+    steps 2-4."""
+    scene, g = scene_of(name, n)
+    cam = scenes.make_cameras(name)[view]
+    L = gs.lib()
+    r = gs.Renderer.for_scene(g, cam, headroom=1.1)
+    outs = {}
+    try:
+        for order in (1, 2):
+            assert L.gs_set_steps_order(order) == native.GS_OK
+            for pdl in (0, 1):
+                L.gs_set_programmatic_launch(pdl)
+                r.image.zero_()
+                r.render(cam)
+                torch.cuda.synchronize()
+                eager = [t.cpu().numpy().copy() for t in (r.image, r.final_T, r.n_contrib)]
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(s):
+                    with torch.cuda.graph(graph, stream=s):
+                        r.render(cam, stream=s)
+                r.image.zero_()
+                r.final_T.zero_()
+                graph.replay()
+                graph.replay()
+                torch.cuda.synchronize()
+                replay = [t.cpu().numpy().copy() for t in (r.image, r.final_T, r.n_contrib)]
+                assert r.status()[0] == native.GS_OK
+                del graph
+                outs[(order, pdl)] = (eager, replay)
+    finally:
+        L.gs_set_programmatic_launch(1)
+        L.gs_set_steps_order(0)
+    ref = outs[(1, 0)][0]
+    for key, (eager, replay) in outs.items():
+        for x, y, z in zip(ref, eager, replay):
+            np.testing.assert_array_equal(x, y, err_msg=str(key))
+            np.testing.assert_array_equal(x, z, err_msg=str(key))
+
+
 def test_tile_order_is_heavy_first_and_leaves_image_unchanged():
     """The heavy-first launch order is a permutation of the tiles with
     non-increasing floor(log2 length); the image, final T and n_contrib do not
