@@ -48,35 +48,67 @@ struct BlockSortSmem {
     uint16_t wh[(T / 32) * kRadixTD];   // per-warp digit counters -> offsets
     uint32_t dstart[kRadixTD];          // first slot of each digit in the staging
     uint32_t part[T / 32];              // block scan of the digit totals
+    uint32_t any_bits, all_bits;        // OR and AND of the keys
     uint32_t keys[T * I];
     uint32_t vals[T * I];
 };
 
-// Stable sort by key of the first n_valid items held in registers, item i of
-// thread (warp, lane) at position warp * 32 I + 32 i + lane. On return the
-// registers hold the sorted items in the same layout.
+// Stable sort by key of the first n_valid items held in registers. ie =
+// ceil(n_valid / T) items per thread are used (a block-uniform count, so a
+// short list keeps every warp busy and ranks no empty item rounds): item i of
+// thread (warp, lane) sits at position warp * 32 ie + 32 i + lane. Passes
+// whose 8-bit digit is the same for every key are skipped (a stable sort on a
+// constant digit leaves the order as it is). On return the registers hold the
+// sorted items in the same layout.
 template <int T, int I>
-__device__ __forceinline__ void block_sort_by_depth(uint32_t (&key)[I], uint32_t (&val)[I], int n_valid,
+__device__ __forceinline__ void block_sort_by_depth(uint32_t (&key)[I], uint32_t (&val)[I], int n_valid, int ie,
                                                     BlockSortSmem<T, I>& sm) {
     constexpr int W = T / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int warp_base = warp * (I * 32);
+    const int warp_base = warp * (ie * 32);
     const uint32_t lt = lane_lt();
     uint16_t* wh = sm.wh + warp * kRadixTD;
+    // which key bits differ anywhere in the list
+    if (tid == 0) {
+        sm.any_bits = 0u;
+        sm.all_bits = 0xffffffffu;
+    }
+    __syncthreads();
+    {
+        uint32_t o = 0u, a = 0xffffffffu;
+#pragma unroll
+        for (int i = 0; i < I; i++)
+            if (i < ie && warp_base + i * 32 + lane < n_valid) {
+                o |= key[i];
+                a &= key[i];
+            }
+        o = __reduce_or_sync(0xffffffffu, o);
+        a = __reduce_and_sync(0xffffffffu, a);
+        if (lane == 0) {
+            atomicOr(&sm.any_bits, o);
+            atomicAnd(&sm.all_bits, a);
+        }
+    }
+    __syncthreads();
+    const uint32_t varying = sm.any_bits ^ sm.all_bits;
 #pragma unroll 1
     for (int shift = 0; shift < 32; shift += 8) {
+        if (((varying >> shift) & 255u) == 0u) continue;   // block-uniform
         for (int i = tid; i < W * kRadixTD; i += T) sm.wh[i] = 0;
         __syncthreads();
         uint32_t rank[I];
 #pragma unroll
         for (int i = 0; i < I; i++) {
+            rank[i] = 0;
+            if (i >= ie) continue;   // block-uniform
             const bool ok = warp_base + i * 32 + lane < n_valid;
             const uint32_t d = (key[i] >> shift) & 255u;
             const uint32_t peers = __match_any_sync(0xffffffffu, ok ? d : 0xffffu) & __ballot_sync(0xffffffffu, ok);
+            const uint32_t below = __popc(peers & lt);
             uint32_t r = 0;
-            if (ok) r = wh[d] + __popc(peers & lt);
+            if (ok) r = wh[d] + below;
             __syncwarp();
-            if (ok && (peers & lt) == 0) wh[d] = (uint16_t)(wh[d] + __popc(peers));
+            if (ok && below == 0) wh[d] = (uint16_t)(r + __popc(peers));
             __syncwarp();
             rank[i] = r;
         }
@@ -120,7 +152,7 @@ __device__ __forceinline__ void block_sort_by_depth(uint32_t (&key)[I], uint32_t
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < I; i++) {
-            if (warp_base + i * 32 + lane < n_valid) {
+            if (i < ie && warp_base + i * 32 + lane < n_valid) {
                 const uint32_t d = (key[i] >> shift) & 255u;
                 const uint32_t loc = sm.dstart[d] + sm.wh[warp * kRadixTD + d] + rank[i];
                 sm.keys[loc] = key[i];
@@ -131,13 +163,31 @@ __device__ __forceinline__ void block_sort_by_depth(uint32_t (&key)[I], uint32_t
 #pragma unroll
         for (int i = 0; i < I; i++) {
             const int li = warp_base + i * 32 + lane;
-            if (li < n_valid) {
+            if (i < ie && li < n_valid) {
                 key[i] = sm.keys[li];
                 val[i] = sm.vals[li];
             }
         }
         __syncthreads();
     }
+}
+
+// A list of at most 32 entries, sorted by one warp: lane l holds entry l and
+// its rank is the number of entries before it in (depth bits, position) order.
+__device__ __forceinline__ void warp_sort_short_list(const uint2 r, uint32_t len, const float* __restrict__ depth,
+                                                     uint32_t n, uint32_t* __restrict__ vals) {
+    const int lane = threadIdx.x & 31;
+    const bool ok = lane < (int)len;
+    const uint32_t v = ok ? vals[r.x + lane] : 0u;
+    const uint32_t k = ok ? depth_bits(depth, v, n) : 0xffffffffu;
+    uint32_t rank = 0;
+#pragma unroll 8
+    for (int j = 0; j < 32; j++) {
+        const uint32_t kj = __shfl_sync(0xffffffffu, k, j);
+        rank += (j < (int)len) && (kj < k || (kj == k && j < lane));
+    }
+    __syncwarp();
+    if (ok) vals[r.x + rank] = v;
 }
 
 // Tile lists handed from one block size to the next: count[0..2] the lengths
@@ -153,19 +203,21 @@ template <int T, int I>
 __device__ __forceinline__ void sort_tile_list(const uint2 r, uint32_t len, const float* __restrict__ depth,
                                                uint32_t n, uint32_t* __restrict__ vals, BlockSortSmem<T, I>& sm) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int warp_base = warp * (I * 32);
+    const int ie = (int)((len + T - 1) / T);   // items per thread, 1..I
+    const int warp_base = warp * (ie * 32);
     uint32_t key[I], val[I];
 #pragma unroll
     for (int i = 0; i < I; i++) {
         const int li = warp_base + i * 32 + lane;
-        val[i] = li < (int)len ? vals[r.x + li] : 0u;
-        key[i] = li < (int)len ? depth_bits(depth, val[i], n) : 0xffffffffu;
+        const bool ok = i < ie && li < (int)len;
+        val[i] = ok ? vals[r.x + li] : 0u;
+        key[i] = ok ? depth_bits(depth, val[i], n) : 0xffffffffu;
     }
-    block_sort_by_depth<T, I>(key, val, (int)len, sm);
+    block_sort_by_depth<T, I>(key, val, (int)len, ie, sm);
 #pragma unroll
     for (int i = 0; i < I; i++) {
         const int li = warp_base + i * 32 + lane;
-        if (li < (int)len) vals[r.x + li] = val[i];
+        if (i < ie && li < (int)len) vals[r.x + li] = val[i];
     }
 }
 
@@ -185,6 +237,10 @@ __global__ void __launch_bounds__(kSmallT) tile_sort_small_kernel(const uint2* _
     const uint2 r = ranges[tile];
     const uint32_t len = r.y > r.x ? r.y - r.x : 0u;
     if (len <= 1) return;
+    if (len <= 32) {
+        if (threadIdx.x < 32) warp_sort_short_list(r, len, depth, n, vals);
+        return;
+    }
     if (len > (uint32_t)kSmallCap) {
         if (threadIdx.x == 0) {
             const int c = len <= (uint32_t)kMidCap ? 0 : len <= (uint32_t)kBigCap ? 1 : 2;
@@ -197,7 +253,7 @@ __global__ void __launch_bounds__(kSmallT) tile_sort_small_kernel(const uint2* _
 }
 
 template <int T, int I>
-__global__ void __launch_bounds__(T) tile_sort_list_kernel(const uint2* __restrict__ ranges,
+__global__ void __launch_bounds__(T, (T <= 256 ? 4 : 1)) tile_sort_list_kernel(const uint2* __restrict__ ranges,
                                                            const uint32_t* __restrict__ count_p,
                                                            const uint32_t* __restrict__ list,
                                                            const float* __restrict__ depth, uint32_t n,
