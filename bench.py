@@ -222,13 +222,24 @@ def tile_depth_launches(key_capacity: int) -> int:
     return 1 + (key_capacity > 512) + (key_capacity > 2048) + (key_capacity > 8192)
 
 
-def frame_launches(tiles: int, tile_first: bool = False, key_capacity: int = 1 << 20) -> int:
-    """Kernels one gs_render frame launches for an image of `tiles` 16x16 tiles: preprocess
+def tile_key_bits(tiles_x: int, tiles_y: int) -> int:
+    """Bits of the frame's tile-sort keys: the tile id below 4096 tiles, else the 8x8-tile
+    block number and 6 bits for the tile inside the block."""
+    tiles = tiles_x * tiles_y
+    if tiles < 4096:
+        return max(1, (tiles - 1).bit_length())
+    blocks = -(-tiles_x // 8) * -(-tiles_y // 8)
+    return max(1, (blocks - 1).bit_length()) + 6
+
+
+def frame_launches(tiles: int, tile_first: bool = False, key_capacity: int = 1 << 20, tiles_xy=None) -> int:
+    """Kernels one gs_render frame launches for an image of `tiles` 16x16 tiles (tiles_xy:
+    its tiles_x, tiles_y, for the tile keys' width; without it, the tile id's): preprocess
     (which, depth-first, also writes the depth keys); depth-first, the depth sort (4 passes);
-    5 binning kernels; the tile-id sort; ranges; the tile order (count and scatter kernels up
+    5 binning kernels; the tile-key sort; ranges; the tile order (count and scatter kernels up
     to 186 blocks of 256 tiles, one kernel beyond); tile-first, the per-tile depth sort
     (tile_depth_launches); rasterize."""
-    tile_bits = max(1, (tiles - 1).bit_length())
+    tile_bits = tile_key_bits(*tiles_xy) if tiles_xy else max(1, (tiles - 1).bit_length())
     order = 2 if -(-tiles // 256) <= 186 else 1
     depth = tile_depth_launches(key_capacity) if tile_first else sort_launches(32)
     return 1 + depth + 5 + sort_launches(tile_bits) + 1 + order + 1
@@ -803,7 +814,7 @@ def run_ours(args, rank, local_rank, world):
     K = head["keys"]
     stages_out = stage_summary(st_ms, n, cfg.sh_degree, K, tx, ty, head["evaluations"], hbm_peak, fp32,
                                head["tile_first"])
-    launches_per_frame = frame_launches(tx * ty, head["tile_first"], r.key_capacity)
+    launches_per_frame = frame_launches(tx * ty, head["tile_first"], r.key_capacity, (tx, ty))
     ras = stages_out["rasterize"]
     evals = head["evaluations"]
     dominant = max(stages_out, key=lambda k: stages_out[k]["ms"])

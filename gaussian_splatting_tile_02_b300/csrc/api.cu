@@ -16,6 +16,7 @@ std::atomic<int> g_programmatic_launch{1};
 constexpr long long kDefaultSpin = 1ll << 22;
 constexpr int64_t kMaxKeyCapacity = (1ll << 30) - 1;   // look-back status words keep 30 bits
 constexpr int64_t kMaxGaussians = (1ll << 32) - 1;     // values are uint32 indices
+constexpr int kCoarseKeyTiles = 4096;                   // block-layout tile keys from this many tiles
 
 CamConst make_cam_const(const gs_camera& c) {
     CamConst k;
@@ -75,13 +76,6 @@ bool projected_ok(const gs_projected* p, int64_t n) {
 }
 
 gs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GS_OK : GS_ERR_CUDA; }
-
-int tile_bits_for(const gs_camera& c) {
-    const int64_t tiles = (int64_t)tiles_x(c) * tiles_y(c);
-    int b = 0;
-    while ((1ll << b) < tiles) b++;
-    return b > 0 ? b : 1;
-}
 
 // gs_render workspace layout. The buffers a frame must find zeroed sit at
 // the start, [header, zero_end), so one memset at the frame's start clears
@@ -211,7 +205,11 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
     auto* ranges = reinterpret_cast<uint32_t*>(w + L.ranges);
     const CamConst cc = make_cam_const(*cam);
 
-    const int tbits = tile_bits_for(*cam);
+    // the tile sort's keys: 8x8-tile block in the low digit from 4096 tiles up
+    // (a warp's first-pass ranking then sees far fewer distinct digits)
+    const TileKeyMap km = cc.tiles_x * cc.tiles_y >= kCoarseKeyTiles ? coarse_block_keys(cc.tiles_x, cc.tiles_y)
+                                                                     : identity_keys(cc.tiles_x);
+    const int tbits = tile_key_bits(km, cc.tiles_x * cc.tiles_y);
     auto mark = [&](int i) {
         return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
     };
@@ -236,13 +234,13 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
         if (e == cudaSuccess) e = mark(1);
         if (e == cudaSuccess)
             e = launch_bin_ordered(p, nullptr, g->n, cc, nullptr, keys, vals, key_capacity, num_keys, header,
-                                   w + L.bin, s, tile_hist, tbits);
+                                   w + L.bin, s, tile_hist, tbits, &km);
         if (e == cudaSuccess) e = mark(2);
         if (e == cudaSuccess)
             e = launch_sort32_split(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, tbits, header,
                                     w + L.tile_head, w + L.tile_lb, g_spin_limit, s, true);
         if (e == cudaSuccess) e = mark(3);
-        if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s, true);
+        if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s, true, &km);
         if (e == cudaSuccess)
             e = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, s, order_done);
         if (e == cudaSuccess) e = mark(4);
@@ -271,13 +269,13 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
     if (e == cudaSuccess) e = mark(2);
     if (e == cudaSuccess)
         e = launch_bin_ordered(p, order, g->n, cc, nullptr, keys, vals, key_capacity, num_keys, header, w + L.bin, s,
-                               tile_hist, tbits);
+                               tile_hist, tbits, &km);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess)
         e = launch_sort32_split(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, tbits, header,
                                 w + L.tile_head, w + L.tile_lb, g_spin_limit, s, true);
     if (e == cudaSuccess) e = mark(4);
-    if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s, true);
+    if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s, true, &km);
     if (e == cudaSuccess) e = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, s, order_done);
     if (e == cudaSuccess) e = mark(5);
     if (e == cudaSuccess)

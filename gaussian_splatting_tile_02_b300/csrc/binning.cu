@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_offsets_kernel(
 // shared memory so that the global stores are coalesced.
 constexpr int kRun = kKeysPerBlock / kExpandThreads;   // 8 slots per thread
 __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
-    const ushort4* __restrict__ rs, const uint32_t* __restrict__ order, int64_t n, int tiles_x,
+    const ushort4* __restrict__ rs, const uint32_t* __restrict__ order, int64_t n, const TileKeyMap km,
     const uint32_t* __restrict__ first_slot, const uint32_t* __restrict__ owner,
     const uint64_t* __restrict__ num_keys, int64_t key_capacity, uint32_t* __restrict__ keys,
     uint32_t* __restrict__ vals, uint32_t* __restrict__ hist, int key_bits) {
@@ -340,12 +340,10 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
     const unsigned long long S1 = S0 + kKeysPerBlock < Keff ? S0 + kKeysPerBlock : Keff;
     if (hist)
         for (int i = threadIdx.x; i < kHistPasses * 256; i += kExpandThreads) s_dhist[i] = 0;
-    // digits above the first are counted per run of keys with equal high bits
+    // each digit is counted per run of consecutive keys with the same value of
+    // that digit (one shared atomic per run): along a rectangle's row the
+    // identity layout's high digits and the block layout's low digit repeat
     const int passes = digit_passes(key_bits);
-    const int s1 = passes > 1 ? digit_shift(key_bits, 1) : 0;
-    auto flush_run = [&](uint32_t h, uint32_t cnt) {
-        for (int q = 1; q < passes; q++) atomicAdd(&s_dhist[q * 256 + digit(h << s1, key_bits, q)], cnt);
-    };
     const unsigned long long r0 = S0 + (unsigned long long)threadIdx.x * kRun;   // this thread's slots
     const unsigned long long r1 = r0 + kRun < S1 ? r0 + kRun : S1;
 
@@ -378,7 +376,12 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
             uint32_t rank = (uint32_t)(a0 - s_first[lo]);
             uint32_t dy = div_small(rank, w);
             uint32_t ty = r.y + dy, tx = r.x + (rank - dy * w);
-            uint32_t run_hi = 0xffffffffu, run_n = 0;
+            uint32_t run_d[kHistPasses], run_n[kHistPasses];
+#pragma unroll
+            for (int q = 0; q < kHistPasses; q++) {
+                run_d[q] = 0xffffffffu;
+                run_n[q] = 0;
+            }
             for (unsigned long long j = a0; j < a1; j++) {
                 // step to the next position once this one's tiles are used up
                 while (lo + 1 < wn && s_first[lo + 1] <= j) {
@@ -388,21 +391,23 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
                     tx = r.x;
                     ty = r.y;
                 }
-                const uint32_t tile = ty * (uint32_t)tiles_x + tx;
+                const uint32_t tile = tile_key(km, tx, ty);
                 const uint32_t si = (uint32_t)(j - S0);
                 GS_CHECK(si < (uint32_t)kKeysPerBlock && j < (unsigned long long)key_capacity && tx <= r.z);
                 s_key[si + (si >> 5)] = tile;
                 s_val[si + (si >> 5)] = s_g[lo];
                 if (hist) {
-                    atomicAdd(&s_dhist[digit(tile, key_bits, 0)], 1u);
-                    if (passes > 1) {
-                        const uint32_t h = tile >> s1;
-                        if (h != run_hi) {
-                            if (run_n) flush_run(run_hi, run_n);
-                            run_hi = h;
-                            run_n = 0;
+#pragma unroll
+                    for (int q = 0; q < kHistPasses; q++) {
+                        if (q < passes) {
+                            const uint32_t d = digit(tile, key_bits, q);
+                            if (d != run_d[q]) {
+                                if (run_n[q]) atomicAdd(&s_dhist[q * 256 + run_d[q]], run_n[q]);
+                                run_d[q] = d;
+                                run_n[q] = 0;
+                            }
+                            run_n[q]++;
                         }
-                        run_n++;
                     }
                 }
                 if (++tx > r.z) {
@@ -410,7 +415,11 @@ __global__ void __launch_bounds__(kExpandThreads) bin_expand_kernel(
                     ty++;
                 }
             }
-            if (hist && run_n) flush_run(run_hi, run_n);
+            if (hist) {
+#pragma unroll
+                for (int q = 0; q < kHistPasses; q++)
+                    if (q < passes && run_n[q]) atomicAdd(&s_dhist[q * 256 + run_d[q]], run_n[q]);
+            }
         }
         if (s_end >= S1 || p + wn >= n) break;
         p += wn;
@@ -492,7 +501,8 @@ size_t bin_ordered_scratch_bytes(int64_t n, int64_t key_capacity) {
 cudaError_t launch_bin_ordered(const gs_projected& p, const uint32_t* order, int64_t n, const CamConst& cam,
                                uint32_t* offsets, uint32_t* tile_keys, uint32_t* vals, int64_t key_capacity,
                                uint64_t* num_keys, StatusHeader* status, void* scratch, cudaStream_t s,
-                               uint32_t* hist, int key_bits) {
+                               uint32_t* hist, int key_bits, const TileKeyMap* keymap) {
+    const TileKeyMap km = keymap ? *keymap : identity_keys(cam.tiles_x);
     if (n == 0) {
         cudaError_t e = cudaMemsetAsync(num_keys, 0, sizeof(uint64_t), s);
         if (e != cudaSuccess) return e;
@@ -513,7 +523,7 @@ cudaError_t launch_bin_ordered(const gs_projected& p, const uint32_t* order, int
     launch_k(bin_offsets_kernel, nb, kBinThreads, 0, s, rs, n, sums, key_capacity, first_slot, owner, offsets);
     if (key_capacity > 0) {
         const unsigned blocks = (unsigned)((key_capacity + kKeysPerBlock - 1) / kKeysPerBlock);
-        launch_k(bin_expand_kernel, blocks, kExpandThreads, 0, s, rs, order, n, cam.tiles_x, first_slot, owner,
+        launch_k(bin_expand_kernel, blocks, kExpandThreads, 0, s, rs, order, n, km, first_slot, owner,
                  num_keys, key_capacity, tile_keys, vals, hist, key_bits);
     }
     return cudaGetLastError();

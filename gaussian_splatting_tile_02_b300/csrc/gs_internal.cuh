@@ -87,6 +87,45 @@ __device__ __forceinline__ void pixel_pair_exponents(float A1, float A2, float k
     e2 = __fmaf_rn(-t22, t22, e1);
 }
 
+// The key a (tile, Gaussian) pair is sorted by, for a tile (tx, ty). Identity
+// (cbx == 0): the tile id ty * tiles_x + tx. Coarse-block layout: the low
+// cbits bits number the 8x8-tile block (ty / 8) * cbx + tx / 8 and the 6 bits
+// above them the tile inside it, so the first radix pass sorts by block (a
+// Gaussian's few tiles mostly share one) and the second by the tile within.
+// Either way each tile's pairs are contiguous after a stable sort, in the same
+// order; only the order of the tiles' lists differs.
+struct TileKeyMap {
+    int tiles_x;
+    int cbx;     // 8x8-tile blocks per row, or 0 for the identity
+    int cbits;   // bits of the block number
+};
+__host__ __device__ inline uint32_t tile_key(const TileKeyMap& m, uint32_t tx, uint32_t ty) {
+    if (m.cbx == 0) return ty * (uint32_t)m.tiles_x + tx;
+    return ((((ty & 7u) << 3) | (tx & 7u)) << m.cbits) | ((ty >> 3) * (uint32_t)m.cbx + (tx >> 3));
+}
+__host__ __device__ inline uint32_t tile_of_key(const TileKeyMap& m, uint32_t key) {
+    if (m.cbx == 0) return key;
+    const uint32_t block = key & ((1u << m.cbits) - 1u), fine = key >> m.cbits;
+    const uint32_t tx = (block % (uint32_t)m.cbx) * 8u + (fine & 7u), ty = (block / (uint32_t)m.cbx) * 8u + (fine >> 3);
+    return ty * (uint32_t)m.tiles_x + tx;
+}
+inline TileKeyMap identity_keys(int tiles_x_) { return TileKeyMap{tiles_x_, 0, 0}; }
+inline TileKeyMap coarse_block_keys(int tiles_x_, int tiles_y_) {
+    TileKeyMap m{tiles_x_, (tiles_x_ + 7) / 8, 0};
+    const int blocks = m.cbx * ((tiles_y_ + 7) / 8);
+    while ((1 << m.cbits) < blocks) m.cbits++;
+    if (m.cbits == 0) m.cbits = 1;
+    return m;
+}
+inline int tile_key_bits(const TileKeyMap& m, int tiles) {
+    if (m.cbx == 0) {
+        int b = 0;
+        while ((1 << b) < tiles) b++;
+        return b > 0 ? b : 1;
+    }
+    return m.cbits + 6;
+}
+
 inline int tiles_x(const gs_camera& c) { return (c.width + kTile - 1) / kTile; }
 inline int tiles_y(const gs_camera& c) { return (c.height + kTile - 1) / kTile; }
 
@@ -230,7 +269,7 @@ size_t bin_ordered_scratch_bytes(int64_t n, int64_t key_capacity);
 cudaError_t launch_bin_ordered(const gs_projected& p, const uint32_t* order, int64_t n, const CamConst& cam,
                                uint32_t* offsets, uint32_t* tile_keys, uint32_t* vals, int64_t key_capacity,
                                uint64_t* num_keys, StatusHeader* status, void* scratch, cudaStream_t s,
-                               uint32_t* hist = nullptr, int key_bits = 0);
+                               uint32_t* hist = nullptr, int key_bits = 0, const TileKeyMap* keymap = nullptr);
 cudaError_t launch_depth_keys(const gs_projected& p, int64_t n, uint32_t* keys, uint32_t* vals, uint32_t* hist,
                               cudaStream_t s);
 
@@ -261,7 +300,7 @@ cudaError_t launch_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_
 // ranges_zeroed: the caller cleared the ranges already (otherwise a memset does)
 cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* num_keys,
                                  int64_t key_capacity, int n_tiles, uint32_t* ranges, cudaStream_t s,
-                                 bool ranges_zeroed = false);
+                                 bool ranges_zeroed = false, const TileKeyMap* keymap = nullptr);
 cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations, cudaStream_t s);
 
 // tiledepth.cu: each tile's list (Gaussians in index order, [ranges.x, ranges.y) of vals)

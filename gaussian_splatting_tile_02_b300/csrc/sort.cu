@@ -677,7 +677,7 @@ template <typename KeyT>
 __global__ void __launch_bounds__(256) tile_ranges_kernel(const KeyT* __restrict__ keys,
                                                           const uint64_t* __restrict__ num_keys, int64_t cap,
                                                           int shift, int n_tiles, bool vec,
-                                                          uint2* __restrict__ ranges) {
+                                                          uint2* __restrict__ ranges, const TileKeyMap km) {
     grid_dependency_begin();
     static_assert(kRangeItems * sizeof(KeyT) % 16 == 0, "a run is whole 16-byte vectors");
     const int64_t K = key_count(num_keys, cap);
@@ -705,10 +705,13 @@ __global__ void __launch_bounds__(256) tile_ranges_kernel(const KeyT* __restrict
             if (j < n) {
                 const uint32_t t = (uint32_t)(k[j] >> shift);
                 const uint32_t next = j + 1 < n ? (uint32_t)(k[j + 1] >> shift) : after;
-                GS_CHECK(t < (uint32_t)n_tiles);
-                if (t < (uint32_t)n_tiles) {
-                    if (t != prev) ranges[t].x = (uint32_t)(i0 + j);
-                    if (t != next) ranges[t].y = (uint32_t)(i0 + j + 1);
+                if (t != prev || t != next) {   // a list's first or last entry
+                    const uint32_t tile = tile_of_key(km, t);
+                    GS_CHECK(tile < (uint32_t)n_tiles);
+                    if (tile < (uint32_t)n_tiles) {
+                        if (t != prev) ranges[tile].x = (uint32_t)(i0 + j);
+                        if (t != next) ranges[tile].y = (uint32_t)(i0 + j + 1);
+                    }
                 }
                 prev = t;
             }
@@ -872,17 +875,18 @@ cudaError_t launch_tile_ranges(const uint64_t* sorted_keys, const uint64_t* num_
     if (e != cudaSuccess || cap == 0) return e;
     const bool vec = (reinterpret_cast<uintptr_t>(sorted_keys) & 15) == 0;
     launch_k(tile_ranges_kernel<uint64_t>, grid_for(cap, 256 * kRangeItems, 148 * 8), 256, 0, s,
-             sorted_keys, num_keys, cap, 32, n_tiles, vec, reinterpret_cast<uint2*>(ranges));
+             sorted_keys, num_keys, cap, 32, n_tiles, vec, reinterpret_cast<uint2*>(ranges), identity_keys(0));
     return cudaGetLastError();
 }
 
 cudaError_t launch_tile_ranges32(const uint32_t* sorted_tiles, const uint64_t* num_keys, int64_t cap, int n_tiles,
-                                 uint32_t* ranges, cudaStream_t s, bool ranges_zeroed) {
+                                 uint32_t* ranges, cudaStream_t s, bool ranges_zeroed, const TileKeyMap* keymap) {
     cudaError_t e = ranges_zeroed ? cudaSuccess : cudaMemsetAsync(ranges, 0, sizeof(uint32_t) * 2 * (size_t)n_tiles, s);
     if (e != cudaSuccess || cap == 0) return e;
     const bool vec = (reinterpret_cast<uintptr_t>(sorted_tiles) & 15) == 0;
     launch_k(tile_ranges_kernel<uint32_t>, grid_for(cap, 256 * kRangeItems, 148 * 8), 256, 0, s,
-             sorted_tiles, num_keys, cap, 0, n_tiles, vec, reinterpret_cast<uint2*>(ranges));
+             sorted_tiles, num_keys, cap, 0, n_tiles, vec, reinterpret_cast<uint2*>(ranges),
+             keymap ? *keymap : identity_keys(0));
     return cudaGetLastError();
 }
 

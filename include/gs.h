@@ -271,9 +271,11 @@ gs_status gs_rasterize(const gs_projected* projected, int64_t n, const uint32_t*
 
 /* The whole frame: step 1, steps 2-4 in one of two orders, and step 5, chained
  * on `stream` with no host synchronisation (so the call can be captured into a
- * CUDA graph). Depth-first (gs_depth_order, gs_bin_ordered, gs_sort32,
+ * CUDA graph). Depth-first (as gs_depth_order, gs_bin_ordered, gs_sort32,
  * gs_tile_ranges32): the Gaussians are sorted by depth, binned in that order
- * and stably sorted by tile. Tile-first, for short tile lists (see
+ * and stably sorted by tile. From 4096 tiles up the tile sort's keys number
+ * the 8x8-tile block in their low digit and the tile inside it above, which
+ * orders the tiles' lists differently in the array, not their contents. Tile-first, for short tile lists (see
  * gs_render_tile_first): binned in index order, stably sorted by tile, then
  * each tile's list is sorted by (depth bits, index) on its own. Both give the
  * same per-tile lists bit for bit. The image equals the one of the staged path
@@ -317,10 +319,13 @@ gs_status gs_set_steps_order(int32_t order);
 
 /* Where a gs_render (or one view of gs_render_batch) workspace keeps the
  * frame's per-tile lists: *sorted_vals receives the device address of the
- * Gaussian indices sorted by (tile, depth bits, index) -- its first K entries
- * are valid after a frame, K as gs_read_status reports it -- and *ranges that
- * of the tile ranges (uint32 [tiles_y * tiles_x][2], [start, end) into the
- * sorted list). n, width, height and key_capacity must be those the workspace
+ * frame's K Gaussian indices -- valid after a frame, K as gs_read_status
+ * reports it -- and *ranges that of the tile ranges (uint32 [tiles_y *
+ * tiles_x][2], [start, end) into the sorted list). Tile t's list is
+ * sorted_vals[ranges[t][0] .. ranges[t][1]), sorted by (depth bits, index),
+ * and the lists tile [0, K). From 4096 tiles up the lists are laid out in the
+ * order of the frame's tile keys (8x8-tile blocks in the low digit), not by
+ * tile id; below that, by tile id. n, width, height and key_capacity must be those the workspace
  * was sized with (gs_render_workspace_bytes). Host-only arithmetic on ws; no
  * CUDA call. The lists are the ones the pages' step "Depth-sort per tile"
  * produces (section "Rastérisation, non rayée"). */

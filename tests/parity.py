@@ -66,6 +66,31 @@ def check_image(oracle, ref, cam, image, final_T=None, n_contrib=None, tol=TOL, 
     return stats
 
 
+def tile_lists_in_tile_order(vals, ranges):
+    """The per-tile lists of a sorted array (vals[ranges[t, 0]:ranges[t, 1]] for tile t),
+    concatenated in tile-id order, with their lengths. Checks that the lists tile [0, K)."""
+    vals = np.asarray(vals).view(np.uint32)
+    r = np.asarray(ranges).view(np.uint32).reshape(-1, 2).astype(np.int64)
+    lens = np.maximum(r[:, 1] - r[:, 0], 0)
+    nz = np.nonzero(lens)[0]
+    by_start = nz[np.argsort(r[nz, 0], kind="stable")]
+    ends = r[by_start, 0] + lens[by_start]
+    assert len(by_start) == 0 or (r[by_start[0], 0] == 0 and np.array_equal(r[by_start[1:], 0], ends[:-1])), \
+        "tile lists overlap or leave gaps"
+    K = int(lens.sum())
+    idx = np.repeat(r[:, 0] - np.concatenate(([0], np.cumsum(lens)[:-1])), lens) + np.arange(K)
+    return vals[idx], lens
+
+
+def assert_same_tile_lists(vals, ranges, ref_vals, ref_ranges):
+    """Every tile's list equal (same Gaussians, same order), whatever the order of the lists
+    in the array."""
+    a, la = tile_lists_in_tile_order(vals, ranges)
+    b, lb = tile_lists_in_tile_order(ref_vals, ref_ranges)
+    np.testing.assert_array_equal(la, lb)
+    np.testing.assert_array_equal(a, b)
+
+
 def assert_image_parity(stats):
     assert stats["n_unexplained"] == 0, stats
     assert stats["max_err_unflipped"] <= TOL, stats

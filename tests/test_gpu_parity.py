@@ -15,7 +15,7 @@ import pytest
 import gaussian_splatting_tile_02_b300 as gs
 from gaussian_splatting_tile_02_b300 import native, scenes
 
-from parity import assert_image_parity, check_image, oracle_render
+from parity import assert_image_parity, assert_same_tile_lists, check_image, oracle_render
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -178,8 +178,7 @@ def test_full_path_parity(oracle_mod, name, view):
         st, flags, K = br.status(view)
         assert st == native.GS_OK and K == ref["num_keys"], (st, flags, K)
         vals, ranges = br.lists(view)
-        np.testing.assert_array_equal(vals.cpu().numpy().view(np.uint32), ref["sorted_vals"])
-        np.testing.assert_array_equal(ranges.cpu().numpy().view(np.uint32), ref["ranges"])
+        assert_same_tile_lists(vals.cpu().numpy(), ranges.cpu().numpy(), ref["sorted_vals"], ref["ranges"])
         bstats = check_image(oracle_mod, ref, cam, br.images[view].cpu().numpy(), br.final_T[view].cpu().numpy(),
                              br.n_contrib[view].cpu().numpy())
         print(name, view, "batch", bstats)
@@ -197,8 +196,7 @@ def test_render_equals_stages_and_graph_replay(oracle_mod):
     st, flags, K = r.status()
     assert st == native.GS_OK and K == out["K"]
     vals, ranges = r.lists()
-    np.testing.assert_array_equal(vals.cpu().numpy().view(np.uint32), out["sorted_vals"])
-    np.testing.assert_array_equal(ranges.cpu().numpy().view(np.uint32), out["ranges"])
+    assert_same_tile_lists(vals.cpu().numpy(), ranges.cpu().numpy(), out["sorted_vals"], out["ranges"])
     np.testing.assert_array_equal(r.image.cpu().numpy(), out["image"])
     # without the per-pixel outputs the compositing kernel skips their bookkeeping: same image
     r.image.zero_()
@@ -250,8 +248,7 @@ def test_tile_first_and_depth_first_orders_agree(oracle_mod, name, n, view):
             st, flags, k = r.status()
             assert st == native.GS_OK and k == K, (order, st, flags, k)
             vals, ranges = r.lists()
-            np.testing.assert_array_equal(vals.cpu().numpy().view(np.uint32)[:K], out["sorted_vals"])
-            np.testing.assert_array_equal(ranges.cpu().numpy().view(np.uint32), out["ranges"])
+            assert_same_tile_lists(vals.cpu().numpy()[:K], ranges.cpu().numpy(), out["sorted_vals"], out["ranges"])
             np.testing.assert_array_equal(r.image.cpu().numpy(), out["image"])
             np.testing.assert_array_equal(r.final_T.cpu().numpy(), out["final_T"])
             np.testing.assert_array_equal(r.n_contrib.cpu().numpy(), out["n_contrib"])
