@@ -31,7 +31,10 @@
 // suffix colour a unchanged and adds no gradient, so both pixels run the same
 // instructions without branching. Per entry, the warp sums its lanes'
 // contributions (a reduce-scatter of the 9 values over the lanes) and nine
-// lanes add them to the Gaussian's gradient with one global atomic instruction.
+// lanes add them into the batch's shared-memory sums for that entry, where the
+// block's other warps add theirs; once the whole block has walked the batch,
+// one thread per entry adds the nine sums to the Gaussian's gradient with
+// global atomics (one set per tile instead of one per warp).
 //
 // Step 1 backward (preprocess_backward_kernel): one thread per Gaussian maps
 // dL/d(u, v), dL/d(conic), dL/do, dL/dc to the parameters through
@@ -145,7 +148,12 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
     __shared__ float4 s_box[2][kBwdThreads];  // alpha >= 1/255 box, tile-local
     __shared__ float4 w_q[kBwdThreads / 32][32];
     __shared__ float4 w_r[kBwdThreads / 32][32];
-    __shared__ float4 w_c[kBwdThreads / 32][32];   // (b, 1/o, list position as bits, Gaussian as bits)
+    __shared__ float4 w_c[kBwdThreads / 32][32];   // (b, 1/o, list position as bits, unused)
+    // the batch's gradient sums, [batch entry][9], added to by every warp that
+    // takes the entry and flushed to global memory once per batch (double-buffered
+    // so that one batch's flush overlaps the next batch's walk)
+    __shared__ float s_acc[2][kBwdThreads * 9];
+    __shared__ uint32_t s_g[2][kBwdThreads];   // the batch entries' Gaussians
     __shared__ uint32_t s_max;
 
     const int tile = a.order ? (int)a.order[blockIdx.x] : (int)blockIdx.x;
@@ -184,6 +192,7 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
     const f2x GG0 = pk2(P1.g0, P2.g0), GG1 = pk2(P1.g1, P2.g1), GG2 = pk2(P1.g2, P2.g2);
 
     if (threadIdx.x == 0) s_max = 0;
+    for (int i = threadIdx.x; i < 2 * kBwdThreads * 9; i += kBwdThreads) (&s_acc[0][0])[i] = 0.0f;
     __syncthreads();
     {
         const uint32_t m = __reduce_max_sync(0xffffffffu, max(P1.last, P2.last));
@@ -195,15 +204,17 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
     GS_CHECK(range.y >= range.x && s_max <= range.y - range.x);
     const uint32_t len = range.y > range.x ? min(s_max, range.y - range.x) : 0u;
 
-    auto fetch = [&](uint32_t pos, float4& r0, float4& r1, float4& r2) {
+    auto fetch = [&](uint32_t pos, float4& r0, float4& r1, float4& r2, uint32_t& gi) {
         uint32_t g = __ldg(a.sorted_vals + range.x + pos);
         GS_CHECK(g < a.n);
+        gi = g;               // an out-of-scene index gets no gradient
         if (g >= a.n) g = 0;   // only a sort cut short (flagged) can give this
         r0 = __ldg(a.raster + 3 * g);
         r1 = __ldg(a.raster + 3 * g + 1);
         r2 = __ldg(a.raster + 3 * g + 2);
     };
-    auto store = [&](int buf, const float4& r0, const float4& r1, const float4& r2) {
+    auto store = [&](int buf, const float4& r0, const float4& r1, const float4& r2, uint32_t gi) {
+        s_g[buf][threadIdx.x] = gi;
         const float mx = (r0.x - tile_x0) + r0.z, my = (r0.y - tile_y0) + r0.w;
         const uint32_t hb = __float_as_uint(r2.w);
         const __half2 h = *reinterpret_cast<const __half2*>(&hb);
@@ -224,22 +235,53 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
         const uint32_t lo = lo_of(0);
         if (lo + threadIdx.x < len) {
             float4 r0, r1, r2;
-            fetch(lo + threadIdx.x, r0, r1, r2);
-            store(0, r0, r1, r2);
+            uint32_t gi;
+            fetch(lo + threadIdx.x, r0, r1, r2, gi);
+            store(0, r0, r1, r2, gi);
         }
     }
     __syncthreads();
 
+    // one thread per entry of a finished batch: its nine sums to the global arrays
+    auto flush = [&](int bf, uint32_t cnt) {
+        const int t = threadIdx.x;
+        if ((uint32_t)t >= cnt) return;
+        float* acc = &s_acc[bf][t * 9];
+        float v[9];
+        bool any = false;
+#pragma unroll
+        for (int q = 0; q < 9; q++) {
+            v[q] = acc[q];
+            any |= v[q] != 0.0f;
+            acc[q] = 0.0f;
+        }
+        const uint32_t g = s_g[bf][t];
+        if (!any || g >= a.n) return;
+        atomicAdd(a.g_mean2d + 2 * g, v[0]);
+        atomicAdd(a.g_mean2d + 2 * g + 1, v[1]);
+        atomicAdd(a.g_conic + 3 * g, v[2]);
+        atomicAdd(a.g_conic + 3 * g + 1, v[3]);
+        atomicAdd(a.g_conic + 3 * g + 2, v[4]);
+        atomicAdd(a.g_opacity + g, v[5]);
+        atomicAdd(a.g_rgb + 3 * g, v[6]);
+        atomicAdd(a.g_rgb + 3 * g + 1, v[7]);
+        atomicAdd(a.g_rgb + 3 * g + 2, v[8]);
+    };
+
+    uint32_t prev_cnt = 0;
     for (uint32_t b = 0; b < nbatch; b++) {
         const int buf = b & 1;
         const uint32_t lo = lo_of(b), hi = len - b * kBwdThreads;
         const uint32_t cnt = hi - lo;
         const bool have_next = b + 1 < nbatch;
         float4 n0, n1, n2;
+        uint32_t ng = 0;
         if (have_next) {
             const uint32_t nlo = lo_of(b + 1);
-            if (nlo + threadIdx.x < lo) fetch(nlo + threadIdx.x, n0, n1, n2);
+            if (nlo + threadIdx.x < lo) fetch(nlo + threadIdx.x, n0, n1, n2, ng);
         }
+        // the previous batch's sums (every warp has passed the barrier after it)
+        if (b > 0) flush(buf ^ 1, prev_cnt);
         // the list positions of this batch, last group first
 #pragma unroll 1
         for (int i = kBwdThreads / 32 - 1; i >= 0; i--) {
@@ -257,8 +299,7 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
                 w_r[warp][pos] = s_r[buf][j];
                 const float2 c = s_c[buf][j];
                 const uint32_t lp = lo + j;
-                w_c[warp][pos] = make_float4(c.x, c.y, __uint_as_float(lp),
-                                             __uint_as_float(__ldg(a.sorted_vals + range.x + lp)));
+                w_c[warp][pos] = make_float4(c.x, c.y, __uint_as_float(lp), 0.0f);
             }
             __syncwarp();
             const int nh = __popc(m);
@@ -309,23 +350,19 @@ __global__ void __launch_bounds__(kBwdThreads) rasterize_backward_kernel(const B
                 const float part[9] = {gu, gv, gA, gB, gC, go, gr, gg, gb};
                 const float sum = warp_reduce_scatter9(part, lane);
                 const int slot = slot_of(lane);
-                const uint32_t g = __float_as_uint(c.w);
-                if (!(lane & 1) && slot < 9 && g < a.n) {
-                    float* dst = slot < 2 ? a.g_mean2d + 2 * g + slot
-                               : slot < 5 ? a.g_conic + 3 * g + (slot - 2)
-                               : slot < 6 ? a.g_opacity + g
-                                          : a.g_rgb + 3 * g + (slot - 6);
-                    atomicAdd(dst, sum);
-                }
+                // into the batch's sums for this entry (the block's other warps add theirs)
+                if (!(lane & 1) && slot < 9) atomicAdd(&s_acc[buf][(lp - lo) * 9 + slot], sum);
             }
             __syncwarp();
         }
         if (have_next) {
             const uint32_t nlo = lo_of(b + 1);
-            if (nlo + threadIdx.x < lo) store(buf ^ 1, n0, n1, n2);
+            if (nlo + threadIdx.x < lo) store(buf ^ 1, n0, n1, n2, ng);
         }
         __syncthreads();
+        prev_cnt = cnt;
     }
+    if (nbatch > 0) flush((nbatch - 1) & 1, prev_cnt);
 }
 
 // ------------------------------------------------------------------ step 1 backward
