@@ -223,13 +223,13 @@ def tile_depth_launches(key_capacity: int) -> int:
 
 
 def tile_key_bits(tiles_x: int, tiles_y: int) -> int:
-    """Bits of the frame's tile-sort keys: the tile id below 4096 tiles, else the 8x8-tile
-    block number and 6 bits for the tile inside the block."""
+    """Bits of the frame's tile-sort keys: the tile id below 4096 tiles, else the number of
+    the block of 8 x 4 tiles and 5 bits for the tile inside the block."""
     tiles = tiles_x * tiles_y
     if tiles < 4096:
         return max(1, (tiles - 1).bit_length())
-    blocks = -(-tiles_x // 8) * -(-tiles_y // 8)
-    return max(1, (blocks - 1).bit_length()) + 6
+    blocks = -(-tiles_x // 8) * -(-tiles_y // 4)
+    return max(1, (blocks - 1).bit_length()) + 5
 
 
 def frame_launches(tiles: int, tile_first: bool = False, key_capacity: int = 1 << 20, tiles_xy=None) -> int:

@@ -205,9 +205,9 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
     auto* ranges = reinterpret_cast<uint32_t*>(w + L.ranges);
     const CamConst cc = make_cam_const(*cam);
 
-    // the tile sort's keys: 8x8-tile block in the low digit from 4096 tiles up
+    // the tile sort's keys: the tile block in the low digit from 4096 tiles up
     // (a warp's first-pass ranking then sees far fewer distinct digits)
-    const TileKeyMap km = cc.tiles_x * cc.tiles_y >= kCoarseKeyTiles ? coarse_block_keys(cc.tiles_x, cc.tiles_y)
+    const TileKeyMap km = cc.tiles_x * cc.tiles_y >= kCoarseKeyTiles ? block_keys(cc.tiles_x, cc.tiles_y)
                                                                      : identity_keys(cc.tiles_x);
     const int tbits = tile_key_bits(km, cc.tiles_x * cc.tiles_y);
     auto mark = [&](int i) {

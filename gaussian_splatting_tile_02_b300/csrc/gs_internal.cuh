@@ -88,31 +88,38 @@ __device__ __forceinline__ void pixel_pair_exponents(float A1, float A2, float k
 }
 
 // The key a (tile, Gaussian) pair is sorted by, for a tile (tx, ty). Identity
-// (cbx == 0): the tile id ty * tiles_x + tx. Coarse-block layout: the low
-// cbits bits number the 8x8-tile block (ty / 8) * cbx + tx / 8 and the 6 bits
-// above them the tile inside it, so the first radix pass sorts by block (a
-// Gaussian's few tiles mostly share one) and the second by the tile within.
-// Either way each tile's pairs are contiguous after a stable sort, in the same
-// order; only the order of the tiles' lists differs.
+// (cbx == 0): the tile id ty * tiles_x + tx. Block layout: the low cbits bits
+// number the block of 8 x kKeyBlockH tiles, (ty / kKeyBlockH) * cbx + tx / 8,
+// and the bits above them the tile inside it, so the first radix pass sorts by
+// block (a Gaussian's few tiles mostly share one) and the next by the tile
+// within. Either way each tile's pairs are contiguous after a stable sort, in
+// the same order; only the order of the tiles' lists differs.
+#ifndef GS_KEY_BLOCK_H
+#define GS_KEY_BLOCK_H 4
+#endif
+constexpr int kKeyBlockH = GS_KEY_BLOCK_H;   // 4 or 8
+constexpr int kKeyFineBits = kKeyBlockH == 8 ? 6 : 5;
 struct TileKeyMap {
     int tiles_x;
-    int cbx;     // 8x8-tile blocks per row, or 0 for the identity
+    int cbx;     // blocks per row, or 0 for the identity
     int cbits;   // bits of the block number
 };
 __host__ __device__ inline uint32_t tile_key(const TileKeyMap& m, uint32_t tx, uint32_t ty) {
     if (m.cbx == 0) return ty * (uint32_t)m.tiles_x + tx;
-    return ((((ty & 7u) << 3) | (tx & 7u)) << m.cbits) | ((ty >> 3) * (uint32_t)m.cbx + (tx >> 3));
+    const uint32_t fine = ((ty % (uint32_t)kKeyBlockH) << 3) | (tx & 7u);
+    return (fine << m.cbits) | ((ty / (uint32_t)kKeyBlockH) * (uint32_t)m.cbx + (tx >> 3));
 }
 __host__ __device__ inline uint32_t tile_of_key(const TileKeyMap& m, uint32_t key) {
     if (m.cbx == 0) return key;
     const uint32_t block = key & ((1u << m.cbits) - 1u), fine = key >> m.cbits;
-    const uint32_t tx = (block % (uint32_t)m.cbx) * 8u + (fine & 7u), ty = (block / (uint32_t)m.cbx) * 8u + (fine >> 3);
+    const uint32_t tx = (block % (uint32_t)m.cbx) * 8u + (fine & 7u);
+    const uint32_t ty = (block / (uint32_t)m.cbx) * (uint32_t)kKeyBlockH + (fine >> 3);
     return ty * (uint32_t)m.tiles_x + tx;
 }
 inline TileKeyMap identity_keys(int tiles_x_) { return TileKeyMap{tiles_x_, 0, 0}; }
-inline TileKeyMap coarse_block_keys(int tiles_x_, int tiles_y_) {
+inline TileKeyMap block_keys(int tiles_x_, int tiles_y_) {
     TileKeyMap m{tiles_x_, (tiles_x_ + 7) / 8, 0};
-    const int blocks = m.cbx * ((tiles_y_ + 7) / 8);
+    const int blocks = m.cbx * ((tiles_y_ + kKeyBlockH - 1) / kKeyBlockH);
     while ((1 << m.cbits) < blocks) m.cbits++;
     if (m.cbits == 0) m.cbits = 1;
     return m;
@@ -123,7 +130,7 @@ inline int tile_key_bits(const TileKeyMap& m, int tiles) {
         while ((1 << b) < tiles) b++;
         return b > 0 ? b : 1;
     }
-    return m.cbits + 6;
+    return m.cbits + kKeyFineBits;
 }
 
 inline int tiles_x(const gs_camera& c) { return (c.width + kTile - 1) / kTile; }

@@ -274,7 +274,7 @@ gs_status gs_rasterize(const gs_projected* projected, int64_t n, const uint32_t*
  * CUDA graph). Depth-first (as gs_depth_order, gs_bin_ordered, gs_sort32,
  * gs_tile_ranges32): the Gaussians are sorted by depth, binned in that order
  * and stably sorted by tile. From 4096 tiles up the tile sort's keys number
- * the 8x8-tile block in their low digit and the tile inside it above, which
+ * the 8x4-tile block in their low digit and the tile inside it above, which
  * orders the tiles' lists differently in the array, not their contents. Tile-first, for short tile lists (see
  * gs_render_tile_first): binned in index order, stably sorted by tile, then
  * each tile's list is sorted by (depth bits, index) on its own. Both give the
@@ -324,7 +324,7 @@ gs_status gs_set_steps_order(int32_t order);
  * tiles_x][2], [start, end) into the sorted list). Tile t's list is
  * sorted_vals[ranges[t][0] .. ranges[t][1]), sorted by (depth bits, index),
  * and the lists tile [0, K). From 4096 tiles up the lists are laid out in the
- * order of the frame's tile keys (8x8-tile blocks in the low digit), not by
+ * order of the frame's tile keys (8x4-tile blocks in the low digit), not by
  * tile id; below that, by tile id. n, width, height and key_capacity must be those the workspace
  * was sized with (gs_render_workspace_bytes). Host-only arithmetic on ws; no
  * CUDA call. The lists are the ones the pages' step "Depth-sort per tile"

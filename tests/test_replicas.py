@@ -130,8 +130,8 @@ def test_frame_launch_count():
     assert bench.frame_launches(4 * 4, tile_first=True, key_capacity=512) == 14
     assert [bench.tile_depth_launches(c) for c in (0, 1, 2, 512, 513, 2048, 2049, 8192, 8193)] == \
         [0, 0, 1, 1, 2, 2, 3, 3, 4]
-    # from 4096 tiles up the tile keys hold the 8x8-tile block and 6 bits of tile within it
-    assert bench.tile_key_bits(120, 68) == 14 and bench.tile_key_bits(40, 30) == 11
+    # from 4096 tiles up the tile keys hold the 8x4-tile block and 5 bits of tile within it
+    assert bench.tile_key_bits(120, 68) == 13 and bench.tile_key_bits(40, 30) == 11
     assert bench.tile_key_bits(512, 270) == 18 and bench.tile_key_bits(240, 135) == 15
     assert bench.frame_launches(120 * 68, tiles_xy=(120, 68)) == 18
     assert bench.frame_launches(512 * 270, tiles_xy=(512, 270)) == 19
