@@ -323,6 +323,36 @@ def test_programmatic_launch_changes_nothing(name, n, view):
             np.testing.assert_array_equal(x, z, err_msg=str(key))
 
 
+@pytest.mark.parametrize("name,order", [("tiny", 1), ("100k", 1), ("100k", 2), ("1M", 1)])
+def test_frame_does_not_depend_on_workspace_contents(name, order):
+    """A frame reads nothing it did not write: rendered into a workspace filled with 0x5a and
+    into one filled with 0xa5 (no earlier frame in either), in the given order of steps 2-4,
+    it gives the staged path's per-tile lists and image bit for bit."""
+    scene, g = scene_of(name)
+    cam = scenes.make_cameras(name)[0]
+    out = run_stages(g, cam)
+    K = out["K"]
+    L = gs.lib()
+    try:
+        assert L.gs_set_steps_order(order) == native.GS_OK
+        for fill in (0x5A, 0xA5):
+            r = gs.Renderer(g, cam["width"], cam["height"], K + 64)
+            r.ws.fill_(fill)
+            r.image.fill_(float("nan"))
+            torch.cuda.synchronize()
+            r.render(cam)
+            torch.cuda.synchronize()
+            st, flags, k = r.status()
+            assert st == native.GS_OK and k == K, (fill, st, flags, k)
+            vals, ranges = r.lists()
+            assert_same_tile_lists(vals.cpu().numpy(), ranges.cpu().numpy(), out["sorted_vals"], out["ranges"])
+            np.testing.assert_array_equal(r.image.cpu().numpy(), out["image"])
+            np.testing.assert_array_equal(r.n_contrib.cpu().numpy(), out["n_contrib"])
+            del r
+    finally:
+        L.gs_set_steps_order(0)
+
+
 def test_tile_order_is_heavy_first_and_leaves_image_unchanged():
     """The heavy-first launch order is a permutation of the tiles with
     non-increasing floor(log2 length); the image, final T and n_contrib do not
@@ -423,7 +453,64 @@ def test_empty_and_all_culled(oracle_mod):
             out = run_stages(g, cam, capacity=16)
             assert out["K"] == 0
             img = out["image"]
+            # the whole frame in both orders of steps 2-4
+            L = gs.lib()
+            try:
+                for order in (1, 2):
+                    assert L.gs_set_steps_order(order) == native.GS_OK
+                    r = gs.Renderer(g, 64, 64, 16)
+                    r.render(cam)
+                    torch.cuda.synchronize()
+                    assert r.status()[0] == native.GS_OK and r.status()[2] == 0
+                    np.testing.assert_array_equal(r.image.cpu().numpy(), img)
+            finally:
+                L.gs_set_steps_order(0)
         np.testing.assert_array_equal(img, np.broadcast_to(np.float32([0.25, 0.5, 0.75]), (64, 64, 3)))
+
+
+@pytest.mark.parametrize("kind", ["one_depth", "one_visible", "close_depths", "moderate_depths", "wide_depths"])
+def test_depth_first_frames_over_depth_distributions(oracle_mod, kind):
+    """Depth-first frames over depth distributions whose keys differ in one to four bytes: a
+    layer of equal depths (every key equal, order by index alone), a single visible
+    Gaussian, depths within 4 +- 0.01, 3 .. 5 (across a power of two) and 0.3 .. 90. Each
+    gives the staged path's per-tile lists and image bit for bit."""
+    rng = np.random.default_rng(11)
+    cam = scenes.axis_camera(4.0, 300.0, 256, 192, 0.2, (0.1, 0.2, 0.3))
+    n = 3000
+    xy = rng.uniform(-1.2, 1.2, (n, 2))
+    if kind == "one_depth":
+        z = np.zeros(n)                                   # all at depth 4.0 exactly
+    elif kind == "one_visible":
+        xy[1:] = 50.0                                     # all but one off screen
+        z = rng.uniform(-1.0, 1.0, n)
+    elif kind == "close_depths":
+        z = rng.uniform(-0.01, 0.01, n)                   # depths 3.99 .. 4.01
+    elif kind == "moderate_depths":
+        z = rng.uniform(-1.0, 1.0, n)                     # depths 3 .. 5
+    else:
+        z = rng.uniform(0.3, 90.0, n) - 4.0               # depths 0.3 .. 90
+        xy *= (z[:, None] + 4.0) / 4.0                    # keep them in view
+    means = np.concatenate([xy, z[:, None]], axis=1)
+    quats = rng.normal(size=(n, 4))
+    scene = _tiny_scene(means, quats=quats / np.linalg.norm(quats, axis=1, keepdims=True),
+                        log_scales=rng.uniform(-4.0, -2.0, (n, 3)), logits=rng.uniform(-1.0, 3.0, n))
+    g = gs.gaussians_to_device(scene)
+    out = run_stages(g, cam)
+    L = gs.lib()
+    try:
+        assert L.gs_set_steps_order(1) == native.GS_OK
+        r = gs.Renderer(g, cam["width"], cam["height"], out["K"] + 64)
+        r.render(cam)
+        torch.cuda.synchronize()
+        st, flags, K = r.status()
+        assert st == native.GS_OK and K == out["K"], (st, flags, K)
+        vals, ranges = r.lists()
+        assert_same_tile_lists(vals.cpu().numpy(), ranges.cpu().numpy(), out["sorted_vals"], out["ranges"])
+        np.testing.assert_array_equal(r.image.cpu().numpy(), out["image"])
+        np.testing.assert_array_equal(r.final_T.cpu().numpy(), out["final_T"])
+        np.testing.assert_array_equal(r.n_contrib.cpu().numpy(), out["n_contrib"])
+    finally:
+        L.gs_set_steps_order(0)
 
 
 def test_border_clipping_and_large_footprints(oracle_mod):
