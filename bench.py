@@ -232,17 +232,29 @@ def tile_key_bits(tiles_x: int, tiles_y: int) -> int:
     return max(1, (blocks - 1).bit_length()) + 5
 
 
-def frame_launches(tiles: int, tile_first: bool = False, key_capacity: int = 1 << 20, tiles_xy=None) -> int:
+def side_ranges(n: int, tiles_x: int, tiles_y: int) -> bool:
+    """Whether a gs_render frame computes its tile ranges from the tile rectangles on a
+    second stream: up to 2^21 Gaussians, when the tile grid's difference array fits in 96 KB
+    of shared memory."""
+    return n <= (1 << 21) and (tiles_x + 1) * (tiles_y + 1) * 4 <= 96 * 1024
+
+
+def frame_launches(tiles: int, tile_first: bool = False, key_capacity: int = 1 << 20, tiles_xy=None,
+                   n: int = 0) -> int:
     """Kernels one gs_render frame launches for an image of `tiles` 16x16 tiles (tiles_xy:
     its tiles_x, tiles_y, for the tile keys' width; without it, the tile id's): preprocess
     (which, depth-first, also writes the depth keys); depth-first, the depth sort (4 passes);
     5 binning kernels; the tile-key sort; ranges; the tile order (count and scatter kernels up
     to 186 blocks of 256 tiles, one kernel beyond); tile-first, the per-tile depth sort
-    (tile_depth_launches); rasterize."""
+    (tile_depth_launches); rasterize. The ranges and the order run on a second stream when
+    side_ranges(n, *tiles_xy) holds; they are counted here all the same."""
     tile_bits = tile_key_bits(*tiles_xy) if tiles_xy else max(1, (tiles - 1).bit_length())
     order = 2 if -(-tiles // 256) <= 186 else 1
     depth = tile_depth_launches(key_capacity) if tile_first else sort_launches(32)
-    return 1 + depth + 5 + sort_launches(tile_bits) + 1 + order + 1
+    # the ranges: one kernel over the sorted keys, or, when the tile grid's difference
+    # array fits in 96 KB of shared memory, two on the side stream (lengths, then ranges)
+    ranges = 2 if tiles_xy and side_ranges(n, *tiles_xy) else 1
+    return 1 + depth + 5 + sort_launches(tile_bits) + ranges + order + 1
 
 
 def code_hash(files) -> str:
@@ -814,7 +826,7 @@ def run_ours(args, rank, local_rank, world):
     K = head["keys"]
     stages_out = stage_summary(st_ms, n, cfg.sh_degree, K, tx, ty, head["evaluations"], hbm_peak, fp32,
                                head["tile_first"])
-    launches_per_frame = frame_launches(tx * ty, head["tile_first"], r.key_capacity, (tx, ty))
+    launches_per_frame = frame_launches(tx * ty, head["tile_first"], r.key_capacity, (tx, ty), int(g["n"]))
     ras = stages_out["rasterize"]
     evals = head["evaluations"]
     dominant = max(stages_out, key=lambda k: stages_out[k]["ms"])

@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libgs_b300.so")
 DEBUG_LIB = os.path.join(HERE, "libgs_b300_debug.so")
 SOURCES = ["api.cu", "preprocess.cu", "binning.cu", "sort.cu", "rasterize.cu", "backward.cu", "splat2d.cu", "densify.cu",
-           "bin_static.cu", "measure.cu", "tiledepth.cu"]
+           "bin_static.cu", "measure.cu", "tiledepth.cu", "tilelen.cu"]
 HEADERS = ["gs_internal.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-O2",

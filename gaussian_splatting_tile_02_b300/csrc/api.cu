@@ -17,6 +17,7 @@ constexpr long long kDefaultSpin = 1ll << 22;
 constexpr int64_t kMaxKeyCapacity = (1ll << 30) - 1;   // look-back status words keep 30 bits
 constexpr int64_t kMaxGaussians = (1ll << 32) - 1;     // values are uint32 indices
 constexpr int kCoarseKeyTiles = 4096;                   // block-layout tile keys from this many tiles
+constexpr int64_t kSideRangesMaxN = 1ll << 21;          // ranges on a second stream up to this many Gaussians
 
 CamConst make_cam_const(const gs_camera& c) {
     CamConst k;
@@ -82,7 +83,7 @@ gs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GS_OK : GS_ERR_
 // them all and no memset separates two kernels of the frame (each kernel is
 // then launched as a programmatic dependent of the one before it).
 struct RenderLayout {
-    size_t header, num_keys, depth_head, ranges, order_done, td_counts, tile_head, zero_end, raster, depth,
+    size_t header, num_keys, depth_head, ranges, order_done, td_counts, tile_head, len_diff, zero_end, raster, depth,
         touched, rect, dkeys, dkeys_alt, order, order_alt, bin, keys, vals, keys_alt, vals_alt, depth_lb, tile_lb,
         tile_order, tdepth, pgrad, total;
 };
@@ -104,6 +105,7 @@ RenderLayout render_layout(int64_t n, int32_t w, int32_t h, int64_t cap) {
     L.order_done = take(sizeof(uint32_t));       // the tile order's finished-block counter
     L.td_counts = take(3 * sizeof(uint32_t));    // the per-tile depth sort's list lengths
     L.tile_head = take(sort_head_bytes());       // the tile sort's digit histograms and counters
+    L.len_diff = take(tile_len_diff_bytes((w + kTile - 1) / kTile, (h + kTile - 1) / kTile));
     L.zero_end = o;
     L.raster = take(48 * un);
     L.depth = take(4 * un);
@@ -185,6 +187,36 @@ bool tile_first(int64_t key_capacity, Step1 step1) {
     return key_capacity <= kTileFirstMaxKeys;
 }
 
+// The second stream a frame computes its tile ranges and launch order on, and
+// the events that fork it from the frame's stream and join it back: one set per
+// host thread and device, created on first use and kept (a cudaDeviceReset
+// invalidates them, as it does gs_render_batch's events).
+struct SideStream {
+    cudaStream_t s;
+    cudaEvent_t fork, join;
+};
+cudaError_t side_stream(SideStream* out) {
+    thread_local std::map<int, SideStream> mine;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    auto it = mine.find(dev);
+    if (it == mine.end()) {
+        SideStream ss{};
+        e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+        it = mine.emplace(dev, ss).first;
+    }
+    *out = it->second;
+    return cudaSuccess;
+}
+
+#ifndef GS_SIDE_RANGES
+#define GS_SIDE_RANGES 1
+#endif
+
 // Steps 2-5 of one view (step 1 as `step1` says), on stream s. events: null,
 // or 7 handles recorded at the stage boundaries (see gs_render_profiled for
 // their order in each order of the steps).
@@ -228,10 +260,38 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
     if (e == cudaSuccess) e = mark(0);
     uint32_t* tile_order = nullptr;
     auto* order_done = reinterpret_cast<uint32_t*>(w + L.order_done);
+    // the tile ranges and the launch order: from the sorted keys, after the tile
+    // sort; or, when the projection runs here, the tile grid's difference array
+    // fits in shared memory and the depth sort's passes leave SMs free (up to
+    // kSideRangesMaxN Gaussians; beyond, its persistent passes fill every SM
+    // and the side work slowed them), from the tile rectangles on a second
+    // stream forked after the projection, while the sorts run
+    const bool overlap = GS_SIDE_RANGES && step1 == Step1::kProject && g->n <= kSideRangesMaxN &&
+                         tile_len_fits(cc.tiles_x, cc.tiles_y);
+    SideStream side{};
+    auto fork_ranges = [&]() {
+        cudaError_t r = side_stream(&side);
+        if (r == cudaSuccess) r = cudaEventRecord(side.fork, s);
+        if (r == cudaSuccess) r = cudaStreamWaitEvent(side.s, side.fork, 0);
+        if (r == cudaSuccess)
+            r = launch_tile_len_ranges(p.tiles_touched, p.rect, g->n, cc.tiles_x, cc.tiles_y, km, tbits,
+                                       key_capacity, reinterpret_cast<int*>(w + L.len_diff), ranges, side.s);
+        if (r == cudaSuccess)
+            r = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, side.s, order_done);
+        if (r == cudaSuccess) r = cudaEventRecord(side.join, side.s);
+        return r;
+    };
+    auto ranges_and_order = [&]() {
+        if (overlap) return cudaStreamWaitEvent(s, side.join, 0);
+        cudaError_t r = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s, true, &km);
+        if (r == cudaSuccess) r = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, s, order_done);
+        return r;
+    };
     if (tile_first(key_capacity, step1)) {
         // bin in index order, stable sort by tile, then each tile's list by (depth bits, index)
         if (e == cudaSuccess && step1 == Step1::kProject) e = launch_preprocess(*g, cc, p, s, nullptr, header);
         if (e == cudaSuccess) e = mark(1);
+        if (e == cudaSuccess && overlap) e = fork_ranges();
         if (e == cudaSuccess)
             e = launch_bin_ordered(p, nullptr, g->n, cc, nullptr, keys, vals, key_capacity, num_keys, header,
                                    w + L.bin, s, tile_hist, tbits, &km);
@@ -240,9 +300,7 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
             e = launch_sort32_split(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, tbits, header,
                                     w + L.tile_head, w + L.tile_lb, g_spin_limit, s, true);
         if (e == cudaSuccess) e = mark(3);
-        if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s, true, &km);
-        if (e == cudaSuccess)
-            e = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, s, order_done);
+        if (e == cudaSuccess) e = ranges_and_order();
         if (e == cudaSuccess) e = mark(4);
         // the tile ids are not read again: their array is the long lists' key scratch
         if (e == cudaSuccess)
@@ -262,6 +320,7 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
     const DepthKeysOut dk = view_depth_keys(w, L);
     if (e == cudaSuccess && step1 == Step1::kProject) e = launch_preprocess(*g, cc, p, s, &dk, header);
     if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess && overlap) e = fork_ranges();
     if (e == cudaSuccess && step1 == Step1::kRecordOnly) e = launch_depth_keys(p, g->n, dkeys, order, dk.hist, s);
     if (e == cudaSuccess)
         e = launch_sort32_split(dkeys, order, dkeys_alt, order_alt, nullptr, g->n, 32, header, w + L.depth_head,
@@ -275,8 +334,7 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
         e = launch_sort32_split(keys, vals, keys_alt, vals_alt, num_keys, key_capacity, tbits, header,
                                 w + L.tile_head, w + L.tile_lb, g_spin_limit, s, true);
     if (e == cudaSuccess) e = mark(4);
-    if (e == cudaSuccess) e = launch_tile_ranges32(keys, num_keys, key_capacity, n_tiles, ranges, s, true, &km);
-    if (e == cudaSuccess) e = launch_tile_order_multi(ranges, n_tiles, w + L.tile_order, &tile_order, s, order_done);
+    if (e == cudaSuccess) e = ranges_and_order();
     if (e == cudaSuccess) e = mark(5);
     if (e == cudaSuccess)
         e = launch_rasterize(p, g->n, vals, ranges, tile_order, cc, image, final_T, n_contrib, s);
@@ -860,6 +918,7 @@ gs_status gs_debug_set_check_counter(uint64_t* device_counter) {
     if (e == cudaSuccess) e = set_check_counter_splat2d(p);
     if (e == cudaSuccess) e = set_check_counter_densify(p);
     if (e == cudaSuccess) e = set_check_counter_tiledepth(p);
+    if (e == cudaSuccess) e = set_check_counter_tilelen(p);
     return cuda_status(e);
 }
 

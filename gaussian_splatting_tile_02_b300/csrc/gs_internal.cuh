@@ -324,6 +324,18 @@ cudaError_t launch_tile_depth_sort(const uint32_t* ranges, const uint32_t* tile_
 int tile_depth_sort_launches(int64_t key_capacity);
 cudaError_t set_check_counter_tiledepth(unsigned long long* p);
 
+// tilelen.cu: the tile ranges from the Gaussians' tile rectangles alone (each
+// tile's list length by a 2D difference array, then an exclusive scan in
+// tile-key order), for grids whose difference array fits in shared memory
+// (tile_len_fits). diff: tile_len_diff_bytes, zeroed by the caller; ranges
+// zeroed by the caller; ranges are clamped to cap.
+bool tile_len_fits(int tiles_x, int tiles_y);
+size_t tile_len_diff_bytes(int tiles_x, int tiles_y);
+cudaError_t launch_tile_len_ranges(const uint32_t* tiles_touched, const uint16_t* rect, int64_t n, int tiles_x,
+                                   int tiles_y, const TileKeyMap& km, int key_bits, int64_t cap, int* diff,
+                                   uint32_t* ranges, cudaStream_t s);
+cudaError_t set_check_counter_tilelen(unsigned long long* p);
+
 // rasterize.cu
 // 2D splats: their per-Gaussian record into p (depth, tiles_touched, rect, raster)
 cudaError_t launch_preprocess2d(const float* means, const float* covs, const float* colours, const float* opacities,

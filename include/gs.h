@@ -29,8 +29,9 @@
  *     different workspaces. gs_render_batch enqueues under one process-wide
  *     lock (its fork/join events are shared per device); gs_set_spin_limit is
  *     not thread-safe.
- *   - cudaDeviceReset: gs_render_batch keeps per-device fork/join events that
- *     a reset destroys; do not call it on a device after resetting that device
+ *   - cudaDeviceReset: gs_render_batch keeps per-device fork/join events, and
+ *     gs_render a per-thread second stream with its events, that a reset
+ *     destroys; do not call them on a device after resetting that device
  *     in the same process. (gs_bin_static looks its scratch address up again
  *     on every call made outside stream capture.)
  */
@@ -275,7 +276,13 @@ gs_status gs_rasterize(const gs_projected* projected, int64_t n, const uint32_t*
  * gs_tile_ranges32): the Gaussians are sorted by depth, binned in that order
  * and stably sorted by tile. From 4096 tiles up the tile sort's keys number
  * the 8x4-tile block in their low digit and the tile inside it above, which
- * orders the tiles' lists differently in the array, not their contents. Tile-first, for short tile lists (see
+ * orders the tiles' lists differently in the array, not their contents. For
+ * frames of at most 2^21 Gaussians whose tile grid's difference array fits in
+ * 96 KB of shared memory (up to about 2560x1440), the tile ranges and the
+ * tiles' launch order are computed from the tile rectangles on a second
+ * stream that the library owns (one per host thread and device), forked from
+ * `stream` after the projection and joined back before they are needed;
+ * inside a CUDA graph capture the fork and the join become graph edges. Tile-first, for short tile lists (see
  * gs_render_tile_first): binned in index order, stably sorted by tile, then
  * each tile's list is sorted by (depth bits, index) on its own. Both give the
  * same per-tile lists bit for bit. The image equals the one of the staged path

@@ -133,5 +133,11 @@ def test_frame_launch_count():
     # from 4096 tiles up the tile keys hold the 8x4-tile block and 5 bits of tile within it
     assert bench.tile_key_bits(120, 68) == 13 and bench.tile_key_bits(40, 30) == 11
     assert bench.tile_key_bits(512, 270) == 18 and bench.tile_key_bits(240, 135) == 15
-    assert bench.frame_launches(120 * 68, tiles_xy=(120, 68)) == 18
-    assert bench.frame_launches(512 * 270, tiles_xy=(512, 270)) == 19
+    # the ranges from the tile rectangles on a second stream (two kernels) up to 2^21
+    # Gaussians where the grid's difference array fits in shared memory: 1080p yes, 8K no
+    assert bench.side_ranges(10**6, 120, 68) and not bench.side_ranges(5 * 10**6, 120, 68)
+    assert not bench.side_ranges(10**6, 240, 135)
+    assert bench.frame_launches(120 * 68, tiles_xy=(120, 68), n=10**6) == 19
+    assert bench.frame_launches(120 * 68, tiles_xy=(120, 68), n=5 * 10**6) == 18
+    assert bench.frame_launches(512 * 270, tiles_xy=(512, 270), n=10**6) == 19
+    assert bench.frame_launches(240 * 135, tiles_xy=(240, 135), n=10**6) == 18
