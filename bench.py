@@ -528,7 +528,7 @@ def measure_view(torch, gs, native, g, cam, r, stream, dev, steps, warmup, use_g
             "evaluations": evals, "graph": use_graph, "tile_first": tile_first}
 
 
-def stage_summary(st_ms, n, sh_degree, K, tiles_x, tiles_y, evals, hbm_peak, fp32, tile_first=False):
+def stage_summary(st_ms, n, sh_degree, K, tiles_x, tiles_y, evals, hbm_peak, fp32, tile_first=False, side=False):
     """Per-stage achieved rates and roofline fractions. HBM-bound stages: algorithmic bytes per
     unit (preprocess also in the method's count: parameters read + the 48-byte projected record
     written). Rasterize: evaluations x 15 flops (the method's count) against the measured FMA
@@ -552,6 +552,11 @@ def stage_summary(st_ms, n, sh_degree, K, tiles_x, tiles_y, evals, hbm_peak, fp3
     for k, b in stage_bytes.items():
         out[k] = {"ms": st_ms[k], "bound": "hbm", "GB/s": gbs(b, st_ms[k]), "frac": gbs(b, st_ms[k]) / hbm_peak,
                   "bytes": b}
+    if side:
+        # the ranges and the launch order ran on the second stream during the sorts; the stage
+        # times the frame's wait for them, so it has no rate of its own
+        out["ranges"] = {"ms": st_ms["ranges"], "bound": "overlapped", "frac": None, "bytes": stage_bytes["ranges"],
+                         "note": "computed from the tile rectangles on a second stream; the stage is the join"}
     mb = (pb + PROJ_BYTES_METHOD) * n
     out["preprocess"].update({"bytes_method": mb, "GB/s_method": gbs(mb, st_ms["preprocess"]),
                               "frac_method": gbs(mb, st_ms["preprocess"]) / hbm_peak})
@@ -807,7 +812,8 @@ def run_ours(args, rank, local_rank, world):
                     recs.append({"view": v, "frame_ms": m["frame_ms"], "fps": 1e3 / m["frame_ms"], "keys": m["keys"],
                                  "tile_first": m["tile_first"],
                                  "stages": stage_summary(m["stage_ms"], cfg_n.n, cfg_n.sh_degree, m["keys"], ctx, cty,
-                                                         m["evaluations"], hbm_peak, fp32, m["tile_first"])})
+                                                         m["evaluations"], hbm_peak, fp32, m["tile_first"],
+                                                         side_ranges(cfg_n.n, ctx, cty))})
                 mean_ms = statistics.mean(x["frame_ms"] for x in recs)
                 mean_st = {}
                 for k in recs[0]["stages"]:
@@ -825,7 +831,7 @@ def run_ours(args, rank, local_rank, world):
     n = int(g["n"])
     K = head["keys"]
     stages_out = stage_summary(st_ms, n, cfg.sh_degree, K, tx, ty, head["evaluations"], hbm_peak, fp32,
-                               head["tile_first"])
+                               head["tile_first"], side_ranges(n, tx, ty))
     launches_per_frame = frame_launches(tx * ty, head["tile_first"], r.key_capacity, (tx, ty), int(g["n"]))
     ras = stages_out["rasterize"]
     evals = head["evaluations"]
