@@ -353,6 +353,45 @@ def test_frame_does_not_depend_on_workspace_contents(name, order):
         L.gs_set_steps_order(0)
 
 
+def test_concurrent_host_threads_render_correct_frames():
+    """gs_render from two host threads at once, each with its own stream, renderer and
+    workspace (and so its own second stream for the ranges): every frame equals the one
+    rendered alone, bit for bit."""
+    import threading
+    scene, g = scene_of("100k")
+    cam0 = scenes.make_cameras("100k")[0]
+    renderers, refs = [], []
+    for cam in (cam0, cam0):
+        r = gs.Renderer.for_scene(g, cam, headroom=1.1)
+        r.render(cam)
+        torch.cuda.synchronize()
+        refs.append(r.image.cpu().numpy().copy())
+        renderers.append((r, cam))
+    errors = []
+
+    def work(i):
+        try:
+            r, cam = renderers[i]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    r.image.zero_()
+                    r.render(cam, stream=s)
+                    img = r.image.cpu().numpy()
+                    if not np.array_equal(img, refs[i]):
+                        errors.append(i)
+                        return
+        except Exception as ex:   # reported below
+            errors.append(repr(ex))
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+
+
 def test_tile_order_is_heavy_first_and_leaves_image_unchanged():
     """The heavy-first launch order is a permutation of the tiles with
     non-increasing floor(log2 length); the image, final T and n_contrib do not
