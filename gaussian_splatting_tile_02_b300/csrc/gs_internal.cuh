@@ -314,14 +314,13 @@ cudaError_t launch_spin_timeout_test(StatusHeader* status, long long iterations,
 // sorted by (depth bits, index) in place, tiles in the given launch order (nullable).
 // keys_a, keys_b, vals_b: scratch of the key capacity (lists longer than a block's
 // shared-memory sort go through them); scratch: tile_depth_scratch_bytes(tiles).
-// One kernel per list-size class that the key capacity allows (tile_depth_sort_launches).
+// One kernel per list-size class that the key capacity allows.
 // counts: three uint32 the caller has zeroed.
 size_t tile_depth_scratch_bytes(int tiles);
 cudaError_t launch_tile_depth_sort(const uint32_t* ranges, const uint32_t* tile_order, int tiles, const float* depth,
                                    int64_t n, int64_t key_capacity, uint32_t* vals, uint32_t* keys_a,
                                    uint32_t* keys_b, uint32_t* vals_b, uint32_t* counts, void* scratch,
                                    cudaStream_t s);
-int tile_depth_sort_launches(int64_t key_capacity);
 cudaError_t set_check_counter_tiledepth(unsigned long long* p);
 
 // tilelen.cu: the tile ranges from the Gaussians' tile rectangles alone (each

@@ -490,12 +490,6 @@ cudaError_t launch_tile_depth_sort(const uint32_t* ranges, const uint32_t* tile_
     return cudaGetLastError();
 }
 
-// Kernels a tile-first frame's per-tile depth sort launches for this key capacity.
-int tile_depth_sort_launches(int64_t key_capacity) {
-    if (key_capacity <= 1) return 0;
-    return 1 + (key_capacity > kSmallCap) + (key_capacity > kMidCap) + (key_capacity > kBigCap);
-}
-
 GS_DEFINE_CHECK_SETTER(tiledepth)
 
 }  // namespace gs
