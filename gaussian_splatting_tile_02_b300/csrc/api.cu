@@ -189,19 +189,26 @@ bool tile_first(int64_t key_capacity, Step1 step1) {
 
 // The second stream a frame computes its tile ranges and launch order on, and
 // the events that fork it from the frame's stream and join it back: one set per
-// host thread and device, created on first use and kept (a cudaDeviceReset
-// invalidates them, as it does gs_render_batch's events).
+// host thread and device, created on first use outside a stream capture and
+// kept (a cudaDeviceReset invalidates them, as it does gs_render_batch's
+// events). *found = false: none exists yet and `main` is capturing, so none is
+// created now (the frame then runs on one stream).
 struct SideStream {
     cudaStream_t s;
     cudaEvent_t fork, join;
 };
-cudaError_t side_stream(SideStream* out) {
+cudaError_t side_stream(cudaStream_t main, SideStream* out, bool* found) {
     thread_local std::map<int, SideStream> mine;
+    *found = false;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     auto it = mine.find(dev);
     if (it == mine.end()) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        e = cudaStreamIsCapturing(main, &cs);
+        if (e != cudaSuccess) return e;
+        if (cs != cudaStreamCaptureStatusNone) return cudaSuccess;
         SideStream ss{};
         e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
@@ -210,6 +217,7 @@ cudaError_t side_stream(SideStream* out) {
         it = mine.emplace(dev, ss).first;
     }
     *out = it->second;
+    *found = true;
     return cudaSuccess;
 }
 
@@ -266,12 +274,12 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
     // kSideRangesMaxN Gaussians; beyond, its persistent passes fill every SM
     // and the side work slowed them), from the tile rectangles on a second
     // stream forked after the projection, while the sorts run
-    const bool overlap = GS_SIDE_RANGES && step1 == Step1::kProject && g->n <= kSideRangesMaxN &&
-                         tile_len_fits(cc.tiles_x, cc.tiles_y);
+    bool overlap = GS_SIDE_RANGES && step1 == Step1::kProject && g->n <= kSideRangesMaxN &&
+                   tile_len_fits(cc.tiles_x, cc.tiles_y);
     SideStream side{};
+    if (overlap && e == cudaSuccess) e = side_stream(s, &side, &overlap);
     auto fork_ranges = [&]() {
-        cudaError_t r = side_stream(&side);
-        if (r == cudaSuccess) r = cudaEventRecord(side.fork, s);
+        cudaError_t r = cudaEventRecord(side.fork, s);
         if (r == cudaSuccess) r = cudaStreamWaitEvent(side.s, side.fork, 0);
         if (r == cudaSuccess)
             r = launch_tile_len_ranges(p.tiles_touched, p.rect, g->n, cc.tiles_x, cc.tiles_y, km, tbits,

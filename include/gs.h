@@ -280,9 +280,11 @@ gs_status gs_rasterize(const gs_projected* projected, int64_t n, const uint32_t*
  * frames of at most 2^21 Gaussians whose tile grid's difference array fits in
  * 96 KB of shared memory (up to about 2560x1440), the tile ranges and the
  * tiles' launch order are computed from the tile rectangles on a second
- * stream that the library owns (one per host thread and device), forked from
+ * stream that the library owns (one per host thread and device, created on
+ * the thread's first such frame outside a stream capture), forked from
  * `stream` after the projection and joined back before they are needed;
- * inside a CUDA graph capture the fork and the join become graph edges. Tile-first, for short tile lists (see
+ * inside a CUDA graph capture the fork and the join become graph edges. A
+ * frame captured before its thread has that stream runs on `stream` alone. Tile-first, for short tile lists (see
  * gs_render_tile_first): binned in index order, stably sorted by tile, then
  * each tile's list is sorted by (depth bits, index) on its own. Both give the
  * same per-tile lists bit for bit. The image equals the one of the staged path

@@ -392,6 +392,45 @@ def test_concurrent_host_threads_render_correct_frames():
     assert not errors, errors
 
 
+def test_first_frame_of_a_thread_captured_into_a_graph():
+    """A host thread whose first gs_render is captured into a CUDA graph (no second stream
+    exists for it yet, and none is created during a capture) renders that frame on one
+    stream; the replayed graph, and an eager frame after it, equal the frame rendered on
+    the main thread, bit for bit."""
+    import threading
+    scene, g = scene_of("100k")
+    cam = scenes.make_cameras("100k")[0]
+    ref_r = gs.Renderer.for_scene(g, cam, headroom=1.1)
+    ref_r.render(cam)
+    torch.cuda.synchronize()
+    ref = ref_r.image.cpu().numpy().copy()
+    r = gs.Renderer(g, cam["width"], cam["height"], ref_r.key_capacity)
+    out = {}
+
+    def work():
+        try:
+            s = torch.cuda.Stream()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(graph, stream=s):
+                    r.render(cam, stream=s)
+                r.image.zero_()
+                graph.replay()
+                out["replay"] = r.image.cpu().numpy().copy()
+                r.image.zero_()
+                r.render(cam, stream=s)
+                out["eager"] = r.image.cpu().numpy().copy()
+        except Exception as ex:   # reported below
+            out["error"] = repr(ex)
+
+    t = threading.Thread(target=work)
+    t.start()
+    t.join()
+    assert "error" not in out, out.get("error")
+    np.testing.assert_array_equal(out["replay"], ref)
+    np.testing.assert_array_equal(out["eager"], ref)
+
+
 def test_tile_order_is_heavy_first_and_leaves_image_unchanged():
     """The heavy-first launch order is a permutation of the tiles with
     non-increasing floor(log2 length); the image, final T and n_contrib do not
