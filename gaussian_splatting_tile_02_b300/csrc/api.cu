@@ -187,6 +187,11 @@ bool tile_first(int64_t key_capacity, Step1 step1) {
     return key_capacity <= kTileFirstMaxKeys;
 }
 
+// The tile-sort key layout of a frame with this tile grid.
+TileKeyMap frame_tile_keys(int tiles_x_, int tiles_y_) {
+    return tiles_x_ * tiles_y_ >= kCoarseKeyTiles ? block_keys(tiles_x_, tiles_y_) : identity_keys(tiles_x_);
+}
+
 // The second stream a frame computes its tile ranges and launch order on, and
 // the events that fork it from the frame's stream and join it back: one set per
 // host thread and device, created on first use outside a stream capture and
@@ -247,8 +252,7 @@ cudaError_t view_pipeline(const gs_gaussians* g, const gs_camera* cam, int64_t k
 
     // the tile sort's keys: the tile block in the low digit from 4096 tiles up
     // (a warp's first-pass ranking then sees far fewer distinct digits)
-    const TileKeyMap km = cc.tiles_x * cc.tiles_y >= kCoarseKeyTiles ? block_keys(cc.tiles_x, cc.tiles_y)
-                                                                     : identity_keys(cc.tiles_x);
+    const TileKeyMap km = frame_tile_keys(cc.tiles_x, cc.tiles_y);
     const int tbits = tile_key_bits(km, cc.tiles_x * cc.tiles_y);
     auto mark = [&](int i) {
         return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
@@ -512,6 +516,28 @@ int32_t gs_render_tile_first(int64_t n, int32_t width, int32_t height, int64_t k
 }
 
 void gs_set_programmatic_launch(int32_t on) { g_programmatic_launch.store(on ? 1 : 0, std::memory_order_relaxed); }
+
+int64_t gs_debug_tile_key(int32_t tiles_x_, int32_t tiles_y_, int32_t tx, int32_t ty) {
+    if (tiles_x_ < 1 || tiles_y_ < 1 || tiles_x_ > 32768 || tiles_y_ > 32768 || tx < 0 || ty < 0 || tx >= tiles_x_ ||
+        ty >= tiles_y_)
+        return -1;
+    return tile_key(frame_tile_keys(tiles_x_, tiles_y_), (uint32_t)tx, (uint32_t)ty);
+}
+
+int32_t gs_debug_tile_key_bits(int32_t tiles_x_, int32_t tiles_y_) {
+    if (tiles_x_ < 1 || tiles_y_ < 1 || tiles_x_ > 32768 || tiles_y_ > 32768) return -1;
+    return tile_key_bits(frame_tile_keys(tiles_x_, tiles_y_), tiles_x_ * tiles_y_);
+}
+
+int64_t gs_debug_tile_of_key(int32_t tiles_x_, int32_t tiles_y_, int64_t key) {
+    if (tiles_x_ < 1 || tiles_y_ < 1 || tiles_x_ > 32768 || tiles_y_ > 32768 || key < 0) return -1;
+    const TileKeyMap km = frame_tile_keys(tiles_x_, tiles_y_);
+    if (key >= (1ll << tile_key_bits(km, tiles_x_ * tiles_y_))) return -1;
+    const uint32_t t = tile_of_key(km, (uint32_t)key);
+    const uint32_t tx = t % (uint32_t)tiles_x_, ty = t / (uint32_t)tiles_x_;
+    if (ty >= (uint32_t)tiles_y_ || tile_key(km, tx, ty) != (uint32_t)key) return -1;
+    return t;
+}
 
 gs_status gs_set_steps_order(int32_t order) {
     if (order < 0 || order > 2) return GS_ERR_INVALID_ARG;

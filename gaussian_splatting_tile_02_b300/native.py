@@ -133,6 +133,9 @@ _SIGNATURES = {
     "gs_set_spin_limit": (None, [ctypes.c_int64]),
     "gs_set_steps_order": (ctypes.c_int32, [ctypes.c_int32]),
     "gs_set_programmatic_launch": (None, [ctypes.c_int32]),
+    "gs_debug_tile_key": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    "gs_debug_tile_key_bits": (ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32]),
+    "gs_debug_tile_of_key": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64]),
     "gs_test_spin_timeout": (ctypes.c_int, [c_void_p, ctypes.c_int64, c_void_p]),
 }
 

@@ -570,6 +570,16 @@ gs_status gs_render_from_host_async(const gs_gaussians* host_gaussians,
 int32_t gs_debug_checks_enabled(void);
 gs_status gs_debug_set_check_counter(uint64_t* device_counter);
 
+/* The key gs_render's tile sort gives tile (tx, ty) of a tiles_x x tiles_y grid
+ * (the tile id ty * tiles_x + tx below 4096 tiles; from 4096 tiles up the
+ * block of 8 x 4 tiles in the low bits and the tile inside it above), the
+ * number of key bits, and the tile id of a key (-1 for a key no tile has).
+ * Host-only arithmetic, the device code's own functions; -1 for arguments
+ * outside the grid. For tests of the key layout. */
+int64_t gs_debug_tile_key(int32_t tiles_x, int32_t tiles_y, int32_t tx, int32_t ty);
+int32_t gs_debug_tile_key_bits(int32_t tiles_x, int32_t tiles_y);
+int64_t gs_debug_tile_of_key(int32_t tiles_x, int32_t tiles_y, int64_t key);
+
 /* Reads the status header at the start of a gs_bin, gs_sort or gs_render
  * workspace. SYNCHRONISES `stream`. flags/num_keys may be NULL. Returns
  * GS_ERR_TIMEOUT, GS_ERR_CAPACITY or GS_OK from the flags. num_keys is the

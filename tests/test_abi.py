@@ -193,3 +193,40 @@ def test_key_bits():
     assert gs.key_bits(scenes.make_cameras("100k")[0]) == 43      # 1200 tiles
     assert gs.key_bits(scenes.make_cameras("tiny")[0]) == 36      # 16 tiles
     assert gs.key_bits(scenes.axis_camera(1, 1, 16, 16)) == 32    # one tile
+
+
+@pytest.mark.parametrize("tiles_x,tiles_y", [(1, 1), (4, 4), (40, 30), (63, 65), (64, 64), (120, 68),
+                                             (121, 67), (240, 135), (9, 500), (512, 270)])
+def test_tile_keys_are_a_bijection_that_keeps_8x4_blocks_together(tiles_x, tiles_y):
+    """The tile-sort keys: one per tile, all distinct and below 2^bits, inverted by
+    gs_debug_tile_of_key; below 4096 tiles the key is the tile id, from 4096 up the tiles of
+    one block of 8 x 4 share the key's low bits and differ only in the five above them."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    L = native.lib()
+    tiles = tiles_x * tiles_y
+    bits = L.gs_debug_tile_key_bits(tiles_x, tiles_y)
+    assert bits == bench.tile_key_bits(tiles_x, tiles_y)
+    assert 1 <= bits <= 32
+    keys = {}
+    for ty in range(tiles_y):
+        for tx in range(tiles_x):
+            k = L.gs_debug_tile_key(tiles_x, tiles_y, tx, ty)
+            assert 0 <= k < (1 << bits)
+            assert k not in keys
+            keys[k] = (tx, ty)
+            assert L.gs_debug_tile_of_key(tiles_x, tiles_y, k) == ty * tiles_x + tx
+            if tiles < 4096:
+                assert k == ty * tiles_x + tx
+            else:
+                low = k & ((1 << (bits - 5)) - 1)
+                assert low == (ty // 4) * -(-tiles_x // 8) + tx // 8
+                assert k >> (bits - 5) == (ty % 4) * 8 + tx % 8
+    # every other key below 2^bits belongs to no tile
+    valid = sum(L.gs_debug_tile_of_key(tiles_x, tiles_y, k) >= 0 for k in range(1 << bits))
+    assert valid == tiles
+    assert L.gs_debug_tile_of_key(tiles_x, tiles_y, 1 << bits) == -1
+    assert L.gs_debug_tile_key(tiles_x, tiles_y, tiles_x, 0) == -1
+    assert L.gs_debug_tile_key(tiles_x, tiles_y, 0, tiles_y) == -1
+    assert L.gs_debug_tile_key_bits(0, 5) == -1
