@@ -70,9 +70,9 @@ __host__ __device__ inline int digit_shift(int key_bits, int p) {
 //   log2(alpha) = log2 o - t1^2 - t2^2,  t1 = k1 (mx - x),  t2 = k3 (mx - x) + k2 (my - y).
 // The terms are expanded around the tile origin, A1 = k1 mx and
 // A2 = k3 mx + k2 my once per entry, so that each pixel pair costs seven
-// FMAs; nx = -x and ny = -y are the lane's constants. Compositing and its
-// backward both use exactly this sequence, so they take the same per-entry
-// decisions bit for bit.
+// FMAs; nx = -x and ny = -y are the lane's constants. Compositing (through
+// the negated form below) and its backward both compute exactly these values,
+// so they take the same per-entry decisions bit for bit.
 __device__ __forceinline__ float2 entry_origin_terms(float mx, float my, float k1, float k2, float k3) {
     return make_float2(__fmul_rn(k1, mx), __fmaf_rn(k3, mx, __fmul_rn(k2, my)));
 }
@@ -85,6 +85,22 @@ __device__ __forceinline__ void pixel_pair_exponents(float A1, float A2, float k
     const float e1 = __fmaf_rn(-t1, t1, log2o);
     e = __fmaf_rn(-t2, t2, e1);
     e2 = __fmaf_rn(-t22, t22, e1);
+}
+// The same exponents negated, -e and -e2, with the independent FMAs paired
+// into packed two-wide ones: (t1, k2 ny + A2) in one, the two squares in
+// another. Round-to-nearest is symmetric, so fma(t, t, -x) is exactly
+// -fma(-t, t, x): every value here is the negation of the one above, bit for
+// bit, and the decisions taken on it are the same. q = (A1, A2, k1, k2),
+// nxy = (nx, ny).
+__device__ __forceinline__ void pixel_pair_neg_exponents(const float4& q, float k3, float log2o, float2 nxy,
+                                                         float& ne, float& ne2) {
+    const float2 tu = __ffma2_rn(make_float2(q.z, q.w), nxy, make_float2(q.x, q.y));
+    const float t2 = __fmaf_rn(k3, nxy.x, tu.y);
+    const float t22 = __fmaf_rn(-4.0f, q.w, t2);
+    const float ne1 = __fmaf_rn(tu.x, tu.x, -log2o);
+    const float2 n = __ffma2_rn(make_float2(t2, t22), make_float2(t2, t22), make_float2(ne1, ne1));
+    ne = n.x;
+    ne2 = n.y;
 }
 
 // The key a (tile, Gaussian) pair is sorted by, for a tile (tx, ty). Identity

@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
     // (its status is flagged): treat it as empty, never read past the list
     GS_CHECK(range0.y >= range0.x);
     const uint2 range = make_uint2(range0.x, max(range0.x, range0.y));
-    const float nfpx = -(float)lx, nfpy = -(float)ly;
+    const float2 nxy = make_float2(-(float)lx, -(float)ly);
 
     float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
     float U = 1.0f, D0 = 0.0f, D1 = 0.0f, D2 = 0.0f;   // second pixel
@@ -367,11 +367,11 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
             for (int k = 0; k < nh; k++) {
                 const float4 q = w_q[warp][k];
                 const float4 r = w_r[warp][k];
-                float t1, t2, t22, e, e2;
-                pixel_pair_exponents(q.x, q.y, q.z, q.w, r.x, r.y, nfpx, nfpy, t1, t2, t22, e, e2);
+                float ne, ne2;   // the exponents negated
+                pixel_pair_neg_exponents(q, r.x, r.y, nxy, ne, ne2);
                 // alpha = min(0.99, 2^e) < 1/255 is e < log2(1/255) (the same
                 // decision in exact arithmetic; ex2 is only evaluated past it)
-                const bool c = !done && e >= kLog2AlphaMin, c2 = !done2 && e2 >= kLog2AlphaMin;
+                const bool c = !done && ne <= -kLog2AlphaMin, c2 = !done2 && ne2 <= -kLog2AlphaMin;
                 if (!(c || c2)) continue;
                 float2 bj;
                 if constexpr (kAux)
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
                 else
                     bj.x = w_bj[warp][k].x;
                 if (c) {
-                    const float alpha = fminf(0.99f, fast_exp2(e));
+                    const float alpha = fminf(0.99f, fast_exp2(-ne));
                     const float w = alpha * T;
                     C0 += w * r.z;
                     C1 += w * r.w;
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kRastThreads, 8) rasterize_kernel(const RastAr
                     if (T < 1e-4f) done = true;
                 }
                 if (c2) {
-                    const float alpha = fminf(0.99f, fast_exp2(e2));
+                    const float alpha = fminf(0.99f, fast_exp2(-ne2));
                     const float w = alpha * U;
                     D0 += w * r.z;
                     D1 += w * r.w;
