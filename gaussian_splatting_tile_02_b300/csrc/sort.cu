@@ -206,10 +206,36 @@ struct PassArgs {
 // wh: the warp's 256 16-bit digit counters. The leader of each group of equal
 // digits (its lowest lane) advances the counter from the value it read.
 // kFull: all kSortItems x 32 positions hold keys (no validity masks).
+// The lanes holding the same digit come from match.any, whose cost grows with
+// the number of distinct digits in the warp; for digits of at most five bits
+// (a pass over the top bits of the tile keys, where most of a warp's 32
+// lanes hold different digits) five ballots give the same lane set at a
+// fixed cost.
 template <bool kFull, typename KeyT>
 __device__ __forceinline__ void rank_in_warp(const KeyT (&key)[kSortItems], uint32_t (&rank)[kSortItems], int shift,
                                              uint32_t dmask, int warp_base, int n_valid, uint16_t* wh,
                                              uint32_t lt, int lane) {
+    if (dmask <= 31u) {
+#pragma unroll
+        for (int i = 0; i < kSortItems; i++) {
+            const uint32_t d = digit_of(key[i], shift, dmask);
+            const bool v = kFull || warp_base + i * 32 + lane < n_valid;
+            uint32_t peers = __ballot_sync(0xffffffffu, v);
+#pragma unroll
+            for (int b = 0; b < 5; b++) {
+                const uint32_t bal = __ballot_sync(0xffffffffu, (d >> b) & 1u);
+                peers &= ((d >> b) & 1u) ? bal : ~bal;
+            }
+            const uint32_t below = __popc(peers & lt);
+            uint32_t r = 0;
+            if (v) r = wh[d] + below;
+            __syncwarp();
+            if (v && below == 0) wh[d] = (uint16_t)(r + __popc(peers));
+            __syncwarp();
+            rank[i] = r;
+        }
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < kSortItems; i++) {
         const uint32_t d = digit_of(key[i], shift, dmask);
